@@ -1,0 +1,209 @@
+/*
+ * kvq.h — C ABI of the low-bit KV-cache library (one GPU, sm_103a).
+ *
+ * What it computes.  A key/value cache for one attention layer, stored with
+ * uniform asymmetric integer quantization, and the decode attention that reads
+ * that packed cache directly.
+ *
+ *   - The quantizer ("Your KV cache doesn't have a bit problem, it has a
+ *     geometry problem", section "What Quantization Error Is Actually Made Of";
+ *     also "Why KV Cache Geometry Matters More Than Bit Precision", section
+ *     "Inside the Attention Equation"): per group, the zero point is the group
+ *     minimum, the step is (max - min) / (2^B - 1), and every element is
+ *     rounded to the nearest step.
+ *   - The group geometry (same page, sections "Keys: The Outliers Live in Fixed
+ *     Channels" and "Values: Where the Intuition Breaks"): keys are grouped per
+ *     channel (G consecutive tokens of one channel), values per token
+ *     (G consecutive channels of one token).  Both axes are selectable, for the
+ *     flipped arms of the ablation.
+ *   - The full-precision residual (section "The Systems Tax, and Why It Is Not a
+ *     Detail"): tokens that do not yet fill a key group stay in an fp16 tail;
+ *     a full tail of G tokens is quantized as one block.
+ *   - Keys quantized before RoPE, RoPE applied after dequantization (section
+ *     "Rotary Embeddings Complicate the Keys").
+ *   - Attention as the softmax-weighted sum of value vectors (section "Values:
+ *     Where the Intuition Breaks").
+ *
+ * Arithmetic, exactly:
+ *   mn, mx  = min and max of the group's fp16 values (converted exactly to fp32)
+ *   step32  = (mx - mn) / (2^B - 1)            fp32 subtract, IEEE fp32 divide
+ *   scale   = fp16(step32), round to nearest even
+ *   zero    = fp16(mn + 0.0f)                  exact; a -0 minimum is stored as +0
+ *   code    = 0 for every element if scale == 0, else
+ *             clamp(rintf((x - mn) / float(scale)), 0, 2^B - 1)   (half-even)
+ *   x_hat   = fmaf(code, float(scale), float(zero))               (fp32)
+ * Inputs must be finite fp16; non-finite inputs give unspecified codes.
+ *
+ * Conventions for every call.
+ *   - All device pointers are raw CUDA device addresses, 16-byte aligned,
+ *     owned by the caller, and must stay valid until the stream reaches the
+ *     work enqueued on them.  Host pointers are plain host memory.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Every call that launches work is asynchronous on that stream
+ *     and never synchronizes, except kvq_check_device_error.
+ *   - Lengths are tracked on the host: every (batch, kv-head) pair holds the
+ *     same number of tokens.
+ *   - Errors are returned as kvq_status; nothing is thrown across the ABI.  A
+ *     call that returns an error other than KVQ_ERR_CUDA leaves the cache
+ *     state unchanged.
+ *   - Kernels never trap.  A bounded wait that runs out sets a device error
+ *     word that kvq_check_device_error reports as KVQ_ERR_DEVICE_CHECK.
+ *
+ * Device layout of the packed cache (P = batch * n_kv_heads pairs,
+ * pair p = b * n_kv_heads + h; NB = max_ctx / G blocks per pair; D = head_dim;
+ * bk, bv = bits of K and V; words are little-endian uint32):
+ *
+ *   block (p, i) starts at byte (p * NB + i) * block_bytes, where
+ *   block_bytes = G*D*(bk+bv)/8 + 8*D, and holds tokens [i*G, (i+1)*G):
+ *     [off_kc, +G*D*bk/8)  K codes, token-major: token j's row is D*bk/32
+ *                          words; channel d sits in word d/(32/bk) at bit
+ *                          (d % (32/bk)) * bk.
+ *     [off_km, +4*D)       K metadata: D entries {fp16 scale, fp16 zero}
+ *                          (scale at the lower address).  Channel axis:
+ *                          entry d is channel d's group.  Token axis: entry
+ *                          j*(D/G) + g is token j, channels [g*G, (g+1)*G).
+ *     [off_vc, +G*D*bv/8)  V codes, in 32-token chunks c = j/32; inside a
+ *                          chunk, channel-major: channel d owns bv words at
+ *                          word offset (c*D + d)*bv; token j sits in word
+ *                          (j%32)/(32/bv) of them at bit ((j%32) % (32/bv))*bv.
+ *     [off_vm, +4*D)       V metadata, indexed as for K by V's axis.
+ *   off_kc = 0, off_km = G*D*bk/8, off_vc = off_km + 4*D,
+ *   off_vm = off_vc + G*D*bv/8.
+ *
+ *   The tail is fp16 [P][G][D] for K and for V; tokens [T_q, T_q + T_tail) of
+ *   every pair sit in rows [0, T_tail).
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_ERR_INVALID_ARG = 1,  /* null handle/pointer, misaligned pointer, bad size */
+  KVQ_ERR_UNSUPPORTED = 2,  /* a valid config this build has no kernel for     */
+  KVQ_ERR_CAPACITY = 3,     /* T_q + T_tail + n would exceed max_ctx            */
+  KVQ_ERR_OOM = 4,          /* device allocation failed                         */
+  KVQ_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed             */
+  KVQ_ERR_DEVICE_CHECK = 6  /* a kernel reported a bounded wait that ran out    */
+} kvq_status;
+
+typedef enum {
+  KVQ_AXIS_CHANNEL = 0, /* group = G consecutive tokens of one channel */
+  KVQ_AXIS_TOKEN = 1    /* group = G consecutive channels of one token */
+} kvq_axis;
+
+typedef struct {
+  int batch;         /* >= 1                                                  */
+  int n_q_heads;     /* multiple of n_kv_heads; ratio in {1, 2, 4, 8}          */
+  int n_kv_heads;    /* >= 1                                                  */
+  int head_dim;      /* 64 or 128                                             */
+  int max_ctx;       /* capacity in tokens per pair, >= 1                     */
+  int bits_k;        /* 2, 4 or 8                                             */
+  int bits_v;        /* 2, 4 or 8                                             */
+  int group;         /* G: 32, 64 or 128; head_dim % G == 0 if an axis is TOKEN */
+  int axis_k;        /* kvq_axis; the pages' choice is KVQ_AXIS_CHANNEL        */
+  int axis_v;        /* kvq_axis; the pages' choice is KVQ_AXIS_TOKEN          */
+  int keys_pre_rope; /* 1: keys are stored before RoPE; decode rotates them    */
+  float rope_base;   /* RoPE base (e.g. 10000), used when keys_pre_rope = 1    */
+} kvq_config;
+
+typedef struct kvq_cache kvq_cache; /* opaque */
+
+/* Device addresses and geometry of a cache, for tests and for callers that
+ * read the packed bytes.  All pointers are owned by the cache. */
+typedef struct {
+  void* blocks;                /* [P][NB][block_bytes] packed blocks            */
+  void* k_tail;                /* active K tail, fp16 [P][G][D]                 */
+  void* v_tail;                /* active V tail, fp16 [P][G][D]                 */
+  size_t block_bytes;
+  size_t off_kc, off_km, off_vc, off_vm;
+  int blocks_per_pair;         /* NB                                            */
+  int n_pairs;                 /* P                                             */
+  int T_q;                     /* quantized tokens per pair (multiple of G)     */
+  int T_tail;                  /* tail tokens per pair, 0 <= T_tail < G         */
+} kvq_buffers;
+
+/* Validates a config on the host (no GPU needed).  Returns KVQ_OK,
+ * KVQ_ERR_INVALID_ARG (malformed) or KVQ_ERR_UNSUPPORTED. */
+KVQ_API kvq_status kvq_config_check(const kvq_config* cfg);
+
+/* Device bytes kvq_create allocates for `cfg` (packed blocks, two tail
+ * buffers, RoPE table, split workspace, error word).  Host only. */
+KVQ_API kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes);
+
+/* Allocates an empty cache on the current CUDA device and builds its RoPE
+ * cos/sin table (fp64 on the host, stored fp32).  *out receives the handle;
+ * on error *out is set to NULL and nothing stays allocated. */
+KVQ_API kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out);
+
+/* Frees everything the cache owns.  Synchronizes the device first.  NULL is
+ * accepted and ignored. */
+KVQ_API kvq_status kvq_destroy(kvq_cache* cache);
+
+/* Prefill: resets the cache, then quantizes tokens [0, floor(T/G)*G) of every
+ * pair into blocks and copies the remaining T mod G tokens into the tail.
+ * k, v: device fp16 [batch][n_kv_heads][T][head_dim], contiguous.
+ * T = 0 empties the cache.  T > max_ctx -> KVQ_ERR_CAPACITY. */
+KVQ_API kvq_status kvq_quantize_prefill(kvq_cache* cache, const void* k,
+                                        const void* v, int T, void* stream);
+
+/* Decode-time append of n tokens per pair: the tail and the new tokens form
+ * one sequence; every full group of G tokens in it is quantized into the next
+ * block (the tail flush) and the rest becomes the new tail.
+ * k, v: device fp16 [batch][n_kv_heads][n][head_dim], contiguous.  n = 0 is a
+ * no-op.  T_q + T_tail + n > max_ctx -> KVQ_ERR_CAPACITY. */
+KVQ_API kvq_status kvq_append(kvq_cache* cache, const void* k, const void* v,
+                              int n, void* stream);
+
+/* Split-K decode attention of one query token per head over every cached
+ * token (T_q dequantized tokens, then the T_tail fp16 tail tokens):
+ *   out[b][hq] = sum_t softmax_t(scale * q[b][hq] . k_t) * v_t
+ * with query head hq reading kv head hq / (n_q_heads / n_kv_heads).  When
+ * keys_pre_rope = 1, key t is rotated (rotate-half RoPE, angle
+ * t * base^(-2i/D) on channel pair (i, i + D/2)) after dequantization; q is
+ * taken as already rotated.
+ * q: device fp16 [batch][n_q_heads][head_dim]; out: device fp32, same shape.
+ * An empty cache writes zeros. */
+KVQ_API kvq_status kvq_decode_attention(kvq_cache* cache, const void* q,
+                                        void* out, float softmax_scale,
+                                        void* stream);
+
+/* Dequantizes the T_q packed tokens of every pair (before any RoPE).
+ * k_out, v_out: device fp32 [batch][n_kv_heads][T_q][head_dim]. */
+KVQ_API kvq_status kvq_dequantize(kvq_cache* cache, void* k_out, void* v_out,
+                                  void* stream);
+
+/* Host-side lengths: quantized tokens and tail tokens per pair. */
+KVQ_API kvq_status kvq_get_state(const kvq_cache* cache, int* T_q,
+                                 int* T_tail);
+
+/* Device addresses and geometry (see the layout above). */
+KVQ_API kvq_status kvq_get_buffers(const kvq_cache* cache, kvq_buffers* out);
+
+/* Synchronizes `stream`, reads and clears the device error word.  Returns
+ * KVQ_OK, KVQ_ERR_DEVICE_CHECK (a bounded wait ran out) or KVQ_ERR_CUDA. */
+KVQ_API kvq_status kvq_check_device_error(kvq_cache* cache, void* stream);
+
+/* Number of kernels this library has launched in this process. */
+KVQ_API uint64_t kvq_launch_count(void);
+
+/* Static description of a status code. */
+KVQ_API const char* kvq_status_string(kvq_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */

@@ -1,0 +1,260 @@
+"""CPU oracle of the low-bit KV-cache path — TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path (the CUDA library and
+its Python binding) never imports it and shares no code with it.
+
+The arithmetic lives in ``kvq_oracle.c`` (plain C, fp32 quantizer, fp64
+attention); this module compiles it with gcc on first use and wraps it with
+numpy.  Everything here works on one (batch, kv-head) pair at a time or loops
+over pairs in plain Python.
+
+Sources (page titles and sections):
+  * quantizer: "Your KV cache doesn't have a bit problem, it has a geometry
+    problem", "What Quantization Error Is Actually Made Of";
+  * key/value grouping: same page, "Keys: The Outliers Live in Fixed Channels"
+    and "Values: Where the Intuition Breaks";
+  * fp16 residual tail: same page, "The Systems Tax, and Why It Is Not a
+    Detail" — a cache built by any sequence of prefill/append calls equals the
+    cache built from the whole token sequence at once, because full groups are
+    always G-aligned; ``build_pair`` uses that definition;
+  * RoPE after dequantization: same page, "Rotary Embeddings Complicate the
+    Keys";
+  * attention output and the error metrics (relative Frobenius norm, the
+    plainest reading of the pages' unnamed error measures): same page, "Keys"
+    and "Values" sections.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "kvq_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+CFLAGS = ["-O2", "-fno-fast-math", "-ffp-contract=off", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile kvq_oracle.c into liboracle.so (gcc); returns the path."""
+    stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    if force or stale:
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    L = ctypes.c_long
+    D = ctypes.c_double
+    lib.kvo_h2f.restype = ctypes.c_float
+    lib.kvo_h2f.argtypes = [ctypes.c_uint16]
+    lib.kvo_f2h.restype = ctypes.c_uint16
+    lib.kvo_f2h.argtypes = [ctypes.c_float]
+    lib.kvo_h2f_array.argtypes = [P, P, L]
+    lib.kvo_f2h_array.argtypes = [P, P, L]
+    lib.kvo_quantize_group.argtypes = [P, L, I, I, P, P, P]
+    lib.kvo_quantize_tensor.restype = I
+    lib.kvo_quantize_tensor.argtypes = [I, I, I, I, I, P, P, P, P]
+    lib.kvo_dequantize_tensor.argtypes = [I, I, I, I, P, P, P, P]
+    lib.kvo_block_bytes.restype = ctypes.c_size_t
+    lib.kvo_block_bytes.argtypes = [I, I, I, I]
+    lib.kvo_block_offsets.argtypes = [I, I, I, I, P]
+    lib.kvo_pack_pair.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P]
+    lib.kvo_unpack_pair.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P]
+    lib.kvo_rope.argtypes = [P, I, L, D]
+    lib.kvo_attention_pair.argtypes = [I, I, I, I, P, P, P, P, P, D, I, D, P, P]
+    _lib = lib
+    return lib
+
+
+def _p(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+# ---- fp16 helpers -----------------------------------------------------------
+
+def h2f(h_bits: np.ndarray) -> np.ndarray:
+    """fp16 bit patterns (uint16) -> float32 values."""
+    h = _c(h_bits, np.uint16)
+    out = np.empty(h.shape, np.float32)
+    _load().kvo_h2f_array(_p(h), _p(out), h.size)
+    return out
+
+
+def f2h(f: np.ndarray) -> np.ndarray:
+    """float32 values -> fp16 bit patterns (round to nearest even)."""
+    x = _c(f, np.float32)
+    out = np.empty(x.shape, np.uint16)
+    _load().kvo_f2h_array(_p(x), _p(out), x.size)
+    return out
+
+
+def bits_of(x: np.ndarray) -> np.ndarray:
+    """np.float16 array -> its uint16 bit patterns."""
+    return _c(x, np.float16).view(np.uint16)
+
+
+# ---- quantizer ----------------------------------------------------------------
+
+def quantize_group(x_f16: np.ndarray, bits: int):
+    """One group: returns (scale fp16 bits, zero fp16 bits, codes uint8[n])."""
+    x = bits_of(x_f16).reshape(-1)
+    s = np.zeros(1, np.uint16)
+    z = np.zeros(1, np.uint16)
+    codes = np.zeros(x.size, np.uint8)
+    _load().kvo_quantize_group(_p(x), 1, x.size, bits, _p(s), _p(z), _p(codes))
+    return int(s[0]), int(z[0]), codes
+
+
+def quantize_tensor(X_f16: np.ndarray, G: int, bits: int, axis: int):
+    """X: fp16 [T][D].  Returns (Tq, codes [Tq][D], scale bits, zero bits) with
+    scale/zero shaped [Tq/G][D] (channel axis) or [Tq][D/G] (token axis)."""
+    T, D = X_f16.shape
+    Tq = (T // G) * G
+    x = bits_of(X_f16)
+    codes = np.zeros((Tq, D), np.uint8)
+    mshape = (Tq // G, D) if axis == 0 else (Tq, D // G)
+    scale = np.zeros(mshape, np.uint16)
+    zero = np.zeros(mshape, np.uint16)
+    got = _load().kvo_quantize_tensor(T, D, G, bits, axis, _p(x), _p(codes), _p(scale), _p(zero))
+    assert got == Tq
+    return Tq, codes, scale, zero
+
+
+def dequantize_tensor(codes, scale, zero, G: int, axis: int) -> np.ndarray:
+    Tq, D = codes.shape
+    out = np.zeros((Tq, D), np.float32)
+    c, s, z = _c(codes, np.uint8), _c(scale, np.uint16), _c(zero, np.uint16)
+    _load().kvo_dequantize_tensor(Tq, D, G, axis, _p(c), _p(s), _p(z), _p(out))
+    return out
+
+
+# ---- layout -----------------------------------------------------------------
+
+def block_bytes(D: int, G: int, bk: int, bv: int) -> int:
+    return int(_load().kvo_block_bytes(D, G, bk, bv))
+
+
+def block_offsets(D: int, G: int, bk: int, bv: int):
+    off = np.zeros(4, np.uint64)
+    _load().kvo_block_offsets(D, G, bk, bv, _p(off))
+    return [int(v) for v in off]
+
+
+def pack_pair(st: dict) -> np.ndarray:
+    """Packs one pair's quantized state into its blocks: uint8 [Tq/G][block_bytes]."""
+    Tq, D = st["kcodes"].shape
+    G, bk, bv, ak, av = st["G"], st["bk"], st["bv"], st["ak"], st["av"]
+    bb = block_bytes(D, G, bk, bv)
+    out = np.zeros((Tq // G, bb), np.uint8)
+    arrs = [_c(st["kcodes"], np.uint8), _c(st["kscale"], np.uint16), _c(st["kzero"], np.uint16),
+            _c(st["vcodes"], np.uint8), _c(st["vscale"], np.uint16), _c(st["vzero"], np.uint16)]
+    _load().kvo_pack_pair(Tq, D, G, bk, bv, ak, av, *[_p(a) for a in arrs], _p(out))
+    return out
+
+
+def unpack_pair(blocks: np.ndarray, D: int, G: int, bk: int, bv: int, ak: int, av: int) -> dict:
+    nb = blocks.shape[0]
+    Tq = nb * G
+    km = (nb, D) if ak == 0 else (Tq, D // G)
+    vm = (nb, D) if av == 0 else (Tq, D // G)
+    st = dict(G=G, bk=bk, bv=bv, ak=ak, av=av,
+              kcodes=np.zeros((Tq, D), np.uint8), kscale=np.zeros(km, np.uint16),
+              kzero=np.zeros(km, np.uint16), vcodes=np.zeros((Tq, D), np.uint8),
+              vscale=np.zeros(vm, np.uint16), vzero=np.zeros(vm, np.uint16))
+    blk = _c(blocks, np.uint8)
+    _load().kvo_unpack_pair(Tq, D, G, bk, bv, ak, av, _p(blk),
+                            _p(st["kcodes"]), _p(st["kscale"]), _p(st["kzero"]),
+                            _p(st["vcodes"]), _p(st["vscale"]), _p(st["vzero"]))
+    return st
+
+
+# ---- one pair's cache -------------------------------------------------------
+
+def build_pair(K_f16: np.ndarray, V_f16: np.ndarray, G: int, bk: int, bv: int,
+               ak: int = 0, av: int = 1) -> dict:
+    """The cache state of one pair after its T tokens arrived (any mix of
+    prefill and appends): the G-aligned prefix quantized, the rest in the
+    fp16 tail."""
+    T, D = K_f16.shape
+    Tq, kc, ks, kz = quantize_tensor(K_f16, G, bk, ak)
+    _, vc, vs, vz = quantize_tensor(V_f16, G, bv, av)
+    return dict(G=G, bk=bk, bv=bv, ak=ak, av=av, Tq=Tq, Tt=T - Tq,
+                kcodes=kc, kscale=ks, kzero=kz, vcodes=vc, vscale=vs, vzero=vz,
+                ktail=np.ascontiguousarray(K_f16[Tq:], np.float16),
+                vtail=np.ascontiguousarray(V_f16[Tq:], np.float16))
+
+
+def dequantize_pair(st: dict):
+    kh = dequantize_tensor(st["kcodes"], st["kscale"], st["kzero"], st["G"], st["ak"])
+    vh = dequantize_tensor(st["vcodes"], st["vscale"], st["vzero"], st["G"], st["av"])
+    return kh, vh
+
+
+# ---- RoPE and attention -----------------------------------------------------
+
+def rope(x: np.ndarray, pos: int, base: float) -> np.ndarray:
+    """Rotate-half RoPE of one vector, fp64."""
+    v = np.array(x, dtype=np.float64, copy=True)
+    _load().kvo_rope(_p(v), v.size, int(pos), float(base))
+    return v
+
+
+def attention_pair(q_f16: np.ndarray, khat: np.ndarray, vhat: np.ndarray,
+                   ktail_f16: np.ndarray, vtail_f16: np.ndarray, scale: float,
+                   rope_on: bool = False, base: float = 10000.0, want_scores: bool = False):
+    """fp64 attention of R query heads over one pair's keys/values.
+    q: fp16 [R][D]; khat/vhat: fp32 [Tq][D]; tails: fp16 [Tt][D]."""
+    R, D = q_f16.shape
+    khat = _c(khat, np.float32).reshape(-1, D)
+    vhat = _c(vhat, np.float32).reshape(-1, D)
+    kt = bits_of(ktail_f16).reshape(-1, D)
+    vt = bits_of(vtail_f16).reshape(-1, D)
+    Tq, Tt = khat.shape[0], kt.shape[0]
+    out = np.zeros((R, D), np.float64)
+    scores = np.zeros((R, Tq + Tt), np.float64) if want_scores else None
+    qb = bits_of(q_f16)
+    _load().kvo_attention_pair(R, D, Tq, Tt, _p(qb), _p(khat), _p(vhat), _p(kt), _p(vt),
+                               float(scale), 1 if rope_on else 0, float(base), _p(out),
+                               _p(scores) if want_scores else None)
+    return (out, scores) if want_scores else out
+
+
+def decode_pair(st: dict, q_f16: np.ndarray, scale: float, rope_on: bool = False,
+                base: float = 10000.0, want_scores: bool = False):
+    """Decode attention of one pair's quantized cache (dequantized values plus
+    the fp16 tail)."""
+    kh, vh = dequantize_pair(st)
+    return attention_pair(q_f16, kh, vh, st["ktail"], st["vtail"], scale, rope_on, base, want_scores)
+
+
+def reference_pair(K_f16, V_f16, q_f16, scale, rope_on=False, base=10000.0, want_scores=False):
+    """fp64 attention over the unquantized fp16 keys/values (the error
+    metrics' reference)."""
+    D = K_f16.shape[1]
+    empty = np.zeros((0, D), np.float32)
+    return attention_pair(q_f16, empty, empty, K_f16, V_f16, scale, rope_on, base, want_scores)
+
+
+def rel_fro(approx: np.ndarray, exact: np.ndarray) -> float:
+    """Relative Frobenius error ||approx - exact|| / ||exact||."""
+    a = np.asarray(approx, np.float64)
+    e = np.asarray(exact, np.float64)
+    return float(np.linalg.norm(a - e) / np.linalg.norm(e))

@@ -1,0 +1,339 @@
+/*
+ * kvq_oracle.c — plain, slow CPU oracle of the low-bit KV-cache path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the tests, the smoke check and the bench's
+ * CPU-baseline leg may load this library.  It shares no code, header, table
+ * or constant with the CUDA library: every definition below is written out
+ * again from the method's description and from the documented byte layout.
+ *
+ * Build: gcc -O2 -fno-fast-math -ffp-contract=off -fPIC -shared (no FMA
+ * contraction, IEEE fp32 arithmetic, round-to-nearest-even).
+ *
+ * Sources of each step ("Your KV cache doesn't have a bit problem, it has a
+ * geometry problem" = GEOMETRY; "Why KV Cache Geometry Matters More Than Bit
+ * Precision" = DIAL):
+ *   quantizer ........ GEOMETRY "What Quantization Error Is Actually Made Of";
+ *                      DIAL "Inside the Attention Equation"
+ *   key grouping ..... GEOMETRY "Keys: The Outliers Live in Fixed Channels"
+ *   value grouping ... GEOMETRY "Values: Where the Intuition Breaks"
+ *   fp16 tail ........ GEOMETRY "The Systems Tax, and Why It Is Not a Detail"
+ *   RoPE after dequant GEOMETRY "Rotary Embeddings Complicate the Keys"
+ *   attention ........ GEOMETRY "Values: Where the Intuition Breaks" (softmax
+ *                      weighted sum of value vectors), evaluated in fp64.
+ *
+ * Every function works on ONE (batch, kv-head) pair; loops are plain and in
+ * the order of the definition.  Parity pins for every function live in the
+ * CPU test suite (hand-worked ties, brute-force nearest-level search, golden
+ * packed words, closed-form attention and RoPE cases).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- fp16 <-> fp32 (C _Float16: IEEE binary16, round to nearest even) ---- */
+
+float kvo_h2f(uint16_t h) {
+  _Float16 v;
+  memcpy(&v, &h, 2);
+  return (float)v;
+}
+
+uint16_t kvo_f2h(float f) {
+  _Float16 v = (_Float16)f;
+  uint16_t h;
+  memcpy(&h, &v, 2);
+  return h;
+}
+
+void kvo_h2f_array(const uint16_t* h, float* f, long n) {
+  for (long i = 0; i < n; ++i) f[i] = kvo_h2f(h[i]);
+}
+
+void kvo_f2h_array(const float* f, uint16_t* h, long n) {
+  for (long i = 0; i < n; ++i) h[i] = kvo_f2h(f[i]);
+}
+
+/* ---- the quantizer on one group ----------------------------------------- */
+
+/* Quantizes the n fp16 values x[0], x[stride], ..., x[(n-1)*stride] with
+ * `bits` bits.  The zero point is the smallest value, the step is the range
+ * divided by 2^bits - 1 (rounded to fp16 for storage), and each element goes
+ * to the nearest step, ties to even.  A stored step of 0 (range 0, or a step
+ * below fp16's smallest subnormal) gives code 0 everywhere. */
+void kvo_quantize_group(const uint16_t* x, long stride, int n, int bits,
+                        uint16_t* scale_out, uint16_t* zero_out,
+                        uint8_t* codes) {
+  float mn = kvo_h2f(x[0]);
+  float mx = mn;
+  for (int i = 1; i < n; ++i) {
+    float v = kvo_h2f(x[(long)i * stride]);
+    if (v < mn) mn = v;
+    if (v > mx) mx = v;
+  }
+  int levels = (1 << bits) - 1;
+  float step = (mx - mn) / (float)levels;
+  uint16_t s_h = kvo_f2h(step);
+  float s = kvo_h2f(s_h);
+  *scale_out = s_h;
+  *zero_out = kvo_f2h(mn + 0.0f);
+  for (int i = 0; i < n; ++i) {
+    float v = kvo_h2f(x[(long)i * stride]);
+    int c = 0;
+    if (s != 0.0f) {
+      float r = rintf((v - mn) / s);
+      if (!(r >= 0.0f)) r = 0.0f;
+      if (r > (float)levels) r = (float)levels;
+      c = (int)r;
+    }
+    codes[i] = (uint8_t)c;
+  }
+}
+
+/* ---- one tensor (K or V) of one pair ------------------------------------- */
+
+/* X: fp16 [T][D].  Quantizes tokens [0, Tq), Tq = floor(T/G)*G.
+ * codes: [Tq][D].  scale/zero: axis 0 (channel) -> [Tq/G][D], entry (i, d) is
+ * channel d over tokens [i*G, (i+1)*G); axis 1 (token) -> [Tq][D/G], entry
+ * (t, g) is token t over channels [g*G, (g+1)*G).  Returns Tq. */
+int kvo_quantize_tensor(int T, int D, int G, int bits, int axis,
+                        const uint16_t* X, uint8_t* codes, uint16_t* scale,
+                        uint16_t* zero) {
+  int Tq = (T / G) * G;
+  uint8_t* tmp = (uint8_t*)malloc((size_t)G);
+  if (axis == 0) {
+    for (int i = 0; i < Tq / G; ++i) {
+      for (int d = 0; d < D; ++d) {
+        const uint16_t* first = X + (size_t)(i * G) * D + d;
+        kvo_quantize_group(first, D, G, bits, &scale[(size_t)i * D + d],
+                           &zero[(size_t)i * D + d], tmp);
+        for (int j = 0; j < G; ++j) codes[(size_t)(i * G + j) * D + d] = tmp[j];
+      }
+    }
+  } else {
+    int ng = D / G;
+    for (int t = 0; t < Tq; ++t) {
+      for (int g = 0; g < ng; ++g) {
+        const uint16_t* first = X + (size_t)t * D + (size_t)g * G;
+        kvo_quantize_group(first, 1, G, bits, &scale[(size_t)t * ng + g],
+                           &zero[(size_t)t * ng + g], tmp);
+        for (int j = 0; j < G; ++j) codes[(size_t)t * D + (size_t)g * G + j] = tmp[j];
+      }
+    }
+  }
+  free(tmp);
+  return Tq;
+}
+
+/* ---- dequantization ------------------------------------------------------ */
+
+/* out[t][d] = fmaf(code, scale, zero) in fp32, with the scale/zero entry the
+ * axis selects. */
+void kvo_dequantize_tensor(int Tq, int D, int G, int axis,
+                           const uint8_t* codes, const uint16_t* scale,
+                           const uint16_t* zero, float* out) {
+  for (int t = 0; t < Tq; ++t) {
+    for (int d = 0; d < D; ++d) {
+      size_t m = (axis == 0) ? (size_t)(t / G) * D + d
+                             : (size_t)t * (D / G) + (size_t)(d / G);
+      float s = kvo_h2f(scale[m]);
+      float z = kvo_h2f(zero[m]);
+      out[(size_t)t * D + d] = fmaf((float)codes[(size_t)t * D + d], s, z);
+    }
+  }
+}
+
+/* ---- the packed byte layout ---------------------------------------------- */
+
+static void put_bits(uint8_t* base, size_t word_index, int bit, int bits,
+                     unsigned value) {
+  /* word `word_index` (little-endian uint32) gets `value` at bit `bit` */
+  uint8_t* w = base + word_index * 4;
+  uint32_t cur = (uint32_t)w[0] | ((uint32_t)w[1] << 8) |
+                 ((uint32_t)w[2] << 16) | ((uint32_t)w[3] << 24);
+  uint32_t mask = ((1u << bits) - 1u) << bit;
+  cur = (cur & ~mask) | ((value << bit) & mask);
+  w[0] = (uint8_t)(cur & 0xff);
+  w[1] = (uint8_t)((cur >> 8) & 0xff);
+  w[2] = (uint8_t)((cur >> 16) & 0xff);
+  w[3] = (uint8_t)((cur >> 24) & 0xff);
+}
+
+static unsigned get_bits(const uint8_t* base, size_t word_index, int bit,
+                         int bits) {
+  const uint8_t* w = base + word_index * 4;
+  uint32_t cur = (uint32_t)w[0] | ((uint32_t)w[1] << 8) |
+                 ((uint32_t)w[2] << 16) | ((uint32_t)w[3] << 24);
+  return (cur >> bit) & ((1u << bits) - 1u);
+}
+
+static void put_meta(uint8_t* base, size_t entry, uint16_t s, uint16_t z) {
+  uint8_t* e = base + entry * 4;
+  e[0] = (uint8_t)(s & 0xff);
+  e[1] = (uint8_t)(s >> 8);
+  e[2] = (uint8_t)(z & 0xff);
+  e[3] = (uint8_t)(z >> 8);
+}
+
+static void get_meta(const uint8_t* base, size_t entry, uint16_t* s,
+                     uint16_t* z) {
+  const uint8_t* e = base + entry * 4;
+  *s = (uint16_t)(e[0] | (e[1] << 8));
+  *z = (uint16_t)(e[2] | (e[3] << 8));
+}
+
+size_t kvo_block_bytes(int D, int G, int bk, int bv) {
+  return (size_t)G * D * (bk + bv) / 8 + 8 * (size_t)D;
+}
+
+/* offsets[0..3] = K codes, K meta, V codes, V meta */
+void kvo_block_offsets(int D, int G, int bk, int bv, size_t* offsets) {
+  offsets[0] = 0;
+  offsets[1] = (size_t)G * D * bk / 8;
+  offsets[2] = offsets[1] + 4 * (size_t)D;
+  offsets[3] = offsets[2] + (size_t)G * D * bv / 8;
+}
+
+/* Writes the Tq/G blocks of one pair into `blocks` (Tq/G * block_bytes). */
+void kvo_pack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
+                   const uint8_t* kcodes, const uint16_t* kscale,
+                   const uint16_t* kzero, const uint8_t* vcodes,
+                   const uint16_t* vscale, const uint16_t* vzero,
+                   uint8_t* blocks) {
+  size_t bb = kvo_block_bytes(D, G, bk, bv);
+  size_t off[4];
+  kvo_block_offsets(D, G, bk, bv, off);
+  int kper = 32 / bk; /* codes per K word */
+  int vper = 32 / bv; /* codes per V word */
+  memset(blocks, 0, (size_t)(Tq / G) * bb);
+  for (int i = 0; i < Tq / G; ++i) {
+    uint8_t* blk = blocks + (size_t)i * bb;
+    /* K codes: token-major rows of D*bk/32 words */
+    for (int j = 0; j < G; ++j) {
+      for (int d = 0; d < D; ++d) {
+        size_t word = (size_t)j * (D * bk / 32) + (size_t)(d / kper);
+        put_bits(blk + off[0], word, (d % kper) * bk, bk,
+                 kcodes[(size_t)(i * G + j) * D + d]);
+      }
+    }
+    /* V codes: 32-token chunks, channel-major inside a chunk, bv words per
+     * channel */
+    for (int j = 0; j < G; ++j) {
+      int c = j / 32, jj = j % 32;
+      for (int d = 0; d < D; ++d) {
+        size_t word = ((size_t)c * D + d) * bv + (size_t)(jj / vper);
+        put_bits(blk + off[2], word, (jj % vper) * bv, bv,
+                 vcodes[(size_t)(i * G + j) * D + d]);
+      }
+    }
+    /* metadata: D entries each */
+    for (int e = 0; e < D; ++e) {
+      size_t km = (ak == 0) ? (size_t)i * D + e
+                            : (size_t)(i * G + e / (D / G)) * (D / G) + e % (D / G);
+      size_t vm = (av == 0) ? (size_t)i * D + e
+                            : (size_t)(i * G + e / (D / G)) * (D / G) + e % (D / G);
+      put_meta(blk + off[1], e, kscale[km], kzero[km]);
+      put_meta(blk + off[3], e, vscale[vm], vzero[vm]);
+    }
+  }
+}
+
+/* Inverse of kvo_pack_pair. */
+void kvo_unpack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
+                     const uint8_t* blocks, uint8_t* kcodes, uint16_t* kscale,
+                     uint16_t* kzero, uint8_t* vcodes, uint16_t* vscale,
+                     uint16_t* vzero) {
+  size_t bb = kvo_block_bytes(D, G, bk, bv);
+  size_t off[4];
+  kvo_block_offsets(D, G, bk, bv, off);
+  int kper = 32 / bk, vper = 32 / bv;
+  for (int i = 0; i < Tq / G; ++i) {
+    const uint8_t* blk = blocks + (size_t)i * bb;
+    for (int j = 0; j < G; ++j) {
+      int c = j / 32, jj = j % 32;
+      for (int d = 0; d < D; ++d) {
+        size_t kw = (size_t)j * (D * bk / 32) + (size_t)(d / kper);
+        kcodes[(size_t)(i * G + j) * D + d] =
+            (uint8_t)get_bits(blk + off[0], kw, (d % kper) * bk, bk);
+        size_t vw = ((size_t)c * D + d) * bv + (size_t)(jj / vper);
+        vcodes[(size_t)(i * G + j) * D + d] =
+            (uint8_t)get_bits(blk + off[2], vw, (jj % vper) * bv, bv);
+      }
+    }
+    for (int e = 0; e < D; ++e) {
+      size_t km = (ak == 0) ? (size_t)i * D + e
+                            : (size_t)(i * G + e / (D / G)) * (D / G) + e % (D / G);
+      size_t vm = (av == 0) ? (size_t)i * D + e
+                            : (size_t)(i * G + e / (D / G)) * (D / G) + e % (D / G);
+      get_meta(blk + off[1], e, &kscale[km], &kzero[km]);
+      get_meta(blk + off[3], e, &vscale[vm], &vzero[vm]);
+    }
+  }
+}
+
+/* ---- RoPE (fp64) --------------------------------------------------------- */
+
+/* Rotate-half RoPE at absolute position pos: for i < D/2 the channel pair
+ * (i, i + D/2) turns by the angle pos * base^(-2i/D). */
+void kvo_rope(double* x, int D, long pos, double base) {
+  int h = D / 2;
+  for (int i = 0; i < h; ++i) {
+    double theta = pow(base, -2.0 * (double)i / (double)D);
+    double a = (double)pos * theta;
+    double c = cos(a), s = sin(a);
+    double x0 = x[i], x1 = x[i + h];
+    x[i] = x0 * c - x1 * s;
+    x[i + h] = x1 * c + x0 * s;
+  }
+}
+
+/* ---- attention (fp64) ----------------------------------------------------- */
+
+/* One pair, R query heads.  Keys/values: tokens [0, Tq) from khat/vhat (fp32
+ * [Tq][D]), then tokens [Tq, Tq + Tt) from ktail/vtail (fp16 [Tt][D]).
+ * q: fp16 [R][D].  With rope != 0 key t is rotated at position t.
+ * score_t = scale * sum_d q_d k_{t,d}; p = softmax(score); out = sum p_t v_t.
+ * out: fp64 [R][D].  scores (optional, may be NULL): fp64 [R][Tq + Tt].
+ * An empty sequence gives out = 0. */
+void kvo_attention_pair(int R, int D, int Tq, int Tt, const uint16_t* q,
+                        const float* khat, const float* vhat,
+                        const uint16_t* ktail, const uint16_t* vtail,
+                        double scale, int rope, double base, double* out,
+                        double* scores) {
+  int T = Tq + Tt;
+  double* s = (double*)malloc(sizeof(double) * (size_t)(T > 0 ? T : 1));
+  double* k = (double*)malloc(sizeof(double) * (size_t)D);
+  for (int r = 0; r < R; ++r) {
+    for (int d = 0; d < D; ++d) out[(size_t)r * D + d] = 0.0;
+    if (T == 0) continue;
+    for (int t = 0; t < T; ++t) {
+      for (int d = 0; d < D; ++d)
+        k[d] = (t < Tq) ? (double)khat[(size_t)t * D + d]
+                        : (double)kvo_h2f(ktail[(size_t)(t - Tq) * D + d]);
+      if (rope) kvo_rope(k, D, t, base);
+      double acc = 0.0;
+      for (int d = 0; d < D; ++d)
+        acc += (double)kvo_h2f(q[(size_t)r * D + d]) * k[d];
+      s[t] = scale * acc;
+      if (scores) scores[(size_t)r * T + t] = s[t];
+    }
+    double m = s[0];
+    for (int t = 1; t < T; ++t)
+      if (s[t] > m) m = s[t];
+    double l = 0.0;
+    for (int t = 0; t < T; ++t) {
+      s[t] = exp(s[t] - m);
+      l += s[t];
+    }
+    for (int t = 0; t < T; ++t) {
+      double p = s[t] / l;
+      for (int d = 0; d < D; ++d) {
+        double v = (t < Tq) ? (double)vhat[(size_t)t * D + d]
+                            : (double)kvo_h2f(vtail[(size_t)(t - Tq) * D + d]);
+        out[(size_t)r * D + d] += p * v;
+      }
+    }
+  }
+  free(k);
+  free(s);
+}
