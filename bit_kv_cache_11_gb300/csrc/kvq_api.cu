@@ -1,0 +1,434 @@
+// kvq_api.cu — the C ABI of include/kvq.h: validation, ownership of the
+// device cache, host-side lengths and kernel launches.
+#include <atomic>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "kvq.h"
+#include "kvq_decode.cuh"
+#include "kvq_device.cuh"
+
+namespace kvq {
+size_t quantize_smem_bytes(int D, int G);
+cudaError_t prepare_quantize();
+cudaError_t launch_quantize(const QuantParams& q, cudaStream_t stream);
+cudaError_t launch_dequantize(const DequantParams& q, cudaStream_t stream);
+cudaError_t launch_merge(const MergeParams& mp, int n_pairs, cudaStream_t stream);
+}  // namespace kvq
+
+using namespace kvq;
+
+namespace {
+
+// Most warps a decode launch uses; the partial workspace is sized for it.
+constexpr long long kMaxDecodeWarps = 4096;
+
+std::atomic<uint64_t> g_launches{0};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Derived {
+  int P, R, NB, G, D;
+  size_t block_bytes, off_kc, off_km, off_vc, off_vm;
+  size_t blocks_bytes, tail_bytes, rope_bytes, part_o_bytes, part_ml_bytes;
+};
+
+kvq_status derive(const kvq_config* c, Derived* d) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (c->batch < 1 || c->n_kv_heads < 1 || c->n_q_heads < 1 || c->max_ctx < 1 ||
+      c->head_dim < 1 || c->group < 1)
+    return KVQ_ERR_INVALID_ARG;
+  if (c->n_q_heads % c->n_kv_heads != 0) return KVQ_ERR_INVALID_ARG;
+  auto bits_ok = [](int b) { return b == 2 || b == 4 || b == 8; };
+  if (!bits_ok(c->bits_k) || !bits_ok(c->bits_v)) return KVQ_ERR_INVALID_ARG;
+  if ((c->axis_k != 0 && c->axis_k != 1) || (c->axis_v != 0 && c->axis_v != 1))
+    return KVQ_ERR_INVALID_ARG;
+  if (c->keys_pre_rope != 0 && c->keys_pre_rope != 1) return KVQ_ERR_INVALID_ARG;
+  if (c->keys_pre_rope && !(c->rope_base > 1.0f && std::isfinite(c->rope_base)))
+    return KVQ_ERR_INVALID_ARG;
+  if ((c->axis_k == 1 || c->axis_v == 1) && c->head_dim % c->group != 0)
+    return KVQ_ERR_INVALID_ARG;
+  const int R = c->n_q_heads / c->n_kv_heads;
+  if (R != 1 && R != 2 && R != 4 && R != 8) return KVQ_ERR_UNSUPPORTED;
+  if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
+  if (c->group != 32 && c->group != 64 && c->group != 128) return KVQ_ERR_UNSUPPORTED;
+  const long long P = static_cast<long long>(c->batch) * c->n_kv_heads;
+  if (P > 65535) return KVQ_ERR_UNSUPPORTED;  // grid.y of the quantize launch
+  if (c->max_ctx > (1 << 26)) return KVQ_ERR_UNSUPPORTED;
+  d->P = static_cast<int>(P);
+  d->R = R;
+  d->G = c->group;
+  d->D = c->head_dim;
+  d->NB = c->max_ctx / c->group;
+  const size_t D = c->head_dim, G = c->group;
+  d->off_kc = 0;
+  d->off_km = G * D * c->bits_k / 8;
+  d->off_vc = d->off_km + 4 * D;
+  d->off_vm = d->off_vc + G * D * c->bits_v / 8;
+  d->block_bytes = d->off_vm + 4 * D;
+  d->blocks_bytes = static_cast<size_t>(P) * d->NB * d->block_bytes;
+  d->tail_bytes = static_cast<size_t>(P) * G * D * 2;  // one fp16 [P][G][D] buffer
+  d->rope_bytes = c->keys_pre_rope ? static_cast<size_t>(c->max_ctx) * (D / 2) * sizeof(float2) : 0;
+  const size_t slots = static_cast<size_t>(kMaxDecodeWarps + P);
+  d->part_o_bytes = slots * R * D * sizeof(float);
+  d->part_ml_bytes = slots * R * sizeof(float2);
+  return KVQ_OK;
+}
+
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = true;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) {
+      ok = false;
+      return;
+    }
+    if (prev != dev && cudaSetDevice(dev) != cudaSuccess) ok = false;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+}  // namespace
+
+struct kvq_cache {
+  kvq_config cfg;
+  Derived dv;
+  int device;
+  int sm_count;
+  int decode_ctas_per_sm;
+  DecodeOps ops;
+  uint8_t* blocks;
+  __half* ktail[2];
+  __half* vtail[2];
+  int active;
+  float2* rope;
+  float* part_o;
+  float2* part_ml;
+  int* err;
+  int T_q, T_t;
+};
+
+static CacheGeom geom_of(const kvq_cache* c) {
+  CacheGeom g;
+  g.blocks = c->blocks;
+  g.block_bytes = c->dv.block_bytes;
+  g.NB = c->dv.NB;
+  g.off_km = static_cast<int>(c->dv.off_km);
+  g.off_vc = static_cast<int>(c->dv.off_vc);
+  g.off_vm = static_cast<int>(c->dv.off_vm);
+  g.D = c->dv.D;
+  g.G = c->dv.G;
+  g.bk = c->cfg.bits_k;
+  g.bv = c->cfg.bits_v;
+  g.ak = c->cfg.axis_k;
+  g.av = c->cfg.axis_v;
+  g.P = c->dv.P;
+  return g;
+}
+
+static void free_all(kvq_cache* c) {
+  cudaFree(c->blocks);
+  for (int i = 0; i < 2; ++i) {
+    cudaFree(c->ktail[i]);
+    cudaFree(c->vtail[i]);
+  }
+  cudaFree(c->rope);
+  cudaFree(c->part_o);
+  cudaFree(c->part_ml);
+  cudaFree(c->err);
+}
+
+// Appends n tokens per pair (the whole combined tail + new sequence is
+// walked once; see QuantParams).
+static kvq_status enqueue_append(kvq_cache* c, const void* k, const void* v, int n,
+                                 cudaStream_t stream) {
+  const int G = c->dv.G;
+  const int combined = c->T_t + n;
+  const int nflush = combined / G;
+  QuantParams q;
+  q.g = geom_of(c);
+  q.knew = static_cast<const __half*>(k);
+  q.vnew = static_cast<const __half*>(v);
+  q.n = n;
+  q.kold = c->ktail[c->active];
+  q.vold = c->vtail[c->active];
+  q.T_t = c->T_t;
+  if (nflush == 0) {
+    q.kdst = c->ktail[c->active];
+    q.vdst = c->vtail[c->active];
+    q.dst_row0 = c->T_t;
+    q.rem_begin = c->T_t;
+  } else {  // the flush reads the old tail: the remainder goes to the other buffer
+    q.kdst = c->ktail[c->active ^ 1];
+    q.vdst = c->vtail[c->active ^ 1];
+    q.dst_row0 = 0;
+    q.rem_begin = nflush * G;
+  }
+  q.rem_end = combined;
+  q.first_block = c->T_q / G;
+  q.nflush = nflush;
+  if (launch_quantize(q, stream) != cudaSuccess) return KVQ_ERR_CUDA;
+  g_launches.fetch_add(1);
+  c->T_q += nflush * G;
+  c->T_t = combined - nflush * G;
+  if (nflush > 0) c->active ^= 1;
+  return KVQ_OK;
+}
+
+extern "C" {
+
+kvq_status kvq_config_check(const kvq_config* cfg) {
+  Derived d;
+  return derive(cfg, &d);
+}
+
+kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {
+  if (bytes == nullptr) return KVQ_ERR_INVALID_ARG;
+  Derived d;
+  kvq_status s = derive(cfg, &d);
+  if (s != KVQ_OK) return s;
+  *bytes = d.blocks_bytes + 4 * d.tail_bytes + d.rope_bytes + d.part_o_bytes +
+           d.part_ml_bytes + sizeof(int);
+  return KVQ_OK;
+}
+
+kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
+  if (out == nullptr) return KVQ_ERR_INVALID_ARG;
+  *out = nullptr;
+  Derived d;
+  kvq_status s = derive(cfg, &d);
+  if (s != KVQ_OK) return s;
+  DecodeOps ops = decode_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
+  if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
+
+  kvq_cache* c = new (std::nothrow) kvq_cache();
+  if (c == nullptr) return KVQ_ERR_OOM;
+  c->cfg = *cfg;
+  c->dv = d;
+  c->ops = ops;
+  if (cudaGetDevice(&c->device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) !=
+          cudaSuccess ||
+      ops.prepare(&c->decode_ctas_per_sm) != cudaSuccess || prepare_quantize() != cudaSuccess) {
+    cudaGetLastError();
+    delete c;
+    return KVQ_ERR_CUDA;
+  }
+  if (c->decode_ctas_per_sm < 1) {
+    delete c;
+    return KVQ_ERR_UNSUPPORTED;
+  }
+  bool ok = cudaMalloc(&c->blocks, d.blocks_bytes > 0 ? d.blocks_bytes : 16) == cudaSuccess;
+  for (int i = 0; i < 2 && ok; ++i) {
+    ok = cudaMalloc(&c->ktail[i], d.tail_bytes) == cudaSuccess &&
+         cudaMalloc(&c->vtail[i], d.tail_bytes) == cudaSuccess;
+  }
+  if (ok && d.rope_bytes) ok = cudaMalloc(&c->rope, d.rope_bytes) == cudaSuccess;
+  if (ok) ok = cudaMalloc(&c->part_o, d.part_o_bytes) == cudaSuccess;
+  if (ok) ok = cudaMalloc(&c->part_ml, d.part_ml_bytes) == cudaSuccess;
+  if (ok) ok = cudaMalloc(&c->err, sizeof(int)) == cudaSuccess;
+  if (!ok) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return KVQ_ERR_OOM;
+  }
+  bool init_ok = cudaMemset(c->err, 0, sizeof(int)) == cudaSuccess;
+  for (int i = 0; i < 2 && init_ok; ++i)
+    init_ok = cudaMemset(c->ktail[i], 0, d.tail_bytes) == cudaSuccess &&
+              cudaMemset(c->vtail[i], 0, d.tail_bytes) == cudaSuccess;
+  if (init_ok && d.rope_bytes) {
+    // RoPE cos/sin table: angle pos * base^(-2i/D), evaluated in fp64.
+    const int half = d.D / 2;
+    std::vector<float2> tab(static_cast<size_t>(cfg->max_ctx) * half);
+    for (int i = 0; i < half; ++i) {
+      const double theta = std::pow(static_cast<double>(cfg->rope_base),
+                                    -2.0 * static_cast<double>(i) / static_cast<double>(d.D));
+      for (int pos = 0; pos < cfg->max_ctx; ++pos) {
+        const double a = static_cast<double>(pos) * theta;
+        tab[static_cast<size_t>(pos) * half + i] =
+            make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+      }
+    }
+    init_ok = cudaMemcpy(c->rope, tab.data(), d.rope_bytes, cudaMemcpyHostToDevice) == cudaSuccess;
+  }
+  if (!init_ok) {
+    cudaGetLastError();
+    free_all(c);
+    delete c;
+    return KVQ_ERR_CUDA;
+  }
+  *out = c;
+  return KVQ_OK;
+}
+
+kvq_status kvq_destroy(kvq_cache* c) {
+  if (c == nullptr) return KVQ_OK;
+  DeviceGuard g(c->device);
+  cudaDeviceSynchronize();
+  free_all(c);
+  delete c;
+  return KVQ_OK;
+}
+
+kvq_status kvq_quantize_prefill(kvq_cache* c, const void* k, const void* v, int T,
+                                void* stream) {
+  if (c == nullptr || T < 0) return KVQ_ERR_INVALID_ARG;
+  if (T > 0 && (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)))
+    return KVQ_ERR_INVALID_ARG;
+  if (T > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  const int saved_q = c->T_q, saved_t = c->T_t;
+  c->T_q = 0;
+  c->T_t = 0;
+  if (T == 0) return KVQ_OK;
+  kvq_status s = enqueue_append(c, k, v, T, static_cast<cudaStream_t>(stream));
+  if (s != KVQ_OK) {
+    c->T_q = saved_q;
+    c->T_t = saved_t;
+  }
+  return s;
+}
+
+kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, int n, void* stream) {
+  if (c == nullptr || n < 0) return KVQ_ERR_INVALID_ARG;
+  if (n == 0) return KVQ_OK;
+  if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(c->T_q) + c->T_t + n > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  return enqueue_append(c, k, v, n, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float softmax_scale,
+                                void* stream) {
+  if (c == nullptr || q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out))
+    return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Derived& d = c->dv;
+  const int nsub = c->T_q / 32;
+  const int upp = nsub + (c->T_t > 0 ? 1 : 0);
+  const long long U = static_cast<long long>(d.P) * upp;
+  if (U == 0) {
+    if (cudaMemsetAsync(out, 0, static_cast<size_t>(d.P) * d.R * d.D * sizeof(float), st) !=
+        cudaSuccess)
+      return KVQ_ERR_CUDA;
+    return KVQ_OK;
+  }
+  long long target = static_cast<long long>(c->sm_count) * c->decode_ctas_per_sm * kDecodeWarps;
+  if (target > kMaxDecodeWarps) target = kMaxDecodeWarps;
+  const long long W = U < target ? U : target;
+
+  DecodeParams p;
+  p.g = geom_of(c);
+  p.ktail = c->ktail[c->active];
+  p.vtail = c->vtail[c->active];
+  p.T_q = c->T_q;
+  p.T_t = c->T_t;
+  p.nsub = nsub;
+  p.upp = upp;
+  p.U = U;
+  p.n_warps = static_cast<int>(W);
+  p.rope = c->cfg.keys_pre_rope;
+  p.rope_tab = c->rope;
+  p.q = static_cast<const __half*>(q);
+  p.qscale = softmax_scale * 1.4426950408889634f;
+  p.part_o = c->part_o;
+  p.part_ml = c->part_ml;
+  p.err = c->err;
+  if (c->ops.launch(p, st) != cudaSuccess) return KVQ_ERR_CUDA;
+  MergeParams mp;
+  mp.part_o = c->part_o;
+  mp.part_ml = c->part_ml;
+  mp.out = static_cast<float*>(out);
+  mp.upp = upp;
+  mp.U = U;
+  mp.n_warps = static_cast<int>(W);
+  mp.R = d.R;
+  mp.D = d.D;
+  if (launch_merge(mp, d.P, st) != cudaSuccess) return KVQ_ERR_CUDA;
+  g_launches.fetch_add(2);
+  return KVQ_OK;
+}
+
+kvq_status kvq_dequantize(kvq_cache* c, void* k_out, void* v_out, void* stream) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARG;
+  if (c->T_q == 0) return KVQ_OK;  // nothing to write; the outputs may be empty
+  if (k_out == nullptr || v_out == nullptr || !aligned16(k_out) || !aligned16(v_out))
+    return KVQ_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  DequantParams p;
+  p.g = geom_of(c);
+  p.T_q = c->T_q;
+  p.kout = static_cast<float*>(k_out);
+  p.vout = static_cast<float*>(v_out);
+  if (launch_dequantize(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
+  g_launches.fetch_add(1);
+  return KVQ_OK;
+}
+
+kvq_status kvq_get_state(const kvq_cache* c, int* T_q, int* T_tail) {
+  if (c == nullptr || T_q == nullptr || T_tail == nullptr) return KVQ_ERR_INVALID_ARG;
+  *T_q = c->T_q;
+  *T_tail = c->T_t;
+  return KVQ_OK;
+}
+
+kvq_status kvq_get_buffers(const kvq_cache* c, kvq_buffers* out) {
+  if (c == nullptr || out == nullptr) return KVQ_ERR_INVALID_ARG;
+  out->blocks = c->blocks;
+  out->k_tail = c->ktail[c->active];
+  out->v_tail = c->vtail[c->active];
+  out->block_bytes = c->dv.block_bytes;
+  out->off_kc = c->dv.off_kc;
+  out->off_km = c->dv.off_km;
+  out->off_vc = c->dv.off_vc;
+  out->off_vm = c->dv.off_vm;
+  out->blocks_per_pair = c->dv.NB;
+  out->n_pairs = c->dv.P;
+  out->T_q = c->T_q;
+  out->T_tail = c->T_t;
+  return KVQ_OK;
+}
+
+kvq_status kvq_check_device_error(kvq_cache* c, void* stream) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  int h = 0;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess ||
+      cudaMemcpy(&h, c->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(c->err, 0, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_ERR_CUDA;
+  }
+  return h == 0 ? KVQ_OK : KVQ_ERR_DEVICE_CHECK;
+}
+
+uint64_t kvq_launch_count(void) { return g_launches.load(); }
+
+const char* kvq_status_string(kvq_status s) {
+  switch (s) {
+    case KVQ_OK: return "ok";
+    case KVQ_ERR_INVALID_ARG: return "invalid argument";
+    case KVQ_ERR_UNSUPPORTED: return "unsupported configuration";
+    case KVQ_ERR_CAPACITY: return "capacity exceeded";
+    case KVQ_ERR_OOM: return "device allocation failed";
+    case KVQ_ERR_CUDA: return "CUDA error";
+    case KVQ_ERR_DEVICE_CHECK: return "device check failed (a bounded wait ran out)";
+  }
+  return "unknown status";
+}
+
+}  // extern "C"

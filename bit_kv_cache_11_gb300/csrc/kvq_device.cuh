@@ -1,0 +1,173 @@
+// kvq_device.cuh — device-side helpers and launch parameter blocks of the
+// CUDA library (sm_103a).  Internal to csrc/.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kvq {
+
+// Number of iterations of a bounded mbarrier wait before a kernel gives up,
+// records KVQ_DEVERR_WAIT in the cache's error word and returns.  Each
+// try_wait may suspend the thread for a hardware-chosen interval, so this is
+// far above any legitimate wait (a few microseconds) and well below a hang.
+constexpr uint32_t kWaitLimit = 1u << 22;
+constexpr int kDevErrWait = 1;
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// One-dimensional bulk copy global -> shared (TMA engine), completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on phase `parity` of `bar`.  Returns false when the limit ran
+// out (the caller records the error and stops).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+  }
+  return false;
+}
+
+// ---------------------------------------------------------------- code -> float
+
+// Exact float value of a small unsigned code (< 2^23) without the
+// quarter-rate integer-to-float converter: OR the code into the mantissa of
+// 2^23 and subtract 2^23 (both steps exact).
+__device__ __forceinline__ float code_to_float(uint32_t c) {
+  return __int_as_float(0x4B000000u | c) - 8388608.0f;
+}
+
+// ---------------------------------------------------------------- warp reductions
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// ---------------------------------------------------------------- parameter blocks
+
+// Geometry of the packed cache, shared by all kernels.
+struct CacheGeom {
+  uint8_t* blocks;     // [P][NB][block_bytes]
+  uint64_t block_bytes;
+  int NB;              // blocks per pair
+  int off_km, off_vc, off_vm;
+  int D, G, bk, bv, ak, av;
+  int P;
+};
+
+// Quantize / append / flush launch: grid (nflush + 1, P).
+struct QuantParams {
+  CacheGeom g;
+  const __half* knew;  // [P][n][D]
+  const __half* vnew;
+  int n;
+  const __half* kold;  // active tail [P][G][D] (rows [0, T_t) valid)
+  const __half* vold;
+  int T_t;
+  __half* kdst;        // tail that receives the remainder
+  __half* vdst;
+  int dst_row0;        // first destination row
+  int rem_begin;       // combined-sequence index of the first remainder token
+  int rem_end;         // one past the last (= T_t + n)
+  int first_block;     // block index of the first flushed block (T_q / G)
+  int nflush;          // blocks to quantize
+};
+
+// Dequantize launch: grid (T_q / G, P).
+struct DequantParams {
+  CacheGeom g;
+  int T_q;
+  float* kout;  // [P][T_q][D]
+  float* vout;
+};
+
+// Split-K decode launch.  The work of all pairs is a flat sequence of units:
+// pair p owns units [p*upp, (p+1)*upp); unit j < nsub of a pair is its j-th
+// 32-token quantized sub-block, unit j == nsub (present when T_t > 0) is its
+// fp16 tail.  Warp w of the grid processes units [w*U/W, (w+1)*U/W) and writes
+// one partial (m, l, o) per pair it touches into slot (w + p).
+struct DecodeParams {
+  CacheGeom g;
+  const __half* ktail;  // active tail [P][G][D]
+  const __half* vtail;
+  int T_q, T_t;
+  int nsub;             // T_q / 32
+  int upp;              // units per pair
+  long long U;          // total units
+  int n_warps;          // W
+  int rope;             // rotate keys after dequantization
+  const float2* rope_tab;  // [max_ctx][D/2] {cos, sin}
+  const __half* q;      // [P][R][D]
+  float qscale;         // softmax scale * log2(e)
+  float* part_o;        // [W + P][R][D]
+  float2* part_ml;      // [W + P][R] {m, l} (m in log2 units)
+  int* err;
+};
+
+struct MergeParams {
+  const float* part_o;
+  const float2* part_ml;
+  float* out;  // [P][R][D]
+  int upp;
+  long long U;
+  int n_warps;
+  int R, D;
+};
+
+// Largest warp whose unit range starts at or before unit x (the warp that
+// owns unit x): start(w) = floor(w*U/W) <= x  <=>  w*U < (x+1)*W.
+__host__ __device__ __forceinline__ long long owner_warp(long long x, long long U, long long W) {
+  return ((x + 1) * W - 1) / U;
+}
+
+}  // namespace kvq

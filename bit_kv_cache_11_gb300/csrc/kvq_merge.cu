@@ -1,0 +1,61 @@
+// kvq_merge.cu — combines the split-K partials of every pair, and the
+// dispatch table of decode instantiations.
+//
+// Merging partial softmax states is the identity behind splitting a softmax
+// sum: with m* = max_s m_s and w_s = 2^(m_s - m*) (scores in log2 units),
+//   out = sum_s w_s o_s / sum_s w_s l_s.
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+DecodeOps decode_ops_d64_r1(int, int);
+DecodeOps decode_ops_d64_r2(int, int);
+DecodeOps decode_ops_d64_r4(int, int);
+DecodeOps decode_ops_d64_r8(int, int);
+DecodeOps decode_ops_d128_r1(int, int);
+DecodeOps decode_ops_d128_r2(int, int);
+DecodeOps decode_ops_d128_r4(int, int);
+DecodeOps decode_ops_d128_r8(int, int);
+
+DecodeOps decode_ops(int D, int R, int bk, int bv) {
+  if (D == 64) {
+    if (R == 1) return decode_ops_d64_r1(bk, bv);
+    if (R == 2) return decode_ops_d64_r2(bk, bv);
+    if (R == 4) return decode_ops_d64_r4(bk, bv);
+    if (R == 8) return decode_ops_d64_r8(bk, bv);
+  } else if (D == 128) {
+    if (R == 1) return decode_ops_d128_r1(bk, bv);
+    if (R == 2) return decode_ops_d128_r2(bk, bv);
+    if (R == 4) return decode_ops_d128_r4(bk, bv);
+    if (R == 8) return decode_ops_d128_r8(bk, bv);
+  }
+  return DecodeOps{nullptr, nullptr};
+}
+
+// grid = P pairs, block = D threads (one output channel each).
+__global__ void merge_kernel(const MergeParams mp) {
+  const long long pr = blockIdx.x;
+  const int d = threadIdx.x;
+  const long long x0 = pr * mp.upp;
+  const long long w0 = owner_warp(x0, mp.U, mp.n_warps);
+  const long long w1 = owner_warp(x0 + mp.upp - 1, mp.U, mp.n_warps);
+  for (int r = 0; r < mp.R; ++r) {
+    float ms = -INFINITY;
+    for (long long w = w0; w <= w1; ++w) ms = fmaxf(ms, mp.part_ml[(w + pr) * mp.R + r].x);
+    float L = 0.f, o = 0.f;
+    for (long long w = w0; w <= w1; ++w) {
+      const float2 ml = mp.part_ml[(w + pr) * mp.R + r];
+      const float f = exp2f(ml.x - ms);
+      L = fmaf(f, ml.y, L);
+      o = fmaf(f, mp.part_o[((w + pr) * mp.R + r) * mp.D + d], o);
+    }
+    mp.out[(pr * mp.R + r) * mp.D + d] = o / L;
+  }
+}
+
+cudaError_t launch_merge(const MergeParams& mp, int n_pairs, cudaStream_t stream) {
+  merge_kernel<<<n_pairs, mp.D, 0, stream>>>(mp);
+  return cudaGetLastError();
+}
+
+}  // namespace kvq

@@ -1,0 +1,270 @@
+"""Thin Python binding of the C ABI in ``include/kvq.h`` (argument marshalling
+only: every step of the path runs in the CUDA library ``libkvq.so``).
+
+The functions carry the C names.  Device arguments are torch CUDA tensors (or
+raw device addresses as ints); streams default to torch's current stream.
+Importing this module raises if the library has not been built — there is no
+CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvq.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(
+        f"CUDA library not built: {LIB_PATH} is missing. Build it with "
+        "`python -c \"import __graft_entry__ as g; g.build()\"` or "
+        "`python -m bit_kv_cache_11_gb300.build`.")
+
+_lib = ctypes.CDLL(LIB_PATH)
+
+KVQ_OK = 0
+KVQ_ERR_INVALID_ARG = 1
+KVQ_ERR_UNSUPPORTED = 2
+KVQ_ERR_CAPACITY = 3
+KVQ_ERR_OOM = 4
+KVQ_ERR_CUDA = 5
+KVQ_ERR_DEVICE_CHECK = 6
+KVQ_AXIS_CHANNEL = 0
+KVQ_AXIS_TOKEN = 1
+
+
+class kvq_config(ctypes.Structure):
+    _fields_ = [("batch", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
+                ("head_dim", ctypes.c_int), ("max_ctx", ctypes.c_int), ("bits_k", ctypes.c_int),
+                ("bits_v", ctypes.c_int), ("group", ctypes.c_int), ("axis_k", ctypes.c_int),
+                ("axis_v", ctypes.c_int), ("keys_pre_rope", ctypes.c_int), ("rope_base", ctypes.c_float)]
+
+
+class kvq_buffers(ctypes.Structure):
+    _fields_ = [("blocks", ctypes.c_void_p), ("k_tail", ctypes.c_void_p), ("v_tail", ctypes.c_void_p),
+                ("block_bytes", ctypes.c_size_t), ("off_kc", ctypes.c_size_t),
+                ("off_km", ctypes.c_size_t), ("off_vc", ctypes.c_size_t), ("off_vm", ctypes.c_size_t),
+                ("blocks_per_pair", ctypes.c_int), ("n_pairs", ctypes.c_int), ("T_q", ctypes.c_int),
+                ("T_tail", ctypes.c_int)]
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_S = ctypes.c_int  # kvq_status
+_CFG = ctypes.POINTER(kvq_config)
+
+_sigs = {
+    "kvq_config_check": (_S, [_CFG]),
+    "kvq_cache_bytes": (_S, [_CFG, ctypes.POINTER(ctypes.c_size_t)]),
+    "kvq_create": (_S, [_CFG, ctypes.POINTER(_P)]),
+    "kvq_destroy": (_S, [_P]),
+    "kvq_quantize_prefill": (_S, [_P, _P, _P, _I, _P]),
+    "kvq_append": (_S, [_P, _P, _P, _I, _P]),
+    "kvq_decode_attention": (_S, [_P, _P, _P, ctypes.c_float, _P]),
+    "kvq_dequantize": (_S, [_P, _P, _P, _P]),
+    "kvq_get_state": (_S, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
+    "kvq_get_buffers": (_S, [_P, ctypes.POINTER(kvq_buffers)]),
+    "kvq_check_device_error": (_S, [_P, _P]),
+    "kvq_launch_count": (ctypes.c_uint64, []),
+    "kvq_status_string": (ctypes.c_char_p, [_S]),
+}
+for _name, (_res, _args) in _sigs.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, call: str):
+        self.status = status
+        super().__init__(f"{call}: {kvq_status_string(status)} (status {status})")
+
+
+def _check(status: int, call: str) -> None:
+    if status != KVQ_OK:
+        raise KvqError(status, call)
+
+
+def _ptr(x) -> int | None:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(stream, int):
+        return stream or None
+    return stream.cuda_stream or None
+
+
+def make_config(batch, n_q_heads, n_kv_heads, head_dim, max_ctx, bits_k=2, bits_v=2, group=32,
+                axis_k=KVQ_AXIS_CHANNEL, axis_v=KVQ_AXIS_TOKEN, keys_pre_rope=False,
+                rope_base=10000.0) -> kvq_config:
+    return kvq_config(int(batch), int(n_q_heads), int(n_kv_heads), int(head_dim), int(max_ctx),
+                      int(bits_k), int(bits_v), int(group), int(axis_k), int(axis_v),
+                      1 if keys_pre_rope else 0, float(rope_base))
+
+
+# ---- the C calls, same names ------------------------------------------------
+
+def kvq_status_string(status: int) -> str:
+    return _lib.kvq_status_string(int(status)).decode()
+
+
+def kvq_config_check(cfg: kvq_config) -> int:
+    return _lib.kvq_config_check(ctypes.byref(cfg))
+
+
+def kvq_cache_bytes(cfg: kvq_config) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.kvq_cache_bytes(ctypes.byref(cfg), ctypes.byref(n)), "kvq_cache_bytes")
+    return n.value
+
+
+def kvq_create(cfg: kvq_config) -> int:
+    h = _P()
+    _check(_lib.kvq_create(ctypes.byref(cfg), ctypes.byref(h)), "kvq_create")
+    return h.value
+
+
+def kvq_destroy(handle) -> None:
+    _check(_lib.kvq_destroy(handle), "kvq_destroy")
+
+
+def kvq_quantize_prefill(handle, k, v, T: int | None = None, stream=None) -> None:
+    if T is None:
+        T = k.shape[-2]
+    _check(_lib.kvq_quantize_prefill(handle, _ptr(k), _ptr(v), int(T), _stream(stream)),
+           "kvq_quantize_prefill")
+
+
+def kvq_append(handle, k, v, n: int | None = None, stream=None) -> None:
+    if n is None:
+        n = k.shape[-2]
+    _check(_lib.kvq_append(handle, _ptr(k), _ptr(v), int(n), _stream(stream)), "kvq_append")
+
+
+def kvq_decode_attention(handle, q, out, softmax_scale: float, stream=None) -> None:
+    _check(_lib.kvq_decode_attention(handle, _ptr(q), _ptr(out), float(softmax_scale),
+                                     _stream(stream)), "kvq_decode_attention")
+
+
+def kvq_dequantize(handle, k_out, v_out, stream=None) -> None:
+    _check(_lib.kvq_dequantize(handle, _ptr(k_out), _ptr(v_out), _stream(stream)), "kvq_dequantize")
+
+
+def kvq_get_state(handle) -> tuple[int, int]:
+    tq, tt = _I(0), _I(0)
+    _check(_lib.kvq_get_state(handle, ctypes.byref(tq), ctypes.byref(tt)), "kvq_get_state")
+    return tq.value, tt.value
+
+
+def kvq_get_buffers(handle) -> kvq_buffers:
+    b = kvq_buffers()
+    _check(_lib.kvq_get_buffers(handle, ctypes.byref(b)), "kvq_get_buffers")
+    return b
+
+
+def kvq_check_device_error(handle, stream=None) -> int:
+    return _lib.kvq_check_device_error(handle, _stream(stream))
+
+
+def kvq_launch_count() -> int:
+    return int(_lib.kvq_launch_count())
+
+
+# ---- convenience -------------------------------------------------------------
+
+class _DeviceArray:
+    """Exposes a library-owned device range to torch without copying."""
+
+    def __init__(self, ptr: int, shape, typestr: str):
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr,
+                                         "data": (int(ptr), False), "version": 3, "strides": None}
+
+
+def device_view(ptr: int, shape, typestr: str = "|u1"):
+    import torch
+    return torch.as_tensor(_DeviceArray(ptr, shape, typestr), device="cuda")
+
+
+class KVCache:
+    """One layer's packed KV cache on the current CUDA device."""
+
+    def __init__(self, **cfg_kw):
+        self.cfg = make_config(**cfg_kw)
+        self.handle = kvq_create(self.cfg)
+
+    @property
+    def gqa(self) -> int:
+        return self.cfg.n_q_heads // self.cfg.n_kv_heads
+
+    def close(self) -> None:
+        if self.handle:
+            kvq_destroy(self.handle)
+            self.handle = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def prefill(self, k, v, stream=None):
+        kvq_quantize_prefill(self.handle, k, v, k.shape[-2], stream)
+
+    def append(self, k, v, stream=None):
+        kvq_append(self.handle, k, v, k.shape[-2], stream)
+
+    def decode(self, q, out=None, softmax_scale=None, stream=None):
+        import torch
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if softmax_scale is None:
+            softmax_scale = self.cfg.head_dim ** -0.5
+        kvq_decode_attention(self.handle, q, out, softmax_scale, stream)
+        return out
+
+    def dequantize(self, stream=None):
+        import torch
+        tq, _ = self.state
+        shape = (self.cfg.batch, self.cfg.n_kv_heads, tq, self.cfg.head_dim)
+        k = torch.empty(shape, dtype=torch.float32, device="cuda")
+        v = torch.empty(shape, dtype=torch.float32, device="cuda")
+        kvq_dequantize(self.handle, k, v, stream)
+        return k, v
+
+    @property
+    def state(self) -> tuple[int, int]:
+        return kvq_get_state(self.handle)
+
+    def buffers(self) -> kvq_buffers:
+        return kvq_get_buffers(self.handle)
+
+    def block_bytes_view(self):
+        """uint8 [P][NB][block_bytes] view of the packed blocks (no copy)."""
+        b = self.buffers()
+        return device_view(b.blocks, (b.n_pairs, b.blocks_per_pair, b.block_bytes))
+
+    def tail_views(self):
+        """fp16 [P][G][D] views of the active K and V tails (no copy)."""
+        import torch
+        b = self.buffers()
+        shape = (b.n_pairs, self.cfg.group, self.cfg.head_dim)
+        k = device_view(b.k_tail, shape, "<f2")
+        v = device_view(b.v_tail, shape, "<f2")
+        return k, v
+
+    def check(self, stream=None) -> None:
+        _check(kvq_check_device_error(self.handle, stream), "kvq_check_device_error")

@@ -1,0 +1,67 @@
+"""Runs one workload's prefill and a few decode calls through the C ABI — the
+small, self-contained program that profiler captures wrap.
+
+    python -m bit_kv_cache_11_gb300.profile_case --config 2 --iters 3
+    python -m bit_kv_cache_11_gb300.profile_case --config 4 --what quantize
+
+Prints the CUDA-event time of each call.
+"""
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import kvq, synth
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--bits", type=int, default=None)
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--what", default="decode", choices=["decode", "quantize", "append"])
+    args = ap.parse_args()
+    w = synth.WORKLOADS[args.config]
+    if args.bits:
+        w = w.with_(bits_k=args.bits, bits_v=args.bits)
+    if args.batch:
+        w = w.with_(batch=args.batch)
+    torch.cuda.set_device(0)
+    case = synth.make_case(w)
+    K = torch.from_numpy(case["K"]).cuda()
+    V = torch.from_numpy(case["V"]).cuda()
+    q = torch.from_numpy(case["q"]).cuda()
+    steps = synth.make_decode_steps(w, args.iters, outliers=case["outliers"])
+    with kvq.KVCache(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                     head_dim=w.head_dim, max_ctx=w.T + args.iters + 32, bits_k=w.bits_k,
+                     bits_v=w.bits_v, group=w.group, axis_k=w.axis_k, axis_v=w.axis_v,
+                     keys_pre_rope=w.keys_pre_rope, rope_base=w.rope_base) as cache:
+        out = torch.empty(w.batch, w.n_q_heads, w.head_dim, device="cuda")
+        times = []
+        for i in range(args.iters):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            if args.what == "quantize" or i == 0:
+                a.record()
+                cache.prefill(K, V)
+                b.record()
+            if args.what == "decode":
+                a.record()
+                cache.decode(q, out, w.scale)
+                b.record()
+            elif args.what == "append":
+                s = {k: v.cuda() for k, v in
+                     ((k, torch.from_numpy(v)) for k, v in steps[i].items())}
+                a.record()
+                cache.append(s["k"], s["v"])
+                b.record()
+            torch.cuda.synchronize()
+            times.append(a.elapsed_time(b))
+        cache.check()
+    print(f"{w.name} {args.what}: " + " ".join(f"{t * 1e3:.1f}us" for t in times))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,101 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads
+and exports exactly the calls include/kvq.h declares; config validation and
+size queries run on the host."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def lib_path():
+    from bit_kv_cache_11_gb300 import build
+    return build.build()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"KVQ_API\s+[\w\s\*]*?\b(kvq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls_and_helpers():
+    syms = declared_symbols()
+    for name in ("kvq_create", "kvq_quantize_prefill", "kvq_append", "kvq_decode_attention",
+                 "kvq_dequantize", "kvq_destroy"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    kvq_exported = sorted(s for s in exported if s.startswith("kvq_"))
+    assert kvq_exported == declared_symbols()
+
+
+def _kvq(lib_path):
+    import importlib
+    return importlib.import_module("bit_kv_cache_11_gb300.kvq")
+
+
+def test_config_check_on_host(lib_path):
+    k = _kvq(lib_path)
+    good = k.make_config(8, 32, 32, 128, 8192)
+    assert k.kvq_config_check(good) == k.KVQ_OK
+    cases = [
+        (dict(batch=0), k.KVQ_ERR_INVALID_ARG),
+        (dict(n_q_heads=30), k.KVQ_ERR_INVALID_ARG),      # not a multiple of n_kv_heads... 30 % 32
+        (dict(bits_k=3), k.KVQ_ERR_INVALID_ARG),
+        (dict(bits_v=16), k.KVQ_ERR_INVALID_ARG),
+        (dict(axis_k=2), k.KVQ_ERR_INVALID_ARG),
+        (dict(head_dim=96), k.KVQ_ERR_UNSUPPORTED),
+        (dict(group=16), k.KVQ_ERR_UNSUPPORTED),
+        (dict(n_q_heads=32 * 16), k.KVQ_ERR_UNSUPPORTED),  # GQA ratio 16
+        (dict(keys_pre_rope=True, rope_base=0.5), k.KVQ_ERR_INVALID_ARG),
+        (dict(head_dim=64, group=128, axis_v=1), k.KVQ_ERR_INVALID_ARG),  # D % G != 0
+        (dict(max_ctx=0), k.KVQ_ERR_INVALID_ARG),
+    ]
+    base = dict(batch=8, n_q_heads=32, n_kv_heads=32, head_dim=128, max_ctx=8192)
+    for over, status in cases:
+        kw = dict(base)
+        kw.update(over)
+        assert k.kvq_config_check(k.make_config(**kw)) == status, over
+    # D % G is only required when an axis groups along channels of one token
+    assert k.kvq_config_check(k.make_config(1, 2, 2, 64, 256, group=128, axis_k=0, axis_v=0)) == k.KVQ_OK
+
+
+def test_cache_bytes_on_host(lib_path):
+    k = _kvq(lib_path)
+    cfg = k.make_config(8, 32, 32, 128, 4096 + 32)
+    n = k.kvq_cache_bytes(cfg)
+    P, NB = 8 * 32, (4096 + 32) // 32
+    block = 32 * 128 * 4 // 8 + 8 * 128          # 3072 bytes per 32-token block at 2/2 bits
+    assert block == 3072
+    tails = 4 * P * 32 * 128 * 2
+    assert n >= P * NB * block + tails
+    assert n < P * NB * block + tails + 64 << 20
+
+
+def test_status_strings(lib_path):
+    k = _kvq(lib_path)
+    for s in range(7):
+        assert k.kvq_status_string(s)
+    assert k.kvq_status_string(99) == "unknown status"
+
+
+def test_null_handles_are_rejected_on_host(lib_path):
+    k = _kvq(lib_path)
+    lib = k._lib
+    assert lib.kvq_append(None, None, None, 1, None) == k.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_decode_attention(None, None, None, 1.0, None) == k.KVQ_ERR_INVALID_ARG
+    assert lib.kvq_destroy(None) == k.KVQ_OK
+    T = ctypes.c_int(0)
+    assert lib.kvq_get_state(None, ctypes.byref(T), ctypes.byref(T)) == k.KVQ_ERR_INVALID_ARG
