@@ -9,6 +9,7 @@
 
 #include "kvq.h"
 #include "kvq_decode.cuh"
+#include "kvq_decode_mma.cuh"
 #include "kvq_device.cuh"
 
 namespace kvq {
@@ -204,7 +205,14 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   Derived d;
   kvq_status s = derive(cfg, &d);
   if (s != KVQ_OK) return s;
-  DecodeOps ops = decode_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
+  // Tensor-core kernel for channel-grouped keys, token-grouped values and
+  // post-RoPE keys; the CUDA-core kernel for every other geometry (and for
+  // all of them when KVQ_DECODE_GENERIC is set in the environment).
+  DecodeOps ops{nullptr, nullptr};
+  if (cfg->axis_k == KVQ_AXIS_CHANNEL && cfg->axis_v == KVQ_AXIS_TOKEN && !cfg->keys_pre_rope &&
+      std::getenv("KVQ_DECODE_GENERIC") == nullptr)
+    ops = decode_mma_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
+  if (ops.launch == nullptr) ops = decode_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
   if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
 
   kvq_cache* c = new (std::nothrow) kvq_cache();
@@ -335,6 +343,8 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float so
   p.vtail = c->vtail[c->active];
   p.T_q = c->T_q;
   p.T_t = c->T_t;
+  p.lg_G = d.G == 32 ? 5 : (d.G == 64 ? 6 : 7);
+  p.lg_sub = p.lg_G - 5;
   p.nsub = nsub;
   p.upp = upp;
   p.U = U;

@@ -85,8 +85,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   float* qg = reinterpret_cast<float*>(ws + C::OFF_QG);  // [R][4] per-group query sums
 
   const int G = p.g.G;
-  const int ng = D / G;        // channel groups per token (token axis); 0 if G > D
-  const int sub_per_blk = G / 32;
+  const int lgG = p.lg_G;
+  const int ng = D >> lgG;     // channel groups per token (token axis); 0 if G > D
+  const int sub_mask = (1 << p.lg_sub) - 1;
   const long long ua = gw * p.U / p.n_warps;
   const long long ub = (gw + 1) * p.U / p.n_warps;
 
@@ -96,17 +97,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   }
   __syncwarp();
 
-  auto is_tail = [&](long long u) { return static_cast<int>(u % p.upp) == p.nsub; };
-  auto next_quant = [&](long long u) {
-    while (u < ub && is_tail(u)) ++u;
-    return u;
+  // Load cursor: the next quantized unit to copy (tail units are skipped).
+  UnitCursor lc;
+  lc.init(ua, p.upp);
+  auto skip_tail = [&]() {
+    while (lc.u < ub && lc.j == p.nsub) lc.next(p.upp);
   };
   // Lane 0: copies of quantized unit u into stage s.
-  auto issue = [&](long long u, int s) {
-    const long long pr = u / p.upp;
-    const int j = static_cast<int>(u % p.upp);
-    const int blk = j / sub_per_blk;
-    const int ch = j % sub_per_blk;
+  auto issue = [&](long long pr, int j, int s) {
+    const int blk = j >> p.lg_sub;
+    const int ch = j & sub_mask;
     const uint8_t* base =
         p.g.blocks + (static_cast<size_t>(pr) * p.g.NB + blk) * p.g.block_bytes;
     uint8_t* st = ws + s * C::STAGE;
@@ -121,12 +121,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     bulk_g2s(st + C::KC_S + C::KM_S + C::VC_S, vm_src, vm_bytes, &bars[s]);
   };
 
-  long long lu = next_quant(ua);
+  skip_tail();
   int issued = 0;
-  for (int s = 0; s < NS && lu < ub; ++s) {
-    if (lane == 0) issue(lu, s);
+  for (int s = 0; s < NS && lc.u < ub; ++s) {
+    if (lane == 0) issue(lc.pr, lc.j, s);
     ++issued;
-    lu = next_quant(lu + 1);
+    lc.next(p.upp);
+    skip_tail();
   }
 
   float m[R], l[R], zacc[R];
@@ -215,8 +216,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
       for (int i = 0; i < D / 2; ++i) {
         const int i1 = i + D / 2;
-        const float2 m0 = __half22float2(km[p.g.ak == 0 ? i : lane * ng + i / G]);
-        const float2 m1 = __half22float2(km[p.g.ak == 0 ? i1 : lane * ng + i1 / G]);
+        const float2 m0 = __half22float2(km[p.g.ak == 0 ? i : lane * ng + (i >> lgG)]);
+        const float2 m1 = __half22float2(km[p.g.ak == 0 ? i1 : lane * ng + (i1 >> lgG)]);
         const float k0 = fmaf(kcode(i), m0.x, m0.y);
         const float k1 = fmaf(kcode(i1), m1.x, m1.y);
         const float2 t = cs[i];
@@ -276,8 +277,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
             part[r] = fmaf(w.w, c3, part[r]);
           }
         }
-        if (((k + 1) * 32) % G == 0) {  // a channel group closes
-          const int g = (k * 32) / G;
+        if ((((k + 1) * 32) & (G - 1)) == 0) {  // a channel group closes
+          const int g = (k * 32) >> lgG;
           const float2 sz = __half22float2(km[lane * ng + g]);
 #pragma unroll
           for (int r = 0; r < R; ++r) {
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       }
     }
     if (p.g.av == 1) {
-      const int g = d0 / G;
+      const int g = d0 >> lgG;
 #pragma unroll
       for (int t = 0; t < 32; ++t) {
         const float2 sz = __half22float2(vm[t * ng + g]);
@@ -413,9 +414,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
   };
 
-  for (long long u = ua; u < ub; ++u) {
-    const long long pr = u / p.upp;
-    const int j = static_cast<int>(u % p.upp);
+  UnitCursor uc;
+  uc.init(ua, p.upp);
+  for (; uc.u < ub; uc.next(p.upp)) {
+    const long long pr = uc.pr;
+    const int j = uc.j;
     if (pr != cur) {
       if (cur >= 0) write_partial(cur);
       enter_pair(pr);
@@ -436,10 +439,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
     process_sub(ws + s * C::STAGE, j);
     ++qi;
-    if (lu < ub) {
-      if (lane == 0) issue(lu, s);
+    if (lc.u < ub) {
+      if (lane == 0) issue(lc.pr, lc.j, s);
       ++issued;
-      lu = next_quant(lu + 1);
+      lc.next(p.upp);
+      skip_tail();
     }
   }
   if (cur >= 0) write_partial(cur);

@@ -1,0 +1,627 @@
+// kvq_decode_mma.cuh — tensor-core decode attention for the pages' geometry
+// (keys grouped per channel, values grouped per token, keys stored after
+// RoPE), the configuration "Your KV cache doesn't have a bit problem, it has a
+// geometry problem" recommends ("What to Do with This").
+//
+// Same work decomposition, TMA pipeline, partials and tail handling as
+// decode_split_kernel; the per-sub-block arithmetic runs on mma.sync
+// m16n8k16 (fp16 inputs, fp32 accumulation):
+//
+//   scores  S[token][n] = sum_c A_K[token][c] * B_K[c][n]
+//           A_K = packed key codes turned into exact fp16 values, B_K = the
+//           query folded with the per-channel key scale;
+//   values  O[c][n]     = sum_tok A_V[c][tok] * B_V[tok][n]
+//           A_V = packed value codes (channel-major words), B_V = the softmax
+//           weight folded with the per-token value scale;
+//   columns n = 2*r + h: query head r of the GQA group, h = 0/1 the high/low
+//   fp16 halves of an fp32 operand (hi + lo keeps ~22 bits, so the products
+//   carry fp32-level accuracy into the fp32 accumulators).
+//
+// Code -> fp16 conversion (one funnel shift and one LOP3 per code pair):
+//   2-bit: a rotated code word gives, with two masks, the fp16 values
+//          1 + c/4 (code at mantissa bits 8-9) and 1 + c/16 (bits 6-7);
+//   4-bit: 1 + c/16 (code at mantissa bits 6-9);
+//   8-bit: a byte permute builds 1024 + c, and one half2 subtraction of 1024
+//          leaves the exact code.
+// The constant 1 of the 2/4-bit encodings is removed with exact per-channel
+// (keys) and per-token (values) corrections computed from the same fp16
+// operands.  The code order inside a 16-element mma slice is a fixed
+// permutation (Frag<B>::lane_t/reg/half) applied identically to both
+// operands, so the contraction is unchanged.
+#pragma once
+
+#include "kvq_decode.cuh"
+
+namespace kvq {
+
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// 2^e for e in [-126, 127] (exact).
+__device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
+
+// floor(log2(x)) for a positive normal x; -127 for zero/subnormal.
+__device__ __forceinline__ int ilog2f(float x) { return ((__float_as_int(x) >> 23) & 0xff) - 127; }
+
+// Code -> fp16 operand registers of one 16-element slice.  `w` points at the
+// slice's words (BITS/2 of them).  x0 covers fragment columns (2t, 2t+1), x2
+// covers (2t+8, 2t+9).  Element e of the slice sits in lane t = lane_t(e),
+// register reg(e) (0 = x0/b0, 1 = x2/b1), half half(e); F(e) is the factor
+// the other operand carries, OFF whether the encoding adds a constant 1.
+template <int BITS>
+struct Frag;
+
+template <>
+struct Frag<2> {
+  static constexpr bool OFF = true;
+  __device__ static __forceinline__ void get(const uint32_t* w, int t, uint32_t rot, uint32_t& x0,
+                                             uint32_t& x2) {
+    const uint32_t x = __funnelshift_r(w[0], w[0], rot);
+    x0 = (x & 0x03000300u) | 0x3C003C00u;  // elements 2t+1, 2t+9 as 1 + c/4
+    x2 = (x & 0x00C000C0u) | 0x3C003C00u;  // elements 2t,   2t+8 as 1 + c/16
+  }
+  __device__ static __forceinline__ int lane_t(int e) { return (e & 7) >> 1; }
+  __device__ static __forceinline__ int reg(int e) { return (e & 1) ? 0 : 1; }
+  __device__ static __forceinline__ int half(int e) { return e >= 8 ? 1 : 0; }
+  __device__ static __forceinline__ float F(int e) { return (e & 1) ? 4.0f : 16.0f; }
+};
+
+template <>
+struct Frag<4> {
+  static constexpr bool OFF = true;
+  __device__ static __forceinline__ void get(const uint32_t* w, int t, uint32_t rot, uint32_t& x0,
+                                             uint32_t& x2) {
+    const uint32_t x = __funnelshift_r(w[0], w[0], rot);
+    const uint32_t y = __funnelshift_r(w[1], w[1], rot);
+    x0 = (x & 0x03C003C0u) | 0x3C003C00u;  // elements t, t+4 as 1 + c/16
+    x2 = (y & 0x03C003C0u) | 0x3C003C00u;  // elements 8+t, 12+t
+  }
+  __device__ static __forceinline__ int lane_t(int e) { return e & 3; }
+  __device__ static __forceinline__ int reg(int e) { return e >= 8 ? 1 : 0; }
+  __device__ static __forceinline__ int half(int e) { return (e & 7) >= 4 ? 1 : 0; }
+  __device__ static __forceinline__ float F(int) { return 16.0f; }
+};
+
+template <>
+struct Frag<8> {
+  static constexpr bool OFF = false;
+  __device__ static __forceinline__ void get(const uint32_t* w, int t, uint32_t, uint32_t& x0,
+                                             uint32_t& x2) {
+    const uint32_t v = w[t];
+    const __half2 k1024 = __float2half2_rn(1024.0f);
+    uint32_t p0 = __byte_perm(v, 0x64646464u, 0x4140u);  // 1024 + byte0, 1024 + byte1
+    uint32_t p2 = __byte_perm(v, 0x64646464u, 0x4342u);  // 1024 + byte2, 1024 + byte3
+    __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&p0), k1024);
+    __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&p2), k1024);
+    x0 = *reinterpret_cast<uint32_t*>(&h0);  // elements 4t, 4t+1 (exact codes)
+    x2 = *reinterpret_cast<uint32_t*>(&h2);  // elements 4t+2, 4t+3
+  }
+  __device__ static __forceinline__ int lane_t(int e) { return e >> 2; }
+  __device__ static __forceinline__ int reg(int e) { return (e & 3) >= 2 ? 1 : 0; }
+  __device__ static __forceinline__ int half(int e) { return e & 1; }
+  __device__ static __forceinline__ float F(int) { return 1.0f; }
+};
+
+template <int D, int BK, int BV, int R>
+struct MmaCfg {
+  static constexpr int NT = (2 * R + 7) / 8;  // n-tiles of 8 columns
+  static constexpr int KS = D / 16;           // key slices (k-steps of the score mma)
+  static constexpr int MT = D / 16;           // value m-tiles (16 channels)
+  static constexpr int CPL = D / 32;
+  static constexpr int KW = D * BK / 32;
+  static constexpr int KC_S = 4 * D * BK;
+  static constexpr int KM_S = 4 * D;
+  static constexpr int VC_S = 4 * D * BV;
+  static constexpr int VM_S = 4 * D;
+  static constexpr int STAGE = KC_S + KM_S + VC_S + VM_S;
+  static constexpr int NS = STAGE <= 4096 ? 3 : 2;
+  static constexpr int OFF_BAR = NS * STAGE;
+  static constexpr int OFF_KF = OFF_BAR + 64;                 // [KS][NT][32] uint2
+  static constexpr int OFF_VF = OFF_KF + KS * NT * 32 * 8;    // [4][2][NT][32] uint2
+  static constexpr int OFF_PB = OFF_VF + 4 * 2 * NT * 32 * 8; // [R][32] float
+  static constexpr int OFF_OS = OFF_PB + R * 32 * 4;          // [R][D] float
+  static constexpr int WARP_BYTES = round_up(OFF_OS + R * D * 4, 128);
+  static constexpr int SMEM = kDecodeWarps * WARP_BYTES;
+};
+
+template <int D, int BK, int BV, int R>
+__global__ void __launch_bounds__(kDecodeWarps * 32)
+    decode_mma_kernel(const DecodeParams p) {
+  using C = MmaCfg<D, BK, BV, R>;
+  using FK = Frag<BK>;
+  using FV = Frag<BV>;
+  constexpr int NS = C::NS, NT = C::NT, KS = C::KS, MT = C::MT, CPL = C::CPL;
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const long long gw = static_cast<long long>(blockIdx.x) * kDecodeWarps + warp;
+  if (gw >= p.n_warps) return;
+
+  uint8_t* ws = smem + warp * C::WARP_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ws + C::OFF_BAR);
+  __half* kf = reinterpret_cast<__half*>(ws + C::OFF_KF);
+  __half* vf = reinterpret_cast<__half*>(ws + C::OFF_VF);
+  float* pb = reinterpret_cast<float*>(ws + C::OFF_PB);
+  float* os = reinterpret_cast<float*>(ws + C::OFF_OS);
+
+  const int G = p.g.G;
+  const int lgG = p.lg_G;
+  const int ng = D >> lgG;
+  const int sub_mask = (1 << p.lg_sub) - 1;
+  const long long ua = gw * p.U / p.n_warps;
+  const long long ub = (gw + 1) * p.U / p.n_warps;
+  const uint32_t rot = static_cast<uint32_t>(4 * t - 6) & 31u;
+
+  // Fragment buffers: columns >= 2R are never written and stay zero.
+  {
+    uint32_t* z = reinterpret_cast<uint32_t*>(ws + C::OFF_KF);
+    for (int i = lane; i < (C::OFF_PB - C::OFF_KF) / 4; i += 32) z[i] = 0u;
+  }
+  if (lane == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+
+  // Load cursor: the next quantized unit to copy (tail units are skipped).
+  UnitCursor lc;
+  lc.init(ua, p.upp);
+  auto skip_tail = [&]() {
+    while (lc.u < ub && lc.j == p.nsub) lc.next(p.upp);
+  };
+  auto issue = [&](long long pr, int j, int s) {
+    const int blk = j >> p.lg_sub;
+    const int ch = j & sub_mask;
+    const uint8_t* base =
+        p.g.blocks + (static_cast<size_t>(pr) * p.g.NB + blk) * p.g.block_bytes;
+    uint8_t* st = ws + s * C::STAGE;
+    const uint32_t vm_bytes = 128u * ng;  // 32 tokens x D/G entries
+    mbar_arrive_expect_tx(&bars[s], C::KC_S + C::KM_S + C::VC_S + vm_bytes);
+    bulk_g2s(st, base + ch * C::KC_S, C::KC_S, &bars[s]);
+    bulk_g2s(st + C::KC_S, base + p.g.off_km, C::KM_S, &bars[s]);
+    bulk_g2s(st + C::KC_S + C::KM_S, base + p.g.off_vc + ch * C::VC_S, C::VC_S, &bars[s]);
+    bulk_g2s(st + C::KC_S + C::KM_S + C::VC_S, base + p.g.off_vm + ch * vm_bytes, vm_bytes,
+             &bars[s]);
+  };
+
+  skip_tail();
+  int issued = 0;
+  for (int s = 0; s < NS && lc.u < ub; ++s) {
+    if (lane == 0) issue(lc.pr, lc.j, s);
+    ++issued;
+    lc.next(p.upp);
+    skip_tail();
+  }
+
+  // ---- state of the current pair
+  float qreg[R][CPL];  // q * scale * log2(e), channels lane + 32 j
+  float m[R], l[R];    // online softmax, identical in all lanes
+  float acc[MT][NT][4];
+  float corr[R][4];    // value corrections of this lane's tokens, per (query, group)
+  float acct[R][CPL];  // fp16-tail contributions, channels lane*CPL + c
+  int ev = -126;       // value operand exponent: B_V = p * s * F * 2^-ev
+  long long cur = -1;
+  int qi = 0;
+
+  auto enter_pair = [&](long long pr) {
+    const __half* qp = p.q + static_cast<size_t>(pr) * R * D;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int j = 0; j < CPL; ++j) qreg[r][j] = __half2float(qp[r * D + lane + 32 * j]) * p.qscale;
+      m[r] = -INFINITY;
+      l[r] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) corr[r][k] = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acct[r][c] = 0.f;
+    }
+#pragma unroll
+    for (int a = 0; a < MT; ++a)
+#pragma unroll
+      for (int b = 0; b < NT; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[a][b][k] = 0.f;
+    ev = -126;
+  };
+
+  // value of f for this lane's accumulator columns (query 4*nt + t)
+  auto lane_factor = [&](const float (&f)[R], int nt) -> float {
+    float v = 1.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (r == 4 * nt + t) v = f[r];
+    return v;
+  };
+
+  // Multiplies the mma accumulators and corrections by per-query factors.
+  auto rescale = [&](const float (&f)[R], float fv) {
+    bool any = fv != 1.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) any |= f[r] != 1.f;
+    if (!any) return;  // warp-uniform
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float lf = lane_factor(f, nt) * fv;
+#pragma unroll
+      for (int a = 0; a < MT; ++a)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) acc[a][nt][k] *= lf;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) corr[r][k] *= f[r];
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) acct[r][c] *= f[r];
+    }
+  };
+
+  auto softmax_merge = [&](const float (&mx)[R], float (&alpha)[R], float (&mnew)[R]) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      mnew[r] = fmaxf(m[r], mx[r]);
+      alpha[r] = exp2f(m[r] - mnew[r]);
+      m[r] = mnew[r];
+    }
+  };
+
+  auto process_sub = [&](const uint8_t* st) {
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
+    const __half2* km = reinterpret_cast<const __half2*>(st + C::KC_S);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + C::KC_S + C::KM_S);
+    const __half2* vm = reinterpret_cast<const __half2*>(st + C::KC_S + C::KM_S + C::VC_S);
+
+    // ---- key operand: B_K[c][2r+h] = hi/lo of q_r[c] * s_c * F(c) * 2^-ek
+    float qh[R][CPL];
+    float kz[R];
+    float amax = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) kz[r] = 0.f;
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      const float2 sz = __half22float2(km[c]);
+      const float f = FK::F(c & 15);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        qh[r][j] = qreg[r][j] * sz.x * f;
+        kz[r] = fmaf(qreg[r][j], sz.y, kz[r]);
+        amax = fmaxf(amax, fabsf(qh[r][j]));
+      }
+    }
+    amax = warp_max(amax);
+    const int ek = max(0, ilog2f(amax) - 13);
+    const float sk = pow2i(-ek), ek2 = pow2i(ek);
+#pragma unroll
+    for (int j = 0; j < CPL; ++j) {
+      const int c = lane + 32 * j;
+      const int e = c & 15, kk = c >> 4;
+      const int slot_t = FK::lane_t(e), rg = FK::reg(e), hf = FK::half(e);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float v = qh[r][j] * sk;
+        const __half hi = __float2half_rn(v);
+        const __half lo = __float2half_rn(v - __half2float(hi));
+        if (FK::OFF) kz[r] -= ek2 * (__half2float(hi) + __half2float(lo));
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int n = 2 * r + h;
+          const int L = (n & 7) * 4 + slot_t;
+          kf[(((kk * NT + (n >> 3)) * 32 + L) * 2 + rg) * 2 + hf] = h ? lo : hi;
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) kz[r] = warp_sum(kz[r]);
+    __syncwarp();
+
+    // ---- scores: tokens 16*mt + g (c0,c1) and 16*mt + g + 8 (c2,c3)
+    float sc[2][NT][4];
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < NT; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sc[a][b][k] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) {
+      uint2 bk[NT];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        bk[nt] = reinterpret_cast<const uint2*>(kf)[(kk * NT + nt) * 32 + lane];
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint32_t* r0 = kc + (16 * mt + g) * C::KW + kk * (BK / 2);
+        const uint32_t* r1 = r0 + 8 * C::KW;
+        uint32_t a0, a1, a2, a3;
+        FK::get(r0, t, rot, a0, a2);
+        FK::get(r1, t, rot, a1, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_16816(sc[mt][nt], a0, a1, a2, a3, bk[nt].x, bk[nt].y);
+      }
+    }
+
+    // ---- online softmax (log2 units); lane holds query 4*nt + t
+    float s4[NT][4];
+    float mx[R], mxl[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float z = lane_factor(kz, nt);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        s4[nt][2 * mt] = fmaf(ek2, sc[mt][nt][0] + sc[mt][nt][1], z);
+        s4[nt][2 * mt + 1] = fmaf(ek2, sc[mt][nt][2] + sc[mt][nt][3], z);
+      }
+      float v = fmaxf(fmaxf(s4[nt][0], s4[nt][1]), fmaxf(s4[nt][2], s4[nt][3]));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      mxl[nt] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) mx[r] = __shfl_sync(0xffffffffu, mxl[r >> 2], r & 3);
+    float alpha[R], mnew[R];
+    softmax_merge(mx, alpha, mnew);
+    float ps[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float mm = lane_factor(mnew, nt);
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        s4[nt][k] = exp2f(s4[nt][k] - mm);
+        sum += s4[nt][k];
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      ps[nt] = sum;
+      const int r = 4 * nt + t;
+      if (r < R) {
+        pb[r * 32 + g] = s4[nt][0];
+        pb[r * 32 + g + 8] = s4[nt][1];
+        pb[r * 32 + g + 16] = s4[nt][2];
+        pb[r * 32 + g + 24] = s4[nt][3];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      l[r] = l[r] * alpha[r] + __shfl_sync(0xffffffffu, ps[r >> 2], r & 3);
+
+    // ---- value operand exponent (lane = token): keep B_V below 2^14
+    float smax = 0.f;
+    for (int gp = 0; gp < ng; ++gp) smax = fmaxf(smax, __half2float(vm[lane * ng + gp].x));
+    smax = warp_max(smax * FV::F(lane & 15));
+    const int ev_need = smax > 0.f ? ilog2f(smax) - 13 : -126;
+    float fv = 1.f;
+    if (ev_need > ev) {  // warp-uniform
+      fv = pow2i(max(ev - ev_need, -126));
+      ev = ev_need;
+    }
+    rescale(alpha, fv);
+    __syncwarp();
+
+    // ---- B_V[tok][2r+h] = hi/lo of p_r[tok] * s[tok][grp] * F(tok) * 2^-ev
+    {
+      const int e = lane & 15, ks = lane >> 4;
+      const int slot_t = FV::lane_t(e), rg = FV::reg(e), hf = FV::half(e);
+      const float f = FV::F(e) * pow2i(-ev);
+      const float e2 = pow2i(ev);
+      float pr[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) pr[r] = pb[r * 32 + lane];
+      for (int gp = 0; gp < ng; ++gp) {
+        const float2 sz = __half22float2(vm[lane * ng + gp]);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float v = pr[r] * sz.x * f;
+          const __half hi = __float2half_rn(v);
+          const __half lo = __float2half_rn(v - __half2float(hi));
+          float cz = pr[r] * sz.y;
+          if (FV::OFF) cz -= e2 * (__half2float(hi) + __half2float(lo));
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            if (k == gp) corr[r][k] += cz;
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int n = 2 * r + h;
+            const int L = (n & 7) * 4 + slot_t;
+            vf[((((gp * 2 + ks) * NT + (n >> 3)) * 32 + L) * 2 + rg) * 2 + hf] = h ? lo : hi;
+          }
+        }
+      }
+    }
+    __syncwarp();
+
+    // ---- values: O[c][2r+h] += sum_tok A_V[c][tok] * B_V[tok][2r+h]
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      const int gp = (16 * mt) >> lgG;
+      const uint32_t* c0 = vc + (16 * mt + g) * BV;
+      const uint32_t* c1 = c0 + 8 * BV;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        uint32_t a0, a1, a2, a3;
+        FV::get(c0 + ks * (BV / 2), t, rot, a0, a2);
+        FV::get(c1 + ks * (BV / 2), t, rot, a1, a3);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const uint2 b = reinterpret_cast<const uint2*>(vf)[((gp * 2 + ks) * NT + nt) * 32 + lane];
+          mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+        }
+      }
+    }
+    __syncwarp();
+  };
+
+  auto process_tail = [&](long long pr) {
+    const __half* kt = p.ktail + static_cast<size_t>(pr) * G * D;
+    const __half* vt = p.vtail + static_cast<size_t>(pr) * G * D;
+    const int d0 = lane * CPL;
+    for (int t0 = 0; t0 < p.T_t; t0 += 32) {
+      const int tk = t0 + lane;
+      float sc[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) sc[r] = 0.f;
+      // scores: the query's channels lane + 32 j are spread over lanes, so
+      // every lane forms partial dots for each token and the warp sums them.
+      for (int tt = 0; tt < 32 && t0 + tt < p.T_t; ++tt) {
+        const __half* row = kt + static_cast<size_t>(t0 + tt) * D;
+        float part[R];
+#pragma unroll
+        for (int r = 0; r < R; ++r) part[r] = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPL; ++j) {
+          const float kv = __half2float(row[lane + 32 * j]);
+#pragma unroll
+          for (int r = 0; r < R; ++r) part[r] = fmaf(qreg[r][j], kv, part[r]);
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float s = warp_sum(part[r]);
+          if (lane == tt) sc[r] = s;
+        }
+      }
+      float mx[R], alpha[R], mnew[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        if (tk >= p.T_t) sc[r] = -INFINITY;
+        mx[r] = warp_max(sc[r]);
+      }
+      softmax_merge(mx, alpha, mnew);
+      rescale(alpha, 1.f);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float pj = exp2f(sc[r] - mnew[r]);
+        l[r] = l[r] * alpha[r] + warp_sum(pj);
+        pb[r * 32 + lane] = pj;
+      }
+      __syncwarp();
+      const int nt = min(32, p.T_t - t0);
+      for (int jj = 0; jj < nt; ++jj) {
+        const __half* vr = vt + static_cast<size_t>(t0 + jj) * D + d0;
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float pj = pb[r * 32 + jj];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) acct[r][c] = fmaf(pj, __half2float(vr[c]), acct[r][c]);
+        }
+      }
+      __syncwarp();
+    }
+  };
+
+  auto write_partial = [&](long long pr) {
+    const long long slot = gw + pr;
+    const float e2 = pow2i(ev);
+    float ct[R][4];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ct[r][k] = warp_sum(corr[r][k]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int r = 4 * nt + t;
+      if (r < R) {
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) {
+          os[r * D + 16 * mt + g] = e2 * (acc[mt][nt][0] + acc[mt][nt][1]);
+          os[r * D + 16 * mt + g + 8] = e2 * (acc[mt][nt][2] + acc[mt][nt][3]);
+        }
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (lane == 0) p.part_ml[slot * R + r] = make_float2(m[r], l[r]);
+      float* o = p.part_o + (slot * R + r) * D + lane * CPL;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int ch = lane * CPL + c;
+        float cz = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          if (k == (ch >> lgG)) cz = ct[r][k];
+        o[c] = os[r * D + ch] + cz + acct[r][c];
+      }
+    }
+    __syncwarp();
+  };
+
+  UnitCursor uc;
+  uc.init(ua, p.upp);
+  for (; uc.u < ub; uc.next(p.upp)) {
+    const long long pr = uc.pr;
+    const int j = uc.j;
+    if (pr != cur) {
+      if (cur >= 0) write_partial(cur);
+      enter_pair(pr);
+      cur = pr;
+    }
+    if (j == p.nsub) {
+      process_tail(pr);
+      continue;
+    }
+    const int s = qi % NS;
+    if (!mbar_wait_bounded(&bars[s], static_cast<uint32_t>((qi / NS) & 1))) {
+      // Give up: record the error, wait (bounded) for this warp's copies in
+      // flight so no bulk copy lands after the CTA exits, and return.
+      if (lane == 0) atomicExch(p.err, kDevErrWait);
+      for (int k = qi; k < issued; ++k)
+        mbar_wait_bounded(&bars[k % NS], static_cast<uint32_t>((k / NS) & 1));
+      return;
+    }
+    process_sub(ws + s * C::STAGE);
+    ++qi;
+    if (lc.u < ub) {
+      if (lane == 0) issue(lc.pr, lc.j, s);
+      ++issued;
+      lc.next(p.upp);
+      skip_tail();
+    }
+  }
+  if (cur >= 0) write_partial(cur);
+}
+
+template <int D, int BK, int BV, int R>
+cudaError_t decode_mma_prepare(int* ctas_per_sm) {
+  using C = MmaCfg<D, BK, BV, R>;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BK, BV, R>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      ctas_per_sm, decode_mma_kernel<D, BK, BV, R>, kDecodeWarps * 32, C::SMEM);
+}
+
+template <int D, int BK, int BV, int R>
+cudaError_t decode_mma_launch(const DecodeParams& p, cudaStream_t stream) {
+  using C = MmaCfg<D, BK, BV, R>;
+  const int grid = (p.n_warps + kDecodeWarps - 1) / kDecodeWarps;
+  decode_mma_kernel<D, BK, BV, R><<<grid, kDecodeWarps * 32, C::SMEM, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int D, int R>
+DecodeOps decode_mma_ops_for(int bk, int bv) {
+#define KVQ_CASE(BK_, BV_)                                                    \
+  if (bk == BK_ && bv == BV_)                                                 \
+    return DecodeOps{decode_mma_prepare<D, BK_, BV_, R>, decode_mma_launch<D, BK_, BV_, R>};
+  KVQ_CASE(2, 2) KVQ_CASE(4, 4) KVQ_CASE(8, 8) KVQ_CASE(8, 4)
+#undef KVQ_CASE
+  return DecodeOps{nullptr, nullptr};
+}
+
+// Defined in the per-(D, R) translation units; {nullptr, nullptr} when no
+// tensor-core instantiation exists for (bk, bv).
+DecodeOps decode_mma_ops(int D, int R, int bk, int bv);
+
+}  // namespace kvq

@@ -141,6 +141,8 @@ struct DecodeParams {
   const __half* ktail;  // active tail [P][G][D]
   const __half* vtail;
   int T_q, T_t;
+  int lg_G;             // log2(G)
+  int lg_sub;           // log2(G / 32): 32-token sub-blocks per block
   int nsub;             // T_q / 32
   int upp;              // units per pair
   long long U;          // total units
@@ -162,6 +164,26 @@ struct MergeParams {
   long long U;
   int n_warps;
   int R, D;
+};
+
+// Walks a warp's units in order as (pair, unit-in-pair) without dividing in
+// the loop (64-bit division is a long software sequence on the GPU).
+struct UnitCursor {
+  long long u;
+  long long pr;
+  int j;
+  __device__ __forceinline__ void init(long long u0, int upp) {
+    u = u0;
+    pr = u0 / upp;
+    j = static_cast<int>(u0 - pr * upp);
+  }
+  __device__ __forceinline__ void next(int upp) {
+    ++u;
+    if (++j == upp) {
+      j = 0;
+      ++pr;
+    }
+  }
 };
 
 // Largest warp whose unit range starts at or before unit x (the warp that

@@ -5,6 +5,7 @@
 // sum: with m* = max_s m_s and w_s = 2^(m_s - m*) (scores in log2 units),
 //   out = sum_s w_s o_s / sum_s w_s l_s.
 #include "kvq_decode.cuh"
+#include "kvq_decode_mma.cuh"
 
 namespace kvq {
 
@@ -16,6 +17,30 @@ DecodeOps decode_ops_d128_r1(int, int);
 DecodeOps decode_ops_d128_r2(int, int);
 DecodeOps decode_ops_d128_r4(int, int);
 DecodeOps decode_ops_d128_r8(int, int);
+
+DecodeOps decode_mma_ops_d64_r1(int, int);
+DecodeOps decode_mma_ops_d64_r2(int, int);
+DecodeOps decode_mma_ops_d64_r4(int, int);
+DecodeOps decode_mma_ops_d64_r8(int, int);
+DecodeOps decode_mma_ops_d128_r1(int, int);
+DecodeOps decode_mma_ops_d128_r2(int, int);
+DecodeOps decode_mma_ops_d128_r4(int, int);
+DecodeOps decode_mma_ops_d128_r8(int, int);
+
+DecodeOps decode_mma_ops(int D, int R, int bk, int bv) {
+  if (D == 64) {
+    if (R == 1) return decode_mma_ops_d64_r1(bk, bv);
+    if (R == 2) return decode_mma_ops_d64_r2(bk, bv);
+    if (R == 4) return decode_mma_ops_d64_r4(bk, bv);
+    if (R == 8) return decode_mma_ops_d64_r8(bk, bv);
+  } else if (D == 128) {
+    if (R == 1) return decode_mma_ops_d128_r1(bk, bv);
+    if (R == 2) return decode_mma_ops_d128_r2(bk, bv);
+    if (R == 4) return decode_mma_ops_d128_r4(bk, bv);
+    if (R == 8) return decode_mma_ops_d128_r8(bk, bv);
+  }
+  return DecodeOps{nullptr, nullptr};
+}
 
 DecodeOps decode_ops(int D, int R, int bk, int bv) {
   if (D == 64) {

@@ -1,5 +1,5 @@
-"""Runs one workload's prefill and a few decode calls through the C ABI — the
-small, self-contained program that profiler captures wrap.
+"""Runs one workload's prefill and a few decode (or append) calls through the C
+ABI — the small, self-contained program that profiler captures wrap.
 
     python -m bit_kv_cache_11_gb300.profile_case --config 2 --iters 3
     python -m bit_kv_cache_11_gb300.profile_case --config 4 --what quantize
@@ -33,30 +33,26 @@ def main():
     K = torch.from_numpy(case["K"]).cuda()
     V = torch.from_numpy(case["V"]).cuda()
     q = torch.from_numpy(case["q"]).cuda()
-    steps = synth.make_decode_steps(w, args.iters, outliers=case["outliers"])
+    steps = [{k: torch.from_numpy(v).cuda() for k, v in s.items()}
+             for s in synth.make_decode_steps(w, args.iters, outliers=case["outliers"])]
     with kvq.KVCache(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
                      head_dim=w.head_dim, max_ctx=w.T + args.iters + 32, bits_k=w.bits_k,
                      bits_v=w.bits_v, group=w.group, axis_k=w.axis_k, axis_v=w.axis_v,
                      keys_pre_rope=w.keys_pre_rope, rope_base=w.rope_base) as cache:
         out = torch.empty(w.batch, w.n_q_heads, w.head_dim, device="cuda")
+        cache.prefill(K, V)
         times = []
         for i in range(args.iters):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
-            if args.what == "quantize" or i == 0:
-                a.record()
+            a.record()
+            if args.what == "quantize":
                 cache.prefill(K, V)
-                b.record()
-            if args.what == "decode":
-                a.record()
+            elif args.what == "decode":
                 cache.decode(q, out, w.scale)
-                b.record()
-            elif args.what == "append":
-                s = {k: v.cuda() for k, v in
-                     ((k, torch.from_numpy(v)) for k, v in steps[i].items())}
-                a.record()
-                cache.append(s["k"], s["v"])
-                b.record()
+            else:
+                cache.append(steps[i]["k"], steps[i]["v"])
+            b.record()
             torch.cuda.synchronize()
             times.append(a.elapsed_time(b))
         cache.check()
