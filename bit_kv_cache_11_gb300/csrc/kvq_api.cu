@@ -442,3 +442,8 @@ const char* kvq_status_string(kvq_status s) {
 }
 
 }  // extern "C"
+
+namespace kvq {
+// Lets other translation units of the library count their launches.
+void count_launches(uint64_t n) { g_launches.fetch_add(n); }
+}  // namespace kvq

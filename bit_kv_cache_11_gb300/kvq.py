@@ -62,6 +62,7 @@ _sigs = {
     "kvq_append": (_S, [_P, _P, _P, _I, _P]),
     "kvq_decode_attention": (_S, [_P, _P, _P, ctypes.c_float, _P]),
     "kvq_dequantize": (_S, [_P, _P, _P, _P]),
+    "kvq_decode_attention_noalloc": (_S, [_CFG, _P, _P, _P, _I, _I, _P, _P, ctypes.c_float, _P, _P]),
     "kvq_get_state": (_S, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
     "kvq_get_buffers": (_S, [_P, ctypes.POINTER(kvq_buffers)]),
     "kvq_check_device_error": (_S, [_P, _P]),
@@ -152,6 +153,17 @@ def kvq_append(handle, k, v, n: int | None = None, stream=None) -> None:
 def kvq_decode_attention(handle, q, out, softmax_scale: float, stream=None) -> None:
     _check(_lib.kvq_decode_attention(handle, _ptr(q), _ptr(out), float(softmax_scale),
                                      _stream(stream)), "kvq_decode_attention")
+
+
+def kvq_decode_attention_noalloc(cfg: kvq_config, blocks, k_tail, v_tail, T_q: int, T_tail: int,
+                                 q, out, softmax_scale: float, device_error=None,
+                                 stream=None) -> None:
+    """Decode over a packed cache the caller owns, allocating no device memory
+    (see include/kvq.h for who needs this and for the workspace limit)."""
+    _check(_lib.kvq_decode_attention_noalloc(ctypes.byref(cfg), _ptr(blocks), _ptr(k_tail),
+                                             _ptr(v_tail), int(T_q), int(T_tail), _ptr(q),
+                                             _ptr(out), float(softmax_scale), _ptr(device_error),
+                                             _stream(stream)), "kvq_decode_attention_noalloc")
 
 
 def kvq_dequantize(handle, k_out, v_out, stream=None) -> None:

@@ -185,6 +185,45 @@ KVQ_API kvq_status kvq_decode_attention(kvq_cache* cache, const void* q,
 KVQ_API kvq_status kvq_dequantize(kvq_cache* cache, void* k_out, void* v_out,
                                   void* stream);
 
+/* Size of the static device workspace of kvq_decode_attention_noalloc. */
+#define KVQ_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Decode attention without allocating device memory (the pages have no
+ * counterpart of this call; it exists for callers, not for the method).
+ * Some callers cannot call cudaMalloc when they decode: a serving runtime
+ * that reserved all device memory in its own arena at start-up, a plugin
+ * host that only hands a library the buffers it owns, or a latency-critical
+ * loop where an allocation (which can synchronize the device) is not
+ * acceptable.  If such a caller holds a packed cache in its own memory, in
+ * the layout described at the top of this header, this call decodes it
+ * without a kvq_cache (whose creation allocates) and calls no allocating
+ * routine.
+ *   cfg            the cache's geometry; keys_pre_rope must be 0
+ *                  (KVQ_ERR_UNSUPPORTED otherwise: the RoPE table would need
+ *                  memory).
+ *   blocks         device, [P][max_ctx/G][block_bytes] packed blocks.
+ *   k_tail, v_tail device, fp16 [P][G][D]; rows [0, T_tail) are read.  May be
+ *                  NULL when T_tail = 0.
+ *   T_q, T_tail    quantized tokens (a multiple of G) and tail tokens
+ *                  (< G) per pair; T_q + T_tail <= max_ctx.
+ *   q, out, softmax_scale  as for kvq_decode_attention.
+ *   device_error   optional device int; receives 0, or nonzero when a
+ *                  bounded wait in the kernel ran out.
+ * The split-K partials live in a file-scope device array of
+ * KVQ_NOALLOC_SCRATCH_BYTES that every GPU loading the library holds until
+ * the process exits.  A shape whose partials cannot fit (P * R * (D + 2) * 4
+ * bytes plus one slot per decode warp) returns KVQ_ERR_CAPACITY.  The first
+ * call on a device looks up the array's device address and the kernels'
+ * occupancy, so make that first call before any stream capture.  All calls
+ * share the array: calls that overlap on the GPU (different streams, or
+ * different host threads) race on it and must be serialized by the caller.
+ * Asynchronous on `stream`. */
+KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const void* blocks,
+                                                const void* k_tail, const void* v_tail,
+                                                int T_q, int T_tail, const void* q, void* out,
+                                                float softmax_scale, int* device_error,
+                                                void* stream);
+
 /* Host-side lengths: quantized tokens and tail tokens per pair. */
 KVQ_API kvq_status kvq_get_state(const kvq_cache* cache, int* T_q,
                                  int* T_tail);
