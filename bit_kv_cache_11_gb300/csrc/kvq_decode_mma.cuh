@@ -46,6 +46,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // 2^e for e in [-126, 127] (exact).
 __device__ __forceinline__ float pow2i(int e) { return __int_as_float((127 + e) << 23); }
 
+// 2^x with the SFU (ex2.approx: relative error about 2^-22; 0 for -inf).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // floor(log2(x)) for a positive normal x; -127 for zero/subnormal.
 __device__ __forceinline__ int ilog2f(float x) { return ((__float_as_int(x) >> 23) & 0xff) - 127; }
 
@@ -54,12 +61,16 @@ __device__ __forceinline__ int ilog2f(float x) { return ((__float_as_int(x) >> 2
 // covers (2t+8, 2t+9).  Element e of the slice sits in lane t = lane_t(e),
 // register reg(e) (0 = x0/b0, 1 = x2/b1), half half(e); F(e) is the factor
 // the other operand carries, OFF whether the encoding adds a constant 1.
+// base(i) + {0, PARTNER}, i < 8, are the two elements (half 0 and half 1) of
+// one register, so the other operand is written one 32-bit word at a time.
 template <int BITS>
 struct Frag;
 
 template <>
 struct Frag<2> {
   static constexpr bool OFF = true;
+  static constexpr int PARTNER = 8;  // element sharing lane and register, other half
+  __device__ static __forceinline__ int base(int i) { return i; }
   __device__ static __forceinline__ void get(const uint32_t* w, int t, uint32_t rot, uint32_t& x0,
                                              uint32_t& x2) {
     const uint32_t x = __funnelshift_r(w[0], w[0], rot);
@@ -75,6 +86,8 @@ struct Frag<2> {
 template <>
 struct Frag<4> {
   static constexpr bool OFF = true;
+  static constexpr int PARTNER = 4;
+  __device__ static __forceinline__ int base(int i) { return (i & 3) | ((i & 4) << 1); }
   __device__ static __forceinline__ void get(const uint32_t* w, int t, uint32_t rot, uint32_t& x0,
                                              uint32_t& x2) {
     const uint32_t x = __funnelshift_r(w[0], w[0], rot);
@@ -91,6 +104,8 @@ struct Frag<4> {
 template <>
 struct Frag<8> {
   static constexpr bool OFF = false;
+  static constexpr int PARTNER = 1;
+  __device__ static __forceinline__ int base(int i) { return 2 * i; }
   __device__ static __forceinline__ void get(const uint32_t* w, int t, uint32_t, uint32_t& x0,
                                              uint32_t& x2) {
     const uint32_t v = w[t];
@@ -131,7 +146,7 @@ struct MmaCfg {
 };
 
 template <int D, int BK, int BV, int R>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
+__global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 1))
     decode_mma_kernel(const DecodeParams p) {
   using C = MmaCfg<D, BK, BV, R>;
   using FK = Frag<BK>;
@@ -202,25 +217,38 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   }
 
   // ---- state of the current pair
-  float qreg[R][CPL];  // q * scale * log2(e), channels lane + 32 j
-  float m[R], l[R];    // online softmax, identical in all lanes
+  // Key channels of this lane: KP pairs (c0, c0 + FK::PARTNER) that share one
+  // fragment register, so each hi/lo split is one packed conversion.
+  constexpr int KP = D / 64;
+  // Value-operand jobs of this lane: (token pair, channel group), 16 token
+  // pairs x up to 4 groups spread over 32 lanes.
+  constexpr int VJ = 2;
+  float qreg[R][KP][2];  // q * scale * log2(e)
+  float m[R], l[R];      // online softmax, identical in all lanes
   float acc[MT][NT][4];
-  float corr[R][4];    // value corrections of this lane's tokens, per (query, group)
-  float acct[R][CPL];  // fp16-tail contributions, channels lane*CPL + c
-  int ev = -126;       // value operand exponent: B_V = p * s * F * 2^-ev
+  float corr[R][VJ];     // value corrections of this lane's jobs
+  float acct[R][CPL];    // fp16-tail contributions, channels lane*CPL + c
+  int ev = -126;         // value operand exponent: B_V = p * s * F * 2^-ev
   long long cur = -1;
   int qi = 0;
+
+  auto kchan = [&](int i, int h) {
+    const int P = lane + 32 * i;
+    return 16 * (P >> 3) + FK::base(P & 7) + h * FK::PARTNER;
+  };
 
   auto enter_pair = [&](long long pr) {
     const __half* qp = p.q + static_cast<size_t>(pr) * R * D;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
-      for (int j = 0; j < CPL; ++j) qreg[r][j] = __half2float(qp[r * D + lane + 32 * j]) * p.qscale;
+      for (int i = 0; i < KP; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) qreg[r][i][h] = __half2float(qp[r * D + kchan(i, h)]) * p.qscale;
       m[r] = -INFINITY;
       l[r] = 0.f;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) corr[r][k] = 0.f;
+      for (int k = 0; k < VJ; ++k) corr[r][k] = 0.f;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) acct[r][c] = 0.f;
     }
@@ -259,7 +287,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
 #pragma unroll
-      for (int k = 0; k < 4; ++k) corr[r][k] *= f[r];
+      for (int k = 0; k < VJ; ++k) corr[r][k] *= f[r];
 #pragma unroll
       for (int c = 0; c < CPL; ++c) acct[r][c] *= f[r];
     }
@@ -269,10 +297,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       mnew[r] = fmaxf(m[r], mx[r]);
-      alpha[r] = exp2f(m[r] - mnew[r]);
+      alpha[r] = fast_exp2(m[r] - mnew[r]);
       m[r] = mnew[r];
     }
   };
+
+  uint32_t* kf32 = reinterpret_cast<uint32_t*>(kf);
+  uint32_t* vf32 = reinterpret_cast<uint32_t*>(vf);
 
   auto process_sub = [&](const uint8_t* st) {
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
@@ -281,43 +312,47 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     const __half2* vm = reinterpret_cast<const __half2*>(st + C::KC_S + C::KM_S + C::VC_S);
 
     // ---- key operand: B_K[c][2r+h] = hi/lo of q_r[c] * s_c * F(c) * 2^-ek
-    float qh[R][CPL];
+    float qh[R][KP][2];
     float kz[R];
     float amax = 0.f;
 #pragma unroll
     for (int r = 0; r < R; ++r) kz[r] = 0.f;
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int c = lane + 32 * j;
-      const float2 sz = __half22float2(km[c]);
-      const float f = FK::F(c & 15);
+    for (int i = 0; i < KP; ++i) {
+      const float2 s0 = __half22float2(km[kchan(i, 0)]);
+      const float2 s1 = __half22float2(km[kchan(i, 1)]);
+      const float f = FK::F(FK::base((lane + 32 * i) & 7));
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        qh[r][j] = qreg[r][j] * sz.x * f;
-        kz[r] = fmaf(qreg[r][j], sz.y, kz[r]);
-        amax = fmaxf(amax, fabsf(qh[r][j]));
+        qh[r][i][0] = qreg[r][i][0] * s0.x * f;
+        qh[r][i][1] = qreg[r][i][1] * s1.x * f;
+        kz[r] = fmaf(qreg[r][i][0], s0.y, fmaf(qreg[r][i][1], s1.y, kz[r]));
+        amax = fmaxf(amax, fmaxf(fabsf(qh[r][i][0]), fabsf(qh[r][i][1])));
       }
     }
     amax = warp_max(amax);
     const int ek = max(0, ilog2f(amax) - 13);
     const float sk = pow2i(-ek), ek2 = pow2i(ek);
 #pragma unroll
-    for (int j = 0; j < CPL; ++j) {
-      const int c = lane + 32 * j;
-      const int e = c & 15, kk = c >> 4;
-      const int slot_t = FK::lane_t(e), rg = FK::reg(e), hf = FK::half(e);
+    for (int i = 0; i < KP; ++i) {
+      const int P = lane + 32 * i;
+      const int kk = P >> 3, e0 = FK::base(P & 7);
+      const int slot_t = FK::lane_t(e0), rg = FK::reg(e0);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const float v = qh[r][j] * sk;
-        const __half hi = __float2half_rn(v);
-        const __half lo = __float2half_rn(v - __half2float(hi));
-        if (FK::OFF) kz[r] -= ek2 * (__half2float(hi) + __half2float(lo));
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const int n = 2 * r + h;
-          const int L = (n & 7) * 4 + slot_t;
-          kf[(((kk * NT + (n >> 3)) * 32 + L) * 2 + rg) * 2 + hf] = h ? lo : hi;
+        const float v0 = qh[r][i][0] * sk, v1 = qh[r][i][1] * sk;
+        const __half2 hi = __floats2half2_rn(v0, v1);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+        if (FK::OFF) {
+          const float2 lf = __half22float2(lo);
+          kz[r] -= ek2 * ((hf.x + lf.x) + (hf.y + lf.y));
         }
+        const int n0 = 2 * r, n1 = 2 * r + 1;
+        kf32[((kk * NT + (n0 >> 3)) * 32 + (n0 & 7) * 4 + slot_t) * 2 + rg] =
+            *reinterpret_cast<const uint32_t*>(&hi);
+        kf32[((kk * NT + (n1 >> 3)) * 32 + (n1 & 7) * 4 + slot_t) * 2 + rg] =
+            *reinterpret_cast<const uint32_t*>(&lo);
       }
     }
 #pragma unroll
@@ -325,6 +360,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     __syncwarp();
 
     // ---- scores: tokens 16*mt + g (c0,c1) and 16*mt + g + 8 (c2,c3)
+    uint2 bk[KS][NT];
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk)
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+        bk[kk][nt] = reinterpret_cast<const uint2*>(kf)[(kk * NT + nt) * 32 + lane];
     float sc[2][NT][4];
 #pragma unroll
     for (int a = 0; a < 2; ++a)
@@ -333,20 +374,37 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
         for (int k = 0; k < 4; ++k) sc[a][b][k] = 0.f;
 #pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      uint2 bk[NT];
+    for (int mt = 0; mt < 2; ++mt) {
+      const uint32_t* r0 = kc + (16 * mt + g) * C::KW;
+      const uint32_t* r1 = r0 + 8 * C::KW;
+      if constexpr (BK <= 4) {
+        uint32_t w0[C::KW], w1[C::KW];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-        bk[nt] = reinterpret_cast<const uint2*>(kf)[(kk * NT + nt) * 32 + lane];
+        for (int v = 0; v < C::KW / 4; ++v) {
+          const uint4 x = reinterpret_cast<const uint4*>(r0)[v];
+          const uint4 y = reinterpret_cast<const uint4*>(r1)[v];
+          w0[4 * v] = x.x; w0[4 * v + 1] = x.y; w0[4 * v + 2] = x.z; w0[4 * v + 3] = x.w;
+          w1[4 * v] = y.x; w1[4 * v + 1] = y.y; w1[4 * v + 2] = y.z; w1[4 * v + 3] = y.w;
+        }
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const uint32_t* r0 = kc + (16 * mt + g) * C::KW + kk * (BK / 2);
-        const uint32_t* r1 = r0 + 8 * C::KW;
-        uint32_t a0, a1, a2, a3;
-        FK::get(r0, t, rot, a0, a2);
-        FK::get(r1, t, rot, a1, a3);
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          FK::get(&w0[kk * (BK / 2)], t, rot, a0, a2);
+          FK::get(&w1[kk * (BK / 2)], t, rot, a1, a3);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_16816(sc[mt][nt], a0, a1, a2, a3, bk[nt].x, bk[nt].y);
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816(sc[mt][nt], a0, a1, a2, a3, bk[kk][nt].x, bk[kk][nt].y);
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          FK::get(r0 + kk * (BK / 2), t, rot, a0, a2);
+          FK::get(r1 + kk * (BK / 2), t, rot, a1, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+            mma_16816(sc[mt][nt], a0, a1, a2, a3, bk[kk][nt].x, bk[kk][nt].y);
+        }
       }
     }
 
@@ -378,7 +436,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       float sum = 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        s4[nt][k] = exp2f(s4[nt][k] - mm);
+        s4[nt][k] = fast_exp2(s4[nt][k] - mm);
         sum += s4[nt][k];
       }
       sum += __shfl_xor_sync(0xffffffffu, sum, 4);
@@ -396,46 +454,68 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
     for (int r = 0; r < R; ++r)
       l[r] = l[r] * alpha[r] + __shfl_sync(0xffffffffu, ps[r >> 2], r & 3);
-
-    // ---- value operand exponent (lane = token): keep B_V below 2^14
-    float smax = 0.f;
-    for (int gp = 0; gp < ng; ++gp) smax = fmaxf(smax, __half2float(vm[lane * ng + gp].x));
-    smax = warp_max(smax * FV::F(lane & 15));
-    const int ev_need = smax > 0.f ? ilog2f(smax) - 13 : -126;
-    float fv = 1.f;
-    if (ev_need > ev) {  // warp-uniform
-      fv = pow2i(max(ev - ev_need, -126));
-      ev = ev_need;
-    }
-    rescale(alpha, fv);
     __syncwarp();
 
-    // ---- B_V[tok][2r+h] = hi/lo of p_r[tok] * s[tok][grp] * F(tok) * 2^-ev
+    // ---- value operand: jobs (token pair, group) -> raw p * s * F
+    float raw[R][VJ][2];
+    float zz[R][VJ];
+    float vmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VJ; ++i) {
+      const int J = lane + 32 * i;
+      const int P = J & 15, gp = J >> 4;
+      const int tau0 = 16 * (P >> 3) + FV::base(P & 7), tau1 = tau0 + FV::PARTNER;
+      const float f = FV::F(FV::base(P & 7));
+      const bool valid = gp < ng;
+      const float2 m0 = valid ? __half22float2(vm[tau0 * ng + gp]) : make_float2(0.f, 0.f);
+      const float2 m1 = valid ? __half22float2(vm[tau1 * ng + gp]) : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float p0 = pb[r * 32 + tau0], p1 = pb[r * 32 + tau1];
+        raw[r][i][0] = p0 * m0.x * f;
+        raw[r][i][1] = p1 * m1.x * f;
+        zz[r][i] = fmaf(p0, m0.y, p1 * m1.y);
+        vmax = fmaxf(vmax, fmaxf(raw[r][i][0], raw[r][i][1]));
+      }
+    }
+    // B_V = raw * 2^-ev must stay below 2^14; a trip (the first sub-block of a
+    // pair, or larger weights/scales later) raises ev and rescales exactly.
+    float fv = 1.f;
+    if (__any_sync(0xffffffffu, vmax * pow2i(-ev) >= 16384.f)) {
+      const float va = warp_max(vmax);
+      const int evn = ilog2f(va) - 13;
+      if (evn > ev) {
+        fv = pow2i(max(ev - evn, -126));
+        ev = evn;
+      }
+    }
+    rescale(alpha, fv);
     {
-      const int e = lane & 15, ks = lane >> 4;
-      const int slot_t = FV::lane_t(e), rg = FV::reg(e), hf = FV::half(e);
-      const float f = FV::F(e) * pow2i(-ev);
-      const float e2 = pow2i(ev);
-      float pr[R];
+      const float sv = pow2i(-ev), e2 = pow2i(ev);
 #pragma unroll
-      for (int r = 0; r < R; ++r) pr[r] = pb[r * 32 + lane];
-      for (int gp = 0; gp < ng; ++gp) {
-        const float2 sz = __half22float2(vm[lane * ng + gp]);
+      for (int i = 0; i < VJ; ++i) {
+        const int J = lane + 32 * i;
+        const int P = J & 15, gp = J >> 4;
+        if (gp < ng) {
+          const int ks = P >> 3, e0 = FV::base(P & 7);
+          const int slot_t = FV::lane_t(e0), rg = FV::reg(e0);
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float v = pr[r] * sz.x * f;
-          const __half hi = __float2half_rn(v);
-          const __half lo = __float2half_rn(v - __half2float(hi));
-          float cz = pr[r] * sz.y;
-          if (FV::OFF) cz -= e2 * (__half2float(hi) + __half2float(lo));
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            if (k == gp) corr[r][k] += cz;
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int n = 2 * r + h;
-            const int L = (n & 7) * 4 + slot_t;
-            vf[((((gp * 2 + ks) * NT + (n >> 3)) * 32 + L) * 2 + rg) * 2 + hf] = h ? lo : hi;
+          for (int r = 0; r < R; ++r) {
+            const float v0 = raw[r][i][0] * sv, v1 = raw[r][i][1] * sv;
+            const __half2 hi = __floats2half2_rn(v0, v1);
+            const float2 hf = __half22float2(hi);
+            const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+            float cz = zz[r][i];
+            if (FV::OFF) {
+              const float2 lf = __half22float2(lo);
+              cz -= e2 * ((hf.x + lf.x) + (hf.y + lf.y));
+            }
+            corr[r][i] += cz;
+            const int n0 = 2 * r, n1 = 2 * r + 1;
+            vf32[(((gp * 2 + ks) * NT + (n0 >> 3)) * 32 + (n0 & 7) * 4 + slot_t) * 2 + rg] =
+                *reinterpret_cast<const uint32_t*>(&hi);
+            vf32[(((gp * 2 + ks) * NT + (n1 >> 3)) * 32 + (n1 & 7) * 4 + slot_t) * 2 + rg] =
+                *reinterpret_cast<const uint32_t*>(&lo);
           }
         }
       }
@@ -448,11 +528,27 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       const int gp = (16 * mt) >> lgG;
       const uint32_t* c0 = vc + (16 * mt + g) * BV;
       const uint32_t* c1 = c0 + 8 * BV;
+      uint32_t w0[BV], w1[BV];
+      if constexpr (BV == 2) {
+        const uint2 x = *reinterpret_cast<const uint2*>(c0);
+        const uint2 y = *reinterpret_cast<const uint2*>(c1);
+        w0[0] = x.x; w0[1] = x.y; w1[0] = y.x; w1[1] = y.y;
+      } else if constexpr (BV == 4) {
+        const uint4 x = *reinterpret_cast<const uint4*>(c0);
+        const uint4 y = *reinterpret_cast<const uint4*>(c1);
+        w0[0] = x.x; w0[1] = x.y; w0[2] = x.z; w0[3] = x.w;
+        w1[0] = y.x; w1[1] = y.y; w1[2] = y.z; w1[3] = y.w;
+      }
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {
         uint32_t a0, a1, a2, a3;
-        FV::get(c0 + ks * (BV / 2), t, rot, a0, a2);
-        FV::get(c1 + ks * (BV / 2), t, rot, a1, a3);
+        if constexpr (BV <= 4) {
+          FV::get(&w0[ks * (BV / 2)], t, rot, a0, a2);
+          FV::get(&w1[ks * (BV / 2)], t, rot, a1, a3);
+        } else {
+          FV::get(c0 + ks * (BV / 2), t, rot, a0, a2);
+          FV::get(c1 + ks * (BV / 2), t, rot, a1, a3);
+        }
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
           const uint2 b = reinterpret_cast<const uint2*>(vf)[((gp * 2 + ks) * NT + nt) * 32 + lane];
@@ -463,57 +559,90 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     __syncwarp();
   };
 
+  // fp16 tail unit: lane = token for the scores (each lane issues its whole
+  // key row as 16-byte loads at once), lane = channels for the values (the
+  // value rows of up to 8 tokens are loaded before they are used).  The
+  // query, scaled, sits in `os` (free until the pair's partial is written).
   auto process_tail = [&](long long pr) {
     const __half* kt = p.ktail + static_cast<size_t>(pr) * G * D;
     const __half* vt = p.vtail + static_cast<size_t>(pr) * G * D;
     const int d0 = lane * CPL;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int i = 0; i < KP; ++i)
+#pragma unroll
+        for (int h = 0; h < 2; ++h) os[r * D + kchan(i, h)] = qreg[r][i][h];
+    __syncwarp();
     for (int t0 = 0; t0 < p.T_t; t0 += 32) {
       const int tk = t0 + lane;
       float sc[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) sc[r] = 0.f;
-      // scores: the query's channels lane + 32 j are spread over lanes, so
-      // every lane forms partial dots for each token and the warp sums them.
-      for (int tt = 0; tt < 32 && t0 + tt < p.T_t; ++tt) {
-        const __half* row = kt + static_cast<size_t>(t0 + tt) * D;
-        float part[R];
+      for (int r = 0; r < R; ++r) sc[r] = -INFINITY;
+      if (tk < p.T_t) {
+        const uint4* row = reinterpret_cast<const uint4*>(kt + static_cast<size_t>(tk) * D);
 #pragma unroll
-        for (int r = 0; r < R; ++r) part[r] = 0.f;
+        for (int r = 0; r < R; ++r) sc[r] = 0.f;
 #pragma unroll
-        for (int j = 0; j < CPL; ++j) {
-          const float kv = __half2float(row[lane + 32 * j]);
+        for (int half = 0; half < 2; ++half) {
+          uint4 kr[D / 16];
 #pragma unroll
-          for (int r = 0; r < R; ++r) part[r] = fmaf(qreg[r][j], kv, part[r]);
-        }
+          for (int v = 0; v < D / 16; ++v) kr[v] = row[half * (D / 16) + v];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float s = warp_sum(part[r]);
-          if (lane == tt) sc[r] = s;
+          for (int v = 0; v < D / 16; ++v) {
+            const __half2* h2 = reinterpret_cast<const __half2*>(&kr[v]);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 kk2 = __half22float2(h2[e]);
+              const int d = 8 * (half * (D / 16) + v) + 2 * e;
+#pragma unroll
+              for (int r = 0; r < R; ++r) {
+                const float2 q2 = *reinterpret_cast<const float2*>(os + r * D + d);
+                sc[r] = fmaf(q2.x, kk2.x, fmaf(q2.y, kk2.y, sc[r]));
+              }
+            }
+          }
         }
       }
       float mx[R], alpha[R], mnew[R];
 #pragma unroll
-      for (int r = 0; r < R; ++r) {
-        if (tk >= p.T_t) sc[r] = -INFINITY;
-        mx[r] = warp_max(sc[r]);
-      }
+      for (int r = 0; r < R; ++r) mx[r] = warp_max(sc[r]);
       softmax_merge(mx, alpha, mnew);
       rescale(alpha, 1.f);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const float pj = exp2f(sc[r] - mnew[r]);
+        const float pj = fast_exp2(sc[r] - mnew[r]);
         l[r] = l[r] * alpha[r] + warp_sum(pj);
         pb[r * 32 + lane] = pj;
       }
       __syncwarp();
       const int nt = min(32, p.T_t - t0);
-      for (int jj = 0; jj < nt; ++jj) {
-        const __half* vr = vt + static_cast<size_t>(t0 + jj) * D + d0;
+      for (int j0 = 0; j0 < nt; j0 += 8) {
+        float vv[8][CPL];
 #pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float pj = pb[r * 32 + jj];
+        for (int jj = 0; jj < 8; ++jj) {
+          const int tj = min(j0 + jj, nt - 1);
+          const __half* vr = vt + static_cast<size_t>(t0 + tj) * D + d0;
+          if constexpr (CPL == 4) {
+            const uint2 x = *reinterpret_cast<const uint2*>(vr);
+            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
+            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
+            vv[jj][0] = a.x; vv[jj][1] = a.y; vv[jj][2] = b.x; vv[jj][3] = b.y;
+          } else {
 #pragma unroll
-          for (int c = 0; c < CPL; ++c) acct[r][c] = fmaf(pj, __half2float(vr[c]), acct[r][c]);
+            for (int c = 0; c < CPL; ++c) vv[jj][c] = __half2float(vr[c]);
+          }
+        }
+#pragma unroll
+        for (int jj = 0; jj < 8; ++jj) {
+          if (j0 + jj < nt) {
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+              const float pj = pb[r * 32 + j0 + jj];
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) acct[r][c] = fmaf(pj, vv[jj][c], acct[r][c]);
+            }
+          }
         }
       }
       __syncwarp();
@@ -527,7 +656,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 #pragma unroll
     for (int r = 0; r < R; ++r)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) ct[r][k] = warp_sum(corr[r][k]);
+      for (int k = 0; k < 4; ++k) {
+        float v = 0.f;
+#pragma unroll
+        for (int i = 0; i < VJ; ++i)
+          if (((lane + 32 * i) >> 4) == k) v += corr[r][i];
+        ct[r][k] = warp_sum(v);
+      }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const int r = 4 * nt + t;
