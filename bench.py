@@ -375,7 +375,7 @@ def run_gpu(args, w):
                    "l2": f"inputs larger than L2: {L} layer caches of {decode_bytes(w, 4096, 17) / 1e6:.1f} MB read in turn"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "decode attention call (split kernel + merge kernel)",
+                     "kernel": "decode_mma_kernel (split-K decode with in-place merge, one launch per call)",
                      "peak_source": f"hbm_gbs of {src}",
                      "ms_per_launch": avg_dec, "bytes_per_launch": per_launch},
         "cpu_baseline": cpu,

@@ -112,6 +112,8 @@ struct kvq_cache {
   float* part_o;
   float2* part_ml;
   int* err;
+  int* tickets;  // [P] fused-merge counters, zero between launches
+  bool mma;      // decode runs the tensor-core kernel (which can merge in place)
   int T_q, T_t;
 };
 
@@ -143,6 +145,7 @@ static void free_all(kvq_cache* c) {
   cudaFree(c->part_o);
   cudaFree(c->part_ml);
   cudaFree(c->err);
+  cudaFree(c->tickets);
 }
 
 // Appends n tokens per pair (the whole combined tail + new sequence is
@@ -195,7 +198,7 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {
   kvq_status s = derive(cfg, &d);
   if (s != KVQ_OK) return s;
   *bytes = d.blocks_bytes + 4 * d.tail_bytes + d.rope_bytes + d.part_o_bytes +
-           d.part_ml_bytes + sizeof(int);
+           d.part_ml_bytes + sizeof(int) + sizeof(int) * static_cast<size_t>(d.P);
   return KVQ_OK;
 }
 
@@ -212,6 +215,7 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   if (cfg->axis_k == KVQ_AXIS_CHANNEL && cfg->axis_v == KVQ_AXIS_TOKEN && !cfg->keys_pre_rope &&
       std::getenv("KVQ_DECODE_GENERIC") == nullptr)
     ops = decode_mma_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
+  const bool mma = ops.launch != nullptr;
   if (ops.launch == nullptr) ops = decode_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
   if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
 
@@ -220,6 +224,7 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   c->cfg = *cfg;
   c->dv = d;
   c->ops = ops;
+  c->mma = mma;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) !=
           cudaSuccess ||
@@ -241,13 +246,15 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   if (ok) ok = cudaMalloc(&c->part_o, d.part_o_bytes) == cudaSuccess;
   if (ok) ok = cudaMalloc(&c->part_ml, d.part_ml_bytes) == cudaSuccess;
   if (ok) ok = cudaMalloc(&c->err, sizeof(int)) == cudaSuccess;
+  if (ok) ok = cudaMalloc(&c->tickets, sizeof(int) * d.P) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_all(c);
     delete c;
     return KVQ_ERR_OOM;
   }
-  bool init_ok = cudaMemset(c->err, 0, sizeof(int)) == cudaSuccess;
+  bool init_ok = cudaMemset(c->err, 0, sizeof(int)) == cudaSuccess &&
+                 cudaMemset(c->tickets, 0, sizeof(int) * d.P) == cudaSuccess;
   for (int i = 0; i < 2 && init_ok; ++i)
     init_ok = cudaMemset(c->ktail[i], 0, d.tail_bytes) == cudaSuccess &&
               cudaMemset(c->vtail[i], 0, d.tail_bytes) == cudaSuccess;
@@ -356,7 +363,17 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float so
   p.part_o = c->part_o;
   p.part_ml = c->part_ml;
   p.err = c->err;
+  // Merge in place when every pair has few partials; the separate merge
+  // kernel otherwise (few pairs over many warps, e.g. one long sequence).
+  const long long max_seg = W / d.P + 2;
+  p.fused = (c->mma && max_seg <= 64) ? 1 : 0;
+  p.tickets = c->tickets;
+  p.out = static_cast<float*>(out);
   if (c->ops.launch(p, st) != cudaSuccess) return KVQ_ERR_CUDA;
+  if (p.fused) {
+    g_launches.fetch_add(1);
+    return KVQ_OK;
+  }
   MergeParams mp;
   mp.part_o = c->part_o;
   mp.part_ml = c->part_ml;
@@ -423,7 +440,12 @@ kvq_status kvq_check_device_error(kvq_cache* c, void* stream) {
     cudaGetLastError();
     return KVQ_ERR_CUDA;
   }
-  return h == 0 ? KVQ_OK : KVQ_ERR_DEVICE_CHECK;
+  if (h != 0) {
+    // A warp that gave up left its pair's ticket short: start clean.
+    cudaMemset(c->tickets, 0, sizeof(int) * c->dv.P);
+    return KVQ_ERR_DEVICE_CHECK;
+  }
+  return KVQ_OK;
 }
 
 uint64_t kvq_launch_count(void) { return g_launches.load(); }

@@ -690,6 +690,42 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
       }
     }
     __syncwarp();
+    if (p.fused) {
+      // Publish this partial, take a ticket; the pair's last warp merges
+      // (it never waits for the others: the ticket tells it they are done).
+      __threadfence();
+      __syncwarp();
+      const long long x0 = pr * p.upp;
+      const long long w0 = owner_warp(x0, p.U, p.n_warps);
+      const long long w1 = owner_warp(x0 + p.upp - 1, p.U, p.n_warps);
+      int last = 0;
+      if (lane == 0) last = atomicAdd(&p.tickets[pr], 1) == static_cast<int>(w1 - w0);
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          float ms = -INFINITY;
+          for (long long w = w0; w <= w1; ++w) ms = fmaxf(ms, __ldcg(&p.part_ml[(w + pr) * R + r]).x);
+          float L = 0.f, o[CPL];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+          for (long long w = w0; w <= w1; ++w) {
+            const float2 ml = __ldcg(&p.part_ml[(w + pr) * R + r]);
+            const float f = fast_exp2(ml.x - ms);
+            L = fmaf(f, ml.y, L);
+            const float* src = p.part_o + ((w + pr) * R + r) * D + lane * CPL;
+#pragma unroll
+            for (int c = 0; c < CPL; ++c) o[c] = fmaf(f, __ldcg(src + c), o[c]);
+          }
+          const float inv = 1.f / L;
+          float* dst = p.out + (pr * R + r) * D + lane * CPL;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) dst[c] = o[c] * inv;
+        }
+        if (lane == 0) p.tickets[pr] = 0;
+      }
+    }
   };
 
   UnitCursor uc;

@@ -154,6 +154,11 @@ struct DecodeParams {
   float* part_o;        // [W + P][R][D]
   float2* part_ml;      // [W + P][R] {m, l} (m in log2 units)
   int* err;
+  // Fused merge: the last warp to finish a pair merges its partials into
+  // `out` (ticket counters, one per pair, start and end at zero).
+  int fused;
+  int* tickets;         // [P]
+  float* out;           // [P][R][D]
 };
 
 struct MergeParams {

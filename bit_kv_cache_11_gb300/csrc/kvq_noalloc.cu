@@ -196,6 +196,9 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.part_o = part_o;
     p.part_ml = part_ml;
     p.err = err;
+    p.fused = 0;
+    p.tickets = nullptr;
+    p.out = nullptr;
     if (ops.launch(p, st) != cudaSuccess) return KVQ_ERR_CUDA;
     MergeParams mp;
     mp.part_o = part_o;

@@ -211,7 +211,9 @@ def test_launch_counter_counts_kernels(kvq):
         cache.prefill(dev(c["K"]), dev(c["V"]))
         cache.decode(dev(c["q"]))
         torch.cuda.synchronize()
-        assert kvq.kvq_launch_count() - n0 == 3  # quantize, split, merge
+        # quantize, then one decode kernel: this geometry runs the tensor-core
+        # kernel, which merges the split partials in place
+        assert kvq.kvq_launch_count() - n0 == 2
 
 
 # ---- the full-size workloads, sampled pairs ----------------------------------
