@@ -13,9 +13,12 @@
 // One CTA quantizes one G-token block of one (batch, kv-head) pair:
 //   1. 16-byte loads of the block's G fp16 K rows and V rows into shared
 //      memory (the rows come from the old tail or the new tokens);
-//   2. per group min/max -> fp32 step -> fp16 {scale, zero} metadata;
-//   3. codes packed into uint32 words, one word per thread, written with
-//      coalesced stores in the block layout of include/kvq.h.
+//   2. one thread per quantization group (D key groups and D value groups
+//      per block, whatever the axis): min/max -> fp32 step -> fp16 {scale,
+//      zero} metadata, then the group's codes as bytes in shared memory,
+//      rounded exactly as (x - min) / step with an IEEE divide would round;
+//   3. one thread per output word packs 32/B byte codes and stores the word
+//      (coalesced) in the block layout of include/kvq.h.
 // The extra CTA x == nflush copies the remainder tokens into the tail.
 #include "kvq_device.cuh"
 
@@ -25,36 +28,50 @@ namespace {
 
 constexpr int kQuantThreads = 256;
 
+// Row pitches of the shared tiles (padding keeps 16-byte accesses of
+// neighbouring rows in different banks).
+__host__ __device__ constexpr int xpitch(int D) { return D + 8; }   // halves
+__host__ __device__ constexpr int kpitch(int D) { return D + 16; }  // bytes
+__host__ __device__ constexpr int vpitch(int G) { return G + 16; }  // bytes
+
+// Quantizer statistics of one group, kept in registers by the thread that
+// owns the group: minimum, stored fp16 step (as fp32) and its correctly
+// rounded reciprocal (0 when the step is 0).
 struct Stat {
-  float mn;
-  float s;  // fp32 value of the stored fp16 step
+  float mn, s, rcp;
 };
 
-// Group statistics of n values x[0], x[stride], ...: writes the fp16 metadata
-// and returns the fp32 minimum and stored step used for the codes.
+// min/max over n values p[0], p[stride], ... (fp16 read exactly as fp32).
 __device__ __forceinline__ Stat group_stat(const __half* x, int stride, int n, int bits,
                                            __half2* meta_out) {
   float mn = __half2float(x[0]);
   float mx = mn;
   for (int i = 1; i < n; ++i) {
-    float v = __half2float(x[i * stride]);
+    const float v = __half2float(x[i * stride]);
     mn = fminf(mn, v);
     mx = fmaxf(mx, v);
   }
   // (mx - mn) + 0: a range of -0 (min and max zeros of opposite sign) is +0.
-  float range = __fadd_rn(__fsub_rn(mx, mn), 0.0f);
-  float step = __fdiv_rn(range, static_cast<float>((1 << bits) - 1));
-  __half s_h = __float2half_rn(step);
-  __half z_h = __float2half_rn(__fadd_rn(mn, 0.0f));  // a -0 minimum is stored as +0
+  const float range = __fadd_rn(__fsub_rn(mx, mn), 0.0f);
+  const float step = __fdiv_rn(range, static_cast<float>((1 << bits) - 1));
+  const __half s_h = __float2half_rn(step);
+  const __half z_h = __float2half_rn(__fadd_rn(mn, 0.0f));  // a -0 minimum is stored as +0
   *meta_out = __halves2half2(s_h, z_h);
-  return Stat{mn, __half2float(s_h)};
+  const float s = __half2float(s_h);
+  return Stat{mn, s, s == 0.0f ? 0.0f : __frcp_rn(s)};
 }
 
-__device__ __forceinline__ uint32_t code_of(float x, Stat st, int bits) {
-  if (st.s == 0.0f) return 0u;
-  float r = rintf(__fdiv_rn(__fsub_rn(x, st.mn), st.s));
-  r = fminf(fmaxf(r, 0.0f), static_cast<float>((1 << bits) - 1));
-  return static_cast<uint32_t>(r);
+// code = clamp(rintf((x - mn) / s), 0, 2^bits - 1) with the IEEE quotient,
+// computed as (x - mn) * (1/s): for codes below 2^9 that product is within
+// 2^-13 of the IEEE quotient, so unless it lies within 2^-12 of a rounding
+// tie both round to the same integer; near a tie the IEEE divide decides.
+__device__ __forceinline__ uint32_t code_of(float x, const Stat& st, float top) {
+  const float d = __fsub_rn(x, st.mn);
+  float r = rintf(__fmul_rn(d, st.rcp));
+  const float t = __fsub_rn(__fmul_rn(d, st.rcp), r);
+  if (fabsf(t) > 0.5f - 0.000244140625f) r = rintf(__fdiv_rn(d, st.s));
+  r = fminf(fmaxf(r, 0.0f), top);
+  return __float_as_uint(r + 8388608.0f) & 0xffu;  // exact: r is an integer in [0, 255]
 }
 
 __device__ __forceinline__ const __half* combined_row(const QuantParams& q, int p, int jc) {
@@ -69,8 +86,38 @@ __device__ __forceinline__ const __half* combined_row_v(const QuantParams& q, in
   return q.vnew + (static_cast<size_t>(p) * q.n + (jc - q.T_t)) * D;
 }
 
+// Packs 32/BITS byte codes (LSB-first order) into one word.
+template <int BITS>
+__device__ __forceinline__ uint32_t pack_word(const uint8_t* b);
+
+template <>
+__device__ __forceinline__ uint32_t pack_word<2>(const uint8_t* b) {
+  const uint4 v = *reinterpret_cast<const uint4*>(b);
+  // four 2-bit bytes b0..b3 -> b0 + 4 b1 + 16 b2 + 64 b3 in the top byte of
+  // v * (2^24 + 2^18 + 2^12 + 2^6) (the lower partial products stay below 2^24)
+  const uint32_t M = 0x01041040u;
+  const uint32_t p0 = v.x * M, p1 = v.y * M, p2 = v.z * M, p3 = v.w * M;
+  return __byte_perm(__byte_perm(p0, p1, 0x0073), __byte_perm(p2, p3, 0x0073), 0x5410);
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack_word<4>(const uint8_t* b) {
+  const uint2 v = *reinterpret_cast<const uint2*>(b);
+  uint32_t x = (v.x | (v.x >> 4)) & 0x00ff00ffu;
+  uint32_t y = (v.y | (v.y >> 4)) & 0x00ff00ffu;
+  x = (x | (x >> 8)) & 0xffffu;
+  y = (y | (y >> 8)) & 0xffffu;
+  return x | (y << 16);
+}
+
+template <>
+__device__ __forceinline__ uint32_t pack_word<8>(const uint8_t* b) {
+  return *reinterpret_cast<const uint32_t*>(b);
+}
+
 }  // namespace
 
+template <int BK, int BV>
 __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantParams q) {
   const int x = blockIdx.x;
   const int p = blockIdx.y;
@@ -95,20 +142,21 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
   }
 
   extern __shared__ __align__(16) uint8_t smem[];
+  const int XP = xpitch(D), KP = kpitch(D), VP = vpitch(G);
   __half* xk = reinterpret_cast<__half*>(smem);
-  __half* xv = xk + G * D;
-  Stat* sk = reinterpret_cast<Stat*>(xv + G * D);
-  Stat* sv = sk + D;
+  __half* xv = xk + G * XP;
+  uint8_t* kcode = reinterpret_cast<uint8_t*>(xv + G * XP);  // [G][KP] token-major
+  uint8_t* vcode = kcode + G * KP;                            // [D][VP] channel-major
 
-  // 1. load the block's rows (combined index x*G + j)
+  // 1. the block's rows (combined index x*G + j), 16-byte loads
   const int chunks = G * (D / 8);
   for (int c = tid; c < chunks; c += blockDim.x) {
     const int j = c / (D / 8);
     const int col = (c % (D / 8)) * 8;
     const int jc = x * G + j;
-    *reinterpret_cast<uint4*>(xk + j * D + col) =
+    *reinterpret_cast<uint4*>(xk + j * XP + col) =
         *reinterpret_cast<const uint4*>(combined_row(q, p, jc) + col);
-    *reinterpret_cast<uint4*>(xv + j * D + col) =
+    *reinterpret_cast<uint4*>(xv + j * XP + col) =
         *reinterpret_cast<const uint4*>(combined_row_v(q, p, jc) + col);
   }
   __syncthreads();
@@ -118,61 +166,59 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
   __half2* kmeta = reinterpret_cast<__half2*>(blk + q.g.off_km);
   __half2* vmeta = reinterpret_cast<__half2*>(blk + q.g.off_vm);
 
-  // 2. statistics: D groups for K and D for V in every block, whatever the axis
-  const int ng = D / G;  // channel groups per token (token axis)
+  // 2. one thread per group: statistics, then the group's codes as bytes.
+  //    Every block has D key groups and D value groups whatever the axis.
+  int lgG = 5;
+  while ((1 << lgG) < G) ++lgG;
+  const int ng = D >> lgG;
   for (int e = tid; e < 2 * D; e += blockDim.x) {
     const bool isv = e >= D;
     const int ee = isv ? e - D : e;
     const int axis = isv ? q.g.av : q.g.ak;
-    const int bits = isv ? q.g.bv : q.g.bk;
-    const __half* base = isv ? xv : xk;
-    Stat st;
-    if (axis == 0) {  // channel ee over G tokens
-      st = group_stat(base + ee, D, G, bits, (isv ? vmeta : kmeta) + ee);
-    } else {          // token ee / ng, channels [(ee % ng) * G, +G)
-      st = group_stat(base + (ee / ng) * D + (ee % ng) * G, 1, G, bits,
-                      (isv ? vmeta : kmeta) + ee);
+    const int bits = isv ? BV : BK;
+    const float top = static_cast<float>((1 << bits) - 1);
+    const __half* X = isv ? xv : xk;
+    if (axis == 0) {  // channel ee over the G tokens
+      const Stat st = group_stat(X + ee, XP, G, bits, (isv ? vmeta : kmeta) + ee);
+      for (int j = 0; j < G; ++j) {
+        const uint8_t c = static_cast<uint8_t>(code_of(__half2float(X[j * XP + ee]), st, top));
+        if (isv) vcode[ee * VP + j] = c;
+        else kcode[j * KP + ee] = c;
+      }
+    } else {          // token j, channels [g*G, (g+1)*G); consecutive threads: consecutive j
+      const int j = ee & (G - 1), g = ee >> lgG;
+      const Stat st = group_stat(X + j * XP + (g << lgG), 1, G, bits,
+                                 (isv ? vmeta : kmeta) + j * ng + g);
+      for (int i = 0; i < G; ++i) {
+        const int d = (g << lgG) + i;
+        const uint8_t c = static_cast<uint8_t>(code_of(__half2float(X[j * XP + d]), st, top));
+        if (isv) vcode[d * VP + j] = c;
+        else kcode[j * KP + d] = c;
+      }
     }
-    (isv ? sv : sk)[ee] = st;
   }
   __syncthreads();
 
-  // 3a. K codes: token-major rows of D*bk/32 words
+  // 3. pack and store: K token-major rows; V 32-token chunks, channel-major
   {
-    const int bits = q.g.bk;
-    const int per = 32 / bits;
-    const int kw = D * bits / 32;
+    constexpr int per = 32 / BK;
+    const int kw = D * BK / 32;
     uint32_t* kc = reinterpret_cast<uint32_t*>(blk);
     for (int w = tid; w < G * kw; w += blockDim.x) {
       const int j = w / kw;
-      const int d0 = (w % kw) * per;
-      uint32_t word = 0;
-      for (int e = 0; e < per; ++e) {
-        const int d = d0 + e;
-        const Stat st = sk[q.g.ak == 0 ? d : j * ng + d / G];
-        word |= code_of(__half2float(xk[j * D + d]), st, bits) << (e * bits);
-      }
-      kc[w] = word;
+      kc[w] = pack_word<BK>(kcode + j * KP + (w - j * kw) * per);
     }
   }
-  // 3b. V codes: 32-token chunks, channel-major, bv words per channel
   {
-    const int bits = q.g.bv;
-    const int per = 32 / bits;
+    constexpr int per = 32 / BV;
     uint32_t* vc = reinterpret_cast<uint32_t*>(blk + q.g.off_vc);
-    const int words = (G / 32) * D * bits;
+    const int words = (G / 32) * D * BV;
     for (int w = tid; w < words; w += blockDim.x) {
-      const int c = w / (D * bits);
-      const int rem = w % (D * bits);
-      const int d = rem / bits;
-      const int j0 = c * 32 + (rem % bits) * per;
-      uint32_t word = 0;
-      for (int e = 0; e < per; ++e) {
-        const int j = j0 + e;
-        const Stat st = sv[q.g.av == 0 ? d : j * ng + d / G];
-        word |= code_of(__half2float(xv[j * D + d]), st, bits) << (e * bits);
-      }
-      vc[w] = word;
+      const int c = w / (D * BV);
+      const int rem = w - c * (D * BV);
+      const int d = rem / BV;
+      const int j0 = c * 32 + (rem - d * BV) * per;
+      vc[w] = pack_word<BV>(vcode + d * VP + j0);
     }
   }
 }
@@ -210,20 +256,42 @@ __global__ void __launch_bounds__(kQuantThreads) dequantize_kernel(const Dequant
 }
 
 size_t quantize_smem_bytes(int D, int G) {
-  return static_cast<size_t>(2) * G * D * sizeof(__half) + 2 * D * sizeof(Stat);
+  return static_cast<size_t>(2) * G * xpitch(D) * sizeof(__half) +
+         static_cast<size_t>(G) * kpitch(D) + static_cast<size_t>(D) * vpitch(G);
 }
 
-// Opts the quantize kernel into the shared memory of the largest block
-// (G = D = 128); called once per cache creation, with its device current.
+namespace {
+using QuantFn = void (*)(const QuantParams);
+QuantFn quant_fn(int bk, int bv) {
+#define KVQ_Q(BK_, BV_) \
+  if (bk == BK_ && bv == BV_) return quantize_kernel<BK_, BV_>;
+  KVQ_Q(2, 2) KVQ_Q(2, 4) KVQ_Q(2, 8)
+  KVQ_Q(4, 2) KVQ_Q(4, 4) KVQ_Q(4, 8)
+  KVQ_Q(8, 2) KVQ_Q(8, 4) KVQ_Q(8, 8)
+#undef KVQ_Q
+  return nullptr;
+}
+}  // namespace
+
+// Opts every quantize instantiation into the shared memory of the largest
+// block (G = D = 128); called once per cache creation, with its device current.
 cudaError_t prepare_quantize() {
-  return cudaFuncSetAttribute(quantize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              static_cast<int>(quantize_smem_bytes(128, 128)));
+  const int bits[3] = {2, 4, 8};
+  for (int a : bits)
+    for (int b : bits) {
+      cudaError_t e = cudaFuncSetAttribute(quant_fn(a, b), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(quantize_smem_bytes(128, 128)));
+      if (e != cudaSuccess) return e;
+    }
+  return cudaSuccess;
 }
 
 cudaError_t launch_quantize(const QuantParams& q, cudaStream_t stream) {
   const size_t smem = quantize_smem_bytes(q.g.D, q.g.G);
+  QuantFn fn = quant_fn(q.g.bk, q.g.bv);
+  if (fn == nullptr) return cudaErrorInvalidValue;
   dim3 grid(q.nflush + 1, q.g.P);
-  quantize_kernel<<<grid, kQuantThreads, smem, stream>>>(q);
+  fn<<<grid, kQuantThreads, q.nflush > 0 ? smem : 0, stream>>>(q);
   return cudaGetLastError();
 }
 
