@@ -46,6 +46,30 @@ def quantize_bytes_per_token(w):
     return 2 * Hkv * D * 2 + Hkv * D * (w.bits_k + w.bits_v) // 8 + 2 * Hkv * D // w.group * 4
 
 
+def csrc_hash() -> str:
+    """Hash of the CUDA sources and the C ABI header (identifies the kernels)."""
+    import glob
+    import hashlib
+    h = hashlib.sha256()
+    files = sorted(glob.glob(os.path.join(ROOT, "bit_kv_cache_11_gb300", "csrc", "*.cu*")))
+    for f in files + [os.path.join(ROOT, "include", "kvq.h")]:
+        h.update(os.path.basename(f).encode())
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernels changed since that capture."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        return rec["dram_bytes_per_launch"] if rec["csrc_sha"] == csrc_hash() else None
+    except Exception:
+        return None
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -374,7 +398,8 @@ def run_gpu(args, w):
                    "group": w.group, "step": "per layer: append 1 token + decode attention",
                    "l2": f"inputs larger than L2: {L} layer caches of {decode_bytes(w, 4096, 17) / 1e6:.1f} MB read in turn"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak,
+                     "traffic": load_traffic(f"decode_mma_kernel<{w.head_dim}, {w.bits_k}, {w.bits_v}, {w.gqa}>"),
                      "kernel": "decode_mma_kernel (split-K decode with in-place merge, one launch per call)",
                      "peak_source": f"hbm_gbs of {src}",
                      "ms_per_launch": avg_dec, "bytes_per_launch": per_launch},
