@@ -208,13 +208,14 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   Derived d;
   kvq_status s = derive(cfg, &d);
   if (s != KVQ_OK) return s;
-  // Tensor-core kernel for channel-grouped keys, token-grouped values and
-  // post-RoPE keys; the CUDA-core kernel for every other geometry (and for
-  // all of them when KVQ_DECODE_GENERIC is set in the environment).
+  // Tensor-core kernel for channel-grouped keys and token-grouped values
+  // (with its rotated-key variant for keys stored before RoPE); the CUDA-core
+  // kernel for every other geometry (and for all of them when
+  // KVQ_DECODE_GENERIC is set in the environment).
   DecodeOps ops{nullptr, nullptr};
-  if (cfg->axis_k == KVQ_AXIS_CHANNEL && cfg->axis_v == KVQ_AXIS_TOKEN && !cfg->keys_pre_rope &&
+  if (cfg->axis_k == KVQ_AXIS_CHANNEL && cfg->axis_v == KVQ_AXIS_TOKEN &&
       std::getenv("KVQ_DECODE_GENERIC") == nullptr)
-    ops = decode_mma_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
+    ops = decode_mma_ops(d.D, d.R, cfg->bits_k, cfg->bits_v, cfg->keys_pre_rope != 0);
   const bool mma = ops.launch != nullptr;
   if (ops.launch == nullptr) ops = decode_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
   if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
@@ -358,6 +359,7 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float so
   p.n_warps = static_cast<int>(W);
   p.rope = c->cfg.keys_pre_rope;
   p.rope_tab = c->rope;
+  p.rope_rows = c->cfg.max_ctx;
   p.q = static_cast<const __half*>(q);
   p.qscale = softmax_scale * 1.4426950408889634f;
   p.part_o = c->part_o;

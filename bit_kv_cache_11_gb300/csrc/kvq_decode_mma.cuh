@@ -123,7 +123,7 @@ struct Frag<8> {
   __device__ static __forceinline__ float F(int) { return 1.0f; }
 };
 
-template <int D, int BK, int BV, int R>
+template <int D, int BK, int BV, int R, bool ROPE = false>
 struct MmaCfg {
   static constexpr int NT = (2 * R + 7) / 8;  // n-tiles of 8 columns
   static constexpr int KS = D / 16;           // key slices (k-steps of the score mma)
@@ -135,20 +135,24 @@ struct MmaCfg {
   static constexpr int VC_S = 4 * D * BV;
   static constexpr int VM_S = 4 * D;
   static constexpr int STAGE = KC_S + KM_S + VC_S + VM_S;
-  static constexpr int NS = STAGE <= 4096 ? 3 : 2;
+  static constexpr int NS = ROPE ? 2 : (STAGE <= 4096 ? 3 : 2);
   static constexpr int OFF_BAR = NS * STAGE;
   static constexpr int OFF_KF = OFF_BAR + 64;                 // [KS][NT][32] uint2
   static constexpr int OFF_VF = OFF_KF + KS * NT * 32 * 8;    // [4][2][NT][32] uint2
   static constexpr int OFF_PB = OFF_VF + 4 * 2 * NT * 32 * 8; // [R][32] float
   static constexpr int OFF_OS = OFF_PB + R * 32 * 4;          // [R][D] float
-  static constexpr int WARP_BYTES = round_up(OFF_OS + R * D * 4, 128);
-  static constexpr int SMEM = kDecodeWarps * WARP_BYTES;
+  // RoPE: per-warp key coefficients [R][D/2][8] floats; per-CTA table of
+  // cos/sin(j * theta_i), j < 32, stored [D/2][32] float2.
+  static constexpr int OFF_CF = OFF_OS + R * D * 4;
+  static constexpr int WARP_BYTES = round_up(OFF_CF + (ROPE ? R * (D / 2) * 32 : 0), 128);
+  static constexpr int CS_BYTES = ROPE ? (D / 2) * 32 * 8 : 0;
+  static constexpr int SMEM = kDecodeWarps * WARP_BYTES + CS_BYTES;
 };
 
-template <int D, int BK, int BV, int R>
-__global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 1))
+template <int D, int BK, int BV, int R, bool ROPE>
+__global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (R <= 4 ? 3 : 1))
     decode_mma_kernel(const DecodeParams p) {
-  using C = MmaCfg<D, BK, BV, R>;
+  using C = MmaCfg<D, BK, BV, R, ROPE>;
   using FK = Frag<BK>;
   using FV = Frag<BV>;
   constexpr int NS = C::NS, NT = C::NT, KS = C::KS, MT = C::MT, CPL = C::CPL;
@@ -158,6 +162,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const long long gw = static_cast<long long>(blockIdx.x) * kDecodeWarps + warp;
+  // RoPE: cos/sin(j * theta_i) for the 32 token offsets of a sub-block (table
+  // rows 0..31), transposed so lane j reads its own column conflict-free.
+  // Loaded before any warp of the CTA can leave.
+  float2* cs_tab = reinterpret_cast<float2*>(smem + kDecodeWarps * C::WARP_BYTES);
+  if constexpr (ROPE) {
+    for (int idx = threadIdx.x; idx < (D / 2) * 32; idx += blockDim.x) {
+      const int i = idx >> 5, j = idx & 31;
+      cs_tab[idx] = j < p.rope_rows ? p.rope_tab[static_cast<size_t>(j) * (D / 2) + i]
+                                    : make_float2(1.f, 0.f);
+    }
+    __syncthreads();
+  }
   if (gw >= p.n_warps) return;
 
   uint8_t* ws = smem + warp * C::WARP_BYTES;
@@ -259,6 +275,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
 #pragma unroll
         for (int k = 0; k < 4; ++k) acc[a][b][k] = 0.f;
     ev = -126;
+    if constexpr (ROPE) {
+      // the scaled query, all channels, for the rotated-key path
+      for (int i = lane; i < R * D; i += 32) os[i] = __half2float(qp[i]) * p.qscale;
+      __syncwarp();
+    }
   };
 
   // value of f for this lane's accumulator columns (query 4*nt + t)
@@ -305,12 +326,76 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
   uint32_t* kf32 = reinterpret_cast<uint32_t*>(kf);
   uint32_t* vf32 = reinterpret_cast<uint32_t*>(vf);
 
-  auto process_sub = [&](const uint8_t* st) {
+  auto process_sub = [&](const uint8_t* st, int ju) {
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
     const __half2* km = reinterpret_cast<const __half2*>(st + C::KC_S);
     const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + C::KC_S + C::KM_S);
     const __half2* vm = reinterpret_cast<const __half2*>(st + C::KC_S + C::KM_S + C::VC_S);
 
+    float alpha[R];
+    if constexpr (ROPE) {
+      // ---- rotated keys (CUDA cores).  Sub-block positions p0 + j, p0 = 32*ju:
+      // q . R(p0 + j) k_j = q' . R(j) k_j with q' = R(-p0) q, and with
+      // k = s*c + z per channel, for the pair (i, i+D/2):
+      //   cos(j th_i) (a c_i + b c_i2 + e) + sin(j th_i) (f c_i - g c_i2 + h).
+      constexpr int H = D / 2;
+      float* cf = reinterpret_cast<float*>(ws + C::OFF_CF);
+      const int p0 = ju * 32;
+      for (int i = lane; i < H; i += 32) {
+        const float2 cs = p.rope_tab[static_cast<size_t>(p0) * H + i];
+        const float2 m0 = __half22float2(km[i]), m1 = __half22float2(km[i + H]);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float qi = os[r * D + i], qh = os[r * D + i + H];
+          const float ui = fmaf(qi, cs.x, qh * cs.y);   // q'_i
+          const float uh = fmaf(qh, cs.x, -qi * cs.y);  // q'_{i+H}
+          float* c = cf + (r * H + i) * 8;
+          *reinterpret_cast<float4*>(c) =
+              make_float4(ui * m0.x, uh * m1.x, fmaf(ui, m0.y, uh * m1.y), uh * m0.x);
+          *reinterpret_cast<float2*>(c + 4) = make_float2(ui * m1.x, fmaf(uh, m0.y, -ui * m1.y));
+        }
+      }
+      __syncwarp();
+      uint32_t kr[C::KW];
+      {
+        const uint4* row = reinterpret_cast<const uint4*>(kc + lane * C::KW);
+#pragma unroll
+        for (int v = 0; v < C::KW / 4; ++v) {
+          const uint4 w4 = row[v];
+          kr[4 * v] = w4.x; kr[4 * v + 1] = w4.y; kr[4 * v + 2] = w4.z; kr[4 * v + 3] = w4.w;
+        }
+      }
+      constexpr int KPER = 32 / BK;
+      constexpr uint32_t KMASK = (1u << BK) - 1u;
+      float sc[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) sc[r] = 0.f;
+#pragma unroll
+      for (int i = 0; i < H; ++i) {
+        const float c0 = code_to_float((kr[i / KPER] >> ((i % KPER) * BK)) & KMASK);
+        const float c1 = code_to_float((kr[(i + H) / KPER] >> (((i + H) % KPER) * BK)) & KMASK);
+        const float2 cs = cs_tab[i * 32 + lane];
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+          const float4 ab = *reinterpret_cast<const float4*>(cf + (r * H + i) * 8);
+          const float2 gh = *reinterpret_cast<const float2*>(cf + (r * H + i) * 8 + 4);
+          const float A = fmaf(ab.x, c0, fmaf(ab.y, c1, ab.z));
+          const float B = fmaf(ab.w, c0, fmaf(-gh.x, c1, gh.y));
+          sc[r] = fmaf(cs.x, A, fmaf(cs.y, B, sc[r]));
+        }
+      }
+      float mx[R], mnew[R];
+#pragma unroll
+      for (int r = 0; r < R; ++r) mx[r] = warp_max(sc[r]);
+      softmax_merge(mx, alpha, mnew);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float pj = fast_exp2(sc[r] - mnew[r]);
+        l[r] = l[r] * alpha[r] + warp_sum(pj);
+        pb[r * 32 + lane] = pj;
+      }
+      __syncwarp();
+    } else {
     // ---- key operand: B_K[c][2r+h] = hi/lo of q_r[c] * s_c * F(c) * 2^-ek
     float qh[R][KP][2];
     float kz[R];
@@ -427,7 +512,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) mx[r] = __shfl_sync(0xffffffffu, mxl[r >> 2], r & 3);
-    float alpha[R], mnew[R];
+    float mnew[R];
     softmax_merge(mx, alpha, mnew);
     float ps[NT];
 #pragma unroll
@@ -455,6 +540,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
     for (int r = 0; r < R; ++r)
       l[r] = l[r] * alpha[r] + __shfl_sync(0xffffffffu, ps[r >> 2], r & 3);
     __syncwarp();
+
+    }
 
     // ---- value operand: jobs (token pair, group) -> raw p * s * F
     float raw[R][VJ][2];
@@ -583,6 +670,31 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
         const uint4* row = reinterpret_cast<const uint4*>(kt + static_cast<size_t>(tk) * D);
 #pragma unroll
         for (int r = 0; r < R; ++r) sc[r] = 0.f;
+        if constexpr (ROPE) {
+          // rotate the fp16 key at its absolute position, then dot with q
+          const float2* cs = p.rope_tab + static_cast<size_t>(p.T_q + tk) * (D / 2);
+#pragma unroll 2
+          for (int v = 0; v < D / 16; ++v) {
+            const uint4 a4 = row[v], b4 = row[v + D / 16];
+            const __half2* a2 = reinterpret_cast<const __half2*>(&a4);
+            const __half2* b2 = reinterpret_cast<const __half2*>(&b4);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 ka = __half22float2(a2[e]), kb = __half22float2(b2[e]);
+#pragma unroll
+              for (int u = 0; u < 2; ++u) {
+                const int i = 8 * v + 2 * e + u;
+                const float k0 = u ? ka.y : ka.x, k1 = u ? kb.y : kb.x;
+                const float2 t2 = cs[i];
+                const float r0 = k0 * t2.x - k1 * t2.y;
+                const float r1 = k1 * t2.x + k0 * t2.y;
+#pragma unroll
+                for (int r = 0; r < R; ++r)
+                  sc[r] = fmaf(os[r * D + i], r0, fmaf(os[r * D + i + D / 2], r1, sc[r]));
+              }
+            }
+          }
+        } else {
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
           uint4 kr[D / 16];
@@ -602,6 +714,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
               }
             }
           }
+        }
         }
       }
       float mx[R], alpha[R], mnew[R];
@@ -751,7 +864,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
         mbar_wait_bounded(&bars[k % NS], static_cast<uint32_t>((k / NS) & 1));
       return;
     }
-    process_sub(ws + s * C::STAGE);
+    process_sub(ws + s * C::STAGE, j);
     ++qi;
     if (lc.u < ub) {
       if (lane == 0) issue(lc.pr, lc.j, s);
@@ -763,36 +876,37 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? 4 : (R <= 4 ? 3 : 
   if (cur >= 0) write_partial(cur);
 }
 
-template <int D, int BK, int BV, int R>
+template <int D, int BK, int BV, int R, bool ROPE>
 cudaError_t decode_mma_prepare(int* ctas_per_sm) {
-  using C = MmaCfg<D, BK, BV, R>;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BK, BV, R>,
+  using C = MmaCfg<D, BK, BV, R, ROPE>;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BK, BV, R, ROPE>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, decode_mma_kernel<D, BK, BV, R>, kDecodeWarps * 32, C::SMEM);
+      ctas_per_sm, decode_mma_kernel<D, BK, BV, R, ROPE>, kDecodeWarps * 32, C::SMEM);
 }
 
-template <int D, int BK, int BV, int R>
+template <int D, int BK, int BV, int R, bool ROPE>
 cudaError_t decode_mma_launch(const DecodeParams& p, cudaStream_t stream) {
-  using C = MmaCfg<D, BK, BV, R>;
+  using C = MmaCfg<D, BK, BV, R, ROPE>;
   const int grid = (p.n_warps + kDecodeWarps - 1) / kDecodeWarps;
-  decode_mma_kernel<D, BK, BV, R><<<grid, kDecodeWarps * 32, C::SMEM, stream>>>(p);
+  decode_mma_kernel<D, BK, BV, R, ROPE><<<grid, kDecodeWarps * 32, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
-template <int D, int R>
+template <int D, int R, bool ROPE>
 DecodeOps decode_mma_ops_for(int bk, int bv) {
-#define KVQ_CASE(BK_, BV_)                                                    \
-  if (bk == BK_ && bv == BV_)                                                 \
-    return DecodeOps{decode_mma_prepare<D, BK_, BV_, R>, decode_mma_launch<D, BK_, BV_, R>};
+#define KVQ_CASE(BK_, BV_)                                                              \
+  if (bk == BK_ && bv == BV_)                                                           \
+    return DecodeOps{decode_mma_prepare<D, BK_, BV_, R, ROPE>,                          \
+                     decode_mma_launch<D, BK_, BV_, R, ROPE>};
   KVQ_CASE(2, 2) KVQ_CASE(4, 4) KVQ_CASE(8, 8) KVQ_CASE(8, 4)
 #undef KVQ_CASE
   return DecodeOps{nullptr, nullptr};
 }
 
 // Defined in the per-(D, R) translation units; {nullptr, nullptr} when no
-// tensor-core instantiation exists for (bk, bv).
-DecodeOps decode_mma_ops(int D, int R, int bk, int bv);
+// tensor-core instantiation exists for (bk, bv, rope).
+DecodeOps decode_mma_ops(int D, int R, int bk, int bv, bool rope);
 
 }  // namespace kvq

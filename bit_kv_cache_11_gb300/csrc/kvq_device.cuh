@@ -149,6 +149,7 @@ struct DecodeParams {
   int n_warps;          // W
   int rope;             // rotate keys after dequantization
   const float2* rope_tab;  // [max_ctx][D/2] {cos, sin}
+  int rope_rows;        // rows of rope_tab (max_ctx)
   const __half* q;      // [P][R][D]
   float qscale;         // softmax scale * log2(e)
   float* part_o;        // [W + P][R][D]

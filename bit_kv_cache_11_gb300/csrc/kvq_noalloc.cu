@@ -131,7 +131,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
 
   DecodeOps ops{nullptr, nullptr};
   if (cfg->axis_k == KVQ_AXIS_CHANNEL && cfg->axis_v == KVQ_AXIS_TOKEN)
-    ops = decode_mma_ops(D, R, cfg->bits_k, cfg->bits_v);
+    ops = decode_mma_ops(D, R, cfg->bits_k, cfg->bits_v, false);
   if (ops.launch == nullptr) ops = decode_ops(D, R, cfg->bits_k, cfg->bits_v);
   if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
 
@@ -191,6 +191,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.n_warps = static_cast<int>(W);
     p.rope = 0;
     p.rope_tab = nullptr;
+    p.rope_rows = 0;
     p.q = static_cast<const __half*>(q);
     p.qscale = softmax_scale * 1.4426950408889634f;
     p.part_o = part_o;
