@@ -18,6 +18,7 @@ cudaError_t prepare_quantize();
 cudaError_t launch_quantize(const QuantParams& q, cudaStream_t stream);
 cudaError_t launch_dequantize(const DequantParams& q, cudaStream_t stream);
 cudaError_t launch_merge(const MergeParams& mp, int n_pairs, cudaStream_t stream);
+cudaError_t launch_merge2(const Merge2Params& mp, int n_pairs, cudaStream_t stream);
 }  // namespace kvq
 
 using namespace kvq;
@@ -33,8 +34,10 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Derived {
   int P, R, NB, G, D;
+  int C2max;  // level-1 chunks per (pair, query) of the two-level merge
   size_t block_bytes, off_kc, off_km, off_vc, off_vm;
   size_t blocks_bytes, tail_bytes, rope_bytes, part_o_bytes, part_ml_bytes;
+  size_t lvl_o_bytes, lvl_ml_bytes;
 };
 
 kvq_status derive(const kvq_config* c, Derived* d) {
@@ -76,6 +79,10 @@ kvq_status derive(const kvq_config* c, Derived* d) {
   const size_t slots = static_cast<size_t>(kMaxDecodeWarps + P);
   d->part_o_bytes = slots * R * D * sizeof(float);
   d->part_ml_bytes = slots * R * sizeof(float2);
+  d->C2max = static_cast<int>((kMaxDecodeWarps / P + 2 + 15) / 16);
+  const size_t lvl = static_cast<size_t>(P) * R * d->C2max;
+  d->lvl_o_bytes = lvl * D * sizeof(float);
+  d->lvl_ml_bytes = lvl * sizeof(float2);
   return KVQ_OK;
 }
 
@@ -113,6 +120,9 @@ struct kvq_cache {
   float2* part_ml;
   int* err;
   int* tickets;  // [P] fused-merge counters, zero between launches
+  float* lvl_o;  // two-level merge: level-2 partials
+  float2* lvl_ml;
+  int* tickets2; // [P*R] two-level merge counters, zero between launches
   bool mma;      // decode runs the tensor-core kernel (which can merge in place)
   int T_q, T_t;
 };
@@ -146,6 +156,9 @@ static void free_all(kvq_cache* c) {
   cudaFree(c->part_ml);
   cudaFree(c->err);
   cudaFree(c->tickets);
+  cudaFree(c->lvl_o);
+  cudaFree(c->lvl_ml);
+  cudaFree(c->tickets2);
 }
 
 // Appends n tokens per pair (the whole combined tail + new sequence is
@@ -198,7 +211,8 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {
   kvq_status s = derive(cfg, &d);
   if (s != KVQ_OK) return s;
   *bytes = d.blocks_bytes + 4 * d.tail_bytes + d.rope_bytes + d.part_o_bytes +
-           d.part_ml_bytes + sizeof(int) + sizeof(int) * static_cast<size_t>(d.P);
+           d.part_ml_bytes + d.lvl_o_bytes + d.lvl_ml_bytes + sizeof(int) +
+           sizeof(int) * static_cast<size_t>(d.P) * (1 + d.R);
   return KVQ_OK;
 }
 
@@ -248,6 +262,9 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   if (ok) ok = cudaMalloc(&c->part_ml, d.part_ml_bytes) == cudaSuccess;
   if (ok) ok = cudaMalloc(&c->err, sizeof(int)) == cudaSuccess;
   if (ok) ok = cudaMalloc(&c->tickets, sizeof(int) * d.P) == cudaSuccess;
+  if (ok) ok = cudaMalloc(&c->lvl_o, d.lvl_o_bytes) == cudaSuccess;
+  if (ok) ok = cudaMalloc(&c->lvl_ml, d.lvl_ml_bytes) == cudaSuccess;
+  if (ok) ok = cudaMalloc(&c->tickets2, sizeof(int) * d.P * d.R) == cudaSuccess;
   if (!ok) {
     cudaGetLastError();
     free_all(c);
@@ -255,7 +272,8 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
     return KVQ_ERR_OOM;
   }
   bool init_ok = cudaMemset(c->err, 0, sizeof(int)) == cudaSuccess &&
-                 cudaMemset(c->tickets, 0, sizeof(int) * d.P) == cudaSuccess;
+                 cudaMemset(c->tickets, 0, sizeof(int) * d.P) == cudaSuccess &&
+                 cudaMemset(c->tickets2, 0, sizeof(int) * d.P * d.R) == cudaSuccess;
   for (int i = 0; i < 2 && init_ok; ++i)
     init_ok = cudaMemset(c->ktail[i], 0, d.tail_bytes) == cudaSuccess &&
               cudaMemset(c->vtail[i], 0, d.tail_bytes) == cudaSuccess;
@@ -376,16 +394,20 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float so
     g_launches.fetch_add(1);
     return KVQ_OK;
   }
-  MergeParams mp;
+  Merge2Params mp;
   mp.part_o = c->part_o;
   mp.part_ml = c->part_ml;
+  mp.lvl_o = c->lvl_o;
+  mp.lvl_ml = c->lvl_ml;
+  mp.tickets = c->tickets2;
   mp.out = static_cast<float*>(out);
   mp.upp = upp;
   mp.U = U;
   mp.n_warps = static_cast<int>(W);
   mp.R = d.R;
   mp.D = d.D;
-  if (launch_merge(mp, d.P, st) != cudaSuccess) return KVQ_ERR_CUDA;
+  mp.C2 = static_cast<int>((max_seg + 15) / 16);
+  if (launch_merge2(mp, d.P, st) != cudaSuccess) return KVQ_ERR_CUDA;
   g_launches.fetch_add(2);
   return KVQ_OK;
 }
@@ -445,6 +467,7 @@ kvq_status kvq_check_device_error(kvq_cache* c, void* stream) {
   if (h != 0) {
     // A warp that gave up left its pair's ticket short: start clean.
     cudaMemset(c->tickets, 0, sizeof(int) * c->dv.P);
+    cudaMemset(c->tickets2, 0, sizeof(int) * c->dv.P * c->dv.R);
     return KVQ_ERR_DEVICE_CHECK;
   }
   return KVQ_OK;

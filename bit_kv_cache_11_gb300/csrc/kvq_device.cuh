@@ -192,6 +192,24 @@ struct UnitCursor {
   }
 };
 
+// Two-level merge of the split partials (few pairs, many partials each):
+// block (pair, query, chunk) merges at most 16 partial slots into a level-2
+// partial; the last block of a (pair, query), found with a ticket, merges the
+// level-2 partials into the output.
+struct Merge2Params {
+  const float* part_o;
+  const float2* part_ml;
+  float* lvl_o;    // [P*R*C2][D]
+  float2* lvl_ml;  // [P*R*C2]
+  int* tickets;    // [P*R], zero between launches
+  float* out;      // [P][R][D]
+  int upp;
+  long long U;
+  int n_warps;
+  int R, D;
+  int C2;          // level-1 chunks per (pair, query)
+};
+
 // Largest warp whose unit range starts at or before unit x (the warp that
 // owns unit x): start(w) = floor(w*U/W) <= x  <=>  w*U < (x+1)*W.
 __host__ __device__ __forceinline__ long long owner_warp(long long x, long long U, long long W) {

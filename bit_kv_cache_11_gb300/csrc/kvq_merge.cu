@@ -78,6 +78,60 @@ __global__ void merge_kernel(const MergeParams mp) {
   }
 }
 
+// grid = P * R * C2 blocks of D threads.
+__global__ void merge2_kernel(const Merge2Params mp) {
+  const int b = blockIdx.x;
+  const int c = b % mp.C2;
+  const int pq = b / mp.C2;
+  const int r = pq % mp.R;
+  const long long pr = pq / mp.R;
+  const int d = threadIdx.x;
+  const long long x0 = pr * mp.upp;
+  const long long w0 = owner_warp(x0, mp.U, mp.n_warps);
+  const long long w1 = owner_warp(x0 + mp.upp - 1, mp.U, mp.n_warps);
+  const long long s0 = w0 + 16LL * c;
+  const long long s1 = s0 + 15 < w1 ? s0 + 15 : w1;
+  float ms = -INFINITY;
+  for (long long w = s0; w <= s1; ++w) ms = fmaxf(ms, mp.part_ml[(w + pr) * mp.R + r].x);
+  // A chunk may hold only empty partials (m = -inf, l = 0): weigh them 0.
+  float mb = ms == -INFINITY ? 0.f : ms;
+  float L = 0.f, o = 0.f;
+  for (long long w = s0; w <= s1; ++w) {
+    const float2 ml = mp.part_ml[(w + pr) * mp.R + r];
+    const float f = exp2f(ml.x - mb);
+    L = fmaf(f, ml.y, L);
+    o = fmaf(f, mp.part_o[((w + pr) * mp.R + r) * mp.D + d], o);
+  }
+  mp.lvl_o[static_cast<size_t>(b) * mp.D + d] = o;
+  if (d == 0) mp.lvl_ml[b] = make_float2(ms, L);
+  __threadfence();
+  __syncthreads();
+  __shared__ int last;
+  if (d == 0) last = atomicAdd(&mp.tickets[pq], 1) == mp.C2 - 1;
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  const size_t base = static_cast<size_t>(pq) * mp.C2;
+  ms = -INFINITY;
+  for (int k = 0; k < mp.C2; ++k) ms = fmaxf(ms, __ldcg(&mp.lvl_ml[base + k]).x);
+  mb = ms == -INFINITY ? 0.f : ms;
+  L = 0.f;
+  o = 0.f;
+  for (int k = 0; k < mp.C2; ++k) {
+    const float2 ml = __ldcg(&mp.lvl_ml[base + k]);
+    const float f = exp2f(ml.x - mb);  // 0 for an empty chunk (m = -inf)
+    L = fmaf(f, ml.y, L);
+    o = fmaf(f, __ldcg(&mp.lvl_o[(base + k) * mp.D + d]), o);
+  }
+  mp.out[(pr * mp.R + r) * mp.D + d] = o / L;
+  if (d == 0) mp.tickets[pq] = 0;
+}
+
+cudaError_t launch_merge2(const Merge2Params& mp, int n_pairs, cudaStream_t stream) {
+  merge2_kernel<<<n_pairs * mp.R * mp.C2, mp.D, 0, stream>>>(mp);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_merge(const MergeParams& mp, int n_pairs, cudaStream_t stream) {
   merge_kernel<<<n_pairs, mp.D, 0, stream>>>(mp);
   return cudaGetLastError();
