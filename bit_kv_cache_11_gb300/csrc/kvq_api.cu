@@ -34,6 +34,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Derived {
   int P, R, NB, G, D;
+  int frag_k, frag_v;  // code order of each side (1 fragment, 0 sequential)
+  bool mma_geom;       // geometry of the tensor-core decode kernel
   int C2max;  // level-1 chunks per (pair, query) of the two-level merge
   size_t block_bytes, off_kc, off_km, off_vc, off_vm;
   size_t blocks_bytes, tail_bytes, rope_bytes, part_o_bytes, part_ml_bytes;
@@ -62,8 +64,13 @@ kvq_status derive(const kvq_config* c, Derived* d) {
   const long long P = static_cast<long long>(c->batch) * c->n_kv_heads;
   if (P > 65535) return KVQ_ERR_UNSUPPORTED;  // grid.y of the quantize launch
   if (c->max_ctx > (1 << 26)) return KVQ_ERR_UNSUPPORTED;
+  // decode units (32-token sub-blocks and tail chunks) are counted in int
+  if (P * (static_cast<long long>(c->max_ctx) / 32 + 32) >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
   d->P = static_cast<int>(P);
   d->R = R;
+  d->mma_geom = mma_geometry(c->group, c->axis_k, c->axis_v);
+  d->frag_k = fragment_order(c->head_dim, c->group, c->bits_k, c->axis_k, c->axis_v) ? 1 : 0;
+  d->frag_v = fragment_order(c->head_dim, c->group, c->bits_v, c->axis_k, c->axis_v) ? 1 : 0;
   d->G = c->group;
   d->D = c->head_dim;
   d->NB = c->max_ctx / c->group;
@@ -137,6 +144,8 @@ static CacheGeom geom_of(const kvq_cache* c) {
   g.off_vm = static_cast<int>(c->dv.off_vm);
   g.D = c->dv.D;
   g.G = c->dv.G;
+  g.frag_k = c->dv.frag_k;
+  g.frag_v = c->dv.frag_v;
   g.bk = c->cfg.bits_k;
   g.bv = c->cfg.bits_v;
   g.ak = c->cfg.axis_k;
@@ -222,15 +231,14 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   Derived d;
   kvq_status s = derive(cfg, &d);
   if (s != KVQ_OK) return s;
-  // Tensor-core kernel for channel-grouped keys and token-grouped values
-  // (with its rotated-key variant for keys stored before RoPE); the CUDA-core
-  // kernel for every other geometry (and for all of them when
-  // KVQ_DECODE_GENERIC is set in the environment).
+  // Tensor-core kernel for channel-grouped keys, token-grouped values and
+  // G = 32 (with its rotated-key variant for keys stored before RoPE); the
+  // CUDA-core kernel for every other geometry.  Codes in fragment order are
+  // read by the tensor-core kernel only.
   DecodeOps ops{nullptr, nullptr};
-  if (cfg->axis_k == KVQ_AXIS_CHANNEL && cfg->axis_v == KVQ_AXIS_TOKEN &&
-      std::getenv("KVQ_DECODE_GENERIC") == nullptr)
-    ops = decode_mma_ops(d.D, d.R, cfg->bits_k, cfg->bits_v, cfg->keys_pre_rope != 0);
+  if (d.mma_geom) ops = decode_mma_ops(d.D, d.R, cfg->bits_k, cfg->bits_v, cfg->keys_pre_rope != 0);
   const bool mma = ops.launch != nullptr;
+  if ((d.frag_k || d.frag_v) && !mma) return KVQ_ERR_UNSUPPORTED;
   if (ops.launch == nullptr) ops = decode_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
   if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
 
@@ -351,7 +359,7 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float so
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Derived& d = c->dv;
   const int nsub = c->T_q / 32;
-  const int upp = nsub + (c->T_t > 0 ? 1 : 0);
+  const int upp = nsub + tail_units(c->mma, c->T_t, c->cfg.bits_k, c->cfg.bits_v);
   const long long U = static_cast<long long>(d.P) * upp;
   if (U == 0) {
     if (cudaMemsetAsync(out, 0, static_cast<size_t>(d.P) * d.R * d.D * sizeof(float), st) !=
@@ -446,6 +454,8 @@ kvq_status kvq_get_buffers(const kvq_cache* c, kvq_buffers* out) {
   out->off_km = c->dv.off_km;
   out->off_vc = c->dv.off_vc;
   out->off_vm = c->dv.off_vm;
+  out->code_order_k = c->dv.frag_k;
+  out->code_order_v = c->dv.frag_v;
   out->blocks_per_pair = c->dv.NB;
   out->n_pairs = c->dv.P;
   out->T_q = c->T_q;

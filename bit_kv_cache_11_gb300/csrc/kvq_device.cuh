@@ -95,6 +95,37 @@ __device__ __forceinline__ float warp_max(float v) {
 
 // ---------------------------------------------------------------- parameter blocks
 
+// The tensor-core decode kernel covers keys grouped per channel, values per
+// token and G = 32 (a 32-token sub-block is then a whole block).
+__host__ __device__ inline bool mma_geometry(int G, int ak, int av) {
+  return ak == 0 && av == 1 && G == 32;
+}
+
+// Code order of one side (include/kvq.h, "Code order of a side"): fragment
+// order for 2- and 4-bit codes in the tensor-core geometry with D = 64 or
+// 128, sequential order otherwise.
+__host__ __device__ inline bool fragment_order(int D, int G, int bits, int ak, int av) {
+  return mma_geometry(G, ak, av) && (D == 64 || D == 128) && (bits == 2 || bits == 4);
+}
+
+// Fragment order: word (within the side's 32-token region) and bit of tile
+// element (row, col) of a tile with `cols` columns (keys: row = token, col =
+// channel, cols = D; values: row = channel, col = token, cols = 32).
+__host__ __device__ inline void frag_position(int row, int col, int cols, int bits, int* word,
+                                              int* bit) {
+  const int mt = row >> 4, hr = (row >> 3) & 1, g = row & 7;
+  const int s = col >> 5, hc = (col >> 4) & 1, t = (col >> 2) & 3, j = col & 3;
+  int w;
+  if (bits == 2) {
+    w = mt * (cols >> 5) + s;
+    *bit = 8 * j + 4 * hr + 2 * hc;
+  } else {
+    w = 2 * (mt * (cols >> 5) + s) + hc;
+    *bit = 8 * j + 4 * hr;
+  }
+  *word = ((w >> 2) * 32 + 4 * g + t) * 4 + (w & 3);
+}
+
 // Geometry of the packed cache, shared by all kernels.
 struct CacheGeom {
   uint8_t* blocks;     // [P][NB][block_bytes]
@@ -103,6 +134,7 @@ struct CacheGeom {
   int off_km, off_vc, off_vm;
   int D, G, bk, bv, ak, av;
   int P;
+  int frag_k, frag_v;  // code order of each side: 1 fragment, 0 sequential
 };
 
 // Quantize / append / flush launch: grid (nflush + 1, P).
@@ -131,11 +163,27 @@ struct DequantParams {
   float* vout;
 };
 
+// Tail tokens per unit of the tensor-core decode kernel: the fp16 tail is
+// streamed through the same copy pipeline as the packed sub-blocks, in chunks
+// whose K and V rows (2 * tch * D fp16 values) fill exactly one stage of
+// D * (4 bk + 4 bv + 8) bytes.
+__host__ __device__ constexpr int mma_tail_chunk(int bk, int bv) { return bk + bv + 2; }
+
+// Units of the fp16 tail of one pair: ceil(T_t / tch) chunks for the
+// tensor-core kernel, one unit for the CUDA-core kernel.
+__host__ __device__ inline int tail_units(bool mma, int T_t, int bk, int bv) {
+  if (T_t <= 0) return 0;
+  if (!mma) return 1;
+  const int tch = mma_tail_chunk(bk, bv);
+  return (T_t + tch - 1) / tch;
+}
+
 // Split-K decode launch.  The work of all pairs is a flat sequence of units:
 // pair p owns units [p*upp, (p+1)*upp); unit j < nsub of a pair is its j-th
-// 32-token quantized sub-block, unit j == nsub (present when T_t > 0) is its
-// fp16 tail.  Warp w of the grid processes units [w*U/W, (w+1)*U/W) and writes
-// one partial (m, l, o) per pair it touches into slot (w + p).
+// 32-token quantized sub-block, units j >= nsub (present when T_t > 0) cover
+// its fp16 tail (see tail_units).  Warp w of the grid processes units
+// [w*U/W, (w+1)*U/W) and writes one partial (m, l, o) per pair it touches
+// into slot (w + p).
 struct DecodeParams {
   CacheGeom g;
   const __half* ktail;  // active tail [P][G][D]

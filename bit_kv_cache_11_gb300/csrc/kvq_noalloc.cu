@@ -130,8 +130,12 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
       static_cast<long long>((KVQ_NOALLOC_SCRATCH_BYTES - fixed) / (slot_o + slot_ml));
 
   DecodeOps ops{nullptr, nullptr};
-  if (cfg->axis_k == KVQ_AXIS_CHANNEL && cfg->axis_v == KVQ_AXIS_TOKEN)
+  if (mma_geometry(G, cfg->axis_k, cfg->axis_v))
     ops = decode_mma_ops(D, R, cfg->bits_k, cfg->bits_v, false);
+  const bool mma = ops.launch != nullptr;
+  if (!mma && (fragment_order(D, G, cfg->bits_k, cfg->axis_k, cfg->axis_v) ||
+               fragment_order(D, G, cfg->bits_v, cfg->axis_k, cfg->axis_v)))
+    return KVQ_ERR_UNSUPPORTED;
   if (ops.launch == nullptr) ops = decode_ops(D, R, cfg->bits_k, cfg->bits_v);
   if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
 
@@ -147,7 +151,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int nsub = T_q / 32;
-  const int upp = nsub + (T_tail > 0 ? 1 : 0);
+  const int upp = nsub + tail_units(mma, T_tail, cfg->bits_k, cfg->bits_v);
   const long long U = P * upp;
   float* part_o = reinterpret_cast<float*>(ds.scratch);
   const size_t ml_off = round256(static_cast<size_t>(max_slots) * slot_o);
@@ -176,6 +180,8 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.g.G = G;
     p.g.bk = cfg->bits_k;
     p.g.bv = cfg->bits_v;
+    p.g.frag_k = fragment_order(D, G, cfg->bits_k, cfg->axis_k, cfg->axis_v) ? 1 : 0;
+    p.g.frag_v = fragment_order(D, G, cfg->bits_v, cfg->axis_k, cfg->axis_v) ? 1 : 0;
     p.g.ak = cfg->axis_k;
     p.g.av = cfg->axis_v;
     p.g.P = static_cast<int>(P);

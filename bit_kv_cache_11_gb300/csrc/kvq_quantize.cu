@@ -178,35 +178,47 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
     const int bits = isv ? BV : BK;
     const float top = static_cast<float>((1 << bits) - 1);
     const __half* X = isv ? xv : xk;
+    // byte slot of code (token j, channel d) in the code tile of its side
+    auto slot = [&](int j, int d) -> int {
+      if (isv ? q.g.frag_v : q.g.frag_k) {
+        int w, bit;
+        if (isv) frag_position(d, j, 32, bits, &w, &bit);
+        else frag_position(j, d, D, bits, &w, &bit);
+        return w * (32 / bits) + bit / bits;
+      }
+      return isv ? d * VP + j : j * KP + d;
+    };
+    uint8_t* code = isv ? vcode : kcode;
     if (axis == 0) {  // channel ee over the G tokens
       const Stat st = group_stat(X + ee, XP, G, bits, (isv ? vmeta : kmeta) + ee);
-      for (int j = 0; j < G; ++j) {
-        const uint8_t c = static_cast<uint8_t>(code_of(__half2float(X[j * XP + ee]), st, top));
-        if (isv) vcode[ee * VP + j] = c;
-        else kcode[j * KP + ee] = c;
-      }
+      for (int j = 0; j < G; ++j)
+        code[slot(j, ee)] = static_cast<uint8_t>(code_of(__half2float(X[j * XP + ee]), st, top));
     } else {          // token j, channels [g*G, (g+1)*G); consecutive threads: consecutive j
       const int j = ee & (G - 1), g = ee >> lgG;
       const Stat st = group_stat(X + j * XP + (g << lgG), 1, G, bits,
                                  (isv ? vmeta : kmeta) + j * ng + g);
       for (int i = 0; i < G; ++i) {
         const int d = (g << lgG) + i;
-        const uint8_t c = static_cast<uint8_t>(code_of(__half2float(X[j * XP + d]), st, top));
-        if (isv) vcode[d * VP + j] = c;
-        else kcode[j * KP + d] = c;
+        code[slot(j, d)] = static_cast<uint8_t>(code_of(__half2float(X[j * XP + d]), st, top));
       }
     }
   }
   __syncthreads();
 
-  // 3. pack and store: K token-major rows; V 32-token chunks, channel-major
+  // 3. pack and store.  Fragment order: the tile already holds each word's
+  // codes as 32/B consecutive bytes, LSB first.  Sequential order: K
+  // token-major rows; V 32-token chunks, channel-major.
   {
     constexpr int per = 32 / BK;
     const int kw = D * BK / 32;
     uint32_t* kc = reinterpret_cast<uint32_t*>(blk);
     for (int w = tid; w < G * kw; w += blockDim.x) {
-      const int j = w / kw;
-      kc[w] = pack_word<BK>(kcode + j * KP + (w - j * kw) * per);
+      if (q.g.frag_k) {
+        kc[w] = pack_word<BK>(kcode + w * per);
+      } else {
+        const int j = w / kw;
+        kc[w] = pack_word<BK>(kcode + j * KP + (w - j * kw) * per);
+      }
     }
   }
   {
@@ -214,11 +226,15 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
     uint32_t* vc = reinterpret_cast<uint32_t*>(blk + q.g.off_vc);
     const int words = (G / 32) * D * BV;
     for (int w = tid; w < words; w += blockDim.x) {
-      const int c = w / (D * BV);
-      const int rem = w - c * (D * BV);
-      const int d = rem / BV;
-      const int j0 = c * 32 + (rem - d * BV) * per;
-      vc[w] = pack_word<BV>(vcode + d * VP + j0);
+      if (q.g.frag_v) {
+        vc[w] = pack_word<BV>(vcode + w * per);
+      } else {
+        const int c = w / (D * BV);
+        const int rem = w - c * (D * BV);
+        const int d = rem / BV;
+        const int j0 = c * 32 + (rem - d * BV) * per;
+        vc[w] = pack_word<BV>(vcode + d * VP + j0);
+      }
     }
   }
 }
@@ -239,16 +255,18 @@ __global__ void __launch_bounds__(kQuantThreads) dequantize_kernel(const Dequant
     const size_t o = (static_cast<size_t>(p) * q.T_q + static_cast<size_t>(i) * G + j) * D + d;
     {
       const int bits = q.g.bk, per = 32 / bits;
-      const uint32_t word = kc[j * (D * bits / 32) + d / per];
-      const uint32_t c = (word >> ((d % per) * bits)) & ((1u << bits) - 1u);
+      int w = j * (D * bits / 32) + d / per, bit = (d % per) * bits;
+      if (q.g.frag_k) frag_position(j, d, D, bits, &w, &bit);
+      const uint32_t c = (kc[w] >> bit) & ((1u << bits) - 1u);
       const float2 sz = __half22float2(km[q.g.ak == 0 ? d : j * ng + d / G]);
       q.kout[o] = fmaf(static_cast<float>(c), sz.x, sz.y);
     }
     {
       const int bits = q.g.bv, per = 32 / bits;
       const int ch = j / 32, jj = j % 32;
-      const uint32_t word = vc[(ch * D + d) * bits + jj / per];
-      const uint32_t c = (word >> ((jj % per) * bits)) & ((1u << bits) - 1u);
+      int w = (ch * D + d) * bits + jj / per, bit = (jj % per) * bits;
+      if (q.g.frag_v) frag_position(d, j, 32, bits, &w, &bit);
+      const uint32_t c = (vc[w] >> bit) & ((1u << bits) - 1u);
       const float2 sz = __half22float2(vm[q.g.av == 0 ? d : j * ng + d / G]);
       q.vout[o] = fmaf(static_cast<float>(c), sz.x, sz.y);
     }

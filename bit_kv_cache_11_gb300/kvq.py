@@ -45,7 +45,7 @@ class kvq_buffers(ctypes.Structure):
                 ("block_bytes", ctypes.c_size_t), ("off_kc", ctypes.c_size_t),
                 ("off_km", ctypes.c_size_t), ("off_vc", ctypes.c_size_t), ("off_vm", ctypes.c_size_t),
                 ("blocks_per_pair", ctypes.c_int), ("n_pairs", ctypes.c_int), ("T_q", ctypes.c_int),
-                ("T_tail", ctypes.c_int)]
+                ("T_tail", ctypes.c_int), ("code_order_k", ctypes.c_int), ("code_order_v", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p

@@ -55,20 +55,36 @@
  *
  *   block (p, i) starts at byte (p * NB + i) * block_bytes, where
  *   block_bytes = G*D*(bk+bv)/8 + 8*D, and holds tokens [i*G, (i+1)*G):
- *     [off_kc, +G*D*bk/8)  K codes, token-major: token j's row is D*bk/32
- *                          words; channel d sits in word d/(32/bk) at bit
- *                          (d % (32/bk)) * bk.
+ *     [off_kc, +G*D*bk/8)  K codes, in the side's code order (below).
  *     [off_km, +4*D)       K metadata: D entries {fp16 scale, fp16 zero}
  *                          (scale at the lower address).  Channel axis:
  *                          entry d is channel d's group.  Token axis: entry
  *                          j*(D/G) + g is token j, channels [g*G, (g+1)*G).
- *     [off_vc, +G*D*bv/8)  V codes, in 32-token chunks c = j/32; inside a
- *                          chunk, channel-major: channel d owns bv words at
- *                          word offset (c*D + d)*bv; token j sits in word
- *                          (j%32)/(32/bv) of them at bit ((j%32) % (32/bv))*bv.
+ *     [off_vc, +G*D*bv/8)  V codes, in the side's code order (below).
  *     [off_vm, +4*D)       V metadata, indexed as for K by V's axis.
  *   off_kc = 0, off_km = G*D*bk/8, off_vc = off_km + 4*D,
  *   off_vm = off_vc + G*D*bv/8.
+ *
+ *   Code order of a side (kvq_buffers.code_order_k / code_order_v):
+ *   FRAGMENT order when keys are grouped per channel, values per token,
+ *   G = 32, D is 64 or 128 and the side has 2 or 4 bits; SEQUENTIAL order
+ *   otherwise.
+ *     Sequential.  K: token-major, token j's row is D*bk/32 words; channel d
+ *       sits in word d/(32/bk) at bit (d % (32/bk))*bk.  V: 32-token chunks
+ *       c = j/32; inside a chunk, channel-major: channel d owns bv words at
+ *       word offset (c*D + d)*bv; token j sits in word (j%32)/(32/bv) of them
+ *       at bit ((j%32) % (32/bv))*bv.
+ *     Fragment (the operand order of the decode kernel's fp8 tensor-core
+ *       tiles, so that each warp lane turns its own words into operand
+ *       registers with masks alone).  The side's codes of a block form a tile
+ *       of rows x cols codes: K rows = the 32 tokens, cols = the D channels;
+ *       V rows = the D channels, cols = the 32 tokens.  Write
+ *         row = 16*mt + 8*hr + g          (g < 8, hr < 2)
+ *         col = 32*s + 16*hc + 4*t + j    (t < 4, j < 4, hc < 2)
+ *       The code belongs to lane l = 4*g + t, in that lane's word
+ *         w = mt*(cols/32) + s            at bit 8*j + 4*hr + 2*hc  (2 bits)
+ *         w = 2*(mt*(cols/32) + s) + hc   at bit 8*j + 4*hr         (4 bits)
+ *       and word w of lane l is word ((w/4)*32 + l)*4 + w%4 of the region.
  *
  *   The tail is fp16 [P][G][D] for K and for V; tokens [T_q, T_q + T_tail) of
  *   every pair sit in rows [0, T_tail).
@@ -133,6 +149,8 @@ typedef struct {
   int n_pairs;                 /* P                                             */
   int T_q;                     /* quantized tokens per pair (multiple of G)     */
   int T_tail;                  /* tail tokens per pair, 0 <= T_tail < G         */
+  int code_order_k;            /* 0 sequential, 1 fragment (see the layout)     */
+  int code_order_v;
 } kvq_buffers;
 
 /* Validates a config on the host (no GPU needed).  Returns KVQ_OK,

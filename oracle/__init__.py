@@ -70,6 +70,8 @@ def _load():
     lib.kvo_quantize_tensor.argtypes = [I, I, I, I, I, P, P, P, P]
     lib.kvo_dequantize_tensor.argtypes = [I, I, I, I, P, P, P, P]
     lib.kvo_block_bytes.restype = ctypes.c_size_t
+    lib.kvo_code_order.argtypes = [I, I, I, I, I]
+    lib.kvo_code_order.restype = I
     lib.kvo_block_bytes.argtypes = [I, I, I, I]
     lib.kvo_block_offsets.argtypes = [I, I, I, I, P]
     lib.kvo_pack_pair.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P]
@@ -147,6 +149,11 @@ def dequantize_tensor(codes, scale, zero, G: int, axis: int) -> np.ndarray:
 
 
 # ---- layout -----------------------------------------------------------------
+
+def code_order(D: int, G: int, bits: int, ak: int, av: int) -> int:
+    """1 when a side's codes are stored in fragment order, 0 for sequential."""
+    return int(_load().kvo_code_order(D, G, bits, ak, av))
+
 
 def block_bytes(D: int, G: int, bk: int, bv: int) -> int:
     return int(_load().kvo_block_bytes(D, G, bk, bv))

@@ -194,6 +194,67 @@ void kvo_block_offsets(int D, int G, int bk, int bv, size_t* offsets) {
   offsets[3] = offsets[2] + (size_t)G * D * bv / 8;
 }
 
+/* Which order a side's codes are stored in: 1 = fragment order, used when
+ * keys are grouped per channel, values per token, G = 32, D is 64 or 128 and
+ * the side has 2 or 4 bits; 0 = sequential order otherwise. */
+int kvo_code_order(int D, int G, int bits, int ak, int av) {
+  return (ak == 0 && av == 1 && G == 32 && (D == 64 || D == 128) &&
+          (bits == 2 || bits == 4)) ? 1 : 0;
+}
+
+/* Fragment order of one 32-token code region, seen as a tile of rows x cols
+ * codes (keys: rows = the 32 tokens, cols = the D channels; values: rows =
+ * the D channels, cols = the 32 tokens).  With
+ *   row = 16*mt + 8*hr + g      (g < 8, hr < 2)
+ *   col = 32*s + 16*hc + 4*t + j  (t < 4, j < 4, hc < 2)
+ * the code belongs to lane l = 4*g + t, in that lane's word
+ *   w = mt*(cols/32) + s             at bit 8*j + 4*hr + 2*hc  (2 bits)
+ *   w = 2*(mt*(cols/32) + s) + hc    at bit 8*j + 4*hr         (4 bits)
+ * and word w of lane l is word ((w/4)*32 + l)*4 + w%4 of the region. */
+static void frag_position(int row, int col, int cols, int bits, size_t* word,
+                          int* bit) {
+  int mt = row / 16, hr = (row % 16) / 8, g = row % 8;
+  int s = col / 32, hc = (col % 32) / 16, t = (col % 16) / 4, j = col % 4;
+  int lane = 4 * g + t;
+  int w;
+  if (bits == 2) {
+    w = mt * (cols / 32) + s;
+    *bit = 8 * j + 4 * hr + 2 * hc;
+  } else {
+    w = 2 * (mt * (cols / 32) + s) + hc;
+    *bit = 8 * j + 4 * hr;
+  }
+  *word = ((size_t)(w / 4) * 32 + (size_t)lane) * 4 + (size_t)(w % 4);
+}
+
+/* Word and bit of key code (token j of the block, channel d).  Sequential
+ * order: token-major rows of D*bk/32 words, channel d in word d/(32/bk) at
+ * bit (d % (32/bk))*bk. */
+static void key_position(int D, int G, int bk, int ak, int av, int j, int d,
+                         size_t* word, int* bit) {
+  if (kvo_code_order(D, G, bk, ak, av)) {
+    frag_position(j, d, D, bk, word, bit);
+  } else {
+    int per = 32 / bk;
+    *word = (size_t)j * (D * bk / 32) + (size_t)(d / per);
+    *bit = (d % per) * bk;
+  }
+}
+
+/* Word and bit of value code (token j of the block, channel d).  Sequential
+ * order: 32-token chunks, channel-major inside a chunk, bv words per channel,
+ * token j in word (j%32)/(32/bv) at bit ((j%32) % (32/bv))*bv. */
+static void value_position(int D, int G, int bv, int ak, int av, int j, int d,
+                           size_t* word, int* bit) {
+  if (kvo_code_order(D, G, bv, ak, av)) {
+    frag_position(d, j, 32, bv, word, bit);
+  } else {
+    int per = 32 / bv, c = j / 32, jj = j % 32;
+    *word = ((size_t)c * D + d) * bv + (size_t)(jj / per);
+    *bit = (jj % per) * bv;
+  }
+}
+
 /* Writes the Tq/G blocks of one pair into `blocks` (Tq/G * block_bytes). */
 void kvo_pack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
                    const uint8_t* kcodes, const uint16_t* kscale,
@@ -203,27 +264,25 @@ void kvo_pack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
   size_t bb = kvo_block_bytes(D, G, bk, bv);
   size_t off[4];
   kvo_block_offsets(D, G, bk, bv, off);
-  int kper = 32 / bk; /* codes per K word */
-  int vper = 32 / bv; /* codes per V word */
   memset(blocks, 0, (size_t)(Tq / G) * bb);
   for (int i = 0; i < Tq / G; ++i) {
     uint8_t* blk = blocks + (size_t)i * bb;
-    /* K codes: token-major rows of D*bk/32 words */
+    /* K codes, in the order kvo_code_order selects */
     for (int j = 0; j < G; ++j) {
       for (int d = 0; d < D; ++d) {
-        size_t word = (size_t)j * (D * bk / 32) + (size_t)(d / kper);
-        put_bits(blk + off[0], word, (d % kper) * bk, bk,
-                 kcodes[(size_t)(i * G + j) * D + d]);
+        size_t word;
+        int bit;
+        key_position(D, G, bk, ak, av, j, d, &word, &bit);
+        put_bits(blk + off[0], word, bit, bk, kcodes[(size_t)(i * G + j) * D + d]);
       }
     }
-    /* V codes: 32-token chunks, channel-major inside a chunk, bv words per
-     * channel */
+    /* V codes, in the order kvo_code_order selects */
     for (int j = 0; j < G; ++j) {
-      int c = j / 32, jj = j % 32;
       for (int d = 0; d < D; ++d) {
-        size_t word = ((size_t)c * D + d) * bv + (size_t)(jj / vper);
-        put_bits(blk + off[2], word, (jj % vper) * bv, bv,
-                 vcodes[(size_t)(i * G + j) * D + d]);
+        size_t word;
+        int bit;
+        value_position(D, G, bv, ak, av, j, d, &word, &bit);
+        put_bits(blk + off[2], word, bit, bv, vcodes[(size_t)(i * G + j) * D + d]);
       }
     }
     /* metadata: D entries each */
@@ -246,18 +305,16 @@ void kvo_unpack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
   size_t bb = kvo_block_bytes(D, G, bk, bv);
   size_t off[4];
   kvo_block_offsets(D, G, bk, bv, off);
-  int kper = 32 / bk, vper = 32 / bv;
   for (int i = 0; i < Tq / G; ++i) {
     const uint8_t* blk = blocks + (size_t)i * bb;
     for (int j = 0; j < G; ++j) {
-      int c = j / 32, jj = j % 32;
       for (int d = 0; d < D; ++d) {
-        size_t kw = (size_t)j * (D * bk / 32) + (size_t)(d / kper);
-        kcodes[(size_t)(i * G + j) * D + d] =
-            (uint8_t)get_bits(blk + off[0], kw, (d % kper) * bk, bk);
-        size_t vw = ((size_t)c * D + d) * bv + (size_t)(jj / vper);
-        vcodes[(size_t)(i * G + j) * D + d] =
-            (uint8_t)get_bits(blk + off[2], vw, (jj % vper) * bv, bv);
+        size_t word;
+        int bit;
+        key_position(D, G, bk, ak, av, j, d, &word, &bit);
+        kcodes[(size_t)(i * G + j) * D + d] = (uint8_t)get_bits(blk + off[0], word, bit, bk);
+        value_position(D, G, bv, ak, av, j, d, &word, &bit);
+        vcodes[(size_t)(i * G + j) * D + d] = (uint8_t)get_bits(blk + off[2], word, bit, bv);
       }
     }
     for (int e = 0; e < D; ++e) {

@@ -199,6 +199,42 @@ def test_packed_words(oracle_mod, row):
     assert got == word
 
 
+def test_code_order_rule(oracle_mod):
+    # fragment order only for keys per channel + values per token, G = 32,
+    # D in {64, 128}, 2/4 bits
+    for D in (64, 128):
+        assert oracle_mod.code_order(D, 32, 2, 0, 1) == 1
+        assert oracle_mod.code_order(D, 32, 4, 0, 1) == 1
+        assert oracle_mod.code_order(D, 32, 8, 0, 1) == 0
+        assert oracle_mod.code_order(D, 128, 2, 0, 1) == 0
+        assert oracle_mod.code_order(D, 64, 4, 0, 1) == 0
+        for ak, av in ((0, 0), (1, 0), (1, 1)):
+            assert oracle_mod.code_order(D, 32, 2, ak, av) == 0
+    assert oracle_mod.code_order(32, 32, 2, 0, 1) == 0
+
+
+@pytest.mark.parametrize("row", _read_golden("fragment_words.txt"))
+def test_fragment_words(oracle_mod, row):
+    kind, bits, D = row[0].split()
+    bits, D = int(bits), int(D)
+    tok, ch, code = (int(v) for v in row[1].split())
+    word_index = int(row[2])
+    word = int(row[3], 16)
+    G = 32
+    st = dict(G=G, bk=bits, bv=bits, ak=0, av=1,
+              kcodes=np.zeros((G, D), np.uint8), kscale=np.zeros((1, D), np.uint16),
+              kzero=np.zeros((1, D), np.uint16), vcodes=np.zeros((G, D), np.uint8),
+              vscale=np.zeros((G, D // G), np.uint16), vzero=np.zeros((G, D // G), np.uint16))
+    (st["kcodes"] if kind == "K" else st["vcodes"])[tok, ch] = code
+    off = oracle_mod.block_offsets(D, G, bits, bits)
+    blk = oracle_mod.pack_pair(st)[0]
+    lo = off[0] if kind == "K" else off[2]
+    region = bytes(blk[lo:lo + G * D * bits // 8])
+    words = np.frombuffer(region, "<u4")
+    assert int(words[word_index]) == word
+    assert np.count_nonzero(words) == 1
+
+
 def test_block_geometry_by_hand(oracle_mod):
     # G*D*(bk+bv)/8 + 8*D bytes; K codes, K meta, V codes, V meta in that order
     assert oracle_mod.block_bytes(128, 32, 2, 2) == 2048 + 1024 == 3072
@@ -229,8 +265,35 @@ def test_block_bytes_by_hand(oracle_mod):
     assert blk[764:768] == bytes([0x1F, 0x40, 0x1F, 0x00])
 
 
+def test_fragment_block_by_hand(oracle_mod):
+    """A whole 32-token block (D = 64) in fragment order: byte j of every word
+    holds the four codes whose column offset (channel for keys, token for
+    values) is j mod 4."""
+    D, G = 64, 32
+    t = np.arange(G)[:, None]
+    d = np.arange(D)[None, :]
+    st = dict(G=G, bk=2, bv=4, ak=0, av=1,
+              kcodes=np.broadcast_to(d % 4, (G, D)).astype(np.uint8),
+              kscale=np.zeros((1, D), np.uint16), kzero=np.zeros((1, D), np.uint16),
+              vcodes=np.broadcast_to(t % 4 + 4 * (d % 2), (G, D)).astype(np.uint8),
+              vscale=np.zeros((G, D // G), np.uint16), vzero=np.zeros((G, D // G), np.uint16))
+    off = oracle_mod.block_offsets(D, G, 2, 4)
+    blk = bytes(oracle_mod.pack_pair(st)[0])
+    # keys, 2 bits: byte j = j * (1 + 4 + 16 + 64)
+    assert blk[off[0]:off[1]] == bytes([0x00, 0x55, 0xAA, 0xFF]) * (G * D * 2 // 32)
+    # values, 4 bits: byte j holds rows g (bits 0-3) and g + 8 (bits 4-7) of
+    # one channel parity (g and g + 8 share it): code j + 4 * (g % 2) twice
+    lanes = np.frombuffer(blk[off[2]:off[3]], np.uint8).reshape(-1, 32, 4, 4)  # [w/4][lane][w%4][byte]
+    for lane in range(32):
+        g = lane // 4
+        for j in range(4):
+            c = j + 4 * (g % 2)
+            assert np.all(lanes[:, lane, :, j] == c | (c << 4))
+
+
 @pytest.mark.parametrize("bk,bv,ak,av,G,D", [(2, 2, 0, 1, 32, 128), (4, 8, 1, 0, 128, 128),
-                                             (8, 4, 0, 1, 32, 64), (2, 4, 1, 1, 64, 128)])
+                                             (8, 4, 0, 1, 32, 64), (2, 4, 1, 1, 64, 128),
+                                             (4, 2, 0, 1, 32, 64), (2, 2, 0, 1, 128, 128)])
 def test_pack_unpack_round_trip(oracle_mod, bk, bv, ak, av, G, D):
     rng = np.random.default_rng(bk * 10 + bv)
     X = rng.standard_normal((2 * G + 5, D)).astype(np.float16)
