@@ -114,14 +114,15 @@ __host__ __device__ inline bool fragment_order(int D, int G, int bits, int ak, i
 __host__ __device__ inline void frag_position(int row, int col, int cols, int bits, int* word,
                                               int* bit) {
   const int mt = row >> 4, hr = (row >> 3) & 1, g = row & 7;
-  const int s = col >> 5, hc = (col >> 4) & 1, t = (col >> 2) & 3, j = col & 3;
+  const int ks = col >> 4, kh = (col >> 3) & 1, t = (col >> 1) & 3, e = col & 1;
   int w;
   if (bits == 2) {
-    w = mt * (cols >> 5) + s;
-    *bit = 8 * j + 4 * hr + 2 * hc;
+    const int pi = 2 * (ks & 1) + kh;  // F2[0] = {0, 10, 12, 14}, F2[1] = {2, 4, 6, 8}
+    w = mt * (cols >> 5) + (ks >> 1);
+    *bit = 16 * e + (hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0));
   } else {
-    w = 2 * (mt * (cols >> 5) + s) + hc;
-    *bit = 8 * j + 4 * hr;
+    w = mt * (cols >> 4) + ks;
+    *bit = 16 * e + 8 * kh + 4 * hr;
   }
   *word = ((w >> 2) * 32 + 4 * g + t) * 4 + (w & 3);
 }

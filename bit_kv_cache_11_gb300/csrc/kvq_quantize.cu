@@ -178,43 +178,67 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
     const int bits = isv ? BV : BK;
     const float top = static_cast<float>((1 << bits) - 1);
     const __half* X = isv ? xv : xk;
-    // byte slot of code (token j, channel d) in the code tile of its side
-    auto slot = [&](int j, int d) -> int {
-      if (isv ? q.g.frag_v : q.g.frag_k) {
-        int w, bit;
-        if (isv) frag_position(d, j, 32, bits, &w, &bit);
-        else frag_position(j, d, D, bits, &w, &bit);
-        return w * (32 / bits) + bit / bits;
-      }
-      return isv ? d * VP + j : j * KP + d;
-    };
-    uint8_t* code = isv ? vcode : kcode;
     if (axis == 0) {  // channel ee over the G tokens
       const Stat st = group_stat(X + ee, XP, G, bits, (isv ? vmeta : kmeta) + ee);
-      for (int j = 0; j < G; ++j)
-        code[slot(j, ee)] = static_cast<uint8_t>(code_of(__half2float(X[j * XP + ee]), st, top));
+      for (int j = 0; j < G; ++j) {
+        const uint8_t c = static_cast<uint8_t>(code_of(__half2float(X[j * XP + ee]), st, top));
+        if (isv) vcode[ee * VP + j] = c;
+        else kcode[j * KP + ee] = c;
+      }
     } else {          // token j, channels [g*G, (g+1)*G); consecutive threads: consecutive j
       const int j = ee & (G - 1), g = ee >> lgG;
       const Stat st = group_stat(X + j * XP + (g << lgG), 1, G, bits,
                                  (isv ? vmeta : kmeta) + j * ng + g);
       for (int i = 0; i < G; ++i) {
         const int d = (g << lgG) + i;
-        code[slot(j, d)] = static_cast<uint8_t>(code_of(__half2float(X[j * XP + d]), st, top));
+        const uint8_t c = static_cast<uint8_t>(code_of(__half2float(X[j * XP + d]), st, top));
+        if (isv) vcode[d * VP + j] = c;
+        else kcode[j * KP + d] = c;
       }
     }
   }
   __syncthreads();
 
-  // 3. pack and store.  Fragment order: the tile already holds each word's
-  // codes as 32/B consecutive bytes, LSB first.  Sequential order: K
-  // token-major rows; V 32-token chunks, channel-major.
+  // 3. pack and store.  Sequential order: K token-major rows; V 32-token
+  // chunks, channel-major.  Fragment order (G = 32): word w of lane l = 4g + t
+  // collects, per (hr, kh) and k-step, the two codes of tile row
+  // 16 mt + 8 hr + g at columns 16 ks + 8 kh + 2 t + {0, 1} -- two adjacent
+  // bytes of the code tile, spread to bits b and b + 16.
+  auto frag_word = [&](const uint8_t* tile, int pitch, int cols, int bits, int w) -> uint32_t {
+    const int l = (w >> 2) & 31, lw = ((w >> 7) << 2) | (w & 3);
+    const int g = l >> 2, t = l & 3;
+    uint32_t word = 0;
+    if (bits == 2) {
+      const int mt = lw / (cols >> 5), kp = lw - mt * (cols >> 5);
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int pi = 0; pi < 4; ++pi) {  // pi = 2 * (ks % 2) + kh
+          const int col = 16 * (2 * kp + (pi >> 1)) + 8 * (pi & 1) + 2 * t;
+          const uint32_t two = *reinterpret_cast<const uint16_t*>(tile + (16 * mt + 8 * hr + g) * pitch + col);
+          const int b = hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0);
+          word |= __byte_perm(two, 0u, 0x7170) << b;  // bytes 0, 1 -> bits 0 and 16
+        }
+    } else {
+      const int mt = lw / (cols >> 4), ks = lw - mt * (cols >> 4);
+#pragma unroll
+      for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+        for (int kh = 0; kh < 2; ++kh) {
+          const int col = 16 * ks + 8 * kh + 2 * t;
+          const uint32_t two = *reinterpret_cast<const uint16_t*>(tile + (16 * mt + 8 * hr + g) * pitch + col);
+          word |= __byte_perm(two, 0u, 0x7170) << (8 * kh + 4 * hr);
+        }
+    }
+    return word;
+  };
   {
     constexpr int per = 32 / BK;
     const int kw = D * BK / 32;
     uint32_t* kc = reinterpret_cast<uint32_t*>(blk);
     for (int w = tid; w < G * kw; w += blockDim.x) {
       if (q.g.frag_k) {
-        kc[w] = pack_word<BK>(kcode + w * per);
+        kc[w] = frag_word(kcode, KP, D, BK, w);
       } else {
         const int j = w / kw;
         kc[w] = pack_word<BK>(kcode + j * KP + (w - j * kw) * per);
@@ -227,7 +251,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
     const int words = (G / 32) * D * BV;
     for (int w = tid; w < words; w += blockDim.x) {
       if (q.g.frag_v) {
-        vc[w] = pack_word<BV>(vcode + w * per);
+        vc[w] = frag_word(vcode, VP, 32, BV, w);
       } else {
         const int c = w / (D * BV);
         const int rem = w - c * (D * BV);

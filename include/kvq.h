@@ -74,17 +74,18 @@
  *       c = j/32; inside a chunk, channel-major: channel d owns bv words at
  *       word offset (c*D + d)*bv; token j sits in word (j%32)/(32/bv) of them
  *       at bit ((j%32) % (32/bv))*bv.
- *     Fragment (the operand order of the decode kernel's fp8 tensor-core
+ *     Fragment (the operand order of the decode kernel's fp16 tensor-core
  *       tiles, so that each warp lane turns its own words into operand
  *       registers with masks alone).  The side's codes of a block form a tile
  *       of rows x cols codes: K rows = the 32 tokens, cols = the D channels;
  *       V rows = the D channels, cols = the 32 tokens.  Write
- *         row = 16*mt + 8*hr + g          (g < 8, hr < 2)
- *         col = 32*s + 16*hc + 4*t + j    (t < 4, j < 4, hc < 2)
+ *         row = 16*mt + 8*hr + g            (g < 8, hr < 2)
+ *         col = 16*ks + 8*kh + 2*t + e      (t < 4, e < 2, kh < 2)
  *       The code belongs to lane l = 4*g + t, in that lane's word
- *         w = mt*(cols/32) + s            at bit 8*j + 4*hr + 2*hc  (2 bits)
- *         w = 2*(mt*(cols/32) + s) + hc   at bit 8*j + 4*hr         (4 bits)
- *       and word w of lane l is word ((w/4)*32 + l)*4 + w%4 of the region.
+ *         w = mt*(cols/32) + ks/2  at bit 16*e + F2[hr][2*(ks%2) + kh]  (2 bits)
+ *         w = mt*(cols/16) + ks    at bit 16*e + 8*kh + 4*hr            (4 bits)
+ *       with F2[0] = {0, 10, 12, 14}, F2[1] = {2, 4, 6, 8}; word w of lane l
+ *       is word ((w/4)*32 + l)*4 + w%4 of the region.
  *
  *   The tail is fp16 [P][G][D] for K and for V; tokens [T_q, T_q + T_tail) of
  *   every pair sit in rows [0, T_tail).

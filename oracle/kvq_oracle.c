@@ -205,24 +205,26 @@ int kvo_code_order(int D, int G, int bits, int ak, int av) {
 /* Fragment order of one 32-token code region, seen as a tile of rows x cols
  * codes (keys: rows = the 32 tokens, cols = the D channels; values: rows =
  * the D channels, cols = the 32 tokens).  With
- *   row = 16*mt + 8*hr + g      (g < 8, hr < 2)
- *   col = 32*s + 16*hc + 4*t + j  (t < 4, j < 4, hc < 2)
+ *   row = 16*mt + 8*hr + g            (g < 8, hr < 2)
+ *   col = 16*ks + 8*kh + 2*t + e      (t < 4, e < 2, kh < 2)
  * the code belongs to lane l = 4*g + t, in that lane's word
- *   w = mt*(cols/32) + s             at bit 8*j + 4*hr + 2*hc  (2 bits)
- *   w = 2*(mt*(cols/32) + s) + hc    at bit 8*j + 4*hr         (4 bits)
- * and word w of lane l is word ((w/4)*32 + l)*4 + w%4 of the region. */
+ *   w = mt*(cols/32) + ks/2   at bit 16*e + F2[hr][2*(ks%2) + kh]   (2 bits)
+ *   w = mt*(cols/16) + ks     at bit 16*e + 8*kh + 4*hr             (4 bits)
+ * with F2[0] = {0, 10, 12, 14} and F2[1] = {2, 4, 6, 8}, and word w of lane
+ * l is word ((w/4)*32 + l)*4 + w%4 of the region. */
 static void frag_position(int row, int col, int cols, int bits, size_t* word,
                           int* bit) {
+  static const int F2[2][4] = {{0, 10, 12, 14}, {2, 4, 6, 8}};
   int mt = row / 16, hr = (row % 16) / 8, g = row % 8;
-  int s = col / 32, hc = (col % 32) / 16, t = (col % 16) / 4, j = col % 4;
+  int ks = col / 16, kh = (col % 16) / 8, t = (col % 8) / 2, e = col % 2;
   int lane = 4 * g + t;
   int w;
   if (bits == 2) {
-    w = mt * (cols / 32) + s;
-    *bit = 8 * j + 4 * hr + 2 * hc;
+    w = mt * (cols / 32) + ks / 2;
+    *bit = 16 * e + F2[hr][2 * (ks % 2) + kh];
   } else {
-    w = 2 * (mt * (cols / 32) + s) + hc;
-    *bit = 8 * j + 4 * hr;
+    w = mt * (cols / 16) + ks;
+    *bit = 16 * e + 8 * kh + 4 * hr;
   }
   *word = ((size_t)(w / 4) * 32 + (size_t)lane) * 4 + (size_t)(w % 4);
 }

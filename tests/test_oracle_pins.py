@@ -266,9 +266,12 @@ def test_block_bytes_by_hand(oracle_mod):
 
 
 def test_fragment_block_by_hand(oracle_mod):
-    """A whole 32-token block (D = 64) in fragment order: byte j of every word
-    holds the four codes whose column offset (channel for keys, token for
-    values) is j mod 4."""
+    """A whole 32-token block (D = 64) in fragment order, worked by hand from
+    the definition.  Keys (2 bits), code d % 4: column 16 ks + 8 kh + 2 t + e
+    has d % 4 = 2 (t % 2) + e, so the low half (e = 0) of every word of lane
+    l holds eight codes 2 (l % 2) and the high half eight codes 2 (l % 2) + 1.
+    Values (4 bits), code (token % 4) + 4 (channel % 2): token % 4 = 2 (t % 2)
+    + e and channel % 2 = g % 2, the same in all four nibbles of a half."""
     D, G = 64, 32
     t = np.arange(G)[:, None]
     d = np.arange(D)[None, :]
@@ -279,16 +282,13 @@ def test_fragment_block_by_hand(oracle_mod):
               vscale=np.zeros((G, D // G), np.uint16), vzero=np.zeros((G, D // G), np.uint16))
     off = oracle_mod.block_offsets(D, G, 2, 4)
     blk = bytes(oracle_mod.pack_pair(st)[0])
-    # keys, 2 bits: byte j = j * (1 + 4 + 16 + 64)
-    assert blk[off[0]:off[1]] == bytes([0x00, 0x55, 0xAA, 0xFF]) * (G * D * 2 // 32)
-    # values, 4 bits: byte j holds rows g (bits 0-3) and g + 8 (bits 4-7) of
-    # one channel parity (g and g + 8 share it): code j + 4 * (g % 2) twice
-    lanes = np.frombuffer(blk[off[2]:off[3]], np.uint8).reshape(-1, 32, 4, 4)  # [w/4][lane][w%4][byte]
+    kw = np.frombuffer(blk[off[0]:off[1]], "<u4").reshape(-1, 32, 4)  # [w/4][lane][w%4]
+    vw = np.frombuffer(blk[off[2]:off[3]], "<u4").reshape(-1, 32, 4)
     for lane in range(32):
-        g = lane // 4
-        for j in range(4):
-            c = j + 4 * (g % 2)
-            assert np.all(lanes[:, lane, :, j] == c | (c << 4))
+        g, tt = lane // 4, lane % 4
+        assert np.all(kw[:, lane, :] == (0x55550000 if tt % 2 == 0 else 0xFFFFAAAA))
+        v0 = 2 * (tt % 2) + 4 * (g % 2)
+        assert np.all(vw[:, lane, :] == ((v0 + 1) * 0x1111) << 16 | v0 * 0x1111)
 
 
 @pytest.mark.parametrize("bk,bv,ak,av,G,D", [(2, 2, 0, 1, 32, 128), (4, 8, 1, 0, 128, 128),
