@@ -150,10 +150,13 @@ struct MmaCfg {
   static constexpr int NS = ROPE ? 2 : (STAGE <= 4096 ? 3 : 2);
   static constexpr int TCH = mma_tail_chunk(BK, BV);
   static constexpr int OFF_BAR = NS * STAGE;
-  static constexpr int OFF_KB = OFF_BAR + 64;                       // [KS][NT][32] uint2
-  static constexpr int KB_BYTES = ROPE ? 0 : KS * NT * 32 * 8;
-  static constexpr int OFF_VB = OFF_KB + KB_BYTES;                  // [NG][2][NT][32] uint2
-  static constexpr int VB_BYTES = NG * 2 * NT * 32 * 8;
+  // B-operand blocks hold only the lanes whose columns exist: BL lanes
+  // (columns < 2R of a single n-tile live in lanes < 8R).
+  static constexpr int BL = NT == 1 ? (8 * R < 32 ? 8 * R : 32) : 32;
+  static constexpr int OFF_KB = OFF_BAR + 64;                       // [KS][NT][BL] uint2
+  static constexpr int KB_BYTES = ROPE ? 0 : KS * NT * BL * 8;
+  static constexpr int OFF_VB = OFF_KB + KB_BYTES;                  // [NG][2][NT][BL] uint2
+  static constexpr int VB_BYTES = NG * 2 * NT * BL * 8;
   static constexpr int OFF_PB = OFF_VB + VB_BYTES;                  // [R][32] float
   static constexpr int OFF_OS = OFF_PB + R * 32 * 4;                // [R][D] float
   // RoPE: per-warp key coefficients [R][D/2][8] floats; per-CTA table of
@@ -167,12 +170,20 @@ struct MmaCfg {
   static_assert(!VFRAG || VWL % 4 == 0, "lane words are read as 16-byte vectors");
 };
 
+// uint2 slot of lane l in B-operand block blk (BL lanes per block): XOR-swizzled
+// so that the lanes storing one column set into several blocks at once hit
+// distinct banks.
+template <int BL>
+__device__ __forceinline__ int bslot(int blk, int l) {
+  return blk * BL + (l ^ (BL == 8 ? 4 * ((blk >> 1) & 1) : 4 * (blk & 3)));
+}
+
 template <int D, int BK, int BV, int R, bool ROPE>
 __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (R <= 4 ? 3 : 1))
     decode_mma_kernel(const DecodeParams p) {
   using C = MmaCfg<D, BK, BV, R, ROPE>;
   constexpr int NS = C::NS, NT = C::NT, NG = C::NG, MTV = C::MTV, CPL = C::CPL, TCH = C::TCH,
-                STAGE = C::STAGE, KS = C::KS;
+                STAGE = C::STAGE, KS = C::KS, BL = C::BL;
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
@@ -202,7 +213,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   float* pb = reinterpret_cast<float*>(ws + C::OFF_PB);
   float* os = reinterpret_cast<float*>(ws + C::OFF_OS);
 
-  // Operand buffers: columns >= 2R are never written and stay zero.
+  // Operand buffers (every entry is rewritten each sub-block; lanes >= BL
+  // read zero columns without touching memory).
   for (int i = lane; i < (C::OFF_PB - C::OFF_KB) / 4; i += 32) kb32[i] = 0u;
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
@@ -470,9 +482,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           const float2 hf = __half22float2(hi);
           const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
           const int n0 = 2 * r, n1 = 2 * r + 1;
-          kb32[((ks * NT + (n0 >> 3)) * 32 + (n0 & 7) * 4 + slot_t) * 2 + rg] =
+          kb32[bslot<BL>(ks * NT + (n0 >> 3), (n0 & 7) * 4 + slot_t) * 2 + rg] =
               *reinterpret_cast<const uint32_t*>(&hi);
-          kb32[((ks * NT + (n1 >> 3)) * 32 + (n1 & 7) * 4 + slot_t) * 2 + rg] =
+          kb32[bslot<BL>(ks * NT + (n1 >> 3), (n1 & 7) * 4 + slot_t) * 2 + rg] =
               *reinterpret_cast<const uint32_t*>(&lo);
         }
       }
@@ -504,7 +516,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
             else frag_a4(kw[mt * KS + ks], a0, a1, a2, a3);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const uint2 b = kbv[(ks * NT + nt) * 32 + lane];
+              const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
               mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
             }
           }
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
             Frag8::get(r1 + ks * 4, t, a1, a3);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              const uint2 b = kbv[(ks * NT + nt) * 32 + lane];
+              const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
               mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
             }
           }
@@ -630,9 +642,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
             const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
             corr[r][i] += zz[r][i];
             const int n0 = 2 * r, n1 = 2 * r + 1;
-            vb32[(((gp * 2 + ks) * NT + (n0 >> 3)) * 32 + (n0 & 7) * 4 + slot_t) * 2 + rg] =
+            vb32[bslot<BL>((gp * 2 + ks) * NT + (n0 >> 3), (n0 & 7) * 4 + slot_t) * 2 + rg] =
                 *reinterpret_cast<const uint32_t*>(&hi);
-            vb32[(((gp * 2 + ks) * NT + (n1 >> 3)) * 32 + (n1 & 7) * 4 + slot_t) * 2 + rg] =
+            vb32[bslot<BL>((gp * 2 + ks) * NT + (n1 >> 3), (n1 & 7) * 4 + slot_t) * 2 + rg] =
                 *reinterpret_cast<const uint32_t*>(&lo);
           }
         }
@@ -658,7 +670,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           else frag_a4(vw[2 * mt + ks], a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = vbv[((gp * 2 + ks) * NT + nt) * 32 + lane];
+            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
             mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -676,7 +688,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           Frag8::get(c1 + ks * 4, t, a1, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = vbv[((gp * 2 + ks) * NT + nt) * 32 + lane];
+            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
             mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
