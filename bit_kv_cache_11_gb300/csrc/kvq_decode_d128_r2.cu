@@ -1,14 +1,12 @@
-// Decode kernels for head_dim 128, 2 query head(s) per kv head: the
-// general CUDA-core kernel for every (bits_k, bits_v) pair and the tensor-core
-// kernel for the pages' geometry (with a rotated-key variant for keys stored
-// before RoPE where instantiated).  One translation unit per (D, R) so the
+// Decode kernels for head_dim 128, 2 query heads per kv head: the general CUDA-core
+// kernel for every (bits_k, bits_v) pair and the tensor-core kernel for the
+// pages' geometry (keys stored after RoPE; the rotated-key variant is in
+// kvq_decode_rope_d128_r2.cu).  One translation unit per (D, R) so the
 // library compiles in parallel.
 #include "kvq_decode.cuh"
 #include "kvq_decode_mma.cuh"
 
 namespace kvq {
 DecodeOps decode_ops_d128_r2(int bk, int bv) { return decode_ops_for<128, 2>(bk, bv); }
-DecodeOps decode_mma_ops_d128_r2(int bk, int bv, bool rope) {
-  return rope ? DecodeOps{nullptr, nullptr} : decode_mma_ops_for<128, 2, false>(bk, bv);
-}
+DecodeOps decode_mma_ops_d128_r2(int bk, int bv) { return decode_mma_ops_for<128, 2, false>(bk, bv); }
 }  // namespace kvq

@@ -992,8 +992,8 @@ DecodeOps decode_mma_ops_for(int bk, int bv) {
   return DecodeOps{nullptr, nullptr};
 }
 
-// Defined in the per-(D, R) translation units; {nullptr, nullptr} when no
-// tensor-core instantiation exists for (bk, bv, rope).
+// Dispatch over the per-(D, R) translation units (kvq_merge.cu);
+// {nullptr, nullptr} when no tensor-core instantiation exists.
 DecodeOps decode_mma_ops(int D, int R, int bk, int bv, bool rope);
 
 }  // namespace kvq

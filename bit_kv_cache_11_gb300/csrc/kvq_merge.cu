@@ -18,26 +18,34 @@ DecodeOps decode_ops_d128_r2(int, int);
 DecodeOps decode_ops_d128_r4(int, int);
 DecodeOps decode_ops_d128_r8(int, int);
 
-DecodeOps decode_mma_ops_d64_r1(int, int, bool);
-DecodeOps decode_mma_ops_d64_r2(int, int, bool);
-DecodeOps decode_mma_ops_d64_r4(int, int, bool);
-DecodeOps decode_mma_ops_d64_r8(int, int, bool);
-DecodeOps decode_mma_ops_d128_r1(int, int, bool);
-DecodeOps decode_mma_ops_d128_r2(int, int, bool);
-DecodeOps decode_mma_ops_d128_r4(int, int, bool);
-DecodeOps decode_mma_ops_d128_r8(int, int, bool);
+DecodeOps decode_mma_ops_d64_r1(int, int);
+DecodeOps decode_mma_ops_d64_r2(int, int);
+DecodeOps decode_mma_ops_d64_r4(int, int);
+DecodeOps decode_mma_ops_d64_r8(int, int);
+DecodeOps decode_mma_ops_d128_r1(int, int);
+DecodeOps decode_mma_ops_d128_r2(int, int);
+DecodeOps decode_mma_ops_d128_r4(int, int);
+DecodeOps decode_mma_ops_d128_r8(int, int);
+DecodeOps decode_mma_rope_ops_d64_r1(int, int);
+DecodeOps decode_mma_rope_ops_d64_r2(int, int);
+DecodeOps decode_mma_rope_ops_d64_r4(int, int);
+DecodeOps decode_mma_rope_ops_d64_r8(int, int);
+DecodeOps decode_mma_rope_ops_d128_r1(int, int);
+DecodeOps decode_mma_rope_ops_d128_r2(int, int);
+DecodeOps decode_mma_rope_ops_d128_r4(int, int);
+DecodeOps decode_mma_rope_ops_d128_r8(int, int);
 
 DecodeOps decode_mma_ops(int D, int R, int bk, int bv, bool rope) {
   if (D == 64) {
-    if (R == 1) return decode_mma_ops_d64_r1(bk, bv, rope);
-    if (R == 2) return decode_mma_ops_d64_r2(bk, bv, rope);
-    if (R == 4) return decode_mma_ops_d64_r4(bk, bv, rope);
-    if (R == 8) return decode_mma_ops_d64_r8(bk, bv, rope);
+    if (R == 1) return rope ? decode_mma_rope_ops_d64_r1(bk, bv) : decode_mma_ops_d64_r1(bk, bv);
+    if (R == 2) return rope ? decode_mma_rope_ops_d64_r2(bk, bv) : decode_mma_ops_d64_r2(bk, bv);
+    if (R == 4) return rope ? decode_mma_rope_ops_d64_r4(bk, bv) : decode_mma_ops_d64_r4(bk, bv);
+    if (R == 8) return rope ? decode_mma_rope_ops_d64_r8(bk, bv) : decode_mma_ops_d64_r8(bk, bv);
   } else if (D == 128) {
-    if (R == 1) return decode_mma_ops_d128_r1(bk, bv, rope);
-    if (R == 2) return decode_mma_ops_d128_r2(bk, bv, rope);
-    if (R == 4) return decode_mma_ops_d128_r4(bk, bv, rope);
-    if (R == 8) return decode_mma_ops_d128_r8(bk, bv, rope);
+    if (R == 1) return rope ? decode_mma_rope_ops_d128_r1(bk, bv) : decode_mma_ops_d128_r1(bk, bv);
+    if (R == 2) return rope ? decode_mma_rope_ops_d128_r2(bk, bv) : decode_mma_ops_d128_r2(bk, bv);
+    if (R == 4) return rope ? decode_mma_rope_ops_d128_r4(bk, bv) : decode_mma_ops_d128_r4(bk, bv);
+    if (R == 8) return rope ? decode_mma_rope_ops_d128_r8(bk, bv) : decode_mma_ops_d128_r8(bk, bv);
   }
   return DecodeOps{nullptr, nullptr};
 }

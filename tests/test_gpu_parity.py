@@ -113,6 +113,18 @@ SMALL = [
     ("tail-only", 128, 1, 2, 2, 0, 1, 32, False, 17),
     ("no-tail", 128, 4, 4, 4, 0, 1, 32, False, 96),
     ("single-token-rope", 64, 1, 8, 8, 0, 1, 32, True, 1),
+    # tensor-core kernel (keys per channel, values per token, G = 32): every
+    # bit-width pair, every GQA ratio, both head dims, keys before RoPE
+    ("mma-2/4-d128-r2", 128, 2, 2, 4, 0, 1, 32, False, 3 * 32 + 11),
+    ("mma-4/2-d64-r8", 64, 8, 4, 2, 0, 1, 32, False, 5 * 32 + 30),
+    ("mma-2/8-d128-r4-rope", 128, 4, 2, 8, 0, 1, 32, True, 2 * 32 + 7),
+    ("mma-8/2-d64-r1", 64, 1, 8, 2, 0, 1, 32, False, 6 * 32 + 1),
+    ("mma-4/8-d128-r8", 128, 8, 4, 8, 0, 1, 32, False, 3 * 32 + 20),
+    ("mma-8/4-d128-r1-rope", 128, 1, 8, 4, 0, 1, 32, True, 4 * 32 + 13),
+    ("mma-2/2-d128-r8", 128, 8, 2, 2, 0, 1, 32, False, 4 * 32 + 31),
+    ("mma-4/4-d64-r2-rope", 64, 2, 4, 4, 0, 1, 32, True, 3 * 32 + 2),
+    ("mma-2/2-d128-r8-rope", 128, 8, 2, 2, 0, 1, 32, True, 2 * 32 + 9),
+    ("mma-4/4-d64-r4", 64, 4, 4, 4, 0, 1, 32, False, 4 * 32),
 ]
 
 
