@@ -344,13 +344,281 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     }
   };
 
-  // One 32-token sub-block (sub-block ju of the pair) in stage `st`.
-  auto process_sub = [&](const uint8_t* st, int ju) {
-    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
-    const __half2* km = reinterpret_cast<const __half2*>(st + C::KC_S);
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + C::KC_S + C::KM_S);
-    const __half2* vm = reinterpret_cast<const __half2*>(st + C::KC_S + C::KM_S + C::VC_S);
 
+  // ---- pieces of a sub-block (keys stored after RoPE), so that the main
+  // loop can put the key mma of one block and the value mma of the previous
+  // block in one basic block (two independent instruction streams).
+  auto k_prep = [&](const uint8_t* st, float (&kz)[R], float& ek2) {
+    const __half2* km = reinterpret_cast<const __half2*>(st + C::KC_S);
+    // ---- key operand: B_K[c][2r+h] = hi/lo of q_r[c] s_c f_c 2^-ek
+    float qh[R][KP][2];
+    float amax = 0.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r) kz[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < KP; ++i) {
+      int ks, rg, slot_t, k0;
+      float f;
+      b_slot<BK>(lane + 32 * i, ks, rg, slot_t, k0, f);
+      const float2 s0 = __half22float2(km[k0]);
+      const float2 s1 = __half22float2(km[k0 + 1]);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        qh[r][i][0] = qreg[r][i][0] * s0.x * f;
+        qh[r][i][1] = qreg[r][i][1] * s1.x * f;
+        kz[r] = fmaf(qreg[r][i][0], s0.y, fmaf(qreg[r][i][1], s1.y, kz[r]));
+        amax = fmaxf(amax, fmaxf(fabsf(qh[r][i][0]), fabsf(qh[r][i][1])));
+      }
+    }
+    amax = warp_max(amax);
+    // |B| < 2^14: one exponent for the sub-block
+    const int ek = min(max(ilog2f(amax) - 13, -120), 120);
+    const float sk = pow2i(-ek);
+    ek2 = pow2i(ek);
+#pragma unroll
+    for (int i = 0; i < KP; ++i) {
+      int ks, rg, slot_t, k0;
+      float f;
+      b_slot<BK>(lane + 32 * i, ks, rg, slot_t, k0, f);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float v0 = qh[r][i][0] * sk, v1 = qh[r][i][1] * sk;
+        const __half2 hi = __floats2half2_rn(v0, v1);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+        const int n0 = 2 * r, n1 = 2 * r + 1;
+        kb32[bslot<BL>(ks * NT + (n0 >> 3), (n0 & 7) * 4 + slot_t) * 2 + rg] =
+            *reinterpret_cast<const uint32_t*>(&hi);
+        kb32[bslot<BL>(ks * NT + (n1 >> 3), (n1 & 7) * 4 + slot_t) * 2 + rg] =
+            *reinterpret_cast<const uint32_t*>(&lo);
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) kz[r] = warp_sum(kz[r]);
+    __syncwarp();
+  };
+
+  auto k_mma = [&](const uint8_t* st, float (&sc)[2][NT][4]) {
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
+    // ---- scores: tokens 16*mt + g (c0,c1) and 16*mt + g + 8 (c2,c3)
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < NT; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sc[a][b][k] = 0.f;
+    if constexpr (C::KFRAG) {
+      uint32_t kw[C::KWL];
+#pragma unroll
+      for (int q = 0; q < C::KWL / 4; ++q) {
+        const uint4 x = reinterpret_cast<const uint4*>(kc)[q * 32 + lane];
+        kw[4 * q] = x.x; kw[4 * q + 1] = x.y; kw[4 * q + 2] = x.z; kw[4 * q + 3] = x.w;
+      }
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          if constexpr (BK == 2) frag_a2(kw[mt * (KS / 2) + (ks >> 1)], ks & 1, a0, a1, a2, a3);
+          else frag_a4(kw[mt * KS + ks], a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
+            mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+          }
+        }
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        const uint32_t* r0 = kc + (16 * mt + g) * C::KWL;
+        const uint32_t* r1 = r0 + 8 * C::KWL;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          Frag8::get(r0 + ks * 4, t, a0, a2);
+          Frag8::get(r1 + ks * 4, t, a1, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
+            mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+          }
+        }
+      }
+    }
+
+  };
+
+  auto softmax_scores = [&](float (&sc)[2][NT][4], const float (&kz)[R], float ek2,
+                            float (&alpha)[R]) {
+    // ---- online softmax (log2 units); lane holds query 4*nt + t
+    float s4[NT][4];
+    float mx[R], mxl[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float z = lane_factor(kz, nt);
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt) {
+        s4[nt][2 * mt] = fmaf(ek2, sc[mt][nt][0] + sc[mt][nt][1], z);
+        s4[nt][2 * mt + 1] = fmaf(ek2 * C::RK, sc[mt][nt][2] + sc[mt][nt][3], z);
+      }
+      float v = fmaxf(fmaxf(s4[nt][0], s4[nt][1]), fmaxf(s4[nt][2], s4[nt][3]));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+      mxl[nt] = v;
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) mx[r] = __shfl_sync(0xffffffffu, mxl[r >> 2], r & 3);
+    float mnew[R];
+    softmax_merge(mx, alpha, mnew);
+    float ps[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float mm = lane_factor(mnew, nt);
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        s4[nt][k] = fast_exp2(s4[nt][k] - mm);
+        sum += s4[nt][k];
+      }
+      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
+      ps[nt] = sum;
+      const int r = 4 * nt + t;
+      if (r < R) {
+        pb[r * 32 + g] = s4[nt][0];
+        pb[r * 32 + g + 8] = s4[nt][1];
+        pb[r * 32 + g + 16] = s4[nt][2];
+        pb[r * 32 + g + 24] = s4[nt][3];
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      l[r] = l[r] * alpha[r] + __shfl_sync(0xffffffffu, ps[r >> 2], r & 3);
+    __syncwarp();
+  };
+
+  auto v_prep = [&](const uint8_t* st, const float (&alpha)[R]) {
+    const __half2* vm = reinterpret_cast<const __half2*>(st + C::KC_S + C::KM_S + C::VC_S);
+    // ---- value operand: items (token pair, group) -> raw p * s * f
+    float raw[R][VJ][2];
+    float zz[R][VJ];
+    float vmax = 0.f;
+#pragma unroll
+    for (int i = 0; i < VJ; ++i) {
+      const int J = lane + 32 * i;
+      const int gp = J >> 4;
+      int ks, rg, slot_t, tau0;
+      float f;
+      b_slot<BV>(J & 15, ks, rg, slot_t, tau0, f);
+      const int tau1 = tau0 + 1;
+      const bool valid = gp < NG;
+      const float2 m0 = valid ? __half22float2(vm[tau0 * NG + gp]) : make_float2(0.f, 0.f);
+      const float2 m1 = valid ? __half22float2(vm[tau1 * NG + gp]) : make_float2(0.f, 0.f);
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float p0 = pb[r * 32 + tau0], p1 = pb[r * 32 + tau1];
+        raw[r][i][0] = p0 * m0.x * f;
+        raw[r][i][1] = p1 * m1.x * f;
+        zz[r][i] = fmaf(p0, m0.y, p1 * m1.y);
+        vmax = fmaxf(vmax, fmaxf(raw[r][i][0], raw[r][i][1]));
+      }
+    }
+    // B_V = raw * 2^-ev must stay below 2^14; a trip (the first sub-block of a
+    // pair, or larger weights/scales later) raises ev and rescales exactly.
+    float fv = 1.f;
+    if (__any_sync(0xffffffffu, vmax * pow2i(min(-ev, 127)) >= 16384.f)) {
+      const float va = warp_max(vmax);
+      const int evn = ilog2f(va) - 13;
+      if (evn > ev) {
+        fv = pow2i(max(ev - evn, -126));
+        ev = evn;
+      }
+    }
+    rescale(alpha, fv);
+    {
+      const float sv = pow2i(min(-ev, 127));
+#pragma unroll
+      for (int i = 0; i < VJ; ++i) {
+        const int J = lane + 32 * i;
+        const int gp = J >> 4;
+        int ks, rg, slot_t, tau0;
+        float f;
+        b_slot<BV>(J & 15, ks, rg, slot_t, tau0, f);
+        if (gp < NG) {
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float v0 = raw[r][i][0] * sv, v1 = raw[r][i][1] * sv;
+            const __half2 hi = __floats2half2_rn(v0, v1);
+            const float2 hf = __half22float2(hi);
+            const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+            corr[r][i] += zz[r][i];
+            const int n0 = 2 * r, n1 = 2 * r + 1;
+            vb32[bslot<BL>((gp * 2 + ks) * NT + (n0 >> 3), (n0 & 7) * 4 + slot_t) * 2 + rg] =
+                *reinterpret_cast<const uint32_t*>(&hi);
+            vb32[bslot<BL>((gp * 2 + ks) * NT + (n1 >> 3), (n1 & 7) * 4 + slot_t) * 2 + rg] =
+                *reinterpret_cast<const uint32_t*>(&lo);
+          }
+        }
+      }
+    }
+    __syncwarp();
+  };
+
+  auto v_mma = [&](const uint8_t* st) {
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + C::KC_S + C::KM_S);
+    // ---- values: O[c][2r+h] += sum_tok A_V[c][tok] * B_V[tok][2r+h]
+    if constexpr (C::VFRAG) {
+      uint32_t vw[C::VWL];
+#pragma unroll
+      for (int q = 0; q < C::VWL / 4; ++q) {
+        const uint4 x = reinterpret_cast<const uint4*>(vc)[q * 32 + lane];
+        vw[4 * q] = x.x; vw[4 * q + 1] = x.y; vw[4 * q + 2] = x.z; vw[4 * q + 3] = x.w;
+      }
+#pragma unroll
+      for (int mt = 0; mt < MTV; ++mt) {
+        const int gp = mt >> 1;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          if constexpr (BV == 2) frag_a2(vw[mt], ks, a0, a1, a2, a3);
+          else frag_a4(vw[2 * mt + ks], a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
+            mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+          }
+        }
+      }
+    } else {
+#pragma unroll
+      for (int mt = 0; mt < MTV; ++mt) {
+        const int gp = mt >> 1;
+        const uint32_t* c0 = vc + (16 * mt + g) * BV;
+        const uint32_t* c1 = c0 + 8 * BV;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          Frag8::get(c0 + ks * 4, t, a0, a2);
+          Frag8::get(c1 + ks * 4, t, a1, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
+            mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+          }
+        }
+      }
+    }
+  };
+
+  // One 32-token sub-block (sub-block ju of the pair) in stage `st`, all parts
+  // in order (keys stored before RoPE; and the pipelined loop's edges).
+  auto process_sub = [&](const uint8_t* st, int ju) {
+    const __half2* km = reinterpret_cast<const __half2*>(st + C::KC_S);
+    const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
+    (void)km;
+    (void)kc;
     float alpha[R];
     if constexpr (ROPE) {
       // ---- rotated keys (CUDA cores).  Sub-block positions p0 + j, p0 = 32*ju:
@@ -445,257 +713,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       }
       __syncwarp();
     } else {
-      // ---- key operand: B_K[c][2r+h] = hi/lo of q_r[c] s_c f_c 2^-ek
-      float qh[R][KP][2];
-      float kz[R];
-      float amax = 0.f;
-#pragma unroll
-      for (int r = 0; r < R; ++r) kz[r] = 0.f;
-#pragma unroll
-      for (int i = 0; i < KP; ++i) {
-        int ks, rg, slot_t, k0;
-        float f;
-        b_slot<BK>(lane + 32 * i, ks, rg, slot_t, k0, f);
-        const float2 s0 = __half22float2(km[k0]);
-        const float2 s1 = __half22float2(km[k0 + 1]);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          qh[r][i][0] = qreg[r][i][0] * s0.x * f;
-          qh[r][i][1] = qreg[r][i][1] * s1.x * f;
-          kz[r] = fmaf(qreg[r][i][0], s0.y, fmaf(qreg[r][i][1], s1.y, kz[r]));
-          amax = fmaxf(amax, fmaxf(fabsf(qh[r][i][0]), fabsf(qh[r][i][1])));
-        }
-      }
-      amax = warp_max(amax);
-      // |B| < 2^14: one exponent for the sub-block
-      const int ek = min(max(ilog2f(amax) - 13, -120), 120);
-      const float sk = pow2i(-ek), ek2 = pow2i(ek);
-#pragma unroll
-      for (int i = 0; i < KP; ++i) {
-        int ks, rg, slot_t, k0;
-        float f;
-        b_slot<BK>(lane + 32 * i, ks, rg, slot_t, k0, f);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float v0 = qh[r][i][0] * sk, v1 = qh[r][i][1] * sk;
-          const __half2 hi = __floats2half2_rn(v0, v1);
-          const float2 hf = __half22float2(hi);
-          const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-          const int n0 = 2 * r, n1 = 2 * r + 1;
-          kb32[bslot<BL>(ks * NT + (n0 >> 3), (n0 & 7) * 4 + slot_t) * 2 + rg] =
-              *reinterpret_cast<const uint32_t*>(&hi);
-          kb32[bslot<BL>(ks * NT + (n1 >> 3), (n1 & 7) * 4 + slot_t) * 2 + rg] =
-              *reinterpret_cast<const uint32_t*>(&lo);
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < R; ++r) kz[r] = warp_sum(kz[r]);
-      __syncwarp();
-
-      // ---- scores: tokens 16*mt + g (c0,c1) and 16*mt + g + 8 (c2,c3)
-      float sc[2][NT][4];
-#pragma unroll
-      for (int a = 0; a < 2; ++a)
-#pragma unroll
-        for (int b = 0; b < NT; ++b)
-#pragma unroll
-          for (int k = 0; k < 4; ++k) sc[a][b][k] = 0.f;
-      if constexpr (C::KFRAG) {
-        uint32_t kw[C::KWL];
-#pragma unroll
-        for (int q = 0; q < C::KWL / 4; ++q) {
-          const uint4 x = reinterpret_cast<const uint4*>(kc)[q * 32 + lane];
-          kw[4 * q] = x.x; kw[4 * q + 1] = x.y; kw[4 * q + 2] = x.z; kw[4 * q + 3] = x.w;
-        }
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            if constexpr (BK == 2) frag_a2(kw[mt * (KS / 2) + (ks >> 1)], ks & 1, a0, a1, a2, a3);
-            else frag_a4(kw[mt * KS + ks], a0, a1, a2, a3);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
-              mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
-            }
-          }
-      } else {
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const uint32_t* r0 = kc + (16 * mt + g) * C::KWL;
-          const uint32_t* r1 = r0 + 8 * C::KWL;
-#pragma unroll
-          for (int ks = 0; ks < KS; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            Frag8::get(r0 + ks * 4, t, a0, a2);
-            Frag8::get(r1 + ks * 4, t, a1, a3);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
-              mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
-            }
-          }
-        }
-      }
-
-      // ---- online softmax (log2 units); lane holds query 4*nt + t
-      float s4[NT][4];
-      float mx[R], mxl[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float z = lane_factor(kz, nt);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          s4[nt][2 * mt] = fmaf(ek2, sc[mt][nt][0] + sc[mt][nt][1], z);
-          s4[nt][2 * mt + 1] = fmaf(ek2 * C::RK, sc[mt][nt][2] + sc[mt][nt][3], z);
-        }
-        float v = fmaxf(fmaxf(s4[nt][0], s4[nt][1]), fmaxf(s4[nt][2], s4[nt][3]));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-        mxl[nt] = v;
-      }
-#pragma unroll
-      for (int r = 0; r < R; ++r) mx[r] = __shfl_sync(0xffffffffu, mxl[r >> 2], r & 3);
-      float mnew[R];
-      softmax_merge(mx, alpha, mnew);
-      float ps[NT];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        const float mm = lane_factor(mnew, nt);
-        float sum = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          s4[nt][k] = fast_exp2(s4[nt][k] - mm);
-          sum += s4[nt][k];
-        }
-        sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-        sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-        ps[nt] = sum;
-        const int r = 4 * nt + t;
-        if (r < R) {
-          pb[r * 32 + g] = s4[nt][0];
-          pb[r * 32 + g + 8] = s4[nt][1];
-          pb[r * 32 + g + 16] = s4[nt][2];
-          pb[r * 32 + g + 24] = s4[nt][3];
-        }
-      }
-#pragma unroll
-      for (int r = 0; r < R; ++r)
-        l[r] = l[r] * alpha[r] + __shfl_sync(0xffffffffu, ps[r >> 2], r & 3);
-      __syncwarp();
+      float kz[R], ek2, sc[2][NT][4];
+      k_prep(st, kz, ek2);
+      k_mma(st, sc);
+      softmax_scores(sc, kz, ek2, alpha);
     }
-
-    // ---- value operand: items (token pair, group) -> raw p * s * f
-    float raw[R][VJ][2];
-    float zz[R][VJ];
-    float vmax = 0.f;
-#pragma unroll
-    for (int i = 0; i < VJ; ++i) {
-      const int J = lane + 32 * i;
-      const int gp = J >> 4;
-      int ks, rg, slot_t, tau0;
-      float f;
-      b_slot<BV>(J & 15, ks, rg, slot_t, tau0, f);
-      const int tau1 = tau0 + 1;
-      const bool valid = gp < NG;
-      const float2 m0 = valid ? __half22float2(vm[tau0 * NG + gp]) : make_float2(0.f, 0.f);
-      const float2 m1 = valid ? __half22float2(vm[tau1 * NG + gp]) : make_float2(0.f, 0.f);
-#pragma unroll
-      for (int r = 0; r < R; ++r) {
-        const float p0 = pb[r * 32 + tau0], p1 = pb[r * 32 + tau1];
-        raw[r][i][0] = p0 * m0.x * f;
-        raw[r][i][1] = p1 * m1.x * f;
-        zz[r][i] = fmaf(p0, m0.y, p1 * m1.y);
-        vmax = fmaxf(vmax, fmaxf(raw[r][i][0], raw[r][i][1]));
-      }
-    }
-    // B_V = raw * 2^-ev must stay below 2^14; a trip (the first sub-block of a
-    // pair, or larger weights/scales later) raises ev and rescales exactly.
-    float fv = 1.f;
-    if (__any_sync(0xffffffffu, vmax * pow2i(min(-ev, 127)) >= 16384.f)) {
-      const float va = warp_max(vmax);
-      const int evn = ilog2f(va) - 13;
-      if (evn > ev) {
-        fv = pow2i(max(ev - evn, -126));
-        ev = evn;
-      }
-    }
-    rescale(alpha, fv);
-    {
-      const float sv = pow2i(min(-ev, 127));
-#pragma unroll
-      for (int i = 0; i < VJ; ++i) {
-        const int J = lane + 32 * i;
-        const int gp = J >> 4;
-        int ks, rg, slot_t, tau0;
-        float f;
-        b_slot<BV>(J & 15, ks, rg, slot_t, tau0, f);
-        if (gp < NG) {
-#pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const float v0 = raw[r][i][0] * sv, v1 = raw[r][i][1] * sv;
-            const __half2 hi = __floats2half2_rn(v0, v1);
-            const float2 hf = __half22float2(hi);
-            const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-            corr[r][i] += zz[r][i];
-            const int n0 = 2 * r, n1 = 2 * r + 1;
-            vb32[bslot<BL>((gp * 2 + ks) * NT + (n0 >> 3), (n0 & 7) * 4 + slot_t) * 2 + rg] =
-                *reinterpret_cast<const uint32_t*>(&hi);
-            vb32[bslot<BL>((gp * 2 + ks) * NT + (n1 >> 3), (n1 & 7) * 4 + slot_t) * 2 + rg] =
-                *reinterpret_cast<const uint32_t*>(&lo);
-          }
-        }
-      }
-    }
-    __syncwarp();
-
-    // ---- values: O[c][2r+h] += sum_tok A_V[c][tok] * B_V[tok][2r+h]
-    if constexpr (C::VFRAG) {
-      uint32_t vw[C::VWL];
-#pragma unroll
-      for (int q = 0; q < C::VWL / 4; ++q) {
-        const uint4 x = reinterpret_cast<const uint4*>(vc)[q * 32 + lane];
-        vw[4 * q] = x.x; vw[4 * q + 1] = x.y; vw[4 * q + 2] = x.z; vw[4 * q + 3] = x.w;
-      }
-#pragma unroll
-      for (int mt = 0; mt < MTV; ++mt) {
-        const int gp = mt >> 1;
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          if constexpr (BV == 2) frag_a2(vw[mt], ks, a0, a1, a2, a3);
-          else frag_a4(vw[2 * mt + ks], a0, a1, a2, a3);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
-            mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int mt = 0; mt < MTV; ++mt) {
-        const int gp = mt >> 1;
-        const uint32_t* c0 = vc + (16 * mt + g) * BV;
-        const uint32_t* c1 = c0 + 8 * BV;
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          Frag8::get(c0 + ks * 4, t, a0, a2);
-          Frag8::get(c1 + ks * 4, t, a1, a3);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
-            mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
-          }
-        }
-      }
-    }
+    v_prep(st, alpha);
+    v_mma(st);
     __syncwarp();
   };
+
 
   // fp16 tail chunk k of the pair (tokens [k*TCH, min(T_t, (k+1)*TCH)), its K
   // rows then its V rows in the stage).  Lane l holds channels
@@ -924,8 +951,25 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   int j = ua - pr * upp;
   int s = 0;
   uint32_t ph = 0u;
+  // the next unit to load goes into `stage` (lane 0 issues the copy)
+  auto refill = [&](int stage) {
+    if (lu < ub) {
+      if (lane == 0) issue(stage);
+      advance_load();
+    }
+  };
+  // stage of the previous sub-block when its value mma is still pending
+  int pend = -1;
   for (int u = ua; u < ub; ++u) {
     if (pr != cur) {
+      if constexpr (!ROPE) {
+        if (pend >= 0) {
+          v_mma(ws + pend * STAGE);
+          __syncwarp();
+          refill(pend);
+          pend = -1;
+        }
+      }
       if (cur >= 0) write_partial(cur);
       enter_pair(pr);
       cur = pr;
@@ -939,13 +983,41 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       return;
     }
     const uint8_t* st = ws + s * STAGE;
-    if (j < nsub)
-      process_sub(st, j);
-    else
-      process_tail_chunk(st, j - nsub);
-    if (lu < ub) {
-      if (lane == 0) issue(s);
-      advance_load();
+    if constexpr (ROPE) {
+      if (j < nsub)
+        process_sub(st, j);
+      else
+        process_tail_chunk(st, j - nsub);
+      refill(s);
+    } else {
+      if (j < nsub) {
+        // keys of this block, then its key mma beside the value mma of the
+        // previous block (independent), then softmax and this block's value
+        // operand; its value mma waits for the next iteration
+        float kz[R], ek2, alpha[R], sc[2][NT][4];
+        k_prep(st, kz, ek2);
+        if (pend >= 0) {
+          k_mma(st, sc);
+          v_mma(ws + pend * STAGE);
+          __syncwarp();
+          refill(pend);
+        } else {
+          k_mma(st, sc);
+          __syncwarp();
+        }
+        softmax_scores(sc, kz, ek2, alpha);
+        v_prep(st, alpha);
+        pend = s;
+      } else {
+        if (pend >= 0) {
+          v_mma(ws + pend * STAGE);
+          __syncwarp();
+          refill(pend);
+          pend = -1;
+        }
+        process_tail_chunk(st, j - nsub);
+        refill(s);
+      }
     }
     if (++s == NS) {
       s = 0;
@@ -954,6 +1026,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     if (++j == upp) {
       j = 0;
       ++pr;
+    }
+  }
+  if constexpr (!ROPE) {
+    if (pend >= 0) {
+      v_mma(ws + pend * STAGE);
+      __syncwarp();
     }
   }
   if (cur >= 0) write_partial(cur);
