@@ -349,19 +349,17 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, int n, void* s
   return enqueue_append(c, k, v, n, static_cast<cudaStream_t>(stream));
 }
 
-kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float softmax_scale,
-                                void* stream) {
-  if (c == nullptr || q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out))
-    return KVQ_ERR_INVALID_ARG;
-  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
-  DeviceGuard g(c->device);
-  if (!g.ok) return KVQ_ERR_CUDA;
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+// Enqueues the decode of the cache's tokens plus, when n_new > 0 (tensor-core
+// kernel only, no flush), the n_new tokens of knew/vnew, which the same launch
+// also stores into the tail.  The caller updates the lengths.
+static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float softmax_scale,
+                                 cudaStream_t st, const void* knew, const void* vnew, int n_new) {
   const Derived& d = c->dv;
+  const int T_t = c->T_t + n_new;
   const int nsub = c->T_q / 32;
-  const int upp = nsub + tail_units(c->mma, c->T_t, c->cfg.bits_k, c->cfg.bits_v);
+  const int upp = nsub + tail_units(c->mma, T_t, c->cfg.bits_k, c->cfg.bits_v);
   const long long U = static_cast<long long>(d.P) * upp;
-  if (U == 0) {
+  if (U == 0) {  // an empty cache (n_new is 0 here)
     if (cudaMemsetAsync(out, 0, static_cast<size_t>(d.P) * d.R * d.D * sizeof(float), st) !=
         cudaSuccess)
       return KVQ_ERR_CUDA;
@@ -376,7 +374,12 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float so
   p.ktail = c->ktail[c->active];
   p.vtail = c->vtail[c->active];
   p.T_q = c->T_q;
-  p.T_t = c->T_t;
+  p.T_t = T_t;
+  p.t_old = c->T_t;
+  p.knew = static_cast<const __half*>(knew);
+  p.vnew = static_cast<const __half*>(vnew);
+  p.ktail_w = c->ktail[c->active];
+  p.vtail_w = c->vtail[c->active];
   p.lg_G = d.G == 32 ? 5 : (d.G == 64 ? 6 : 7);
   p.lg_sub = p.lg_G - 5;
   p.nsub = nsub;
@@ -418,6 +421,42 @@ kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float so
   if (launch_merge2(mp, d.P, st) != cudaSuccess) return KVQ_ERR_CUDA;
   g_launches.fetch_add(2);
   return KVQ_OK;
+}
+
+kvq_status kvq_decode_attention(kvq_cache* c, const void* q, void* out, float softmax_scale,
+                                void* stream) {
+  if (c == nullptr || q == nullptr || out == nullptr || !aligned16(q) || !aligned16(out))
+    return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  return enqueue_decode(c, q, out, softmax_scale, static_cast<cudaStream_t>(stream), nullptr,
+                        nullptr, 0);
+}
+
+kvq_status kvq_append_decode(kvq_cache* c, const void* k, const void* v, int n, const void* q,
+                             void* out, float softmax_scale, void* stream) {
+  if (c == nullptr || n < 0 || q == nullptr || out == nullptr || !aligned16(q) ||
+      !aligned16(out))
+    return KVQ_ERR_INVALID_ARG;
+  if (n > 0 && (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)))
+    return KVQ_ERR_INVALID_ARG;
+  if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(c->T_q) + c->T_t + n > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n > 0 && c->mma && c->T_t + n < c->dv.G) {
+    // one launch: the new tokens stay in the tail, no block is flushed
+    const kvq_status s = enqueue_decode(c, q, out, softmax_scale, st, k, v, n);
+    if (s == KVQ_OK) c->T_t += n;
+    return s;
+  }
+  if (n > 0) {
+    const kvq_status s = enqueue_append(c, k, v, n, st);
+    if (s != KVQ_OK) return s;
+  }
+  return enqueue_decode(c, q, out, softmax_scale, st, nullptr, nullptr, 0);
 }
 
 kvq_status kvq_dequantize(kvq_cache* c, void* k_out, void* v_out, void* stream) {

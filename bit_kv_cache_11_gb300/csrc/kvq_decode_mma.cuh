@@ -202,6 +202,24 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     }
     __syncthreads();
   }
+  // Fused append: store the new tokens into the tail for later calls (no
+  // access of this launch reads those tail rows).
+  if (p.T_t > p.t_old) {
+    const int n_new = p.T_t - p.t_old;
+    const long long chunks = static_cast<long long>(p.g.P) * n_new * (D / 8);
+    for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+         c += static_cast<long long>(gridDim.x) * blockDim.x) {
+      const long long rowi = c / (D / 8);
+      const int col = static_cast<int>(c - rowi * (D / 8)) * 8;
+      const long long pr = rowi / n_new;
+      const int r = static_cast<int>(rowi - pr * n_new);
+      const size_t dst = (static_cast<size_t>(pr) * C::G + p.t_old + r) * D + col;
+      *reinterpret_cast<uint4*>(p.ktail_w + dst) =
+          *reinterpret_cast<const uint4*>(p.knew + rowi * D + col);
+      *reinterpret_cast<uint4*>(p.vtail_w + dst) =
+          *reinterpret_cast<const uint4*>(p.vnew + rowi * D + col);
+    }
+  }
   if (gw >= p.n_warps) return;
 
   uint8_t* ws = smem + warp * C::WARP_BYTES;
@@ -235,12 +253,25 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       mbar_arrive_expect_tx(&bars[s], STAGE);
       bulk_g2s(st, lbase + static_cast<size_t>(lj) * STAGE, STAGE, &bars[s]);
     } else {
+      // tail rows [t0, t1): those below t_old from the tail buffer, the rest
+      // (tokens appended by this call) from knew / vnew
       const int t0 = (lj - nsub) * TCH;
-      const uint32_t bytes = static_cast<uint32_t>(min(TCH, p.T_t - t0)) * D * 2;
-      const size_t row = static_cast<size_t>(lpr) * C::G + t0;
-      mbar_arrive_expect_tx(&bars[s], 2 * bytes);
-      bulk_g2s(st, p.ktail + row * D, bytes, &bars[s]);
-      bulk_g2s(st + TCH * D * 2, p.vtail + row * D, bytes, &bars[s]);
+      const int t1 = min(t0 + TCH, p.T_t);
+      const int tm = max(t0, min(t1, p.t_old));
+      mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(t1 - t0) * D * 4);
+      if (tm > t0) {
+        const uint32_t bytes = static_cast<uint32_t>(tm - t0) * D * 2;
+        const size_t row = static_cast<size_t>(lpr) * C::G + t0;
+        bulk_g2s(st, p.ktail + row * D, bytes, &bars[s]);
+        bulk_g2s(st + TCH * D * 2, p.vtail + row * D, bytes, &bars[s]);
+      }
+      if (t1 > tm) {
+        const int n_new = p.T_t - p.t_old;
+        const uint32_t bytes = static_cast<uint32_t>(t1 - tm) * D * 2;
+        const size_t row = static_cast<size_t>(lpr) * n_new + (tm - p.t_old);
+        bulk_g2s(st + (tm - t0) * D * 2, p.knew + row * D, bytes, &bars[s]);
+        bulk_g2s(st + (TCH + tm - t0) * D * 2, p.vnew + row * D, bytes, &bars[s]);
+      }
     }
   };
   auto advance_load = [&]() {

@@ -190,6 +190,14 @@ struct DecodeParams {
   const __half* ktail;  // active tail [P][G][D]
   const __half* vtail;
   int T_q, T_t;
+  // Append fused into the decode (tensor-core kernel, no flush): tail rows
+  // [t_old, T_t) are the n_new tokens of knew/vnew ([P][n_new][D]); the
+  // kernel also stores them into rows [t_old, T_t) of the tail (ktail_w).
+  int t_old;            // tail rows already in the buffer (== T_t when not fused)
+  const __half* knew;
+  const __half* vnew;
+  __half* ktail_w;
+  __half* vtail_w;
   int lg_G;             // log2(G)
   int lg_sub;           // log2(G / 32): 32-token sub-blocks per block
   int nsub;             // T_q / 32

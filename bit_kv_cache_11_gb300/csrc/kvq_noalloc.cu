@@ -189,6 +189,11 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.vtail = static_cast<const __half*>(v_tail);
     p.T_q = T_q;
     p.T_t = T_tail;
+    p.t_old = T_tail;
+    p.knew = nullptr;
+    p.vnew = nullptr;
+    p.ktail_w = nullptr;
+    p.vtail_w = nullptr;
     p.lg_G = G == 32 ? 5 : (G == 64 ? 6 : 7);
     p.lg_sub = p.lg_G - 5;
     p.nsub = nsub;

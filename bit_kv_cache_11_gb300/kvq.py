@@ -61,6 +61,7 @@ _sigs = {
     "kvq_quantize_prefill": (_S, [_P, _P, _P, _I, _P]),
     "kvq_append": (_S, [_P, _P, _P, _I, _P]),
     "kvq_decode_attention": (_S, [_P, _P, _P, ctypes.c_float, _P]),
+    "kvq_append_decode": (_S, [_P, _P, _P, _I, _P, _P, ctypes.c_float, _P]),
     "kvq_dequantize": (_S, [_P, _P, _P, _P]),
     "kvq_decode_attention_noalloc": (_S, [_CFG, _P, _P, _P, _I, _I, _P, _P, ctypes.c_float, _P, _P]),
     "kvq_get_state": (_S, [_P, ctypes.POINTER(_I), ctypes.POINTER(_I)]),
@@ -155,6 +156,12 @@ def kvq_decode_attention(handle, q, out, softmax_scale: float, stream=None) -> N
                                      _stream(stream)), "kvq_decode_attention")
 
 
+def kvq_append_decode(handle, k, v, n: int, q, out, softmax_scale: float, stream=None) -> None:
+    _check(_lib.kvq_append_decode(handle, _ptr(k) if n else None, _ptr(v) if n else None, int(n),
+                                  _ptr(q), _ptr(out), float(softmax_scale), _stream(stream)),
+           "kvq_append_decode")
+
+
 def kvq_decode_attention_noalloc(cfg: kvq_config, blocks, k_tail, v_tail, T_q: int, T_tail: int,
                                  q, out, softmax_scale: float, device_error=None,
                                  stream=None) -> None:
@@ -246,6 +253,18 @@ class KVCache:
         if softmax_scale is None:
             softmax_scale = self.cfg.head_dim ** -0.5
         kvq_decode_attention(self.handle, q, out, softmax_scale, stream)
+        return out
+
+    def append_decode(self, k, v, q, out=None, softmax_scale=None, stream=None):
+        """Appends k, v ([batch][n_kv_heads][n][head_dim] fp16) and decodes q,
+        in one launch when no group is completed."""
+        import torch
+        if out is None:
+            out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+        if softmax_scale is None:
+            softmax_scale = self.cfg.head_dim ** -0.5
+        n = 0 if k is None else k.shape[-2]
+        kvq_append_decode(self.handle, k, v, n, q, out, softmax_scale, stream)
         return out
 
     def dequantize(self, stream=None):

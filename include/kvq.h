@@ -199,6 +199,22 @@ KVQ_API kvq_status kvq_decode_attention(kvq_cache* cache, const void* q,
                                         void* out, float softmax_scale,
                                         void* stream);
 
+/* One decode step: kvq_append(cache, k, v, n) then kvq_decode_attention
+ * (cache, q, out), with the same results and errors.  When the appended
+ * tokens do not complete a group (T_tail + n < G) and the cache uses the
+ * tensor-core kernel (keys per channel, values per token, G = 32), both run
+ * as one launch: the decode reads the new tokens straight from k and v and
+ * stores them into the tail.  Otherwise the append (with its flush) and the
+ * decode are enqueued one after the other.  The fp16 tail is the pages'
+ * full-precision residual ("Your KV cache doesn't have a bit problem, it has
+ * a geometry problem", section "The Systems Tax, and Why It Is Not a
+ * Detail").  k, v as for kvq_append (may be NULL when n = 0); q, out as for
+ * kvq_decode_attention. */
+KVQ_API kvq_status kvq_append_decode(kvq_cache* cache, const void* k,
+                                     const void* v, int n, const void* q,
+                                     void* out, float softmax_scale,
+                                     void* stream);
+
 /* Dequantizes the T_q packed tokens of every pair (before any RoPE).
  * k_out, v_out: device fp32 [batch][n_kv_heads][T_q][head_dim]. */
 KVQ_API kvq_status kvq_dequantize(kvq_cache* cache, void* k_out, void* v_out,

@@ -173,6 +173,51 @@ def test_append_flush_sequences(kvq, orc, case, T0, ns):
         cache.check()
 
 
+@pytest.mark.parametrize("case,T0,ns", [
+    (SMALL[0], 3, [1, 1, 5, 20, 2, 1, 1, 33, 1, 60]),
+    (SMALL[2], 30, [1, 1, 1, 29, 1, 2]),
+    (SMALL[1], 0, [1, 31, 1, 1]),
+    (SMALL[3], 10, [1, 20, 1, 9, 1]),
+], ids=["g32-r1", "g32-r4", "d64-from-empty", "rope-4bit"])
+def test_append_decode_steps(kvq, orc, case, T0, ns):
+    """kvq_append_decode (one launch when no group completes) equals
+    kvq_append + kvq_decode_attention on a second cache bit for bit, keeps the
+    same state, and matches the oracle."""
+    name, D, R, bk, bv, ak, av, G, rope, _ = case
+    total = T0 + sum(ns)
+    w = small_workload(D, R, bk, bv, ak, av, G, rope, total)
+    c = synth.make_case(w, seed=91)
+    K, V = c["K"], c["V"]
+    pairs = list(range(w.n_pairs))
+    q = dev(c["q"])
+    with make_cache(kvq, w, max_ctx=total) as fused, make_cache(kvq, w, max_ctx=total) as split:
+        fused.prefill(dev(K[:, :, :T0]), dev(V[:, :, :T0]))
+        split.prefill(dev(K[:, :, :T0]), dev(V[:, :, :T0]))
+        T = T0
+        for n in ns:
+            k, v = dev(K[:, :, T:T + n]), dev(V[:, :, T:T + n])
+            launches = kvq.kvq_launch_count()
+            a = fused.append_decode(k, v, q, softmax_scale=w.scale)
+            torch.cuda.synchronize()
+            if (T - (T // G) * G) + n < G:
+                assert kvq.kvq_launch_count() - launches == 1   # one fused launch
+            split.append(k, v)
+            b = split.decode(q, softmax_scale=w.scale)
+            T += n
+            torch.cuda.synchronize()
+            assert torch.equal(a, b)
+            assert fused.state == split.state
+            check_state(orc, fused, w, K[:, :, :T], V[:, :, :T], pairs)
+            got = a.cpu().numpy().astype(np.float64)
+            for p in pairs:
+                bb, h = divmod(p, w.n_kv_heads)
+                st = orc.build_pair(K[bb, h, :T], V[bb, h, :T], G, bk, bv, ak, av)
+                ref = orc.decode_pair(st, c["q"][bb, h * R:(h + 1) * R], w.scale, rope, w.rope_base)
+                assert np.abs(got[bb, h * R:(h + 1) * R] - ref).max() <= ATOL
+        fused.check()
+        split.check()
+
+
 def test_empty_cache_decodes_to_zero(kvq):
     w = small_workload(128, 4, 2, 2, 0, 1, 32, False, 0)
     with make_cache(kvq, w, max_ctx=64) as cache:
