@@ -190,6 +190,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const long long gw = static_cast<long long>(blockIdx.x) * kDecodeWarps + warp;
+  // Launched as a programmatic dependent: wait until the preceding grid in
+  // the stream has completed (and its writes are visible) before touching
+  // global memory, and let the next grid launch while this one runs.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // RoPE: cos/sin(j * theta_i) for the 32 token offsets of a sub-block (table
   // rows 0..31), transposed so lane j reads its own column conflict-free.
   // Loaded before any warp of the CTA can leave.
@@ -1081,9 +1086,19 @@ cudaError_t decode_mma_prepare(int* ctas_per_sm) {
 template <int D, int BK, int BV, int R, bool ROPE>
 cudaError_t decode_mma_launch(const DecodeParams& p, cudaStream_t stream) {
   using C = MmaCfg<D, BK, BV, R, ROPE>;
-  const int grid = (p.n_warps + kDecodeWarps - 1) / kDecodeWarps;
-  decode_mma_kernel<D, BK, BV, R, ROPE><<<grid, kDecodeWarps * 32, C::SMEM, stream>>>(p);
-  return cudaGetLastError();
+  // programmatic stream serialization: the grid may start while the previous
+  // kernel of the stream finishes; it waits for it before any global access
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((p.n_warps + kDecodeWarps - 1) / kDecodeWarps);
+  cfg.blockDim = dim3(kDecodeWarps * 32);
+  cfg.dynamicSmemBytes = C::SMEM;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BK, BV, R, ROPE>, p);
 }
 
 // Every (bits_k, bits_v) pair of the geometry (G = 32, keys per channel,
