@@ -41,6 +41,18 @@ struct Stat {
   float mn, s, rcp;
 };
 
+// Statistics from the group's minimum and maximum (exact fp16 values).
+__device__ __forceinline__ Stat stat_of(float mn, float mx, int bits, __half2* meta_out) {
+  // (mx - mn) + 0: a range of -0 (min and max zeros of opposite sign) is +0.
+  const float range = __fadd_rn(__fsub_rn(mx, mn), 0.0f);
+  const float step = __fdiv_rn(range, static_cast<float>((1 << bits) - 1));
+  const __half s_h = __float2half_rn(step);
+  const __half z_h = __float2half_rn(__fadd_rn(mn, 0.0f));  // a -0 minimum is stored as +0
+  *meta_out = __halves2half2(s_h, z_h);
+  const float s = __half2float(s_h);
+  return Stat{mn, s, s == 0.0f ? 0.0f : __frcp_rn(s)};
+}
+
 // min/max over n values p[0], p[stride], ... (fp16 read exactly as fp32).
 __device__ __forceinline__ Stat group_stat(const __half* x, int stride, int n, int bits,
                                            __half2* meta_out) {
@@ -51,14 +63,7 @@ __device__ __forceinline__ Stat group_stat(const __half* x, int stride, int n, i
     mn = fminf(mn, v);
     mx = fmaxf(mx, v);
   }
-  // (mx - mn) + 0: a range of -0 (min and max zeros of opposite sign) is +0.
-  const float range = __fadd_rn(__fsub_rn(mx, mn), 0.0f);
-  const float step = __fdiv_rn(range, static_cast<float>((1 << bits) - 1));
-  const __half s_h = __float2half_rn(step);
-  const __half z_h = __float2half_rn(__fadd_rn(mn, 0.0f));  // a -0 minimum is stored as +0
-  *meta_out = __halves2half2(s_h, z_h);
-  const float s = __half2float(s_h);
-  return Stat{mn, s, s == 0.0f ? 0.0f : __frcp_rn(s)};
+  return stat_of(mn, mx, bits, meta_out);
 }
 
 // code = clamp(rintf((x - mn) / s), 0, 2^bits - 1) with the IEEE quotient,
@@ -70,7 +75,7 @@ __device__ __forceinline__ uint32_t code_of(float x, const Stat& st, float top) 
   float r = rintf(__fmul_rn(d, st.rcp));
   const float t = __fsub_rn(__fmul_rn(d, st.rcp), r);
   if (fabsf(t) > 0.5f - 0.000244140625f) r = rintf(__fdiv_rn(d, st.s));
-  r = fminf(fmaxf(r, 0.0f), top);
+  r = fminf(r, top);  // d >= 0 and rcp >= 0, so r >= 0 (+0 when s == 0)
   return __float_as_uint(r + 8388608.0f) & 0xffu;  // exact: r is an integer in [0, 255]
 }
 
@@ -186,14 +191,40 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
         else kcode[j * KP + ee] = c;
       }
     } else {          // token j, channels [g*G, (g+1)*G); consecutive threads: consecutive j
+      // the group's G contiguous values, 16 bytes at a time (row pitch 16 mod
+      // 128 bytes: eight consecutive j cover all banks)
       const int j = ee & (G - 1), g = ee >> lgG;
-      const Stat st = group_stat(X + j * XP + (g << lgG), 1, G, bits,
-                                 (isv ? vmeta : kmeta) + j * ng + g);
-      for (int i = 0; i < G; ++i) {
-        const int d = (g << lgG) + i;
-        const uint8_t c = static_cast<uint8_t>(code_of(__half2float(X[j * XP + d]), st, top));
-        if (isv) vcode[d * VP + j] = c;
-        else kcode[j * KP + d] = c;
+      const __half* row = X + j * XP + (g << lgG);
+      __half2 lo = *reinterpret_cast<const __half2*>(row), hi = lo;
+      for (int i = 0; i < G; i += 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + i);
+        const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          lo = __hmin2(lo, h[k]);
+          hi = __hmax2(hi, h[k]);
+        }
+      }
+      const Stat st = stat_of(fminf(__low2float(lo), __high2float(lo)),
+                              fmaxf(__low2float(hi), __high2float(hi)), bits,
+                              (isv ? vmeta : kmeta) + j * ng + g);
+      for (int i = 0; i < G; i += 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(row + i);
+        const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 f = __half22float2(h[k]);
+          const int d = (g << lgG) + i + 2 * k;
+          const uint8_t c0 = static_cast<uint8_t>(code_of(f.x, st, top));
+          const uint8_t c1 = static_cast<uint8_t>(code_of(f.y, st, top));
+          if (isv) {
+            vcode[d * VP + j] = c0;
+            vcode[(d + 1) * VP + j] = c1;
+          } else {
+            kcode[j * KP + d] = c0;
+            kcode[j * KP + d + 1] = c1;
+          }
+        }
       }
     }
   }
