@@ -42,6 +42,59 @@ def decode_bytes(w, T_q, T_t):
     return codes + meta + tail + qo
 
 
+def windows_leg(w, dev, stream, n_sink, residual, n_layers, warmup, steps):
+    """The same decode step on caches that keep the first n_sink tokens and a
+    window of `residual` recent tokens in fp16 (kvq_append_decode per layer).
+    Algorithmic bytes count the sink rows like tail rows; the single-launch
+    steps are averaged, as for the main line."""
+    import torch
+    from bit_kv_cache_11_gb300 import kvq
+    caches, steps_dev = [], []
+    for layer in range(n_layers):
+        seed = rank_seed(w.config_id, 0, layer) + 7
+        case = synth.make_case(w, seed=seed)
+        c = kvq.KVCache(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
+                        head_dim=w.head_dim, max_ctx=w.T + warmup + steps + 32, bits_k=w.bits_k,
+                        bits_v=w.bits_v, group=w.group, axis_k=w.axis_k, axis_v=w.axis_v,
+                        n_sink=n_sink, residual=residual)
+        c.prefill(torch.from_numpy(case["K"]).to(dev), torch.from_numpy(case["V"]).to(dev))
+        st = synth.make_decode_steps(w, warmup + steps, seed=seed + 500, outliers=case["outliers"])
+        steps_dev.append([{k: torch.from_numpy(v).to(dev) for k, v in x.items()} for x in st])
+        caches.append(c)
+    outs = [torch.empty(w.batch, w.n_q_heads, w.head_dim, dtype=torch.float32, device=dev)
+            for _ in range(n_layers)]
+    for i in range(warmup):
+        for layer in range(n_layers):
+            s = steps_dev[layer][i]
+            caches[layer].append_decode(s["k"], s["v"], s["q"], outs[layer], w.scale)
+    torch.cuda.synchronize()
+    timed = []
+    for i in range(warmup, warmup + steps):
+        for layer in range(n_layers):
+            s = steps_dev[layer][i]
+            b0 = caches[layer].buffers()
+            fused = b0.T_sink == n_sink and b0.T_tail + 1 < residual + w.group
+            a = torch.cuda.Event(enable_timing=True)
+            e = torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            caches[layer].append_decode(s["k"], s["v"], s["q"], outs[layer], w.scale)
+            e.record(stream)
+            tq, tt = caches[layer].state
+            if fused:
+                timed.append((a, e, decode_bytes(w, tq, tt + n_sink)))
+    torch.cuda.synchronize()
+    for c in caches:
+        c.check()
+        c.close()
+    ms = statistics.mean(a.elapsed_time(e) for a, e, _ in timed)
+    nb = statistics.mean(b for _, _, b in timed)
+    peak, src = load_peaks()
+    gbs = nb / (ms * 1e-3) / 1e9
+    return {"workload": f"{w.name}-sink{n_sink}-res{residual}", "n_sink": n_sink,
+            "residual": residual, "GB/s": gbs, "frac": gbs / peak, "peak_source": f"hbm_gbs of {src}",
+            "ms_per_launch": ms, "bytes_per_launch": nb, "launches_timed": len(timed)}
+
+
 def quantize_bytes_per_token(w):
     Hkv, D = w.n_kv_heads, w.head_dim
     return 2 * Hkv * D * 2 + Hkv * D * (w.bits_k + w.bits_v) // 8 + 2 * Hkv * D // w.group * 4
@@ -377,6 +430,10 @@ def run_gpu(args, w):
                   "cpu_oracle_Mtok_s": (t_cpu_tokens / w4.n_kv_heads / t_cpu / 1e6) if t_cpu else None}
         del K4, V4, flush
 
+    win_line = None
+    if rank == 0 and not args.skip_windows:
+        win_line = windows_leg(w, dev, stream, 4, 128, L, 3, min(args.steps, 10))
+
     if rank != 0:
         if ws > 1:
             import torch.distributed as dist
@@ -418,6 +475,7 @@ def run_gpu(args, w):
         "gpu_launches": int(launches),
         "clocks": clk.summary(),
         "quantize": q_line,
+        "windows": win_line,
         "frac_of_8tbs_spec": achieved / 8000.0,
     }
     print(json.dumps(line), flush=True)
@@ -435,6 +493,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--skip-cpu", action="store_true")
     ap.add_argument("--skip-quantize", action="store_true")
+    ap.add_argument("--skip-windows", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")

@@ -1,5 +1,6 @@
 // kvq_api.cu — the C ABI of include/kvq.h: validation, ownership of the
 // device cache, host-side lengths and kernel launches.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdlib>
@@ -34,11 +35,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Derived {
   int P, R, NB, G, D;
+  int NSK;             // sink window rows per pair (n_sink)
+  int residual;        // recent tokens kept in fp16 beyond the partial group
+  int TC;              // rows per pair of a tail buffer: residual + G
   int frag_k, frag_v;  // code order of each side (1 fragment, 0 sequential)
   bool mma_geom;       // geometry of the tensor-core decode kernel
   int C2max;  // level-1 chunks per (pair, query) of the two-level merge
   size_t block_bytes, off_kc, off_km, off_vc, off_vm;
-  size_t blocks_bytes, tail_bytes, rope_bytes, part_o_bytes, part_ml_bytes;
+  size_t blocks_bytes, tail_bytes, sink_bytes, rope_bytes, part_o_bytes, part_ml_bytes;
   size_t lvl_o_bytes, lvl_ml_bytes;
 };
 
@@ -55,6 +59,8 @@ kvq_status derive(const kvq_config* c, Derived* d) {
   if (c->keys_pre_rope != 0 && c->keys_pre_rope != 1) return KVQ_ERR_INVALID_ARG;
   if (c->keys_pre_rope && !(c->rope_base > 1.0f && std::isfinite(c->rope_base)))
     return KVQ_ERR_INVALID_ARG;
+  if (c->n_sink < 0 || c->n_sink > 1024 || c->residual < 0 || c->residual > 4096)
+    return KVQ_ERR_INVALID_ARG;
   if ((c->axis_k == 1 || c->axis_v == 1) && c->head_dim % c->group != 0)
     return KVQ_ERR_INVALID_ARG;
   const int R = c->n_q_heads / c->n_kv_heads;
@@ -64,8 +70,11 @@ kvq_status derive(const kvq_config* c, Derived* d) {
   const long long P = static_cast<long long>(c->batch) * c->n_kv_heads;
   if (P > 65535) return KVQ_ERR_UNSUPPORTED;  // grid.y of the quantize launch
   if (c->max_ctx > (1 << 26)) return KVQ_ERR_UNSUPPORTED;
-  // decode units (32-token sub-blocks and tail chunks) are counted in int
-  if (P * (static_cast<long long>(c->max_ctx) / 32 + 32) >= (1LL << 31)) return KVQ_ERR_UNSUPPORTED;
+  // decode units (32-token sub-blocks, tail and sink chunks of at least six
+  // tokens) are counted in int
+  if (P * (static_cast<long long>(c->max_ctx) / 32 + (c->n_sink + c->residual + c->group) / 6 + 2) >=
+      (1LL << 31))
+    return KVQ_ERR_UNSUPPORTED;
   d->P = static_cast<int>(P);
   d->R = R;
   d->mma_geom = mma_geometry(c->group, c->axis_k, c->axis_v);
@@ -73,6 +82,9 @@ kvq_status derive(const kvq_config* c, Derived* d) {
   d->frag_v = fragment_order(c->head_dim, c->group, c->bits_v, c->axis_k, c->axis_v) ? 1 : 0;
   d->G = c->group;
   d->D = c->head_dim;
+  d->NSK = c->n_sink;
+  d->residual = c->residual;
+  d->TC = c->residual + c->group;
   d->NB = c->max_ctx / c->group;
   const size_t D = c->head_dim, G = c->group;
   d->off_kc = 0;
@@ -81,7 +93,8 @@ kvq_status derive(const kvq_config* c, Derived* d) {
   d->off_vm = d->off_vc + G * D * c->bits_v / 8;
   d->block_bytes = d->off_vm + 4 * D;
   d->blocks_bytes = static_cast<size_t>(P) * d->NB * d->block_bytes;
-  d->tail_bytes = static_cast<size_t>(P) * G * D * 2;  // one fp16 [P][G][D] buffer
+  d->tail_bytes = static_cast<size_t>(P) * d->TC * D * 2;  // one fp16 [P][TC][D] buffer
+  d->sink_bytes = static_cast<size_t>(P) * d->NSK * D * 2;  // one fp16 [P][NSK][D] buffer
   d->rope_bytes = c->keys_pre_rope ? static_cast<size_t>(c->max_ctx) * (D / 2) * sizeof(float2) : 0;
   const size_t slots = static_cast<size_t>(kMaxDecodeWarps + P);
   d->part_o_bytes = slots * R * D * sizeof(float);
@@ -122,6 +135,8 @@ struct kvq_cache {
   __half* ktail[2];
   __half* vtail[2];
   int active;
+  __half* ksink;  // sink window [P][NSK][D], nullptr when n_sink = 0
+  __half* vsink;
   float2* rope;
   float* part_o;
   float2* part_ml;
@@ -131,7 +146,7 @@ struct kvq_cache {
   float2* lvl_ml;
   int* tickets2; // [P*R] two-level merge counters, zero between launches
   bool mma;      // decode runs the tensor-core kernel (which can merge in place)
-  int T_q, T_t;
+  int T_s, T_q, T_t;  // sink, quantized and tail tokens per pair
 };
 
 static CacheGeom geom_of(const kvq_cache* c) {
@@ -151,6 +166,8 @@ static CacheGeom geom_of(const kvq_cache* c) {
   g.ak = c->cfg.axis_k;
   g.av = c->cfg.axis_v;
   g.P = c->dv.P;
+  g.TC = c->dv.TC;
+  g.NSK = c->dv.NSK;
   return g;
 }
 
@@ -160,6 +177,8 @@ static void free_all(kvq_cache* c) {
     cudaFree(c->ktail[i]);
     cudaFree(c->vtail[i]);
   }
+  cudaFree(c->ksink);
+  cudaFree(c->vsink);
   cudaFree(c->rope);
   cudaFree(c->part_o);
   cudaFree(c->part_ml);
@@ -170,18 +189,36 @@ static void free_all(kvq_cache* c) {
   cudaFree(c->tickets2);
 }
 
-// Appends n tokens per pair (the whole combined tail + new sequence is
-// walked once; see QuantParams).
+// Appends n tokens per pair: the first ones fill the sink window while it
+// is short, the others join the tail; every group of G that leaves at least
+// `residual` newer tail tokens is quantized (the whole combined tail + new
+// sequence is walked once; see QuantParams).
 static kvq_status enqueue_append(kvq_cache* c, const void* k, const void* v, int n,
                                  cudaStream_t stream) {
-  const int G = c->dv.G;
-  const int combined = c->T_t + n;
-  const int nflush = combined / G;
+  const int G = c->dv.G, D = c->dv.D;
+  const __half* kn = static_cast<const __half*>(k);
+  const __half* vn = static_cast<const __half*>(v);
+  const int m = std::min(n, c->dv.NSK - c->T_s);
+  if (m > 0) {
+    const size_t row = static_cast<size_t>(D) * sizeof(__half);
+    const size_t off = static_cast<size_t>(c->T_s) * D;
+    if (cudaMemcpy2DAsync(c->ksink + off, c->dv.NSK * row, kn, n * row, m * row, c->dv.P,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess ||
+        cudaMemcpy2DAsync(c->vsink + off, c->dv.NSK * row, vn, n * row, m * row, c->dv.P,
+                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+      return KVQ_ERR_CUDA;
+    c->T_s += m;
+  }
+  const int nr = n - m;
+  if (nr == 0) return KVQ_OK;
+  const int combined = c->T_t + nr;
+  const int nflush = combined >= c->dv.residual ? (combined - c->dv.residual) / G : 0;
   QuantParams q;
   q.g = geom_of(c);
-  q.knew = static_cast<const __half*>(k);
-  q.vnew = static_cast<const __half*>(v);
-  q.n = n;
+  q.knew = kn + static_cast<size_t>(m) * D;
+  q.vnew = vn + static_cast<size_t>(m) * D;
+  q.n = nr;
+  q.new_stride = n;
   q.kold = c->ktail[c->active];
   q.vold = c->vtail[c->active];
   q.T_t = c->T_t;
@@ -219,7 +256,7 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {
   Derived d;
   kvq_status s = derive(cfg, &d);
   if (s != KVQ_OK) return s;
-  *bytes = d.blocks_bytes + 4 * d.tail_bytes + d.rope_bytes + d.part_o_bytes +
+  *bytes = d.blocks_bytes + 4 * d.tail_bytes + 2 * d.sink_bytes + d.rope_bytes + d.part_o_bytes +
            d.part_ml_bytes + d.lvl_o_bytes + d.lvl_ml_bytes + sizeof(int) +
            sizeof(int) * static_cast<size_t>(d.P) * (1 + d.R);
   return KVQ_OK;
@@ -265,6 +302,9 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
     ok = cudaMalloc(&c->ktail[i], d.tail_bytes) == cudaSuccess &&
          cudaMalloc(&c->vtail[i], d.tail_bytes) == cudaSuccess;
   }
+  if (ok && d.sink_bytes)
+    ok = cudaMalloc(&c->ksink, d.sink_bytes) == cudaSuccess &&
+         cudaMalloc(&c->vsink, d.sink_bytes) == cudaSuccess;
   if (ok && d.rope_bytes) ok = cudaMalloc(&c->rope, d.rope_bytes) == cudaSuccess;
   if (ok) ok = cudaMalloc(&c->part_o, d.part_o_bytes) == cudaSuccess;
   if (ok) ok = cudaMalloc(&c->part_ml, d.part_ml_bytes) == cudaSuccess;
@@ -285,6 +325,9 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   for (int i = 0; i < 2 && init_ok; ++i)
     init_ok = cudaMemset(c->ktail[i], 0, d.tail_bytes) == cudaSuccess &&
               cudaMemset(c->vtail[i], 0, d.tail_bytes) == cudaSuccess;
+  if (init_ok && d.sink_bytes)
+    init_ok = cudaMemset(c->ksink, 0, d.sink_bytes) == cudaSuccess &&
+              cudaMemset(c->vsink, 0, d.sink_bytes) == cudaSuccess;
   if (init_ok && d.rope_bytes) {
     // RoPE cos/sin table: angle pos * base^(-2i/D), evaluated in fp64.
     const int half = d.D / 2;
@@ -327,12 +370,14 @@ kvq_status kvq_quantize_prefill(kvq_cache* c, const void* k, const void* v, int 
   if (T > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return KVQ_ERR_CUDA;
-  const int saved_q = c->T_q, saved_t = c->T_t;
+  const int saved_s = c->T_s, saved_q = c->T_q, saved_t = c->T_t;
+  c->T_s = 0;
   c->T_q = 0;
   c->T_t = 0;
   if (T == 0) return KVQ_OK;
   kvq_status s = enqueue_append(c, k, v, T, static_cast<cudaStream_t>(stream));
   if (s != KVQ_OK) {
+    c->T_s = saved_s;
     c->T_q = saved_q;
     c->T_t = saved_t;
   }
@@ -343,7 +388,7 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, int n, void* s
   if (c == nullptr || n < 0) return KVQ_ERR_INVALID_ARG;
   if (n == 0) return KVQ_OK;
   if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
-  if (static_cast<long long>(c->T_q) + c->T_t + n > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
+  if (static_cast<long long>(c->T_s) + c->T_q + c->T_t + n > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return KVQ_ERR_CUDA;
   return enqueue_append(c, k, v, n, static_cast<cudaStream_t>(stream));
@@ -357,7 +402,8 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   const Derived& d = c->dv;
   const int T_t = c->T_t + n_new;
   const int nsub = c->T_q / 32;
-  const int upp = nsub + tail_units(c->mma, T_t, c->cfg.bits_k, c->cfg.bits_v);
+  const int ntu = tail_units(c->mma, T_t, c->cfg.bits_k, c->cfg.bits_v);
+  const int upp = nsub + ntu + tail_units(c->mma, c->T_s, c->cfg.bits_k, c->cfg.bits_v);
   const long long U = static_cast<long long>(d.P) * upp;
   if (U == 0) {  // an empty cache (n_new is 0 here)
     if (cudaMemsetAsync(out, 0, static_cast<size_t>(d.P) * d.R * d.D * sizeof(float), st) !=
@@ -373,8 +419,12 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   p.g = geom_of(c);
   p.ktail = c->ktail[c->active];
   p.vtail = c->vtail[c->active];
+  p.ksink = c->ksink;
+  p.vsink = c->vsink;
+  p.T_s = c->T_s;
   p.T_q = c->T_q;
   p.T_t = T_t;
+  p.n_tail_u = ntu;
   p.t_old = c->T_t;
   p.knew = static_cast<const __half*>(knew);
   p.vnew = static_cast<const __half*>(vnew);
@@ -442,11 +492,12 @@ kvq_status kvq_append_decode(kvq_cache* c, const void* k, const void* v, int n, 
   if (n > 0 && (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)))
     return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
-  if (static_cast<long long>(c->T_q) + c->T_t + n > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
+  if (static_cast<long long>(c->T_s) + c->T_q + c->T_t + n > c->cfg.max_ctx)
+    return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return KVQ_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (n > 0 && c->mma && c->T_t + n < c->dv.G) {
+  if (n > 0 && c->mma && c->T_s == c->dv.NSK && c->T_t + n < c->dv.residual + c->dv.G) {
     // one launch: the new tokens stay in the tail, no block is flushed
     const kvq_status s = enqueue_decode(c, q, out, softmax_scale, st, k, v, n);
     if (s == KVQ_OK) c->T_t += n;
@@ -499,6 +550,10 @@ kvq_status kvq_get_buffers(const kvq_cache* c, kvq_buffers* out) {
   out->n_pairs = c->dv.P;
   out->T_q = c->T_q;
   out->T_tail = c->T_t;
+  out->k_sink = c->ksink;
+  out->v_sink = c->vsink;
+  out->T_sink = c->T_s;
+  out->tail_rows = c->dv.TC;
   return KVQ_OK;
 }
 

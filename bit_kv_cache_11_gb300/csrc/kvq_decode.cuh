@@ -7,8 +7,8 @@
 // reads the whole cache once per generated token (section "Why the KV Cache
 // Is Where This Bites"), so the kernel is built to stream HBM.
 //
-// Work decomposition.  Units are (pair, 32-token sub-block) plus one fp16-tail
-// unit per pair; warp w of the grid owns units [w*U/W, (w+1)*U/W) — a
+// Work decomposition.  Units are (pair, 32-token sub-block) plus one fp16
+// unit per pair for the tail and one for the sink window (when present); warp w of the grid owns units [w*U/W, (w+1)*U/W) — a
 // contiguous range, so every warp streams contiguous memory and all warps get
 // the same amount of work whatever the batch/head/context shape.  A warp keeps
 // one online-softmax state (m, l, o) per query head of the GQA group and
@@ -97,11 +97,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   }
   __syncwarp();
 
-  // Load cursor: the next quantized unit to copy (tail units are skipped).
+  // Load cursor: the next quantized unit to copy (fp16 units are skipped).
   UnitCursor lc;
   lc.init(ua, p.upp);
   auto skip_tail = [&]() {
-    while (lc.u < ub && lc.j == p.nsub) lc.next(p.upp);
+    while (lc.u < ub && lc.j >= p.nsub) lc.next(p.upp);
   };
   // Lane 0: copies of quantized unit u into stage s.
   auto issue = [&](long long pr, int j, int s) {
@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       return code_to_float((kr[d / KPER] >> ((d % KPER) * BK)) & KMASK);
     };
     if (p.rope) {
-      const int pos = j * 32 + lane;
+      const int pos = p.T_s + j * 32 + lane;
       const float2* cs = p.rope_tab + static_cast<size_t>(pos) * (D / 2);
 #pragma unroll
       for (int r = 0; r < R; ++r) sc[r] = 0.f;
@@ -346,19 +346,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     __syncwarp();
   };
 
-  auto process_tail = [&](long long pr) {
-    const __half* kt = p.ktail + static_cast<size_t>(pr) * G * D;
-    const __half* vt = p.vtail + static_cast<size_t>(pr) * G * D;
+  // fp16 rows [0, nrows) of kt / vt (the tail, or the sink window), row t
+  // at position pos0 + t.
+  auto process_rows = [&](const __half* kt, const __half* vt, int nrows, int pos0) {
     const int d0 = lane * CPL;
-    for (int t0 = 0; t0 < p.T_t; t0 += 32) {
+    for (int t0 = 0; t0 < nrows; t0 += 32) {
       const int t = t0 + lane;
       float sc[R];
 #pragma unroll
       for (int r = 0; r < R; ++r) sc[r] = 0.f;
-      if (t < p.T_t) {
+      if (t < nrows) {
         const __half* row = kt + static_cast<size_t>(t) * D;
         if (p.rope) {
-          const float2* cs = p.rope_tab + static_cast<size_t>(p.T_q + t) * (D / 2);
+          const float2* cs = p.rope_tab + static_cast<size_t>(pos0 + t) * (D / 2);
           for (int i = 0; i < D / 2; i += 8) {
             const uint4 a4 = *reinterpret_cast<const uint4*>(row + i);
             const uint4 b4 = *reinterpret_cast<const uint4*>(row + i + D / 2);
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       }
       float psum[R];
       softmax_update(sc, psum);
-      const int nt = min(32, p.T_t - t0);
+      const int nt = min(32, nrows - t0);
       for (int jj = 0; jj < nt; ++jj) {
         const __half* vr = vt + static_cast<size_t>(t0 + jj) * D + d0;
         float vv[CPL];
@@ -424,8 +424,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       enter_pair(pr);
       cur = pr;
     }
-    if (j == p.nsub) {
-      process_tail(pr);
+    if (j >= p.nsub) {
+      if (j < p.nsub + p.n_tail_u)
+        process_rows(p.ktail + static_cast<size_t>(pr) * p.g.TC * D,
+                     p.vtail + static_cast<size_t>(pr) * p.g.TC * D, p.T_t, p.T_s + p.T_q);
+      else
+        process_rows(p.ksink + static_cast<size_t>(pr) * p.g.NSK * D,
+                     p.vsink + static_cast<size_t>(pr) * p.g.NSK * D, p.T_s, 0);
       continue;
     }
     const int s = qi % NS;

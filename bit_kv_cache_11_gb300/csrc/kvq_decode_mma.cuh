@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       const int col = static_cast<int>(c - rowi * (D / 8)) * 8;
       const long long pr = rowi / n_new;
       const int r = static_cast<int>(rowi - pr * n_new);
-      const size_t dst = (static_cast<size_t>(pr) * C::G + p.t_old + r) * D + col;
+      const size_t dst = (static_cast<size_t>(pr) * p.g.TC + p.t_old + r) * D + col;
       *reinterpret_cast<uint4*>(p.ktail_w + dst) =
           *reinterpret_cast<const uint4*>(p.knew + rowi * D + col);
       *reinterpret_cast<uint4*>(p.vtail_w + dst) =
@@ -257,6 +257,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     if (lj < nsub) {
       mbar_arrive_expect_tx(&bars[s], STAGE);
       bulk_g2s(st, lbase + static_cast<size_t>(lj) * STAGE, STAGE, &bars[s]);
+    } else if (lj >= nsub + p.n_tail_u) {
+      // sink rows [t0, t1): K rows, then V rows, one copy each
+      const int t0 = (lj - nsub - p.n_tail_u) * TCH;
+      const int t1 = min(t0 + TCH, p.T_s);
+      const uint32_t bytes = static_cast<uint32_t>(t1 - t0) * D * 2;
+      const size_t row = static_cast<size_t>(lpr) * p.g.NSK + t0;
+      mbar_arrive_expect_tx(&bars[s], 2 * bytes);
+      bulk_g2s(st, p.ksink + row * D, bytes, &bars[s]);
+      bulk_g2s(st + TCH * D * 2, p.vsink + row * D, bytes, &bars[s]);
     } else {
       // tail rows [t0, t1): those below t_old from the tail buffer, the rest
       // (tokens appended by this call) from knew / vnew
@@ -266,7 +275,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(t1 - t0) * D * 4);
       if (tm > t0) {
         const uint32_t bytes = static_cast<uint32_t>(tm - t0) * D * 2;
-        const size_t row = static_cast<size_t>(lpr) * C::G + t0;
+        const size_t row = static_cast<size_t>(lpr) * p.g.TC + t0;
         bulk_g2s(st, p.ktail + row * D, bytes, &bars[s]);
         bulk_g2s(st + TCH * D * 2, p.vtail + row * D, bytes, &bars[s]);
       }
@@ -663,7 +672,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       //   cos(j th_i) (a c_i + b c_i2 + e) + sin(j th_i) (f c_i - g c_i2 + h).
       constexpr int H = D / 2;
       float* cf = reinterpret_cast<float*>(ws + C::OFF_CF);
-      const int p0 = ju * 32;
+      const int p0 = p.T_s + ju * 32;
       for (int i = lane; i < H; i += 32) {
         const float2 cs = p.rope_tab[static_cast<size_t>(p0) * H + i];
         const float2 m0 = __half22float2(km[i]), m1 = __half22float2(km[i + H]);
@@ -760,18 +769,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   };
 
 
-  // fp16 tail chunk k of the pair (tokens [k*TCH, min(T_t, (k+1)*TCH)), its K
-  // rows then its V rows in the stage).  Lane l holds channels
+  // fp16 chunk of n <= TCH rows (tail or sink window; its K rows then its V
+  // rows in the stage), row j at position pos0 + j.  Lane l holds channels
   // [l*CPL, (l+1)*CPL) (rotated keys: the frequency pairs (i, i + D/2),
   // i = l + 32f); a token's score is the warp sum of the lanes' dot products.
   // The scaled query sits in `os` (free until the pair's partial is written).
-  auto process_tail_chunk = [&](const uint8_t* st, int k) {
+  auto process_chunk = [&](const uint8_t* st, int n, int pos0) {
     const __half* kt = reinterpret_cast<const __half*>(st);
     const __half* vt = kt + TCH * D;
-    const int t0 = k * TCH;
-    const int n = min(TCH, p.T_t - t0);
     if constexpr (ROPE) {
-      // key of tail token t at absolute position T_q + t, rotated after
+      // key of row j at absolute position pos0 + j, rotated after
       // dequantization: (k_i cos - k_{i+H} sin, k_{i+H} cos + k_i sin)
       constexpr int H = D / 2, FPL = H / 32;
       float qa[R][FPL], qb[R][FPL];
@@ -785,8 +792,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
 #pragma unroll
       for (int j = 0; j < TCH; ++j) {
         if (j < n) {
-          const float2* cs =
-              p.rope_tab + static_cast<size_t>(p.T_q + t0 + j) * H + lane;
+          const float2* cs = p.rope_tab + static_cast<size_t>(pos0 + j) * H + lane;
           float v[R];
 #pragma unroll
           for (int r = 0; r < R; ++r) v[r] = 0.f;
@@ -879,6 +885,18 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     __syncwarp();
   };
 
+
+  // unit j >= nsub of a pair: a chunk of its tail, then of its sink window
+  auto process_fp16_unit = [&](const uint8_t* st, int j) {
+    const int k = j - nsub;
+    if (k < p.n_tail_u) {
+      const int t0 = k * TCH;
+      process_chunk(st, min(TCH, p.T_t - t0), p.T_s + p.T_q + t0);
+    } else {
+      const int t0 = (k - p.n_tail_u) * TCH;
+      process_chunk(st, min(TCH, p.T_s - t0), t0);
+    }
+  };
 
   auto write_partial = [&](int prr) {
     const long long pr = prr;
@@ -1023,7 +1041,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       if (j < nsub)
         process_sub(st, j);
       else
-        process_tail_chunk(st, j - nsub);
+        process_fp16_unit(st, j);
       refill(s);
     } else {
       if (j < nsub) {
@@ -1051,7 +1069,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           refill(pend);
           pend = -1;
         }
-        process_tail_chunk(st, j - nsub);
+        process_fp16_unit(st, j);
         refill(s);
       }
     }

@@ -136,15 +136,18 @@ struct CacheGeom {
   int D, G, bk, bv, ak, av;
   int P;
   int frag_k, frag_v;  // code order of each side: 1 fragment, 0 sequential
+  int TC;              // rows per pair of a tail buffer (residual + G)
+  int NSK;             // rows per pair of the sink window (n_sink)
 };
 
 // Quantize / append / flush launch: grid (nflush + 1, P).
 struct QuantParams {
   CacheGeom g;
-  const __half* knew;  // [P][n][D]
+  const __half* knew;  // pair p's new token r at row p * new_stride + r
   const __half* vnew;
   int n;
-  const __half* kold;  // active tail [P][G][D] (rows [0, T_t) valid)
+  int new_stride;      // rows per pair of knew / vnew (>= n)
+  const __half* kold;  // active tail [P][TC][D] (rows [0, T_t) valid)
   const __half* vold;
   int T_t;
   __half* kdst;        // tail that receives the remainder
@@ -181,15 +184,19 @@ __host__ __device__ inline int tail_units(bool mma, int T_t, int bk, int bv) {
 
 // Split-K decode launch.  The work of all pairs is a flat sequence of units:
 // pair p owns units [p*upp, (p+1)*upp); unit j < nsub of a pair is its j-th
-// 32-token quantized sub-block, units j >= nsub (present when T_t > 0) cover
-// its fp16 tail (see tail_units).  Warp w of the grid processes units
-// [w*U/W, (w+1)*U/W) and writes one partial (m, l, o) per pair it touches
-// into slot (w + p).
+// 32-token quantized sub-block, the next n_tail_u units cover its fp16 tail
+// and the rest its fp16 sink window (tail_units of T_t and of T_s).  Warp w
+// of the grid processes units [w*U/W, (w+1)*U/W) and writes one partial
+// (m, l, o) per pair it touches into slot (w + p).  Token positions (RoPE):
+// sink row t at t, quantized token i at T_s + i, tail row t at T_s + T_q + t.
 struct DecodeParams {
   CacheGeom g;
-  const __half* ktail;  // active tail [P][G][D]
+  const __half* ktail;  // active tail [P][TC][D]
   const __half* vtail;
-  int T_q, T_t;
+  const __half* ksink;  // sink window [P][NSK][D]
+  const __half* vsink;
+  int T_s, T_q, T_t;
+  int n_tail_u;         // tail units per pair
   // Append fused into the decode (tensor-core kernel, no flush): tail rows
   // [t_old, T_t) are the n_new tokens of knew/vnew ([P][n_new][D]); the
   // kernel also stores them into rows [t_old, T_t) of the tail (ktail_w).

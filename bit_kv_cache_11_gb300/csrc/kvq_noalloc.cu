@@ -103,6 +103,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   const kvq_status cs = kvq_config_check(cfg);
   if (cs != KVQ_OK) return cs;
   if (cfg->keys_pre_rope) return KVQ_ERR_UNSUPPORTED;  // the RoPE table would need memory
+  if (cfg->n_sink != 0 || cfg->residual != 0) return KVQ_ERR_UNSUPPORTED;  // no window buffers
   const int D = cfg->head_dim, G = cfg->group;
   const int R = cfg->n_q_heads / cfg->n_kv_heads;
   const long long P = static_cast<long long>(cfg->batch) * cfg->n_kv_heads;
@@ -185,10 +186,16 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.g.ak = cfg->axis_k;
     p.g.av = cfg->axis_v;
     p.g.P = static_cast<int>(P);
+    p.g.TC = G;
+    p.g.NSK = 0;
     p.ktail = static_cast<const __half*>(k_tail);
     p.vtail = static_cast<const __half*>(v_tail);
+    p.ksink = nullptr;
+    p.vsink = nullptr;
+    p.T_s = 0;
     p.T_q = T_q;
     p.T_t = T_tail;
+    p.n_tail_u = upp - nsub;
     p.t_old = T_tail;
     p.knew = nullptr;
     p.vnew = nullptr;

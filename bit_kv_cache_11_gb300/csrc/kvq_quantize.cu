@@ -81,14 +81,14 @@ __device__ __forceinline__ uint32_t code_of(float x, const Stat& st, float top) 
 
 __device__ __forceinline__ const __half* combined_row(const QuantParams& q, int p, int jc) {
   const int D = q.g.D;
-  if (jc < q.T_t) return q.kold + (static_cast<size_t>(p) * q.g.G + jc) * D;
-  return q.knew + (static_cast<size_t>(p) * q.n + (jc - q.T_t)) * D;
+  if (jc < q.T_t) return q.kold + (static_cast<size_t>(p) * q.g.TC + jc) * D;
+  return q.knew + (static_cast<size_t>(p) * q.new_stride + (jc - q.T_t)) * D;
 }
 
 __device__ __forceinline__ const __half* combined_row_v(const QuantParams& q, int p, int jc) {
   const int D = q.g.D;
-  if (jc < q.T_t) return q.vold + (static_cast<size_t>(p) * q.g.G + jc) * D;
-  return q.vnew + (static_cast<size_t>(p) * q.n + (jc - q.T_t)) * D;
+  if (jc < q.T_t) return q.vold + (static_cast<size_t>(p) * q.g.TC + jc) * D;
+  return q.vnew + (static_cast<size_t>(p) * q.new_stride + (jc - q.T_t)) * D;
 }
 
 // Packs 32/BITS byte codes (LSB-first order) into one word.
@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
       const int r = c / (D / 8);
       const int col = (c % (D / 8)) * 8;
       const int jc = q.rem_begin + r;
-      const size_t dst = (static_cast<size_t>(p) * G + q.dst_row0 + r) * D + col;
+      const size_t dst = (static_cast<size_t>(p) * q.g.TC + q.dst_row0 + r) * D + col;
       *reinterpret_cast<uint4*>(q.kdst + dst) =
           *reinterpret_cast<const uint4*>(combined_row(q, p, jc) + col);
       *reinterpret_cast<uint4*>(q.vdst + dst) =

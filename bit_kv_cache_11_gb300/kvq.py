@@ -37,7 +37,8 @@ class kvq_config(ctypes.Structure):
     _fields_ = [("batch", ctypes.c_int), ("n_q_heads", ctypes.c_int), ("n_kv_heads", ctypes.c_int),
                 ("head_dim", ctypes.c_int), ("max_ctx", ctypes.c_int), ("bits_k", ctypes.c_int),
                 ("bits_v", ctypes.c_int), ("group", ctypes.c_int), ("axis_k", ctypes.c_int),
-                ("axis_v", ctypes.c_int), ("keys_pre_rope", ctypes.c_int), ("rope_base", ctypes.c_float)]
+                ("axis_v", ctypes.c_int), ("keys_pre_rope", ctypes.c_int), ("rope_base", ctypes.c_float),
+                ("n_sink", ctypes.c_int), ("residual", ctypes.c_int)]
 
 
 class kvq_buffers(ctypes.Structure):
@@ -45,7 +46,9 @@ class kvq_buffers(ctypes.Structure):
                 ("block_bytes", ctypes.c_size_t), ("off_kc", ctypes.c_size_t),
                 ("off_km", ctypes.c_size_t), ("off_vc", ctypes.c_size_t), ("off_vm", ctypes.c_size_t),
                 ("blocks_per_pair", ctypes.c_int), ("n_pairs", ctypes.c_int), ("T_q", ctypes.c_int),
-                ("T_tail", ctypes.c_int), ("code_order_k", ctypes.c_int), ("code_order_v", ctypes.c_int)]
+                ("T_tail", ctypes.c_int), ("code_order_k", ctypes.c_int), ("code_order_v", ctypes.c_int),
+                ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p), ("T_sink", ctypes.c_int),
+                ("tail_rows", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -106,10 +109,10 @@ def _stream(stream) -> int | None:
 
 def make_config(batch, n_q_heads, n_kv_heads, head_dim, max_ctx, bits_k=2, bits_v=2, group=32,
                 axis_k=KVQ_AXIS_CHANNEL, axis_v=KVQ_AXIS_TOKEN, keys_pre_rope=False,
-                rope_base=10000.0) -> kvq_config:
+                rope_base=10000.0, n_sink=0, residual=0) -> kvq_config:
     return kvq_config(int(batch), int(n_q_heads), int(n_kv_heads), int(head_dim), int(max_ctx),
                       int(bits_k), int(bits_v), int(group), int(axis_k), int(axis_v),
-                      1 if keys_pre_rope else 0, float(rope_base))
+                      1 if keys_pre_rope else 0, float(rope_base), int(n_sink), int(residual))
 
 
 # ---- the C calls, same names ------------------------------------------------
@@ -289,13 +292,21 @@ class KVCache:
         return device_view(b.blocks, (b.n_pairs, b.blocks_per_pair, b.block_bytes))
 
     def tail_views(self):
-        """fp16 [P][G][D] views of the active K and V tails (no copy)."""
-        import torch
+        """fp16 [P][tail_rows][D] views of the active K and V tails (no copy)."""
         b = self.buffers()
-        shape = (b.n_pairs, self.cfg.group, self.cfg.head_dim)
+        shape = (b.n_pairs, b.tail_rows, self.cfg.head_dim)
         k = device_view(b.k_tail, shape, "<f2")
         v = device_view(b.v_tail, shape, "<f2")
         return k, v
+
+    def sink_views(self):
+        """fp16 [P][n_sink][D] views of the K and V sink windows (no copy);
+        None when the cache has no sink window."""
+        b = self.buffers()
+        if not b.k_sink:
+            return None
+        shape = (b.n_pairs, self.cfg.n_sink, self.cfg.head_dim)
+        return device_view(b.k_sink, shape, "<f2"), device_view(b.v_sink, shape, "<f2")
 
     def check(self, stream=None) -> None:
         _check(kvq_check_device_error(self.handle, stream), "kvq_check_device_error")

@@ -18,7 +18,12 @@
  *     flipped arms of the ablation.
  *   - The full-precision residual (section "The Systems Tax, and Why It Is Not a
  *     Detail"): tokens that do not yet fill a key group stay in an fp16 tail;
- *     a full tail of G tokens is quantized as one block.
+ *     a full tail of G tokens is quantized as one block.  Optionally the tail
+ *     also keeps a window of the `residual` most recent tokens in fp16 (a
+ *     group is quantized only when it leaves at least `residual` newer tokens
+ *     behind), and the first `n_sink` tokens (attention sinks) stay in fp16
+ *     for good (section "Where the Work Is Headed": high-precision windows for
+ *     recent tokens and for sink tokens).
  *   - Keys quantized before RoPE, RoPE applied after dequantization (section
  *     "Rotary Embeddings Complicate the Keys").
  *   - Attention as the softmax-weighted sum of value vectors (section "Values:
@@ -87,8 +92,14 @@
  *       with F2[0] = {0, 10, 12, 14}, F2[1] = {2, 4, 6, 8}; word w of lane l
  *       is word ((w/4)*32 + l)*4 + w%4 of the region.
  *
- *   The tail is fp16 [P][G][D] for K and for V; tokens [T_q, T_q + T_tail) of
- *   every pair sit in rows [0, T_tail).
+ *   Token order of a pair: T_sink sink tokens, then T_q quantized tokens,
+ *   then T_tail tail tokens (positions 0 .. T_sink + T_q + T_tail - 1, used
+ *   for RoPE).  Block (p, i) holds quantized tokens [i*G, (i+1)*G), i.e.
+ *   positions T_sink + i*G onwards (T_sink = n_sink whenever T_q > 0).
+ *
+ *   The sink window is fp16 [P][n_sink][D] for K and for V, rows [0, T_sink)
+ *   valid.  The tail is fp16 [P][residual + G][D] for K and for V
+ *   (kvq_buffers.tail_rows rows per pair), rows [0, T_tail) valid.
  */
 #ifndef KVQ_H_
 #define KVQ_H_
@@ -110,7 +121,7 @@ typedef enum {
   KVQ_OK = 0,
   KVQ_ERR_INVALID_ARG = 1,  /* null handle/pointer, misaligned pointer, bad size */
   KVQ_ERR_UNSUPPORTED = 2,  /* a valid config this build has no kernel for     */
-  KVQ_ERR_CAPACITY = 3,     /* T_q + T_tail + n would exceed max_ctx            */
+  KVQ_ERR_CAPACITY = 3,     /* T_sink + T_q + T_tail + n would exceed max_ctx   */
   KVQ_ERR_OOM = 4,          /* device allocation failed                         */
   KVQ_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed             */
   KVQ_ERR_DEVICE_CHECK = 6  /* a kernel reported a bounded wait that ran out    */
@@ -134,6 +145,9 @@ typedef struct {
   int axis_v;        /* kvq_axis; the pages' choice is KVQ_AXIS_TOKEN          */
   int keys_pre_rope; /* 1: keys are stored before RoPE; decode rotates them    */
   float rope_base;   /* RoPE base (e.g. 10000), used when keys_pre_rope = 1    */
+  int n_sink;        /* first tokens kept in fp16, never quantized; 0..1024   */
+  int residual;      /* most recent tokens kept in fp16 beyond the partial
+                        group; 0..4096 (0: the tail holds < G tokens)         */
 } kvq_config;
 
 typedef struct kvq_cache kvq_cache; /* opaque */
@@ -142,16 +156,20 @@ typedef struct kvq_cache kvq_cache; /* opaque */
  * read the packed bytes.  All pointers are owned by the cache. */
 typedef struct {
   void* blocks;                /* [P][NB][block_bytes] packed blocks            */
-  void* k_tail;                /* active K tail, fp16 [P][G][D]                 */
-  void* v_tail;                /* active V tail, fp16 [P][G][D]                 */
+  void* k_tail;                /* active K tail, fp16 [P][tail_rows][D]         */
+  void* v_tail;                /* active V tail, fp16 [P][tail_rows][D]         */
   size_t block_bytes;
   size_t off_kc, off_km, off_vc, off_vm;
   int blocks_per_pair;         /* NB                                            */
   int n_pairs;                 /* P                                             */
   int T_q;                     /* quantized tokens per pair (multiple of G)     */
-  int T_tail;                  /* tail tokens per pair, 0 <= T_tail < G         */
+  int T_tail;                  /* tail tokens per pair, < residual + G          */
   int code_order_k;            /* 0 sequential, 1 fragment (see the layout)     */
   int code_order_v;
+  void* k_sink;                /* K sink window, fp16 [P][n_sink][D]; NULL if n_sink = 0 */
+  void* v_sink;                /* V sink window, same                           */
+  int T_sink;                  /* sink tokens per pair, <= n_sink               */
+  int tail_rows;               /* rows per pair of each tail buffer (residual + G) */
 } kvq_buffers;
 
 /* Validates a config on the host (no GPU needed).  Returns KVQ_OK,
@@ -171,23 +189,29 @@ KVQ_API kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out);
  * accepted and ignored. */
 KVQ_API kvq_status kvq_destroy(kvq_cache* cache);
 
-/* Prefill: resets the cache, then quantizes tokens [0, floor(T/G)*G) of every
- * pair into blocks and copies the remaining T mod G tokens into the tail.
+/* Prefill: resets the cache, then stores every pair's T tokens: the first
+ * min(T, n_sink) in the sink window; of the rest (T' tokens), the first
+ * T_q = floor((T' - residual) / G) * G (0 if T' < residual) are quantized into
+ * blocks and the remaining T' - T_q go to the tail.  With n_sink = residual =
+ * 0: tokens [0, floor(T/G)*G) are quantized and T mod G stay in the tail.
  * k, v: device fp16 [batch][n_kv_heads][T][head_dim], contiguous.
  * T = 0 empties the cache.  T > max_ctx -> KVQ_ERR_CAPACITY. */
 KVQ_API kvq_status kvq_quantize_prefill(kvq_cache* cache, const void* k,
                                         const void* v, int T, void* stream);
 
-/* Decode-time append of n tokens per pair: the tail and the new tokens form
- * one sequence; every full group of G tokens in it is quantized into the next
- * block (the tail flush) and the rest becomes the new tail.
+/* Decode-time append of n tokens per pair.  New tokens first fill the sink
+ * window (while T_sink < n_sink); the others join the tail, which with them
+ * forms one sequence: while it holds at least residual + G tokens, its oldest
+ * G are quantized into the next block (the tail flush); the rest becomes the
+ * new tail.  The result equals a prefill of all tokens at once.
  * k, v: device fp16 [batch][n_kv_heads][n][head_dim], contiguous.  n = 0 is a
- * no-op.  T_q + T_tail + n > max_ctx -> KVQ_ERR_CAPACITY. */
+ * no-op.  T_sink + T_q + T_tail + n > max_ctx -> KVQ_ERR_CAPACITY. */
 KVQ_API kvq_status kvq_append(kvq_cache* cache, const void* k, const void* v,
                               int n, void* stream);
 
 /* Split-K decode attention of one query token per head over every cached
- * token (T_q dequantized tokens, then the T_tail fp16 tail tokens):
+ * token (T_sink fp16 sink tokens, T_q dequantized tokens, T_tail fp16 tail
+ * tokens; key t below is the token at position t):
  *   out[b][hq] = sum_t softmax_t(scale * q[b][hq] . k_t) * v_t
  * with query head hq reading kv head hq / (n_q_heads / n_kv_heads).  When
  * keys_pre_rope = 1, key t is rotated (rotate-half RoPE, angle
@@ -201,7 +225,8 @@ KVQ_API kvq_status kvq_decode_attention(kvq_cache* cache, const void* q,
 
 /* One decode step: kvq_append(cache, k, v, n) then kvq_decode_attention
  * (cache, q, out), with the same results and errors.  When the appended
- * tokens do not complete a group (T_tail + n < G) and the cache uses the
+ * tokens cause no flush (T_tail + n < residual + G) and go to the tail only
+ * (T_sink = n_sink), and the cache uses the
  * tensor-core kernel (keys per channel, values per token, G = 32), both run
  * as one launch: the decode reads the new tokens straight from k and v and
  * stores them into the tail.  Otherwise the append (with its flush) and the
@@ -233,9 +258,9 @@ KVQ_API kvq_status kvq_dequantize(kvq_cache* cache, void* k_out, void* v_out,
  * the layout described at the top of this header, this call decodes it
  * without a kvq_cache (whose creation allocates) and calls no allocating
  * routine.
- *   cfg            the cache's geometry; keys_pre_rope must be 0
- *                  (KVQ_ERR_UNSUPPORTED otherwise: the RoPE table would need
- *                  memory).
+ *   cfg            the cache's geometry; keys_pre_rope, n_sink and residual
+ *                  must be 0 (KVQ_ERR_UNSUPPORTED otherwise: the RoPE table
+ *                  would need memory; this call has no window buffers).
  *   blocks         device, [P][max_ctx/G][block_bytes] packed blocks.
  *   k_tail, v_tail device, fp16 [P][G][D]; rows [0, T_tail) are read.  May be
  *                  NULL when T_tail = 0.

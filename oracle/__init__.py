@@ -195,18 +195,42 @@ def unpack_pair(blocks: np.ndarray, D: int, G: int, bk: int, bv: int, ak: int, a
 
 # ---- one pair's cache -------------------------------------------------------
 
+def window_lengths(T: int, G: int, n_sink: int = 0, residual: int = 0):
+    """Token counts (Ts, Tq, Tt) of a pair holding T tokens.
+
+    Sinks: the first n_sink tokens stay fp16 (the high-precision sink window
+    of "Your KV cache doesn't have a bit problem, it has a geometry problem",
+    section "Where the Work Is Headed").  Residual window: the most recent
+    tokens stay fp16 and a group of G is quantized only when it leaves a
+    window of at least `residual` recent tokens behind (section "The Systems
+    Tax, and Why It Is Not a Detail": a full-precision window of recently
+    produced tokens, groups quantized once enough have accumulated).  With
+    n_sink = residual = 0 this is the plain rule: the G-aligned prefix is
+    quantized and fewer than G tokens stay in the tail."""
+    Ts = min(T, n_sink)
+    rest = T - Ts
+    Tq = (rest - residual) // G * G if rest >= residual else 0
+    return Ts, Tq, rest - Tq
+
+
 def build_pair(K_f16: np.ndarray, V_f16: np.ndarray, G: int, bk: int, bv: int,
-               ak: int = 0, av: int = 1) -> dict:
+               ak: int = 0, av: int = 1, n_sink: int = 0, residual: int = 0) -> dict:
     """The cache state of one pair after its T tokens arrived (any mix of
-    prefill and appends): the G-aligned prefix quantized, the rest in the
-    fp16 tail."""
+    prefill and appends): the sink tokens in fp16, then the quantized groups,
+    then the fp16 tail (window_lengths gives the three counts).  The state
+    does not depend on how the tokens were split into calls, because every
+    flush leaves the same G-aligned boundary."""
     T, D = K_f16.shape
-    Tq, kc, ks, kz = quantize_tensor(K_f16, G, bk, ak)
-    _, vc, vs, vz = quantize_tensor(V_f16, G, bv, av)
-    return dict(G=G, bk=bk, bv=bv, ak=ak, av=av, Tq=Tq, Tt=T - Tq,
+    Ts, Tq, Tt = window_lengths(T, G, n_sink, residual)
+    Tq_, kc, ks, kz = quantize_tensor(K_f16[Ts:Ts + Tq], G, bk, ak)
+    _, vc, vs, vz = quantize_tensor(V_f16[Ts:Ts + Tq], G, bv, av)
+    assert Tq_ == Tq
+    return dict(G=G, bk=bk, bv=bv, ak=ak, av=av, Ts=Ts, Tq=Tq, Tt=Tt,
                 kcodes=kc, kscale=ks, kzero=kz, vcodes=vc, vscale=vs, vzero=vz,
-                ktail=np.ascontiguousarray(K_f16[Tq:], np.float16),
-                vtail=np.ascontiguousarray(V_f16[Tq:], np.float16))
+                ksink=np.ascontiguousarray(K_f16[:Ts], np.float16),
+                vsink=np.ascontiguousarray(V_f16[:Ts], np.float16),
+                ktail=np.ascontiguousarray(K_f16[Ts + Tq:], np.float16),
+                vtail=np.ascontiguousarray(V_f16[Ts + Tq:], np.float16))
 
 
 def dequantize_pair(st: dict):
@@ -246,9 +270,15 @@ def attention_pair(q_f16: np.ndarray, khat: np.ndarray, vhat: np.ndarray,
 
 def decode_pair(st: dict, q_f16: np.ndarray, scale: float, rope_on: bool = False,
                 base: float = 10000.0, want_scores: bool = False):
-    """Decode attention of one pair's quantized cache (dequantized values plus
-    the fp16 tail)."""
+    """Decode attention of one pair's cache: the fp16 sink tokens, the
+    dequantized tokens and the fp16 tail, in token order (positions 0..T-1
+    for RoPE).  Sink rows are fp16 values, exact in fp32, so they join the
+    dequantized rows ahead of them."""
     kh, vh = dequantize_pair(st)
+    D = kh.shape[1]
+    if st.get("Ts", 0):
+        kh = np.concatenate([st["ksink"].astype(np.float32).reshape(-1, D), kh])
+        vh = np.concatenate([st["vsink"].astype(np.float32).reshape(-1, D), vh])
     return attention_pair(q_f16, kh, vh, st["ktail"], st["vtail"], scale, rope_on, base, want_scores)
 
 

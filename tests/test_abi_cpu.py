@@ -62,6 +62,12 @@ def test_config_check_on_host(lib_path):
         (dict(keys_pre_rope=True, rope_base=0.5), k.KVQ_ERR_INVALID_ARG),
         (dict(head_dim=64, group=128, axis_v=1), k.KVQ_ERR_INVALID_ARG),  # D % G != 0
         (dict(max_ctx=0), k.KVQ_ERR_INVALID_ARG),
+        (dict(n_sink=-1), k.KVQ_ERR_INVALID_ARG),
+        (dict(n_sink=1025), k.KVQ_ERR_INVALID_ARG),
+        (dict(residual=-32), k.KVQ_ERR_INVALID_ARG),
+        (dict(residual=4097), k.KVQ_ERR_INVALID_ARG),
+        (dict(n_sink=1024, residual=4096), k.KVQ_OK),
+        (dict(n_sink=4, residual=100, group=64), k.KVQ_OK),
     ]
     base = dict(batch=8, n_q_heads=32, n_kv_heads=32, head_dim=128, max_ctx=8192)
     for over, status in cases:
@@ -82,6 +88,16 @@ def test_cache_bytes_on_host(lib_path):
     tails = 4 * P * 32 * 128 * 2
     assert n >= P * NB * block + tails
     assert n < P * NB * block + tails + 64 << 20
+
+
+def test_cache_bytes_count_the_windows(lib_path):
+    """Sink windows are fp16 [P][n_sink][D] for K and V; each of the four tail
+    buffers grows to [P][residual + G][D]."""
+    k = _kvq(lib_path)
+    P, D = 8 * 32, 128
+    base = k.kvq_cache_bytes(k.make_config(8, 32, 32, D, 4096))
+    win = k.kvq_cache_bytes(k.make_config(8, 32, 32, D, 4096, n_sink=4, residual=128))
+    assert win - base == 2 * P * 4 * D * 2 + 4 * P * 128 * D * 2
 
 
 def test_status_strings(lib_path):

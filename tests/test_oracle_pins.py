@@ -451,3 +451,129 @@ def test_per_channel_keys_beat_per_token_keys_on_outlier_channels(oracle_mod):
         err[ak] = (np.mean(ke), np.mean(se))
     assert err[0][0] < err[1][0]
     assert err[0][1] < err[1][1]
+
+
+# ---- fp16 windows: attention sinks and the recent-token residual ------------
+
+def _append_rule(T, G, n_sink, residual):
+    """The windows grown one token at a time: a token fills the sink window
+    first, then joins the tail; whenever the tail holds a full group beyond
+    the residual window, its oldest G tokens are quantized."""
+    Ts = Tq = Tt = 0
+    for _ in range(T):
+        if Ts < n_sink:
+            Ts += 1
+            continue
+        Tt += 1
+        while Tt >= residual + G:
+            Tq += G
+            Tt -= G
+    return Ts, Tq, Tt
+
+
+@pytest.mark.parametrize("G", [32, 64])
+def test_window_lengths_follow_the_append_rule(oracle_mod, G):
+    for n_sink in (0, 1, 4, 40):
+        for residual in (0, 3, G, 2 * G + 5):
+            for T in range(0, 4 * G + 2 * residual + n_sink + 3):
+                got = oracle_mod.window_lengths(T, G, n_sink, residual)
+                assert got == _append_rule(T, G, n_sink, residual), (T, n_sink, residual)
+                Ts, Tq, Tt = got
+                assert Tq % G == 0 and Tt < residual + G
+
+
+@pytest.mark.parametrize("rope_on", [False, True])
+def test_all_fp16_windows_reduce_to_plain_attention(oracle_mod, rope_on):
+    """When the sink and residual windows cover every token nothing is
+    quantized, and the decode is the textbook attention over the fp16 keys
+    and values (same fp64 sums, bit for bit)."""
+    rng = np.random.default_rng(21)
+    T, D = 70, 64
+    K = rng.standard_normal((T, D)).astype(np.float16)
+    V = rng.standard_normal((T, D)).astype(np.float16)
+    q = rng.standard_normal((2, D)).astype(np.float16)
+    ref = oracle_mod.reference_pair(K, V, q, 0.125, rope_on, 10000.0)
+    for n_sink, residual in ((T, 0), (0, T), (30, 40), (T + 5, 200)):
+        st = oracle_mod.build_pair(K, V, 32, 2, 2, 0, 1, n_sink, residual)
+        assert st["Tq"] == 0
+        out = oracle_mod.decode_pair(st, q, 0.125, rope_on, 10000.0)
+        assert np.array_equal(out, ref), (n_sink, residual)
+
+
+@pytest.mark.parametrize("rope_on", [False, True])
+def test_window_tokens_keep_exact_scores(oracle_mod, rope_on):
+    """Sink tokens and the tail keep their fp16 keys: their scores equal the
+    unquantized scores exactly (RoPE at their absolute positions), while the
+    quantized tokens' scores move."""
+    rng = np.random.default_rng(22)
+    T, D, G = 150, 64, 32
+    K = rng.standard_normal((T, D)).astype(np.float16)
+    V = rng.standard_normal((T, D)).astype(np.float16)
+    q = rng.standard_normal((1, D)).astype(np.float16)
+    _, s_ref = oracle_mod.reference_pair(K, V, q, 0.125, rope_on, 10000.0, want_scores=True)
+    st = oracle_mod.build_pair(K, V, G, 2, 2, 0, 1, n_sink=5, residual=40)
+    Ts, Tq, Tt = st["Ts"], st["Tq"], st["Tt"]
+    assert (Ts, Tq, Tt) == (5, 96, 49)
+    _, s = oracle_mod.decode_pair(st, q, 0.125, rope_on, 10000.0, want_scores=True)
+    assert np.array_equal(s[:, :Ts], s_ref[:, :Ts])
+    assert np.array_equal(s[:, Ts + Tq:], s_ref[:, Ts + Tq:])
+    assert not np.array_equal(s[:, Ts:Ts + Tq], s_ref[:, Ts:Ts + Tq])
+    kh, _ = oracle_mod.dequantize_pair(oracle_mod.build_pair(K[Ts:Ts + Tq], V[Ts:Ts + Tq], G, 2, 2))
+    assert np.array_equal(kh, oracle_mod.dequantize_pair(st)[0])
+
+
+def _window_errors(oracle_mod, n_sink, residual):
+    from bit_kv_cache_11_gb300 import synth
+    w = synth.small(synth.WORKLOADS[2], batch=1, n_kv_heads=4, T=300)
+    case = synth.make_case(w, seed=2024)
+    se, oe = [], []
+    for h in range(w.n_kv_heads):
+        K, V, q = case["K"][0, h], case["V"][0, h], case["q"][0, h:h + 1]
+        st = oracle_mod.build_pair(K, V, w.group, w.bits_k, w.bits_v, 0, 1, n_sink, residual)
+        o, s = oracle_mod.decode_pair(st, q, w.scale, want_scores=True)
+        o_r, s_r = oracle_mod.reference_pair(K, V, q, w.scale, want_scores=True)
+        se.append(oracle_mod.rel_fro(s, s_r))
+        oe.append(oracle_mod.rel_fro(o, o_r))
+    return np.mean(se), np.mean(oe)
+
+
+def _sink_spike_errors(oracle_mod, n_sink):
+    """Attention sinks with massive activations: K, V ~ N(0, 1); tokens 0-3
+    have keys 8 q / |q| (they draw attention) plus 40 on two fixed channels
+    (the sink channels).  2-bit, G = 32, D = 128, T = 300, four heads."""
+    rng = np.random.default_rng(77)
+    T, D = 300, 128
+    se, oe = [], []
+    for _ in range(4):
+        q = rng.standard_normal((1, D)).astype(np.float16)
+        K = rng.standard_normal((T, D)).astype(np.float32)
+        V = rng.standard_normal((T, D)).astype(np.float16)
+        qf = q[0].astype(np.float32)
+        K[:4] = 8.0 * qf / np.linalg.norm(qf)
+        K[:4, [5, 77]] += 40.0
+        K = K.astype(np.float16)
+        st = oracle_mod.build_pair(K, V, 32, 2, 2, 0, 1, n_sink, 0)
+        o, s = oracle_mod.decode_pair(st, q, D ** -0.5, want_scores=True)
+        o_r, s_r = oracle_mod.reference_pair(K, V, q, D ** -0.5, want_scores=True)
+        se.append(oracle_mod.rel_fro(s[:, 4:32], s_r[:, 4:32]))
+        oe.append(oracle_mod.rel_fro(o, o_r))
+    return np.mean(se), np.mean(oe)
+
+
+def test_sink_window_lowers_error_on_sink_tokens(oracle_mod):
+    """Outliers in the sink tokens' channels widen the key groups they share
+    with ordinary tokens; keeping the sinks in fp16 (quantized groups start
+    after them) lowers the score error of the ordinary tokens that would have
+    shared the sinks' groups (positions 4-31) and the attention-output error
+    — the pages' reason for high-precision sink windows (direction only)."""
+    s0, o0 = _sink_spike_errors(oracle_mod, 0)
+    s4, o4 = _sink_spike_errors(oracle_mod, 4)
+    assert s4 < s0 and o4 < 0.5 * o0
+
+
+def test_residual_window_lowers_error(oracle_mod):
+    """A full-precision window of the most recent tokens lowers the
+    attention error (the pages' residual-buffer result, direction only)."""
+    s0, o0 = _window_errors(oracle_mod, 0, 0)
+    s1, o1 = _window_errors(oracle_mod, 0, 128)
+    assert s1 < s0 and o1 < o0
