@@ -67,8 +67,15 @@ def _load():
     lib.kvo_f2h_array.argtypes = [P, P, L]
     lib.kvo_quantize_group.argtypes = [P, L, I, I, P, P, P]
     lib.kvo_quantize_tensor.restype = I
-    lib.kvo_quantize_tensor.argtypes = [I, I, I, I, I, P, P, P, P]
-    lib.kvo_dequantize_tensor.argtypes = [I, I, I, I, P, P, P, P]
+    lib.kvo_quantize_tensor.argtypes = [I, I, I, I, I, I, P, P, P, P]
+    lib.kvo_dequantize_tensor.argtypes = [I, I, I, I, I, P, P, P, P]
+    lib.kvo_quantize_group_fp8.argtypes = [P, L, I, P, P, P]
+    lib.kvo_e4m3_value.restype = ctypes.c_float
+    lib.kvo_e4m3_value.argtypes = [ctypes.c_uint8]
+    lib.kvo_e4m3_encode.restype = ctypes.c_uint8
+    lib.kvo_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.kvo_e4m3_value_array.argtypes = [P, P, L]
+    lib.kvo_e4m3_encode_array.argtypes = [P, P, L]
     lib.kvo_block_bytes.restype = ctypes.c_size_t
     lib.kvo_code_order.argtypes = [I, I, I, I, I]
     lib.kvo_code_order.restype = I
@@ -125,9 +132,36 @@ def quantize_group(x_f16: np.ndarray, bits: int):
     return int(s[0]), int(z[0]), codes
 
 
-def quantize_tensor(X_f16: np.ndarray, G: int, bits: int, axis: int):
+def e4m3_value(codes) -> np.ndarray:
+    """fp32 values of E4M3 codes (NaN for 0x7F and 0xFF)."""
+    c = _c(np.asarray(codes, np.uint8).reshape(-1), np.uint8)
+    out = np.zeros(c.size, np.float32)
+    _load().kvo_e4m3_value_array(_p(c), _p(out), c.size)
+    return out.reshape(np.shape(codes))
+
+
+def e4m3_encode(y) -> np.ndarray:
+    """Nearest E4M3 codes of fp32 values (ties to even, saturating at 448)."""
+    f = _c(np.asarray(y, np.float32).reshape(-1), np.float32)
+    out = np.zeros(f.size, np.uint8)
+    _load().kvo_e4m3_encode_array(_p(f), _p(out), f.size)
+    return out.reshape(np.shape(y))
+
+
+def quantize_group_fp8(x_f16: np.ndarray):
+    """One FP8 group: returns (scale fp16 bits, zero fp16 bits, E4M3 codes)."""
+    x = bits_of(x_f16).reshape(-1)
+    s = np.zeros(1, np.uint16)
+    z = np.zeros(1, np.uint16)
+    codes = np.zeros(x.size, np.uint8)
+    _load().kvo_quantize_group_fp8(_p(x), 1, x.size, _p(s), _p(z), _p(codes))
+    return int(s[0]), int(z[0]), codes
+
+
+def quantize_tensor(X_f16: np.ndarray, G: int, bits: int, axis: int, fp8: bool = False):
     """X: fp16 [T][D].  Returns (Tq, codes [Tq][D], scale bits, zero bits) with
-    scale/zero shaped [Tq/G][D] (channel axis) or [Tq][D/G] (token axis)."""
+    scale/zero shaped [Tq/G][D] (channel axis) or [Tq][D/G] (token axis).
+    fp8: E4M3 codes with absmax scales (bits must be 8)."""
     T, D = X_f16.shape
     Tq = (T // G) * G
     x = bits_of(X_f16)
@@ -135,16 +169,17 @@ def quantize_tensor(X_f16: np.ndarray, G: int, bits: int, axis: int):
     mshape = (Tq // G, D) if axis == 0 else (Tq, D // G)
     scale = np.zeros(mshape, np.uint16)
     zero = np.zeros(mshape, np.uint16)
-    got = _load().kvo_quantize_tensor(T, D, G, bits, axis, _p(x), _p(codes), _p(scale), _p(zero))
+    got = _load().kvo_quantize_tensor(T, D, G, bits, 1 if fp8 else 0, axis, _p(x), _p(codes),
+                                      _p(scale), _p(zero))
     assert got == Tq
     return Tq, codes, scale, zero
 
 
-def dequantize_tensor(codes, scale, zero, G: int, axis: int) -> np.ndarray:
+def dequantize_tensor(codes, scale, zero, G: int, axis: int, fp8: bool = False) -> np.ndarray:
     Tq, D = codes.shape
     out = np.zeros((Tq, D), np.float32)
     c, s, z = _c(codes, np.uint8), _c(scale, np.uint16), _c(zero, np.uint16)
-    _load().kvo_dequantize_tensor(Tq, D, G, axis, _p(c), _p(s), _p(z), _p(out))
+    _load().kvo_dequantize_tensor(Tq, D, G, axis, 1 if fp8 else 0, _p(c), _p(s), _p(z), _p(out))
     return out
 
 
@@ -214,18 +249,21 @@ def window_lengths(T: int, G: int, n_sink: int = 0, residual: int = 0):
 
 
 def build_pair(K_f16: np.ndarray, V_f16: np.ndarray, G: int, bk: int, bv: int,
-               ak: int = 0, av: int = 1, n_sink: int = 0, residual: int = 0) -> dict:
+               ak: int = 0, av: int = 1, n_sink: int = 0, residual: int = 0,
+               fp8: bool = False) -> dict:
     """The cache state of one pair after its T tokens arrived (any mix of
     prefill and appends): the sink tokens in fp16, then the quantized groups,
     then the fp16 tail (window_lengths gives the three counts).  The state
     does not depend on how the tokens were split into calls, because every
-    flush leaves the same G-aligned boundary."""
+    flush leaves the same G-aligned boundary.  fp8: both sides stored as E4M3
+    with absmax scales (bk = bv = 8)."""
     T, D = K_f16.shape
+    assert not fp8 or bk == bv == 8
     Ts, Tq, Tt = window_lengths(T, G, n_sink, residual)
-    Tq_, kc, ks, kz = quantize_tensor(K_f16[Ts:Ts + Tq], G, bk, ak)
-    _, vc, vs, vz = quantize_tensor(V_f16[Ts:Ts + Tq], G, bv, av)
+    Tq_, kc, ks, kz = quantize_tensor(K_f16[Ts:Ts + Tq], G, bk, ak, fp8)
+    _, vc, vs, vz = quantize_tensor(V_f16[Ts:Ts + Tq], G, bv, av, fp8)
     assert Tq_ == Tq
-    return dict(G=G, bk=bk, bv=bv, ak=ak, av=av, Ts=Ts, Tq=Tq, Tt=Tt,
+    return dict(G=G, bk=bk, bv=bv, ak=ak, av=av, fp8=fp8, Ts=Ts, Tq=Tq, Tt=Tt,
                 kcodes=kc, kscale=ks, kzero=kz, vcodes=vc, vscale=vs, vzero=vz,
                 ksink=np.ascontiguousarray(K_f16[:Ts], np.float16),
                 vsink=np.ascontiguousarray(V_f16[:Ts], np.float16),
@@ -234,8 +272,9 @@ def build_pair(K_f16: np.ndarray, V_f16: np.ndarray, G: int, bk: int, bv: int,
 
 
 def dequantize_pair(st: dict):
-    kh = dequantize_tensor(st["kcodes"], st["kscale"], st["kzero"], st["G"], st["ak"])
-    vh = dequantize_tensor(st["vcodes"], st["vscale"], st["vzero"], st["G"], st["av"])
+    f8 = st.get("fp8", False)
+    kh = dequantize_tensor(st["kcodes"], st["kscale"], st["kzero"], st["G"], st["ak"], f8)
+    vh = dequantize_tensor(st["vcodes"], st["vscale"], st["vzero"], st["G"], st["av"], f8)
     return kh, vh
 
 

@@ -90,13 +90,101 @@ void kvo_quantize_group(const uint16_t* x, long stride, int n, int bits,
   }
 }
 
+/* ---- FP8 (E4M3) ------------------------------------------------------------
+ * The 8-bit floating-point format E4M3 of the OCP 8-bit floating point
+ * specification: 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits.
+ * Exponent field 0 holds zero and the subnormals m * 2^-9; there are no
+ * infinities and S.1111.111 is NaN, so the largest finite magnitude is
+ * S.1111.110 = 1.75 * 2^8 = 448.  An FP8 cache ("Rotate, Then Round: The
+ * Geometry of KV-Cache Compression", "Key takeaway" and "In practice") stores
+ * each element as E4M3 after dividing it by its group's scale. */
+
+/* Value of an E4M3 code (NaN for the two NaN codes). */
+float kvo_e4m3_value(uint8_t c) {
+  int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+  if (e == 15 && m == 7) return NAN;
+  double v = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return (float)(sign ? -v : v);
+}
+
+/* Nearest E4M3 code of a finite fp32 value, ties to the even mantissa;
+ * magnitudes at or above 448 give +-448 (saturation).  The sign is kept,
+ * also for values that round to zero. */
+uint8_t kvo_e4m3_encode(float y) {
+  int neg = signbit(y) ? 1 : 0;
+  double a = fabs((double)y);
+  uint8_t code;
+  if (a >= 448.0) {
+    code = 0x7E;
+  } else {
+    /* spacing of the representable values around a: 2^(e-3) in the binade
+     * [2^e, 2^(e+1)) for e >= -6, and 2^-9 below 2^-6 (subnormals) */
+    int e = -6;
+    if (a >= ldexp(1.0, -6)) {
+      frexp(a, &e);
+      e -= 1;
+    }
+    double q = ldexp(1.0, e - 3);
+    double v = rint(a / q) * q; /* a / q is exact; rint rounds half to even */
+    if (v == 0.0) {
+      code = 0;
+    } else if (v < ldexp(1.0, -6)) {
+      code = (uint8_t)(v / ldexp(1.0, -9));
+    } else {
+      int e2;
+      frexp(v, &e2);
+      e2 -= 1;
+      code = (uint8_t)(((e2 + 7) << 3) | (int)((v / ldexp(1.0, e2) - 1.0) * 8.0));
+    }
+  }
+  return neg ? (uint8_t)(code | 0x80) : code;
+}
+
+void kvo_e4m3_value_array(const uint8_t* c, float* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = kvo_e4m3_value(c[i]);
+}
+
+void kvo_e4m3_encode_array(const float* y, uint8_t* out, long n) {
+  for (long i = 0; i < n; ++i) out[i] = kvo_e4m3_encode(y[i]);
+}
+
+/* One group of an FP8 cache: scale = fp16(max |x| / 448) (IEEE fp32 divide,
+ * then round to fp16), zero point 0, code = E4M3(x / scale) with the IEEE
+ * fp32 quotient.  A stored scale of 0 gives code 0 everywhere. */
+void kvo_quantize_group_fp8(const uint16_t* x, long stride, int n,
+                            uint16_t* scale_out, uint16_t* zero_out,
+                            uint8_t* codes) {
+  float amax = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    float v = fabsf(kvo_h2f(x[(long)i * stride]));
+    if (v > amax) amax = v;
+  }
+  uint16_t s_h = kvo_f2h(amax / 448.0f);
+  float s = kvo_h2f(s_h);
+  *scale_out = s_h;
+  *zero_out = 0;
+  for (int i = 0; i < n; ++i) {
+    float v = kvo_h2f(x[(long)i * stride]);
+    codes[i] = (s != 0.0f) ? kvo_e4m3_encode(v / s) : 0;
+  }
+}
+
 /* ---- one tensor (K or V) of one pair ------------------------------------- */
 
 /* X: fp16 [T][D].  Quantizes tokens [0, Tq), Tq = floor(T/G)*G.
  * codes: [Tq][D].  scale/zero: axis 0 (channel) -> [Tq/G][D], entry (i, d) is
  * channel d over tokens [i*G, (i+1)*G); axis 1 (token) -> [Tq][D/G], entry
  * (t, g) is token t over channels [g*G, (g+1)*G).  Returns Tq. */
-int kvo_quantize_tensor(int T, int D, int G, int bits, int axis,
+static void quantize_group_fmt(const uint16_t* x, long stride, int n, int bits,
+                               int fp8, uint16_t* scale_out, uint16_t* zero_out,
+                               uint8_t* codes) {
+  if (fp8)
+    kvo_quantize_group_fp8(x, stride, n, scale_out, zero_out, codes);
+  else
+    kvo_quantize_group(x, stride, n, bits, scale_out, zero_out, codes);
+}
+
+int kvo_quantize_tensor(int T, int D, int G, int bits, int fp8, int axis,
                         const uint16_t* X, uint8_t* codes, uint16_t* scale,
                         uint16_t* zero) {
   int Tq = (T / G) * G;
@@ -105,7 +193,7 @@ int kvo_quantize_tensor(int T, int D, int G, int bits, int axis,
     for (int i = 0; i < Tq / G; ++i) {
       for (int d = 0; d < D; ++d) {
         const uint16_t* first = X + (size_t)(i * G) * D + d;
-        kvo_quantize_group(first, D, G, bits, &scale[(size_t)i * D + d],
+        quantize_group_fmt(first, D, G, bits, fp8, &scale[(size_t)i * D + d],
                            &zero[(size_t)i * D + d], tmp);
         for (int j = 0; j < G; ++j) codes[(size_t)(i * G + j) * D + d] = tmp[j];
       }
@@ -115,7 +203,7 @@ int kvo_quantize_tensor(int T, int D, int G, int bits, int axis,
     for (int t = 0; t < Tq; ++t) {
       for (int g = 0; g < ng; ++g) {
         const uint16_t* first = X + (size_t)t * D + (size_t)g * G;
-        kvo_quantize_group(first, 1, G, bits, &scale[(size_t)t * ng + g],
+        quantize_group_fmt(first, 1, G, bits, fp8, &scale[(size_t)t * ng + g],
                            &zero[(size_t)t * ng + g], tmp);
         for (int j = 0; j < G; ++j) codes[(size_t)t * D + (size_t)g * G + j] = tmp[j];
       }
@@ -127,9 +215,10 @@ int kvo_quantize_tensor(int T, int D, int G, int bits, int axis,
 
 /* ---- dequantization ------------------------------------------------------ */
 
-/* out[t][d] = fmaf(code, scale, zero) in fp32, with the scale/zero entry the
- * axis selects. */
-void kvo_dequantize_tensor(int Tq, int D, int G, int axis,
+/* out[t][d] = fmaf(value, scale, zero) in fp32, with the scale/zero entry the
+ * axis selects; value is the integer code, or its E4M3 value for an FP8
+ * cache. */
+void kvo_dequantize_tensor(int Tq, int D, int G, int axis, int fp8,
                            const uint8_t* codes, const uint16_t* scale,
                            const uint16_t* zero, float* out) {
   for (int t = 0; t < Tq; ++t) {
@@ -138,7 +227,9 @@ void kvo_dequantize_tensor(int Tq, int D, int G, int axis,
                              : (size_t)t * (D / G) + (size_t)(d / G);
       float s = kvo_h2f(scale[m]);
       float z = kvo_h2f(zero[m]);
-      out[(size_t)t * D + d] = fmaf((float)codes[(size_t)t * D + d], s, z);
+      uint8_t c = codes[(size_t)t * D + d];
+      float v = fp8 ? kvo_e4m3_value(c) : (float)c;
+      out[(size_t)t * D + d] = fmaf(v, s, z);
     }
   }
 }

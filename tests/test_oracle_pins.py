@@ -577,3 +577,104 @@ def test_residual_window_lowers_error(oracle_mod):
     s0, o0 = _window_errors(oracle_mod, 0, 0)
     s1, o1 = _window_errors(oracle_mod, 0, 128)
     assert s1 < s0 and o1 < o0
+
+
+# ---- FP8 (E4M3) -----------------------------------------------------------
+
+def test_e4m3_anchor_values(oracle_mod):
+    """Codes whose values the format fixes: zero, the smallest subnormal and
+    normal, one, two, the largest finite value, signs, NaN."""
+    v = oracle_mod.e4m3_value
+    assert v(0x00) == 0.0 and v(0x80) == 0.0 and np.signbit(v(0x80))
+    assert v(0x01) == 2.0 ** -9 and v(0x07) == 7 * 2.0 ** -9
+    assert v(0x08) == 2.0 ** -6 and v(0x38) == 1.0 and v(0x40) == 2.0
+    assert v(0x3F) == 1.875 and v(0x77) == 240.0 and v(0x7E) == 448.0
+    assert v(0xB8) == -1.0 and v(0xFE) == -448.0
+    assert np.isnan(v(0x7F)) and np.isnan(v(0xFF))
+    pos = oracle_mod.e4m3_value(np.arange(0x7F, dtype=np.uint8))
+    assert np.all(np.diff(pos) > 0)                      # increasing over the finite codes
+    neg = oracle_mod.e4m3_value(np.arange(0x80, 0xFF, dtype=np.uint8))
+    assert np.array_equal(neg, -pos)
+
+
+def test_e4m3_matches_torch_float8(oracle_mod):
+    """An independent implementation: torch's float8_e4m3fn (decode every
+    code; encode values inside the finite range, where both round to the
+    nearest value with ties to even)."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().numpy()
+    got = oracle_mod.e4m3_value(codes)
+    fin = ~np.isnan(ref)
+    assert np.array_equal(np.isnan(got), ~fin)
+    assert np.array_equal(got[fin], ref[fin])
+    rng = np.random.default_rng(31)
+    y = np.concatenate([rng.uniform(-448, 448, 20000), rng.standard_normal(20000) * 2.0 ** -7,
+                        oracle_mod.e4m3_value(codes[fin]).astype(np.float64) * (1 + 2.0 ** -5)])
+    y = np.clip(y, -448, 448).astype(np.float32)
+    want = torch.from_numpy(y).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle_mod.e4m3_encode(y), want)
+
+
+def test_e4m3_encode_is_nearest_even(oracle_mod):
+    """Brute force over the finite values, hand-made ties and saturation."""
+    finite = np.arange(0x7F, dtype=np.uint8)
+    vals = oracle_mod.e4m3_value(finite).astype(np.float64)
+    rng = np.random.default_rng(32)
+    y = np.concatenate([rng.uniform(0, 460, 5000), rng.uniform(0, 2.0 ** -5, 5000)]).astype(np.float32)
+    got = oracle_mod.e4m3_encode(y)
+    for yi, ci in zip(y.astype(np.float64), got):
+        d = np.abs(vals - yi)
+        best = np.flatnonzero(d == d.min())
+        want = best[0] if best.size == 1 else [b for b in best if b % 2 == 0][0]
+        if yi >= 448:
+            want = 0x7E
+        assert ci == want, (yi, ci, want)
+    ties = {1.0625: 0x38, 1.1875: 0x3A, 2.0 ** -10: 0x00, 3 * 2.0 ** -10: 0x02,
+            432.0: 0x7E, 400.0: 0x7C, 464.0: 0x7E, 1.0e6: 0x7E}
+    for yi, ci in ties.items():
+        assert oracle_mod.e4m3_encode(np.float32(yi)) == ci, yi
+        assert oracle_mod.e4m3_encode(np.float32(-yi)) == ci | 0x80, -yi
+
+
+def test_fp8_group_rule(oracle_mod):
+    """Scale = fp16(max|x| / 448), zero 0; the largest magnitude codes to
+    +-448; every other element to its nearest E4M3 multiple of the scale; a
+    group of zeros gives scale 0 and codes 0."""
+    rng = np.random.default_rng(33)
+    for _ in range(200):
+        x = (rng.standard_normal(32) * rng.choice([1e-3, 1.0, 30.0, 3000.0])).astype(np.float16)
+        s_h, z_h, codes = oracle_mod.quantize_group_fp8(x)
+        xf = x.astype(np.float32)
+        amax = np.abs(xf).max()
+        assert s_h == oracle_mod.f2h(np.float32(amax / np.float32(448.0))).item() and z_h == 0
+        s = oracle_mod.h2f(np.uint16(s_h)).item()
+        i = int(np.argmax(np.abs(xf)))
+        assert codes[i] & 0x7F == 0x7E
+        assert np.array_equal(codes, oracle_mod.e4m3_encode((xf / np.float32(s)).astype(np.float32)))
+        xh = oracle_mod.e4m3_value(codes).astype(np.float64) * s
+        # relative error at most 2^-4 (three mantissa bits) above the subnormal range
+        big = np.abs(xf) >= 2.0 ** -6 * s * 1.0001
+        assert np.all(np.abs(xh - xf)[big] <= 2.0 ** -4 * np.abs(xf)[big] * (1 + 2.0 ** -10))
+    s_h, z_h, codes = oracle_mod.quantize_group_fp8(np.zeros(32, np.float16))
+    assert s_h == 0 and not codes.any()
+
+
+def test_fp8_dequantize_is_value_times_scale(oracle_mod):
+    rng = np.random.default_rng(34)
+    X = (rng.standard_normal((64, 64)) * 5).astype(np.float16)
+    for axis in (0, 1):
+        _, codes, sc, zr = oracle_mod.quantize_tensor(X, 32, 8, axis, fp8=True)
+        assert not zr.any()
+        got = oracle_mod.dequantize_tensor(codes, sc, zr, 32, axis, fp8=True)
+        s = oracle_mod.h2f(sc).astype(np.float64)
+        s = np.repeat(s, 32, axis=0) if axis == 0 else np.repeat(s, 32, axis=1)
+        want = oracle_mod.e4m3_value(codes).astype(np.float64) * s
+        assert np.array_equal(got.astype(np.float64), want)
+        # FP8 keeps more of the signal than 4-bit integer codes on the same groups
+        _, c4, s4, z4 = oracle_mod.quantize_tensor(X, 32, 4, axis)
+        e8 = oracle_mod.rel_fro(got, X.astype(np.float32))
+        e4 = oracle_mod.rel_fro(oracle_mod.dequantize_tensor(c4, s4, z4, 32, axis), X.astype(np.float32))
+        assert e8 < e4
