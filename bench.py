@@ -42,11 +42,11 @@ def decode_bytes(w, T_q, T_t):
     return codes + meta + tail + qo
 
 
-def windows_leg(w, dev, stream, n_sink, residual, n_layers, warmup, steps):
-    """The same decode step on caches that keep the first n_sink tokens and a
-    window of `residual` recent tokens in fp16 (kvq_append_decode per layer).
-    Algorithmic bytes count the sink rows like tail rows; the single-launch
-    steps are averaged, as for the main line."""
+def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, fp8=False):
+    """The same decode step on a variant of the cache: fp16 windows (the first
+    n_sink tokens and `residual` recent tokens kept in fp16) or the FP8 (E4M3)
+    format (w with 8-bit sides).  Algorithmic bytes count sink rows like tail
+    rows; the single-launch steps are averaged, as for the main line."""
     import torch
     from bit_kv_cache_11_gb300 import kvq
     caches, steps_dev = [], []
@@ -56,7 +56,7 @@ def windows_leg(w, dev, stream, n_sink, residual, n_layers, warmup, steps):
         c = kvq.KVCache(batch=w.batch, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads,
                         head_dim=w.head_dim, max_ctx=w.T + warmup + steps + 32, bits_k=w.bits_k,
                         bits_v=w.bits_v, group=w.group, axis_k=w.axis_k, axis_v=w.axis_v,
-                        n_sink=n_sink, residual=residual)
+                        n_sink=n_sink, residual=residual, fp8=fp8)
         c.prefill(torch.from_numpy(case["K"]).to(dev), torch.from_numpy(case["V"]).to(dev))
         st = synth.make_decode_steps(w, warmup + steps, seed=seed + 500, outliers=case["outliers"])
         steps_dev.append([{k: torch.from_numpy(v).to(dev) for k, v in x.items()} for x in st])
@@ -90,8 +90,8 @@ def windows_leg(w, dev, stream, n_sink, residual, n_layers, warmup, steps):
     nb = statistics.mean(b for _, _, b in timed)
     peak, src = load_peaks()
     gbs = nb / (ms * 1e-3) / 1e9
-    return {"workload": f"{w.name}-sink{n_sink}-res{residual}", "n_sink": n_sink,
-            "residual": residual, "GB/s": gbs, "frac": gbs / peak, "peak_source": f"hbm_gbs of {src}",
+    name = w.name.replace("-2bit", "-fp8") if fp8 else f"{w.name}-sink{n_sink}-res{residual}"
+    return {"workload": name, "n_sink": n_sink, "residual": residual, "fp8": fp8, "GB/s": gbs, "frac": gbs / peak, "peak_source": f"hbm_gbs of {src}",
             "ms_per_launch": ms, "bytes_per_launch": nb, "launches_timed": len(timed)}
 
 
@@ -430,9 +430,11 @@ def run_gpu(args, w):
                   "cpu_oracle_Mtok_s": (t_cpu_tokens / w4.n_kv_heads / t_cpu / 1e6) if t_cpu else None}
         del K4, V4, flush
 
-    win_line = None
+    win_line = fp8_line = None
     if rank == 0 and not args.skip_windows:
-        win_line = windows_leg(w, dev, stream, 4, 128, L, 3, min(args.steps, 10))
+        win_line = variant_leg(w, dev, stream, L, 3, min(args.steps, 10), n_sink=4, residual=128)
+        fp8_line = variant_leg(w.with_(bits_k=8, bits_v=8), dev, stream, L, 3, min(args.steps, 10),
+                               fp8=True)
 
     if rank != 0:
         if ws > 1:
@@ -476,6 +478,7 @@ def run_gpu(args, w):
         "clocks": clk.summary(),
         "quantize": q_line,
         "windows": win_line,
+        "fp8": fp8_line,
         "frac_of_8tbs_spec": achieved / 8000.0,
     }
     print(json.dumps(line), flush=True)

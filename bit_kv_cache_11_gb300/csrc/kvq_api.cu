@@ -61,6 +61,8 @@ kvq_status derive(const kvq_config* c, Derived* d) {
     return KVQ_ERR_INVALID_ARG;
   if (c->n_sink < 0 || c->n_sink > 1024 || c->residual < 0 || c->residual > 4096)
     return KVQ_ERR_INVALID_ARG;
+  if (c->fp8 != 0 && c->fp8 != 1) return KVQ_ERR_INVALID_ARG;
+  if (c->fp8 && (c->bits_k != 8 || c->bits_v != 8)) return KVQ_ERR_INVALID_ARG;
   if ((c->axis_k == 1 || c->axis_v == 1) && c->head_dim % c->group != 0)
     return KVQ_ERR_INVALID_ARG;
   const int R = c->n_q_heads / c->n_kv_heads;
@@ -166,6 +168,7 @@ static CacheGeom geom_of(const kvq_cache* c) {
   g.ak = c->cfg.axis_k;
   g.av = c->cfg.axis_v;
   g.P = c->dv.P;
+  g.fp8 = c->cfg.fp8;
   g.TC = c->dv.TC;
   g.NSK = c->dv.NSK;
   return g;
@@ -272,11 +275,13 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   // G = 32 (with its rotated-key variant for keys stored before RoPE); the
   // CUDA-core kernel for every other geometry.  Codes in fragment order are
   // read by the tensor-core kernel only.
+  // (an FP8 cache dispatches on the E4M3 tag instead of its 8 bits)
+  const int bk = cfg->fp8 ? kBitsE4M3 : cfg->bits_k, bv = cfg->fp8 ? kBitsE4M3 : cfg->bits_v;
   DecodeOps ops{nullptr, nullptr};
-  if (d.mma_geom) ops = decode_mma_ops(d.D, d.R, cfg->bits_k, cfg->bits_v, cfg->keys_pre_rope != 0);
+  if (d.mma_geom) ops = decode_mma_ops(d.D, d.R, bk, bv, cfg->keys_pre_rope != 0);
   const bool mma = ops.launch != nullptr;
   if ((d.frag_k || d.frag_v) && !mma) return KVQ_ERR_UNSUPPORTED;
-  if (ops.launch == nullptr) ops = decode_ops(d.D, d.R, cfg->bits_k, cfg->bits_v);
+  if (ops.launch == nullptr) ops = decode_ops(d.D, d.R, bk, bv);
   if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
 
   kvq_cache* c = new (std::nothrow) kvq_cache();

@@ -60,7 +60,7 @@ struct DecodeCfg {
   static_assert((CPL * BV) % 2 == 0, "V words are read in pairs");
 };
 
-template <int D, int BK, int BV, int R>
+template <int D, int BK, int BV, int R, bool F8 = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
     decode_split_kernel(const DecodeParams p) {
   using C = DecodeCfg<D, BK, BV, R>;
@@ -206,7 +206,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       }
     }
     auto kcode = [&](int d) -> float {
-      return code_to_float((kr[d / KPER] >> ((d % KPER) * BK)) & KMASK);
+      return code_value<F8>((kr[d / KPER] >> ((d % KPER) * BK)) & KMASK);
     };
     if (p.rope) {
       const int pos = p.T_s + j * 32 + lane;
@@ -316,7 +316,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
           zacc[r] = fmaf(pr, sz.y, zacc[r]);
 #pragma unroll
           for (int c = 0; c < CPL; ++c)
-            acc[r][c] = fmaf(pt, code_to_float((vw[c * BV + w] >> sh) & VMASK), acc[r][c]);
+            acc[r][c] = fmaf(pt, code_value<F8>((vw[c * BV + w] >> sh) & VMASK), acc[r][c]);
         }
       }
     } else {
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
           const float pr = pb[r * 32 + t];
 #pragma unroll
           for (int c = 0; c < CPL; ++c)
-            a[r][c] = fmaf(pr, code_to_float((vw[c * BV + w] >> sh) & VMASK), a[r][c]);
+            a[r][c] = fmaf(pr, code_value<F8>((vw[c * BV + w] >> sh) & VMASK), a[r][c]);
         }
       }
 #pragma unroll
@@ -455,21 +455,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 }
 
 // Host-side entry points of one instantiation.
-template <int D, int BK, int BV, int R>
+template <int D, int BK, int BV, int R, bool F8 = false>
 cudaError_t decode_prepare(int* ctas_per_sm) {
   using C = DecodeCfg<D, BK, BV, R>;
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, BK, BV, R>,
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, BK, BV, R, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, decode_split_kernel<D, BK, BV, R>, kDecodeWarps * 32, C::SMEM);
+      ctas_per_sm, decode_split_kernel<D, BK, BV, R, F8>, kDecodeWarps * 32, C::SMEM);
 }
 
-template <int D, int BK, int BV, int R>
+template <int D, int BK, int BV, int R, bool F8 = false>
 cudaError_t decode_launch(const DecodeParams& p, cudaStream_t stream) {
   using C = DecodeCfg<D, BK, BV, R>;
   const int grid = (p.n_warps + kDecodeWarps - 1) / kDecodeWarps;
-  decode_split_kernel<D, BK, BV, R><<<grid, kDecodeWarps * 32, C::SMEM, stream>>>(p);
+  decode_split_kernel<D, BK, BV, R, F8><<<grid, kDecodeWarps * 32, C::SMEM, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -486,6 +486,8 @@ DecodeOps decode_ops_for(int bk, int bv) {
   KVQ_CASE(4, 2) KVQ_CASE(4, 4) KVQ_CASE(4, 8)
   KVQ_CASE(8, 2) KVQ_CASE(8, 4) KVQ_CASE(8, 8)
 #undef KVQ_CASE
+  if (bk == kBitsE4M3 && bv == kBitsE4M3)
+    return DecodeOps{decode_prepare<D, 8, 8, R, true>, decode_launch<D, 8, 8, R, true>};
   return DecodeOps{nullptr, nullptr};
 }
 

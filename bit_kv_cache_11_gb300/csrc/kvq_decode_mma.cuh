@@ -88,12 +88,20 @@ __device__ __forceinline__ void frag_a4(uint32_t w, uint32_t& a0, uint32_t& a1, 
 
 // 8-bit codes in sequential order -> fp16 operand registers of one
 // 16-element slice.  x0 covers fragment columns (2t, 2t+1), x2 covers
-// (2t+8, 2t+9); element e sits in lane lane_t(e), register reg(e).
+// (2t+8, 2t+9); element e sits in lane lane_t(e), register reg(e).  Integer
+// codes become exact fp16 values through 1024 + c; E4M3 codes (F8) through
+// the fp8-pair conversion, also exact.
 struct Frag8 {
   static constexpr int PARTNER = 1;  // element sharing lane and register, other half
   __device__ static __forceinline__ int base(int i) { return 2 * i; }
+  template <bool F8>
   __device__ static __forceinline__ void get(const uint32_t* w, int t, uint32_t& x0, uint32_t& x2) {
     const uint32_t v = w[t];
+    if constexpr (F8) {
+      x0 = e4m3x2_to_half2(v);        // elements 4t, 4t+1
+      x2 = e4m3x2_to_half2(v >> 16);  // elements 4t+2, 4t+3
+      return;
+    }
     const __half2 k1024 = __float2half2_rn(1024.0f);
     uint32_t p0 = __byte_perm(v, 0x64646464u, 0x4140u);  // 1024 + byte0, 1024 + byte1
     uint32_t p2 = __byte_perm(v, 0x64646464u, 0x4342u);  // 1024 + byte2, 1024 + byte3
@@ -178,7 +186,7 @@ __device__ __forceinline__ int bslot(int blk, int l) {
   return blk * BL + (l ^ (BL == 8 ? 4 * ((blk >> 1) & 1) : 4 * (blk & 3)));
 }
 
-template <int D, int BK, int BV, int R, bool ROPE>
+template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (R <= 4 ? 3 : 1))
     decode_mma_kernel(const DecodeParams p) {
   using C = MmaCfg<D, BK, BV, R, ROPE>;
@@ -480,8 +488,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t a0, a1, a2, a3;
-          Frag8::get(r0 + ks * 4, t, a0, a2);
-          Frag8::get(r1 + ks * 4, t, a1, a3);
+          Frag8::get<F8>(r0 + ks * 4, t, a0, a2);
+          Frag8::get<F8>(r1 + ks * 4, t, a1, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
@@ -645,8 +653,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
           uint32_t a0, a1, a2, a3;
-          Frag8::get(c0 + ks * 4, t, a0, a2);
-          Frag8::get(c1 + ks * 4, t, a1, a3);
+          Frag8::get<F8>(c0 + ks * 4, t, a0, a2);
+          Frag8::get<F8>(c1 + ks * 4, t, a1, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
@@ -734,8 +742,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       for (int r = 0; r < R; ++r) sc[r] = 0.f;
 #pragma unroll
       for (int i = 0; i < H; ++i) {
-        const float c0 = code_to_float(kcode(i));
-        const float c1 = code_to_float(kcode(i + H));
+        const float c0 = code_value<F8>(kcode(i));
+        const float c1 = code_value<F8>(kcode(i + H));
         const float2 cs = cs_tab[i * 32 + lane];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
@@ -1091,17 +1099,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   if (cur >= 0) write_partial(cur);
 }
 
-template <int D, int BK, int BV, int R, bool ROPE>
+template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false>
 cudaError_t decode_mma_prepare(int* ctas_per_sm) {
   using C = MmaCfg<D, BK, BV, R, ROPE>;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BK, BV, R, ROPE>,
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BK, BV, R, ROPE, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, decode_mma_kernel<D, BK, BV, R, ROPE>, kDecodeWarps * 32, C::SMEM);
+      ctas_per_sm, decode_mma_kernel<D, BK, BV, R, ROPE, F8>, kDecodeWarps * 32, C::SMEM);
 }
 
-template <int D, int BK, int BV, int R, bool ROPE>
+template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false>
 cudaError_t decode_mma_launch(const DecodeParams& p, cudaStream_t stream) {
   using C = MmaCfg<D, BK, BV, R, ROPE>;
   // programmatic stream serialization: the grid may start while the previous
@@ -1116,7 +1124,7 @@ cudaError_t decode_mma_launch(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BK, BV, R, ROPE>, p);
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BK, BV, R, ROPE, F8>, p);
 }
 
 // Every (bits_k, bits_v) pair of the geometry (G = 32, keys per channel,
@@ -1131,6 +1139,9 @@ DecodeOps decode_mma_ops_for(int bk, int bv) {
   KVQ_CASE(4, 2) KVQ_CASE(4, 4) KVQ_CASE(4, 8)
   KVQ_CASE(8, 2) KVQ_CASE(8, 4) KVQ_CASE(8, 8)
 #undef KVQ_CASE
+  if (bk == kBitsE4M3 && bv == kBitsE4M3)
+    return DecodeOps{decode_mma_prepare<D, 8, 8, R, ROPE, true>,
+                     decode_mma_launch<D, 8, 8, R, ROPE, true>};
   return DecodeOps{nullptr, nullptr};
 }
 

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -79,6 +80,39 @@ __device__ __forceinline__ float code_to_float(uint32_t c) {
   return __int_as_float(0x4B000000u | c) - 8388608.0f;
 }
 
+// ---------------------------------------------------------------- FP8 (E4M3)
+
+// Dispatch tag for a side stored as E4M3 (an 8-bit side of an FP8 cache).
+constexpr int kBitsE4M3 = -8;
+
+// E4M3 code of a finite fp32 value: nearest, ties to even, saturating at
+// +-448 (the conversion instruction's satfinite mode).
+__device__ __forceinline__ uint32_t e4m3_encode(float y) {
+  return static_cast<uint32_t>(__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3));
+}
+
+// Exact fp32 value of an E4M3 code.
+__device__ __forceinline__ float e4m3_value(uint32_t c) {
+  const __half_raw h =
+      __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c & 0xffu), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Bytes 0 and 1 of v (two E4M3 codes) -> an exact fp16 pair, byte 0 in the
+// low half.
+__device__ __forceinline__ uint32_t e4m3x2_to_half2(uint32_t v) {
+  const __half2_raw h =
+      __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v & 0xffffu), __NV_E4M3);
+  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+}
+
+// Value of a code: the integer itself, or its E4M3 value.
+template <bool F8>
+__device__ __forceinline__ float code_value(uint32_t c) {
+  if constexpr (F8) return e4m3_value(c);
+  else return code_to_float(c);
+}
+
 // ---------------------------------------------------------------- warp reductions
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -136,6 +170,7 @@ struct CacheGeom {
   int D, G, bk, bv, ak, av;
   int P;
   int frag_k, frag_v;  // code order of each side: 1 fragment, 0 sequential
+  int fp8;             // 1: both sides hold E4M3 codes with absmax scales
   int TC;              // rows per pair of a tail buffer (residual + G)
   int NSK;             // rows per pair of the sink window (n_sink)
 };

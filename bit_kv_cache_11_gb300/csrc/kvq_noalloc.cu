@@ -130,14 +130,15 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   const long long max_slots =
       static_cast<long long>((KVQ_NOALLOC_SCRATCH_BYTES - fixed) / (slot_o + slot_ml));
 
+  const int bk = cfg->fp8 ? kBitsE4M3 : cfg->bits_k, bv = cfg->fp8 ? kBitsE4M3 : cfg->bits_v;
   DecodeOps ops{nullptr, nullptr};
   if (mma_geometry(G, cfg->axis_k, cfg->axis_v))
-    ops = decode_mma_ops(D, R, cfg->bits_k, cfg->bits_v, false);
+    ops = decode_mma_ops(D, R, bk, bv, false);
   const bool mma = ops.launch != nullptr;
   if (!mma && (fragment_order(D, G, cfg->bits_k, cfg->axis_k, cfg->axis_v) ||
                fragment_order(D, G, cfg->bits_v, cfg->axis_k, cfg->axis_v)))
     return KVQ_ERR_UNSUPPORTED;
-  if (ops.launch == nullptr) ops = decode_ops(D, R, cfg->bits_k, cfg->bits_v);
+  if (ops.launch == nullptr) ops = decode_ops(D, R, bk, bv);
   if (ops.launch == nullptr) return KVQ_ERR_UNSUPPORTED;
 
   int dev = -1;
@@ -186,6 +187,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.g.ak = cfg->axis_k;
     p.g.av = cfg->axis_v;
     p.g.P = static_cast<int>(P);
+    p.g.fp8 = cfg->fp8;
     p.g.TC = G;
     p.g.NSK = 0;
     p.ktail = static_cast<const __half*>(k_tail);

@@ -20,6 +20,10 @@
 //   3. one thread per output word packs 32/B byte codes and stores the word
 //      (coalesced) in the block layout of include/kvq.h.
 // The extra CTA x == nflush copies the remainder tokens into the tail.
+//
+// FP8 cache ("Rotate, Then Round: The Geometry of KV-Cache Compression",
+// "Key takeaway"): the same groups, scale = fp16(max|x| / 448), zero 0, each
+// element stored as the E4M3 code of x / scale.
 #include "kvq_device.cuh"
 
 namespace kvq {
@@ -42,7 +46,14 @@ struct Stat {
 };
 
 // Statistics from the group's minimum and maximum (exact fp16 values).
-__device__ __forceinline__ Stat stat_of(float mn, float mx, int bits, __half2* meta_out) {
+// FP8 cache: scale = fp16(max|x| / 448), zero 0 (mn and rcp unused).
+__device__ __forceinline__ Stat stat_of(float mn, float mx, int bits, bool f8, __half2* meta_out) {
+  if (f8) {
+    const float amax = fmaxf(fabsf(mn), fabsf(mx));
+    const __half s_h = __float2half_rn(__fdiv_rn(amax, 448.0f));
+    *meta_out = __halves2half2(s_h, __float2half_rn(0.0f));
+    return Stat{0.0f, __half2float(s_h), 0.0f};
+  }
   // (mx - mn) + 0: a range of -0 (min and max zeros of opposite sign) is +0.
   const float range = __fadd_rn(__fsub_rn(mx, mn), 0.0f);
   const float step = __fdiv_rn(range, static_cast<float>((1 << bits) - 1));
@@ -54,7 +65,7 @@ __device__ __forceinline__ Stat stat_of(float mn, float mx, int bits, __half2* m
 }
 
 // min/max over n values p[0], p[stride], ... (fp16 read exactly as fp32).
-__device__ __forceinline__ Stat group_stat(const __half* x, int stride, int n, int bits,
+__device__ __forceinline__ Stat group_stat(const __half* x, int stride, int n, int bits, bool f8,
                                            __half2* meta_out) {
   float mn = __half2float(x[0]);
   float mx = mn;
@@ -63,7 +74,12 @@ __device__ __forceinline__ Stat group_stat(const __half* x, int stride, int n, i
     mn = fminf(mn, v);
     mx = fmaxf(mx, v);
   }
-  return stat_of(mn, mx, bits, meta_out);
+  return stat_of(mn, mx, bits, f8, meta_out);
+}
+
+// FP8 cache: code = E4M3(x / s) with the IEEE quotient; 0 when s is 0.
+__device__ __forceinline__ uint32_t code_fp8(float x, const Stat& st) {
+  return st.s == 0.0f ? 0u : e4m3_encode(__fdiv_rn(x, st.s));
 }
 
 // code = clamp(rintf((x - mn) / s), 0, 2^bits - 1) with the IEEE quotient,
@@ -176,6 +192,10 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
   int lgG = 5;
   while ((1 << lgG) < G) ++lgG;
   const int ng = D >> lgG;
+  const bool f8 = BK == 8 && BV == 8 && q.g.fp8;
+  auto code = [&](float v, const Stat& st, float top) -> uint8_t {
+    return static_cast<uint8_t>(f8 ? code_fp8(v, st) : code_of(v, st, top));
+  };
   for (int e = tid; e < 2 * D; e += blockDim.x) {
     const bool isv = e >= D;
     const int ee = isv ? e - D : e;
@@ -184,9 +204,9 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
     const float top = static_cast<float>((1 << bits) - 1);
     const __half* X = isv ? xv : xk;
     if (axis == 0) {  // channel ee over the G tokens
-      const Stat st = group_stat(X + ee, XP, G, bits, (isv ? vmeta : kmeta) + ee);
+      const Stat st = group_stat(X + ee, XP, G, bits, f8, (isv ? vmeta : kmeta) + ee);
       for (int j = 0; j < G; ++j) {
-        const uint8_t c = static_cast<uint8_t>(code_of(__half2float(X[j * XP + ee]), st, top));
+        const uint8_t c = code(__half2float(X[j * XP + ee]), st, top);
         if (isv) vcode[ee * VP + j] = c;
         else kcode[j * KP + ee] = c;
       }
@@ -206,7 +226,7 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
         }
       }
       const Stat st = stat_of(fminf(__low2float(lo), __high2float(lo)),
-                              fmaxf(__low2float(hi), __high2float(hi)), bits,
+                              fmaxf(__low2float(hi), __high2float(hi)), bits, f8,
                               (isv ? vmeta : kmeta) + j * ng + g);
       for (int i = 0; i < G; i += 8) {
         const uint4 v = *reinterpret_cast<const uint4*>(row + i);
@@ -215,8 +235,8 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
         for (int k = 0; k < 4; ++k) {
           const float2 f = __half22float2(h[k]);
           const int d = (g << lgG) + i + 2 * k;
-          const uint8_t c0 = static_cast<uint8_t>(code_of(f.x, st, top));
-          const uint8_t c1 = static_cast<uint8_t>(code_of(f.y, st, top));
+          const uint8_t c0 = code(f.x, st, top);
+          const uint8_t c1 = code(f.y, st, top);
           if (isv) {
             vcode[d * VP + j] = c0;
             vcode[(d + 1) * VP + j] = c1;
@@ -314,7 +334,7 @@ __global__ void __launch_bounds__(kQuantThreads) dequantize_kernel(const Dequant
       if (q.g.frag_k) frag_position(j, d, D, bits, &w, &bit);
       const uint32_t c = (kc[w] >> bit) & ((1u << bits) - 1u);
       const float2 sz = __half22float2(km[q.g.ak == 0 ? d : j * ng + d / G]);
-      q.kout[o] = fmaf(static_cast<float>(c), sz.x, sz.y);
+      q.kout[o] = fmaf(q.g.fp8 ? e4m3_value(c) : static_cast<float>(c), sz.x, sz.y);
     }
     {
       const int bits = q.g.bv, per = 32 / bits;
@@ -323,7 +343,7 @@ __global__ void __launch_bounds__(kQuantThreads) dequantize_kernel(const Dequant
       if (q.g.frag_v) frag_position(d, j, 32, bits, &w, &bit);
       const uint32_t c = (vc[w] >> bit) & ((1u << bits) - 1u);
       const float2 sz = __half22float2(vm[q.g.av == 0 ? d : j * ng + d / G]);
-      q.vout[o] = fmaf(static_cast<float>(c), sz.x, sz.y);
+      q.vout[o] = fmaf(q.g.fp8 ? e4m3_value(c) : static_cast<float>(c), sz.x, sz.y);
     }
   }
 }

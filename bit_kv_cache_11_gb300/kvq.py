@@ -38,7 +38,7 @@ class kvq_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("max_ctx", ctypes.c_int), ("bits_k", ctypes.c_int),
                 ("bits_v", ctypes.c_int), ("group", ctypes.c_int), ("axis_k", ctypes.c_int),
                 ("axis_v", ctypes.c_int), ("keys_pre_rope", ctypes.c_int), ("rope_base", ctypes.c_float),
-                ("n_sink", ctypes.c_int), ("residual", ctypes.c_int)]
+                ("n_sink", ctypes.c_int), ("residual", ctypes.c_int), ("fp8", ctypes.c_int)]
 
 
 class kvq_buffers(ctypes.Structure):
@@ -109,10 +109,11 @@ def _stream(stream) -> int | None:
 
 def make_config(batch, n_q_heads, n_kv_heads, head_dim, max_ctx, bits_k=2, bits_v=2, group=32,
                 axis_k=KVQ_AXIS_CHANNEL, axis_v=KVQ_AXIS_TOKEN, keys_pre_rope=False,
-                rope_base=10000.0, n_sink=0, residual=0) -> kvq_config:
+                rope_base=10000.0, n_sink=0, residual=0, fp8=False) -> kvq_config:
     return kvq_config(int(batch), int(n_q_heads), int(n_kv_heads), int(head_dim), int(max_ctx),
                       int(bits_k), int(bits_v), int(group), int(axis_k), int(axis_v),
-                      1 if keys_pre_rope else 0, float(rope_base), int(n_sink), int(residual))
+                      1 if keys_pre_rope else 0, float(rope_base), int(n_sink), int(residual),
+                      1 if fp8 else 0)
 
 
 # ---- the C calls, same names ------------------------------------------------

@@ -37,6 +37,15 @@
  *   code    = 0 for every element if scale == 0, else
  *             clamp(rintf((x - mn) / float(scale)), 0, 2^B - 1)   (half-even)
  *   x_hat   = fmaf(code, float(scale), float(zero))               (fp32)
+ * FP8 cache (kvq_config.fp8 = 1; "Rotate, Then Round: The Geometry of
+ * KV-Cache Compression", "Key takeaway": FP8 first), same groups:
+ *   amax    = max |x| over the group
+ *   scale   = fp16(amax / 448)                 IEEE fp32 divide, round to even
+ *   zero    = +0
+ *   code    = 0 if scale == 0, else E4M3(x / float(scale)): the OCP E4M3
+ *             value nearest to the IEEE fp32 quotient, ties to the even
+ *             mantissa, saturating at +-448 (bit layout s.eeee.mmm, bias 7)
+ *   x_hat   = fmaf(E4M3 value of code, float(scale), float(zero))  (exact)
  * Inputs must be finite fp16; non-finite inputs give unspecified codes.
  *
  * Conventions for every call.
@@ -148,6 +157,8 @@ typedef struct {
   int n_sink;        /* first tokens kept in fp16, never quantized; 0..1024   */
   int residual;      /* most recent tokens kept in fp16 beyond the partial
                         group; 0..4096 (0: the tail holds < G tokens)         */
+  int fp8;           /* 1: FP8 cache (requires bits_k = bits_v = 8): codes are
+                        E4M3, scale = fp16(max|x| / 448), zero = 0            */
 } kvq_config;
 
 typedef struct kvq_cache kvq_cache; /* opaque */

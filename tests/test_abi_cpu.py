@@ -68,6 +68,10 @@ def test_config_check_on_host(lib_path):
         (dict(residual=4097), k.KVQ_ERR_INVALID_ARG),
         (dict(n_sink=1024, residual=4096), k.KVQ_OK),
         (dict(n_sink=4, residual=100, group=64), k.KVQ_OK),
+        (dict(fp8=True), k.KVQ_ERR_INVALID_ARG),                  # FP8 needs 8-bit sides
+        (dict(fp8=True, bits_k=8, bits_v=4), k.KVQ_ERR_INVALID_ARG),
+        (dict(fp8=True, bits_k=8, bits_v=8), k.KVQ_OK),
+        (dict(fp8=True, bits_k=8, bits_v=8, axis_k=1, group=128), k.KVQ_OK),
     ]
     base = dict(batch=8, n_q_heads=32, n_kv_heads=32, head_dim=128, max_ctx=8192)
     for over, status in cases:

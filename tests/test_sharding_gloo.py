@@ -43,7 +43,7 @@ def _worker(rank, ws, port, out):
 
 def test_two_rank_replicas_gloo():
     ws = 2
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     mp.spawn(_worker, args=(ws, _free_port(), out), nprocs=ws, join=True)
     for rank in range(ws):
