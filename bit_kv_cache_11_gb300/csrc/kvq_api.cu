@@ -136,7 +136,6 @@ struct kvq_cache {
   uint8_t* blocks;
   __half* ktail[2];
   __half* vtail[2];
-  int active;
   __half* ksink;  // sink window [P][NSK][D], nullptr when n_sink = 0
   __half* vsink;
   float2* rope;
@@ -148,8 +147,37 @@ struct kvq_cache {
   float2* lvl_ml;
   int* tickets2; // [P*R] two-level merge counters, zero between launches
   bool mma;      // decode runs the tensor-core kernel (which can merge in place)
-  int T_s, T_q, T_t;  // sink, quantized and tail tokens per pair
+  // Token counts per batch row: sink, quantized, tail, and the row's active
+  // tail buffer.  A uniform cache keeps every entry equal to row 0; a ragged
+  // cache (rows of different lengths, batch <= kMaxRows) one entry per row.
+  bool ragged;
+  int T_s[kMaxRows], T_q[kMaxRows], T_t[kMaxRows], act[kMaxRows];
 };
+
+// Row records a launch describes: every row of a ragged cache, row 0 of a
+// uniform one.
+static int row_records(const kvq_cache* c) { return c->ragged ? c->cfg.batch : 1; }
+
+// A uniform cache mirrors row 0 into every record.
+static void sync_uniform(kvq_cache* c) {
+  if (c->ragged) return;
+  for (int b = 1; b < kMaxRows; ++b) {
+    c->T_s[b] = c->T_s[0];
+    c->T_q[b] = c->T_q[0];
+    c->T_t[b] = c->T_t[0];
+    c->act[b] = c->act[0];
+  }
+}
+
+static void reset_lengths(kvq_cache* c) {
+  c->ragged = false;
+  for (int b = 0; b < kMaxRows; ++b) c->T_s[b] = c->T_q[b] = c->T_t[b] = c->act[b] = 0;
+}
+
+// Tokens of row b.
+static long long row_tokens(const kvq_cache* c, int b) {
+  return static_cast<long long>(c->T_s[b]) + c->T_q[b] + c->T_t[b];
+}
 
 static CacheGeom geom_of(const kvq_cache* c) {
   CacheGeom g;
@@ -192,58 +220,62 @@ static void free_all(kvq_cache* c) {
   cudaFree(c->tickets2);
 }
 
-// Appends n tokens per pair: the first ones fill the sink window while it
-// is short, the others join the tail; every group of G that leaves at least
-// `residual` newer tail tokens is quantized (the whole combined tail + new
-// sequence is walked once; see QuantParams).
-static kvq_status enqueue_append(kvq_cache* c, const void* k, const void* v, int n,
-                                 cudaStream_t stream) {
-  const int G = c->dv.G, D = c->dv.D;
-  const __half* kn = static_cast<const __half*>(k);
-  const __half* vn = static_cast<const __half*>(v);
-  const int m = std::min(n, c->dv.NSK - c->T_s);
-  if (m > 0) {
-    const size_t row = static_cast<size_t>(D) * sizeof(__half);
-    const size_t off = static_cast<size_t>(c->T_s) * D;
-    if (cudaMemcpy2DAsync(c->ksink + off, c->dv.NSK * row, kn, n * row, m * row, c->dv.P,
-                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess ||
-        cudaMemcpy2DAsync(c->vsink + off, c->dv.NSK * row, vn, n * row, m * row, c->dv.P,
-                          cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
-      return KVQ_ERR_CUDA;
-    c->T_s += m;
-  }
-  const int nr = n - m;
-  if (nr == 0) return KVQ_OK;
-  const int combined = c->T_t + nr;
-  const int nflush = combined >= c->dv.residual ? (combined - c->dv.residual) / G : 0;
+// Appends to every pair of row b its n_rows[b] tokens (n_all for every row
+// when n_rows is null); k, v: [P][stride][D].  The first tokens of a row fill
+// its sink window while it is short, the others join the tail; every group of
+// G that leaves at least `residual` newer tail tokens is quantized.  The whole
+// combined tail + new sequence is walked once (see QuantParams).
+static kvq_status enqueue_append(kvq_cache* c, const void* k, const void* v, const int* n_rows,
+                                 int n_all, int stride, cudaStream_t stream) {
+  const int G = c->dv.G;
+  const int nr = row_records(c);
   QuantParams q;
   q.g = geom_of(c);
-  q.knew = kn + static_cast<size_t>(m) * D;
-  q.vnew = vn + static_cast<size_t>(m) * D;
-  q.n = nr;
-  q.new_stride = n;
-  q.kold = c->ktail[c->active];
-  q.vold = c->vtail[c->active];
-  q.T_t = c->T_t;
-  if (nflush == 0) {
-    q.kdst = c->ktail[c->active];
-    q.vdst = c->vtail[c->active];
-    q.dst_row0 = c->T_t;
-    q.rem_begin = c->T_t;
-  } else {  // the flush reads the old tail: the remainder goes to the other buffer
-    q.kdst = c->ktail[c->active ^ 1];
-    q.vdst = c->vtail[c->active ^ 1];
-    q.dst_row0 = 0;
-    q.rem_begin = nflush * G;
+  q.knew = static_cast<const __half*>(k);
+  q.vnew = static_cast<const __half*>(v);
+  q.new_stride = stride;
+  for (int i = 0; i < 2; ++i) {
+    q.ktail[i] = c->ktail[i];
+    q.vtail[i] = c->vtail[i];
   }
-  q.rem_end = combined;
-  q.first_block = c->T_q / G;
-  q.nflush = nflush;
+  q.ksink = c->ksink;
+  q.vsink = c->vsink;
+  q.ragged = c->ragged ? 1 : 0;
+  q.hkv = c->cfg.n_kv_heads;
+  bool any = false;
+  for (int b = 0; b < nr; ++b) {
+    QuantRow& r = q.rows[b];
+    r.n = n_rows ? n_rows[b] : n_all;
+    r.sink0 = c->T_s[b];
+    r.nsink = std::min(r.n, c->dv.NSK - c->T_s[b]);
+    const int combined = c->T_t[b] + (r.n - r.nsink);
+    r.nflush = combined >= c->dv.residual ? (combined - c->dv.residual) / G : 0;
+    r.T_t = c->T_t[b];
+    r.src = c->act[b];
+    r.first_block = c->T_q[b] / G;
+    if (r.nflush == 0) {
+      r.dst = r.src;
+      r.dst_row0 = c->T_t[b];
+      r.rem_begin = c->T_t[b];
+    } else {  // the flush reads the old tail: the remainder goes to the other buffer
+      r.dst = r.src ^ 1;
+      r.dst_row0 = 0;
+      r.rem_begin = r.nflush * G;
+    }
+    r.rem_end = combined;
+    any = any || r.n > 0;
+  }
+  if (!any) return KVQ_OK;
   if (launch_quantize(q, stream) != cudaSuccess) return KVQ_ERR_CUDA;
   g_launches.fetch_add(1);
-  c->T_q += nflush * G;
-  c->T_t = combined - nflush * G;
-  if (nflush > 0) c->active ^= 1;
+  for (int b = 0; b < nr; ++b) {
+    const QuantRow& r = q.rows[b];
+    c->T_s[b] += r.nsink;
+    c->T_q[b] += r.nflush * G;
+    c->T_t[b] = r.rem_end - r.nflush * G;
+    c->act[b] = r.dst;
+  }
+  sync_uniform(c);
   return KVQ_OK;
 }
 
@@ -367,6 +399,25 @@ kvq_status kvq_destroy(kvq_cache* c) {
   return KVQ_OK;
 }
 
+// Saved host lengths, restored when an enqueue fails before any launch.
+struct SavedLengths {
+  bool ragged;
+  int T_s[kMaxRows], T_q[kMaxRows], T_t[kMaxRows], act[kMaxRows];
+  explicit SavedLengths(const kvq_cache* c) : ragged(c->ragged) {
+    std::memcpy(T_s, c->T_s, sizeof(T_s));
+    std::memcpy(T_q, c->T_q, sizeof(T_q));
+    std::memcpy(T_t, c->T_t, sizeof(T_t));
+    std::memcpy(act, c->act, sizeof(act));
+  }
+  void restore(kvq_cache* c) const {
+    c->ragged = ragged;
+    std::memcpy(c->T_s, T_s, sizeof(T_s));
+    std::memcpy(c->T_q, T_q, sizeof(T_q));
+    std::memcpy(c->T_t, T_t, sizeof(T_t));
+    std::memcpy(c->act, act, sizeof(act));
+  }
+};
+
 kvq_status kvq_quantize_prefill(kvq_cache* c, const void* k, const void* v, int T,
                                 void* stream) {
   if (c == nullptr || T < 0) return KVQ_ERR_INVALID_ARG;
@@ -375,17 +426,37 @@ kvq_status kvq_quantize_prefill(kvq_cache* c, const void* k, const void* v, int 
   if (T > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return KVQ_ERR_CUDA;
-  const int saved_s = c->T_s, saved_q = c->T_q, saved_t = c->T_t;
-  c->T_s = 0;
-  c->T_q = 0;
-  c->T_t = 0;
+  const SavedLengths saved(c);
+  reset_lengths(c);
   if (T == 0) return KVQ_OK;
-  kvq_status s = enqueue_append(c, k, v, T, static_cast<cudaStream_t>(stream));
-  if (s != KVQ_OK) {
-    c->T_s = saved_s;
-    c->T_q = saved_q;
-    c->T_t = saved_t;
+  kvq_status s = enqueue_append(c, k, v, nullptr, T, T, static_cast<cudaStream_t>(stream));
+  if (s != KVQ_OK) saved.restore(c);
+  return s;
+}
+
+kvq_status kvq_quantize_prefill_ragged(kvq_cache* c, const void* k, const void* v,
+                                       const int* lengths, int T_stride, void* stream) {
+  if (c == nullptr || lengths == nullptr || T_stride < 1) return KVQ_ERR_INVALID_ARG;
+  if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
+  const int B = c->cfg.batch;
+  if (B > kMaxRows) return KVQ_ERR_UNSUPPORTED;
+  bool same = true;
+  for (int b = 0; b < B; ++b) {
+    if (lengths[b] < 1 || lengths[b] > T_stride) return KVQ_ERR_INVALID_ARG;
+    same = same && lengths[b] == lengths[0];
   }
+  for (int b = 0; b < B; ++b)
+    if (lengths[b] > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  const SavedLengths saved(c);
+  reset_lengths(c);
+  c->ragged = !same;
+  kvq_status s = same ? enqueue_append(c, k, v, nullptr, lengths[0], T_stride,
+                                       static_cast<cudaStream_t>(stream))
+                      : enqueue_append(c, k, v, lengths, 0, T_stride,
+                                       static_cast<cudaStream_t>(stream));
+  if (s != KVQ_OK) saved.restore(c);
   return s;
 }
 
@@ -393,23 +464,71 @@ kvq_status kvq_append(kvq_cache* c, const void* k, const void* v, int n, void* s
   if (c == nullptr || n < 0) return KVQ_ERR_INVALID_ARG;
   if (n == 0) return KVQ_OK;
   if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
-  if (static_cast<long long>(c->T_s) + c->T_q + c->T_t + n > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
+  for (int b = 0; b < row_records(c); ++b)
+    if (row_tokens(c, b) + n > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return KVQ_ERR_CUDA;
-  return enqueue_append(c, k, v, n, static_cast<cudaStream_t>(stream));
+  return enqueue_append(c, k, v, nullptr, n, n, static_cast<cudaStream_t>(stream));
+}
+
+kvq_status kvq_append_ragged(kvq_cache* c, const void* k, const void* v, const int* n_rows,
+                             int n_stride, void* stream) {
+  if (c == nullptr || n_rows == nullptr || n_stride < 1) return KVQ_ERR_INVALID_ARG;
+  const int B = c->cfg.batch;
+  if (B > kMaxRows) return KVQ_ERR_UNSUPPORTED;
+  bool same = true, any = false;
+  for (int b = 0; b < B; ++b) {
+    if (n_rows[b] < 0 || n_rows[b] > n_stride) return KVQ_ERR_INVALID_ARG;
+    same = same && n_rows[b] == n_rows[0];
+    any = any || n_rows[b] > 0;
+  }
+  if (!any) return KVQ_OK;
+  if (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)) return KVQ_ERR_INVALID_ARG;
+  for (int b = 0; b < B; ++b)
+    if (row_tokens(c, c->ragged ? b : 0) + n_rows[b] > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  const SavedLengths saved(c);
+  if (!same) c->ragged = true;  // uniform records already mirror row 0
+  kvq_status s = enqueue_append(c, k, v, c->ragged ? n_rows : nullptr, n_rows[0], n_stride,
+                                static_cast<cudaStream_t>(stream));
+  if (s != KVQ_OK) saved.restore(c);
+  return s;
 }
 
 // Enqueues the decode of the cache's tokens plus, when n_new > 0 (tensor-core
-// kernel only, no flush), the n_new tokens of knew/vnew, which the same launch
-// also stores into the tail.  The caller updates the lengths.
+// kernel only, no flush), the n_new tokens of knew/vnew of every pair, which
+// the same launch also stores into the tail.  The caller updates the lengths.
 static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float softmax_scale,
                                  cudaStream_t st, const void* knew, const void* vnew, int n_new) {
   const Derived& d = c->dv;
-  const int T_t = c->T_t + n_new;
-  const int nsub = c->T_q / 32;
-  const int ntu = tail_units(c->mma, T_t, c->cfg.bits_k, c->cfg.bits_v);
-  const int upp = nsub + ntu + tail_units(c->mma, c->T_s, c->cfg.bits_k, c->cfg.bits_v);
-  const long long U = static_cast<long long>(d.P) * upp;
+  const int nr = row_records(c);
+  DecodeParams p;
+  UnitMap& m = p.map;
+  m.ragged = c->ragged ? 1 : 0;
+  m.hkv = c->cfg.n_kv_heads;
+  const int tch = c->mma ? mma_tail_chunk(c->cfg.bits_k, c->cfg.bits_v) : 0;
+  p.act = 0;
+  for (int b = 0; b < nr; ++b) {
+    m.Ts[b] = c->T_s[b];
+    m.Tq[b] = c->T_q[b];
+    m.Tt[b] = c->T_t[b] + n_new;
+    set_row_units(m, b, tch);
+    if (c->act[b]) p.act |= 1ull << b;
+  }
+  long long U;
+  int max_upp = 0;
+  if (m.ragged) {
+    m.uoff[0] = 0;
+    for (int b = 0; b < nr; ++b) {
+      m.uoff[b + 1] = m.uoff[b] + m.hkv * units_of_row(m, b);
+      max_upp = std::max(max_upp, units_of_row(m, b));
+    }
+    U = m.uoff[nr];
+  } else {
+    max_upp = units_of_row(m, 0);
+    U = static_cast<long long>(d.P) * max_upp;
+  }
   if (U == 0) {  // an empty cache (n_new is 0 here)
     if (cudaMemsetAsync(out, 0, static_cast<size_t>(d.P) * d.R * d.D * sizeof(float), st) !=
         cudaSuccess)
@@ -420,25 +539,18 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   if (target > kMaxDecodeWarps) target = kMaxDecodeWarps;
   const long long W = U < target ? U : target;
 
-  DecodeParams p;
   p.g = geom_of(c);
-  p.ktail = c->ktail[c->active];
-  p.vtail = c->vtail[c->active];
+  for (int i = 0; i < 2; ++i) {
+    p.ktail[i] = c->ktail[i];
+    p.vtail[i] = c->vtail[i];
+  }
   p.ksink = c->ksink;
   p.vsink = c->vsink;
-  p.T_s = c->T_s;
-  p.T_q = c->T_q;
-  p.T_t = T_t;
-  p.n_tail_u = ntu;
-  p.t_old = c->T_t;
+  p.n_new = n_new;
   p.knew = static_cast<const __half*>(knew);
   p.vnew = static_cast<const __half*>(vnew);
-  p.ktail_w = c->ktail[c->active];
-  p.vtail_w = c->vtail[c->active];
   p.lg_G = d.G == 32 ? 5 : (d.G == 64 ? 6 : 7);
   p.lg_sub = p.lg_G - 5;
-  p.nsub = nsub;
-  p.upp = upp;
   p.U = U;
   p.n_warps = static_cast<int>(W);
   p.rope = c->cfg.keys_pre_rope;
@@ -451,7 +563,8 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   p.err = c->err;
   // Merge in place when every pair has few partials; the separate merge
   // kernel otherwise (few pairs over many warps, e.g. one long sequence).
-  const long long max_seg = W / d.P + 2;
+  // A pair's units [x, x + upp) touch at most upp * W / U + 2 warps.
+  const long long max_seg = static_cast<long long>(max_upp) * W / U + 2;
   p.fused = (c->mma && max_seg <= 64) ? 1 : 0;
   p.tickets = c->tickets;
   p.out = static_cast<float*>(out);
@@ -467,12 +580,14 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   mp.lvl_ml = c->lvl_ml;
   mp.tickets = c->tickets2;
   mp.out = static_cast<float*>(out);
-  mp.upp = upp;
+  mp.map = m;
   mp.U = U;
   mp.n_warps = static_cast<int>(W);
   mp.R = d.R;
   mp.D = d.D;
-  mp.C2 = static_cast<int>((max_seg + 15) / 16);
+  // chunks of CS partial slots, at most C2max chunks per (pair, query)
+  mp.CS = static_cast<int>(std::max<long long>(16, (max_seg + d.C2max - 1) / d.C2max));
+  mp.C2 = static_cast<int>((max_seg + mp.CS - 1) / mp.CS);
   if (launch_merge2(mp, d.P, st) != cudaSuccess) return KVQ_ERR_CUDA;
   g_launches.fetch_add(2);
   return KVQ_OK;
@@ -497,19 +612,25 @@ kvq_status kvq_append_decode(kvq_cache* c, const void* k, const void* v, int n, 
   if (n > 0 && (k == nullptr || v == nullptr || !aligned16(k) || !aligned16(v)))
     return KVQ_ERR_INVALID_ARG;
   if (!std::isfinite(softmax_scale)) return KVQ_ERR_INVALID_ARG;
-  if (static_cast<long long>(c->T_s) + c->T_q + c->T_t + n > c->cfg.max_ctx)
-    return KVQ_ERR_CAPACITY;
+  const int nr = row_records(c);
+  for (int b = 0; b < nr; ++b)
+    if (row_tokens(c, b) + n > c->cfg.max_ctx) return KVQ_ERR_CAPACITY;
   DeviceGuard g(c->device);
   if (!g.ok) return KVQ_ERR_CUDA;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (n > 0 && c->mma && c->T_s == c->dv.NSK && c->T_t + n < c->dv.residual + c->dv.G) {
-    // one launch: the new tokens stay in the tail, no block is flushed
+  // one launch when every row's new tokens go to its tail without a flush
+  bool fuse = n > 0 && c->mma;
+  for (int b = 0; b < nr && fuse; ++b)
+    fuse = c->T_s[b] == c->dv.NSK && c->T_t[b] + n < c->dv.residual + c->dv.G;
+  if (fuse) {
     const kvq_status s = enqueue_decode(c, q, out, softmax_scale, st, k, v, n);
-    if (s == KVQ_OK) c->T_t += n;
+    if (s == KVQ_OK) {
+      for (int b = 0; b < kMaxRows; ++b) c->T_t[b] += n;
+    }
     return s;
   }
   if (n > 0) {
-    const kvq_status s = enqueue_append(c, k, v, n, st);
+    const kvq_status s = enqueue_append(c, k, v, nullptr, n, n, st);
     if (s != KVQ_OK) return s;
   }
   return enqueue_decode(c, q, out, softmax_scale, st, nullptr, nullptr, 0);
@@ -517,14 +638,15 @@ kvq_status kvq_append_decode(kvq_cache* c, const void* k, const void* v, int n, 
 
 kvq_status kvq_dequantize(kvq_cache* c, void* k_out, void* v_out, void* stream) {
   if (c == nullptr) return KVQ_ERR_INVALID_ARG;
-  if (c->T_q == 0) return KVQ_OK;  // nothing to write; the outputs may be empty
+  if (c->ragged) return KVQ_ERR_UNSUPPORTED;  // rows of different lengths
+  if (c->T_q[0] == 0) return KVQ_OK;  // nothing to write; the outputs may be empty
   if (k_out == nullptr || v_out == nullptr || !aligned16(k_out) || !aligned16(v_out))
     return KVQ_ERR_INVALID_ARG;
   DeviceGuard g(c->device);
   if (!g.ok) return KVQ_ERR_CUDA;
   DequantParams p;
   p.g = geom_of(c);
-  p.T_q = c->T_q;
+  p.T_q = c->T_q[0];
   p.kout = static_cast<float*>(k_out);
   p.vout = static_cast<float*>(v_out);
   if (launch_dequantize(p, static_cast<cudaStream_t>(stream)) != cudaSuccess) return KVQ_ERR_CUDA;
@@ -534,16 +656,30 @@ kvq_status kvq_dequantize(kvq_cache* c, void* k_out, void* v_out, void* stream) 
 
 kvq_status kvq_get_state(const kvq_cache* c, int* T_q, int* T_tail) {
   if (c == nullptr || T_q == nullptr || T_tail == nullptr) return KVQ_ERR_INVALID_ARG;
-  *T_q = c->T_q;
-  *T_tail = c->T_t;
+  if (c->ragged) return KVQ_ERR_UNSUPPORTED;
+  *T_q = c->T_q[0];
+  *T_tail = c->T_t[0];
+  return KVQ_OK;
+}
+
+kvq_status kvq_get_row_state(const kvq_cache* c, int row, int* T_sink, int* T_q, int* T_tail,
+                             int* tail_buffer) {
+  if (c == nullptr || row < 0 || row >= c->cfg.batch || T_sink == nullptr || T_q == nullptr ||
+      T_tail == nullptr || tail_buffer == nullptr)
+    return KVQ_ERR_INVALID_ARG;
+  const int b = c->ragged ? row : 0;
+  *T_sink = c->T_s[b];
+  *T_q = c->T_q[b];
+  *T_tail = c->T_t[b];
+  *tail_buffer = c->act[b];
   return KVQ_OK;
 }
 
 kvq_status kvq_get_buffers(const kvq_cache* c, kvq_buffers* out) {
   if (c == nullptr || out == nullptr) return KVQ_ERR_INVALID_ARG;
   out->blocks = c->blocks;
-  out->k_tail = c->ktail[c->active];
-  out->v_tail = c->vtail[c->active];
+  out->k_tail = c->ktail[c->act[0]];
+  out->v_tail = c->vtail[c->act[0]];
   out->block_bytes = c->dv.block_bytes;
   out->off_kc = c->dv.off_kc;
   out->off_km = c->dv.off_km;
@@ -553,12 +689,17 @@ kvq_status kvq_get_buffers(const kvq_cache* c, kvq_buffers* out) {
   out->code_order_v = c->dv.frag_v;
   out->blocks_per_pair = c->dv.NB;
   out->n_pairs = c->dv.P;
-  out->T_q = c->T_q;
-  out->T_tail = c->T_t;
+  out->T_q = c->T_q[0];
+  out->T_tail = c->T_t[0];
   out->k_sink = c->ksink;
   out->v_sink = c->vsink;
-  out->T_sink = c->T_s;
+  out->T_sink = c->T_s[0];
   out->tail_rows = c->dv.TC;
+  for (int i = 0; i < 2; ++i) {
+    out->k_tail_buffer[i] = c->ktail[i];
+    out->v_tail_buffer[i] = c->vtail[i];
+  }
+  out->ragged = c->ragged ? 1 : 0;
   return KVQ_OK;
 }
 

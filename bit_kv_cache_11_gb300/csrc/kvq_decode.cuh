@@ -62,7 +62,7 @@ struct DecodeCfg {
 
 template <int D, int BK, int BV, int R, bool F8 = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32)
-    decode_split_kernel(const DecodeParams p) {
+    decode_split_kernel(const __grid_constant__ DecodeParams p) {
   using C = DecodeCfg<D, BK, BV, R>;
   constexpr int NS = C::NS;
   constexpr uint32_t KMASK = (1u << BK) - 1u;
@@ -99,10 +99,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
   // Load cursor: the next quantized unit to copy (fp16 units are skipped).
   UnitCursor lc;
-  lc.init(ua, p.upp);
+  lc.init(p, ua, ub);
   auto skip_tail = [&]() {
-    while (lc.u < ub && lc.j >= p.nsub) lc.next(p.upp);
+    while (lc.u < ub && lc.j >= lc.l.nsub) lc.next(p);
   };
+  UnitCursor uc;  // the compute cursor
+  uc.init(p, ua, ub);
   // Lane 0: copies of quantized unit u into stage s.
   auto issue = [&](long long pr, int j, int s) {
     const int blk = j >> p.lg_sub;
@@ -126,7 +128,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   for (int s = 0; s < NS && lc.u < ub; ++s) {
     if (lane == 0) issue(lc.pr, lc.j, s);
     ++issued;
-    lc.next(p.upp);
+    lc.next(p);
     skip_tail();
   }
 
@@ -209,7 +211,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       return code_value<F8>((kr[d / KPER] >> ((d % KPER) * BK)) & KMASK);
     };
     if (p.rope) {
-      const int pos = p.T_s + j * 32 + lane;
+      const int pos = uc.l.Ts + j * 32 + lane;
       const float2* cs = p.rope_tab + static_cast<size_t>(pos) * (D / 2);
 #pragma unroll
       for (int r = 0; r < R; ++r) sc[r] = 0.f;
@@ -414,9 +416,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     }
   };
 
-  UnitCursor uc;
-  uc.init(ua, p.upp);
-  for (; uc.u < ub; uc.next(p.upp)) {
+  for (; uc.u < ub; uc.next(p)) {
     const long long pr = uc.pr;
     const int j = uc.j;
     if (pr != cur) {
@@ -424,13 +424,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       enter_pair(pr);
       cur = pr;
     }
-    if (j >= p.nsub) {
-      if (j < p.nsub + p.n_tail_u)
-        process_rows(p.ktail + static_cast<size_t>(pr) * p.g.TC * D,
-                     p.vtail + static_cast<size_t>(pr) * p.g.TC * D, p.T_t, p.T_s + p.T_q);
+    if (j >= uc.l.nsub) {
+      const PairLens& l = uc.l;
+      if (j < l.nsub + l.ntu)
+        process_rows(p.ktail[l.buf] + static_cast<size_t>(pr) * p.g.TC * D,
+                     p.vtail[l.buf] + static_cast<size_t>(pr) * p.g.TC * D, l.Tt, l.Ts + l.Tq);
       else
         process_rows(p.ksink + static_cast<size_t>(pr) * p.g.NSK * D,
-                     p.vsink + static_cast<size_t>(pr) * p.g.NSK * D, p.T_s, 0);
+                     p.vsink + static_cast<size_t>(pr) * p.g.NSK * D, l.Ts, 0);
       continue;
     }
     const int s = qi % NS;
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
     if (lc.u < ub) {
       if (lane == 0) issue(lc.pr, lc.j, s);
       ++issued;
-      lc.next(p.upp);
+      lc.next(p);
       skip_tail();
     }
   }

@@ -188,7 +188,7 @@ __device__ __forceinline__ int bslot(int blk, int l) {
 
 template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (R <= 4 ? 3 : 1))
-    decode_mma_kernel(const DecodeParams p) {
+    decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   using C = MmaCfg<D, BK, BV, R, ROPE>;
   constexpr int NS = C::NS, NT = C::NT, NG = C::NG, MTV = C::MTV, CPL = C::CPL, TCH = C::TCH,
                 STAGE = C::STAGE, KS = C::KS, BL = C::BL;
@@ -217,8 +217,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   }
   // Fused append: store the new tokens into the tail for later calls (no
   // access of this launch reads those tail rows).
-  if (p.T_t > p.t_old) {
-    const int n_new = p.T_t - p.t_old;
+  if (p.n_new > 0) {
+    const int n_new = p.n_new;
     const long long chunks = static_cast<long long>(p.g.P) * n_new * (D / 8);
     for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
          c += static_cast<long long>(gridDim.x) * blockDim.x) {
@@ -226,10 +226,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       const int col = static_cast<int>(c - rowi * (D / 8)) * 8;
       const long long pr = rowi / n_new;
       const int r = static_cast<int>(rowi - pr * n_new);
-      const size_t dst = (static_cast<size_t>(pr) * p.g.TC + p.t_old + r) * D + col;
-      *reinterpret_cast<uint4*>(p.ktail_w + dst) =
+      const int b = row_of(p.map, pr);
+      const int buf = static_cast<int>((p.act >> b) & 1ull);
+      const size_t dst = (static_cast<size_t>(pr) * p.g.TC + (p.map.Tt[b] - n_new) + r) * D + col;
+      *reinterpret_cast<uint4*>(p.ktail[buf] + dst) =
           *reinterpret_cast<const uint4*>(p.knew + rowi * D + col);
-      *reinterpret_cast<uint4*>(p.vtail_w + dst) =
+      *reinterpret_cast<uint4*>(p.vtail[buf] + dst) =
           *reinterpret_cast<const uint4*>(p.vnew + rowi * D + col);
     }
   }
@@ -256,19 +258,25 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   // ---- this warp's units [ua, ub) and the load cursor, NS units ahead
   const int ua = static_cast<int>(gw * p.U / p.n_warps);
   const int ub = static_cast<int>((gw + 1) * p.U / p.n_warps);
-  const int upp = p.upp, nsub = p.nsub;
-  int lu = ua, lpr = ua / upp;
-  int lj = ua - lpr * upp;
+  int lu = ua;
+  int lpr = static_cast<int>(pair_of_unit(p.map, ua));
+  int lj = ua - static_cast<int>(first_unit(p.map, lpr));
+  int lnsub = pair_nsub(p, lpr), lupp = pair_upp(p, lpr);  // the load cursor's pair
+  int pr = lpr, j = lj;             // the compute cursor (unit j of pair pr)
+  int cnsub = lnsub, cupp = lupp;
   const uint8_t* lbase = p.g.blocks + static_cast<size_t>(lpr) * p.g.NB * STAGE;
   auto issue = [&](int s) {  // lane 0: unit (lpr, lj) -> stage s
     uint8_t* st = ws + s * STAGE;
-    if (lj < nsub) {
+    if (lj < lnsub) {
       mbar_arrive_expect_tx(&bars[s], STAGE);
       bulk_g2s(st, lbase + static_cast<size_t>(lj) * STAGE, STAGE, &bars[s]);
-    } else if (lj >= nsub + p.n_tail_u) {
+      return;
+    }
+    const PairLens ll = pair_lens(p, lpr);
+    if (lj >= ll.nsub + ll.ntu) {
       // sink rows [t0, t1): K rows, then V rows, one copy each
-      const int t0 = (lj - nsub - p.n_tail_u) * TCH;
-      const int t1 = min(t0 + TCH, p.T_s);
+      const int t0 = (lj - ll.nsub - ll.ntu) * TCH;
+      const int t1 = min(t0 + TCH, ll.Ts);
       const uint32_t bytes = static_cast<uint32_t>(t1 - t0) * D * 2;
       const size_t row = static_cast<size_t>(lpr) * p.g.NSK + t0;
       mbar_arrive_expect_tx(&bars[s], 2 * bytes);
@@ -277,20 +285,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     } else {
       // tail rows [t0, t1): those below t_old from the tail buffer, the rest
       // (tokens appended by this call) from knew / vnew
-      const int t0 = (lj - nsub) * TCH;
-      const int t1 = min(t0 + TCH, p.T_t);
-      const int tm = max(t0, min(t1, p.t_old));
+      const int t0 = (lj - ll.nsub) * TCH;
+      const int t1 = min(t0 + TCH, ll.Tt);
+      const int tm = max(t0, min(t1, ll.t_old));
       mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(t1 - t0) * D * 4);
       if (tm > t0) {
         const uint32_t bytes = static_cast<uint32_t>(tm - t0) * D * 2;
         const size_t row = static_cast<size_t>(lpr) * p.g.TC + t0;
-        bulk_g2s(st, p.ktail + row * D, bytes, &bars[s]);
-        bulk_g2s(st + TCH * D * 2, p.vtail + row * D, bytes, &bars[s]);
+        bulk_g2s(st, p.ktail[ll.buf] + row * D, bytes, &bars[s]);
+        bulk_g2s(st + TCH * D * 2, p.vtail[ll.buf] + row * D, bytes, &bars[s]);
       }
       if (t1 > tm) {
-        const int n_new = p.T_t - p.t_old;
+        const int n_new = p.n_new;
         const uint32_t bytes = static_cast<uint32_t>(t1 - tm) * D * 2;
-        const size_t row = static_cast<size_t>(lpr) * n_new + (tm - p.t_old);
+        const size_t row = static_cast<size_t>(lpr) * n_new + (tm - ll.t_old);
         bulk_g2s(st + (tm - t0) * D * 2, p.knew + row * D, bytes, &bars[s]);
         bulk_g2s(st + (TCH + tm - t0) * D * 2, p.vnew + row * D, bytes, &bars[s]);
       }
@@ -298,10 +306,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   };
   auto advance_load = [&]() {
     ++lu;
-    if (++lj == upp) {
+    if (++lj == lupp) {
       lj = 0;
       ++lpr;
       lbase += static_cast<size_t>(p.g.NB) * STAGE;
+      if (lu < ub) {
+        lnsub = pair_nsub(p, lpr);
+        lupp = pair_upp(p, lpr);
+      }
     }
   };
   for (int s = 0; s < NS && lu < ub; ++s) {
@@ -680,7 +692,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       //   cos(j th_i) (a c_i + b c_i2 + e) + sin(j th_i) (f c_i - g c_i2 + h).
       constexpr int H = D / 2;
       float* cf = reinterpret_cast<float*>(ws + C::OFF_CF);
-      const int p0 = p.T_s + ju * 32;
+      const int p0 = p.map.Ts[row_of(p.map, pr)] + ju * 32;
       for (int i = lane; i < H; i += 32) {
         const float2 cs = p.rope_tab[static_cast<size_t>(p0) * H + i];
         const float2 m0 = __half22float2(km[i]), m1 = __half22float2(km[i + H]);
@@ -896,13 +908,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
 
   // unit j >= nsub of a pair: a chunk of its tail, then of its sink window
   auto process_fp16_unit = [&](const uint8_t* st, int j) {
-    const int k = j - nsub;
-    if (k < p.n_tail_u) {
+    const PairLens cl = pair_lens(p, pr);
+    const int k = j - cl.nsub;
+    if (k < cl.ntu) {
       const int t0 = k * TCH;
-      process_chunk(st, min(TCH, p.T_t - t0), p.T_s + p.T_q + t0);
+      process_chunk(st, min(TCH, cl.Tt - t0), cl.Ts + cl.Tq + t0);
     } else {
-      const int t0 = (k - p.n_tail_u) * TCH;
-      process_chunk(st, min(TCH, p.T_s - t0), t0);
+      const int t0 = (k - cl.ntu) * TCH;
+      process_chunk(st, min(TCH, cl.Ts - t0), t0);
     }
   };
 
@@ -951,9 +964,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       // (it never waits for the others: the ticket tells it they are done).
       __threadfence();
       __syncwarp();
-      const long long x0 = pr * p.upp;
+      const long long x0 = first_unit(p.map, pr);
       const long long w0 = owner_warp(x0, p.U, p.n_warps);
-      const long long w1 = owner_warp(x0 + p.upp - 1, p.U, p.n_warps);
+      const long long w1 =
+          owner_warp(x0 + units_of_row(p.map, row_of(p.map, pr)) - 1, p.U, p.n_warps);
       int last = 0;
       if (lane == 0) last = atomicAdd(&p.tickets[pr], 1) == static_cast<int>(w1 - w0);
       last = __shfl_sync(0xffffffffu, last, 0);
@@ -1009,8 +1023,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   };
 
   // ---- main loop: unit n = u - ua sits in stage n % NS, phase (n / NS) & 1
-  int pr = ua / upp;
-  int j = ua - pr * upp;
   int s = 0;
   uint32_t ph = 0u;
   // the next unit to load goes into `stage` (lane 0 issues the copy)
@@ -1046,13 +1058,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     }
     const uint8_t* st = ws + s * STAGE;
     if constexpr (ROPE) {
-      if (j < nsub)
+      if (j < cnsub)
         process_sub(st, j);
       else
         process_fp16_unit(st, j);
       refill(s);
     } else {
-      if (j < nsub) {
+      if (j < cnsub) {
         // keys of this block, then its key mma beside the value mma of the
         // previous block (independent), then softmax and this block's value
         // operand; its value mma waits for the next iteration
@@ -1085,9 +1097,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       s = 0;
       ph ^= 1u;
     }
-    if (++j == upp) {
+    if (++j == cupp) {
       j = 0;
       ++pr;
+      if (u + 1 < ub) {
+        cnsub = pair_nsub(p, pr);
+        cupp = pair_upp(p, pr);
+      }
     }
   }
   if constexpr (!ROPE) {

@@ -175,23 +175,43 @@ struct CacheGeom {
   int NSK;             // rows per pair of the sink window (n_sink)
 };
 
-// Quantize / append / flush launch: grid (nflush + 1, P).
+// ---------------------------------------------------------------- batch rows
+
+// Batch rows whose sequences differ in length (a ragged cache) number at most
+// kMaxRows; a uniform cache describes every row by row 0.
+constexpr int kMaxRows = 64;
+
+// Quantize / append / flush of one batch row (every pair of the row).  The
+// row's n new tokens first fill its sink window (tokens [0, nsink) -> sink
+// rows [sink0, sink0 + nsink)); the others follow its T_t tail rows as one
+// combined sequence, whose first nflush * G tokens become blocks
+// first_block, ... and whose tokens [rem_begin, rem_end) are copied into tail
+// buffer `dst` from row dst_row0 on.
+struct QuantRow {
+  int n;
+  int sink0, nsink;
+  int T_t;
+  int src, dst;        // tail buffer (0 or 1) read / written
+  int nflush;
+  int first_block;
+  int rem_begin, rem_end, dst_row0;
+};
+
+// Quantize / append / flush launch: grid (max nflush + 1, P).  CTA x of pair
+// p quantizes block x of its row's flush (x < nflush) or copies the row's
+// remainder and sink tokens (x == nflush).
 struct QuantParams {
   CacheGeom g;
   const __half* knew;  // pair p's new token r at row p * new_stride + r
   const __half* vnew;
-  int n;
-  int new_stride;      // rows per pair of knew / vnew (>= n)
-  const __half* kold;  // active tail [P][TC][D] (rows [0, T_t) valid)
-  const __half* vold;
-  int T_t;
-  __half* kdst;        // tail that receives the remainder
-  __half* vdst;
-  int dst_row0;        // first destination row
-  int rem_begin;       // combined-sequence index of the first remainder token
-  int rem_end;         // one past the last (= T_t + n)
-  int first_block;     // block index of the first flushed block (T_q / G)
-  int nflush;          // blocks to quantize
+  int new_stride;      // rows per pair of knew / vnew
+  __half* ktail[2];    // the two tail buffers, [P][TC][D] each
+  __half* vtail[2];
+  __half* ksink;       // sink windows [P][NSK][D]
+  __half* vsink;
+  int ragged;          // 0: rows[0] describes every row
+  int hkv;             // pairs per row
+  QuantRow rows[kMaxRows];
 };
 
 // Dequantize launch: grid (T_q / G, P).
@@ -208,42 +228,77 @@ struct DequantParams {
 // D * (4 bk + 4 bv + 8) bytes.
 __host__ __device__ constexpr int mma_tail_chunk(int bk, int bv) { return bk + bv + 2; }
 
-// Units of the fp16 tail of one pair: ceil(T_t / tch) chunks for the
-// tensor-core kernel, one unit for the CUDA-core kernel.
-__host__ __device__ inline int tail_units(bool mma, int T_t, int bk, int bv) {
-  if (T_t <= 0) return 0;
-  if (!mma) return 1;
-  const int tch = mma_tail_chunk(bk, bv);
-  return (T_t + tch - 1) / tch;
+// Units of `rows` fp16 rows (tail or sink window) of one pair: ceil(rows /
+// tch) chunks for the tensor-core kernel, one unit for the CUDA-core kernel
+// (tch = 0).
+__host__ __device__ inline int fp16_units(int rows, int tch) {
+  if (rows <= 0) return 0;
+  return tch > 0 ? (rows + tch - 1) / tch : 1;
 }
 
-// Split-K decode launch.  The work of all pairs is a flat sequence of units:
-// pair p owns units [p*upp, (p+1)*upp); unit j < nsub of a pair is its j-th
-// 32-token quantized sub-block, the next n_tail_u units cover its fp16 tail
-// and the rest its fp16 sink window (tail_units of T_t and of T_s).  Warp w
-// of the grid processes units [w*U/W, (w+1)*U/W) and writes one partial
-// (m, l, o) per pair it touches into slot (w + p).  Token positions (RoPE):
-// sink row t at t, quantized token i at T_s + i, tail row t at T_s + T_q + t.
+// The decode work as a flat sequence of units: pair p = b * hkv + h of row b
+// owns units [first_unit(p), first_unit(p) + units_of_row(b)): its 32-token
+// quantized sub-blocks, then its fp16 tail units, then its fp16 sink units.
+// Token positions (RoPE): sink row t at t, quantized token i at Ts + i, tail
+// row t at Ts + Tq + t.
+struct UnitMap {
+  int ragged;              // 0: row 0's counts hold for every row
+  int hkv;                 // pairs per row
+  int Ts[kMaxRows];        // sink tokens of each row
+  int Tq[kMaxRows];        // quantized tokens
+  int Tt[kMaxRows];        // tail tokens, including those a fused append adds
+  int ntu[kMaxRows];       // fp16 tail units of a pair of the row
+  int upp[kMaxRows];       // units of a pair of the row
+  int uoff[kMaxRows + 1];  // ragged: first unit of each row
+};
+
+// Fills ntu and upp of row b from its token counts (tch: fp16 rows per unit,
+// 0 for one unit per fp16 region).
+__host__ __device__ inline void set_row_units(UnitMap& m, int b, int tch) {
+  m.ntu[b] = fp16_units(m.Tt[b], tch);
+  m.upp[b] = m.Tq[b] / 32 + m.ntu[b] + fp16_units(m.Ts[b], tch);
+}
+
+__host__ __device__ inline int row_of(const UnitMap& m, long long pr) {
+  if (!m.ragged) return 0;
+  return static_cast<int>(pr / m.hkv);
+}
+
+__host__ __device__ inline int units_of_row(const UnitMap& m, int b) { return m.upp[b]; }
+
+__host__ __device__ inline long long first_unit(const UnitMap& m, long long pr) {
+  if (!m.ragged) return pr * m.upp[0];
+  const int b = static_cast<int>(pr / m.hkv);
+  return m.uoff[b] + (pr - static_cast<long long>(b) * m.hkv) * m.upp[b];
+}
+
+// The pair that owns unit u (u < the total).
+__host__ __device__ inline long long pair_of_unit(const UnitMap& m, long long u) {
+  if (!m.ragged) return u / m.upp[0];
+  int b = 0;
+  while (m.uoff[b + 1] <= u) ++b;
+  return static_cast<long long>(b) * m.hkv + (u - m.uoff[b]) / m.upp[b];
+}
+
+// Split-K decode launch.  Warp w of the grid processes units [w*U/W,
+// (w+1)*U/W) of the unit map and writes one partial (m, l, o) per pair it
+// touches into slot (w + p).
 struct DecodeParams {
   CacheGeom g;
-  const __half* ktail;  // active tail [P][TC][D]
-  const __half* vtail;
-  const __half* ksink;  // sink window [P][NSK][D]
+  UnitMap map;
+  __half* ktail[2];     // the two tail buffers [P][TC][D]
+  __half* vtail[2];
+  unsigned long long act;  // bit b (bit 0 for a uniform cache): row b's tail is buffer 1
+  const __half* ksink;  // sink windows [P][NSK][D]
   const __half* vsink;
-  int T_s, T_q, T_t;
-  int n_tail_u;         // tail units per pair
-  // Append fused into the decode (tensor-core kernel, no flush): tail rows
-  // [t_old, T_t) are the n_new tokens of knew/vnew ([P][n_new][D]); the
-  // kernel also stores them into rows [t_old, T_t) of the tail (ktail_w).
-  int t_old;            // tail rows already in the buffer (== T_t when not fused)
+  // Append fused into the decode (tensor-core kernel, no flush): the last
+  // n_new tail rows of every pair are the tokens of knew/vnew
+  // ([P][n_new][D]); the kernel also stores them into the pair's tail.
+  int n_new;
   const __half* knew;
   const __half* vnew;
-  __half* ktail_w;
-  __half* vtail_w;
   int lg_G;             // log2(G)
   int lg_sub;           // log2(G / 32): 32-token sub-blocks per block
-  int nsub;             // T_q / 32
-  int upp;              // units per pair
   long long U;          // total units
   int n_warps;          // W
   int rope;             // rotate keys after dequantization
@@ -261,38 +316,78 @@ struct DecodeParams {
   float* out;           // [P][R][D]
 };
 
+// The counts of pair pr that a decode kernel uses.
+struct PairLens {
+  int nsub, ntu, upp;   // 32-token sub-blocks, tail units, all units
+  int Ts, Tq, Tt;       // token counts (Tt includes a fused append's tokens)
+  int t_old;            // tail rows already stored (Tt - n_new)
+  long long u0;         // first unit
+  int buf;              // active tail buffer of the pair's row
+};
+
+__device__ __forceinline__ PairLens pair_lens(const DecodeParams& p, long long pr) {
+  const int b = row_of(p.map, pr);
+  PairLens l;
+  l.Ts = p.map.Ts[b];
+  l.Tq = p.map.Tq[b];
+  l.Tt = p.map.Tt[b];
+  l.t_old = l.Tt - p.n_new;
+  l.nsub = l.Tq >> 5;
+  l.ntu = p.map.ntu[b];
+  l.upp = p.map.upp[b];
+  l.u0 = first_unit(p.map, pr);
+  l.buf = static_cast<int>((p.act >> b) & 1ull);
+  return l;
+}
+
+// Sub-blocks and units of pair pr (the counts a decode loop tests per unit).
+__device__ __forceinline__ int pair_nsub(const DecodeParams& p, long long pr) {
+  return p.map.Tq[row_of(p.map, pr)] >> 5;
+}
+__device__ __forceinline__ int pair_upp(const DecodeParams& p, long long pr) {
+  return p.map.upp[row_of(p.map, pr)];
+}
+
+// Walks a warp's units [u0, u1) in order as (pair, unit-in-pair) without
+// dividing in the loop; the pair's counts are reloaded when it enters a pair.
+struct UnitCursor {
+  long long u, end;
+  long long pr;
+  int j;
+  PairLens l;
+  __device__ __forceinline__ void init(const DecodeParams& p, long long u0, long long u1) {
+    u = u0;
+    end = u1;
+    pr = 0;
+    j = 0;
+    if (u < end) {
+      pr = pair_of_unit(p.map, u);
+      l = pair_lens(p, pr);
+      j = static_cast<int>(u - l.u0);
+    }
+  }
+  __device__ __forceinline__ void next(const DecodeParams& p) {
+    ++u;
+    if (++j == l.upp) {
+      j = 0;
+      ++pr;
+      if (u < end) l = pair_lens(p, pr);
+    }
+  }
+};
+
 struct MergeParams {
   const float* part_o;
   const float2* part_ml;
   float* out;  // [P][R][D]
-  int upp;
+  UnitMap map;
   long long U;
   int n_warps;
   int R, D;
 };
 
-// Walks a warp's units in order as (pair, unit-in-pair) without dividing in
-// the loop (64-bit division is a long software sequence on the GPU).
-struct UnitCursor {
-  long long u;
-  long long pr;
-  int j;
-  __device__ __forceinline__ void init(long long u0, int upp) {
-    u = u0;
-    pr = u0 / upp;
-    j = static_cast<int>(u0 - pr * upp);
-  }
-  __device__ __forceinline__ void next(int upp) {
-    ++u;
-    if (++j == upp) {
-      j = 0;
-      ++pr;
-    }
-  }
-};
-
 // Two-level merge of the split partials (few pairs, many partials each):
-// block (pair, query, chunk) merges at most 16 partial slots into a level-2
+// block (pair, query, chunk) merges at most CS partial slots into a level-2
 // partial; the last block of a (pair, query), found with a ticket, merges the
 // level-2 partials into the output.
 struct Merge2Params {
@@ -302,11 +397,12 @@ struct Merge2Params {
   float2* lvl_ml;  // [P*R*C2]
   int* tickets;    // [P*R], zero between launches
   float* out;      // [P][R][D]
-  int upp;
+  UnitMap map;
   long long U;
   int n_warps;
   int R, D;
   int C2;          // level-1 chunks per (pair, query)
+  int CS;          // partial slots per chunk
 };
 
 // Largest warp whose unit range starts at or before unit x (the warp that

@@ -69,9 +69,10 @@ DecodeOps decode_ops(int D, int R, int bk, int bv) {
 __global__ void merge_kernel(const MergeParams mp) {
   const long long pr = blockIdx.x;
   const int d = threadIdx.x;
-  const long long x0 = pr * mp.upp;
+  const long long x0 = first_unit(mp.map, pr);
+  const int upp = units_of_row(mp.map, row_of(mp.map, pr));
   const long long w0 = owner_warp(x0, mp.U, mp.n_warps);
-  const long long w1 = owner_warp(x0 + mp.upp - 1, mp.U, mp.n_warps);
+  const long long w1 = owner_warp(x0 + upp - 1, mp.U, mp.n_warps);
   for (int r = 0; r < mp.R; ++r) {
     float ms = -INFINITY;
     for (long long w = w0; w <= w1; ++w) ms = fmaxf(ms, mp.part_ml[(w + pr) * mp.R + r].x);
@@ -94,11 +95,12 @@ __global__ void merge2_kernel(const Merge2Params mp) {
   const int r = pq % mp.R;
   const long long pr = pq / mp.R;
   const int d = threadIdx.x;
-  const long long x0 = pr * mp.upp;
+  const long long x0 = first_unit(mp.map, pr);
+  const int upp = units_of_row(mp.map, row_of(mp.map, pr));
   const long long w0 = owner_warp(x0, mp.U, mp.n_warps);
-  const long long w1 = owner_warp(x0 + mp.upp - 1, mp.U, mp.n_warps);
-  const long long s0 = w0 + 16LL * c;
-  const long long s1 = s0 + 15 < w1 ? s0 + 15 : w1;
+  const long long w1 = owner_warp(x0 + upp - 1, mp.U, mp.n_warps);
+  const long long s0 = w0 + static_cast<long long>(mp.CS) * c;
+  const long long s1 = s0 + mp.CS - 1 < w1 ? s0 + mp.CS - 1 : w1;
   float ms = -INFINITY;
   for (long long w = s0; w <= s1; ++w) ms = fmaxf(ms, mp.part_ml[(w + pr) * mp.R + r].x);
   // A chunk may hold only empty partials (m = -inf, l = 0): weigh them 0.

@@ -152,9 +152,14 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   if (ss != KVQ_OK) return ss;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const int nsub = T_q / 32;
-  const int upp = nsub + tail_units(mma, T_tail, cfg->bits_k, cfg->bits_v);
-  const long long U = P * upp;
+  UnitMap map;
+  map.ragged = 0;
+  map.hkv = cfg->n_kv_heads;
+  map.Ts[0] = 0;
+  map.Tq[0] = T_q;
+  map.Tt[0] = T_tail;
+  set_row_units(map, 0, mma ? mma_tail_chunk(cfg->bits_k, cfg->bits_v) : 0);
+  const long long U = P * units_of_row(map, 0);
   float* part_o = reinterpret_cast<float*>(ds.scratch);
   const size_t ml_off = round256(static_cast<size_t>(max_slots) * slot_o);
   float2* part_ml = reinterpret_cast<float2*>(ds.scratch + ml_off);
@@ -190,23 +195,19 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.g.fp8 = cfg->fp8;
     p.g.TC = G;
     p.g.NSK = 0;
-    p.ktail = static_cast<const __half*>(k_tail);
-    p.vtail = static_cast<const __half*>(v_tail);
+    p.map = map;
+    for (int i = 0; i < 2; ++i) {  // the caller's one tail, read only
+      p.ktail[i] = static_cast<__half*>(const_cast<void*>(k_tail));
+      p.vtail[i] = static_cast<__half*>(const_cast<void*>(v_tail));
+    }
+    p.act = 0;
     p.ksink = nullptr;
     p.vsink = nullptr;
-    p.T_s = 0;
-    p.T_q = T_q;
-    p.T_t = T_tail;
-    p.n_tail_u = upp - nsub;
-    p.t_old = T_tail;
+    p.n_new = 0;
     p.knew = nullptr;
     p.vnew = nullptr;
-    p.ktail_w = nullptr;
-    p.vtail_w = nullptr;
     p.lg_G = G == 32 ? 5 : (G == 64 ? 6 : 7);
     p.lg_sub = p.lg_G - 5;
-    p.nsub = nsub;
-    p.upp = upp;
     p.U = U;
     p.n_warps = static_cast<int>(W);
     p.rope = 0;
@@ -225,7 +226,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     mp.part_o = part_o;
     mp.part_ml = part_ml;
     mp.out = static_cast<float*>(out);
-    mp.upp = upp;
+    mp.map = map;
     mp.U = U;
     mp.n_warps = static_cast<int>(W);
     mp.R = R;

@@ -95,16 +95,17 @@ __device__ __forceinline__ uint32_t code_of(float x, const Stat& st, float top) 
   return __float_as_uint(r + 8388608.0f) & 0xffu;  // exact: r is an integer in [0, 255]
 }
 
-__device__ __forceinline__ const __half* combined_row(const QuantParams& q, int p, int jc) {
+// Row jc of pair p's combined sequence (its row's tail rows, then the new
+// tokens that follow the sink window's share), K or V.
+__device__ __forceinline__ const __half* combined_row(const QuantParams& q, const QuantRow& r,
+                                                      int p, int jc, bool isv) {
   const int D = q.g.D;
-  if (jc < q.T_t) return q.kold + (static_cast<size_t>(p) * q.g.TC + jc) * D;
-  return q.knew + (static_cast<size_t>(p) * q.new_stride + (jc - q.T_t)) * D;
-}
-
-__device__ __forceinline__ const __half* combined_row_v(const QuantParams& q, int p, int jc) {
-  const int D = q.g.D;
-  if (jc < q.T_t) return q.vold + (static_cast<size_t>(p) * q.g.TC + jc) * D;
-  return q.vnew + (static_cast<size_t>(p) * q.new_stride + (jc - q.T_t)) * D;
+  if (jc < r.T_t) {
+    const __half* t = isv ? (r.src ? q.vtail[1] : q.vtail[0]) : (r.src ? q.ktail[1] : q.ktail[0]);
+    return t + (static_cast<size_t>(p) * q.g.TC + jc) * D;
+  }
+  return (isv ? q.vnew : q.knew) +
+         (static_cast<size_t>(p) * q.new_stride + r.nsink + (jc - r.T_t)) * D;
 }
 
 // Packs 32/BITS byte codes (LSB-first order) into one word.
@@ -138,26 +139,37 @@ __device__ __forceinline__ uint32_t pack_word<8>(const uint8_t* b) {
 
 }  // namespace
 
+// CTA x of pair p, whose row record is `row` (see QuantParams).
 template <int BK, int BV>
-__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantParams q) {
-  const int x = blockIdx.x;
-  const int p = blockIdx.y;
+__device__ __forceinline__ void quantize_block(const QuantParams& q, const QuantRow& row, int x,
+                                               int p) {
   const int D = q.g.D, G = q.g.G;
   const int tid = threadIdx.x;
+  if (x > row.nflush) return;
 
-  if (x == q.nflush) {
-    // remainder -> tail rows [dst_row0, ...)
-    const int rows = q.rem_end - q.rem_begin;
+  if (x == row.nflush) {
+    // remainder -> tail rows [dst_row0, ...) of buffer dst
+    const int rows = row.rem_end - row.rem_begin;
     const int chunks = rows * (D / 8);
     for (int c = tid; c < chunks; c += blockDim.x) {
       const int r = c / (D / 8);
       const int col = (c % (D / 8)) * 8;
-      const int jc = q.rem_begin + r;
-      const size_t dst = (static_cast<size_t>(p) * q.g.TC + q.dst_row0 + r) * D + col;
-      *reinterpret_cast<uint4*>(q.kdst + dst) =
-          *reinterpret_cast<const uint4*>(combined_row(q, p, jc) + col);
-      *reinterpret_cast<uint4*>(q.vdst + dst) =
-          *reinterpret_cast<const uint4*>(combined_row_v(q, p, jc) + col);
+      const int jc = row.rem_begin + r;
+      const size_t dst = (static_cast<size_t>(p) * q.g.TC + row.dst_row0 + r) * D + col;
+      *reinterpret_cast<uint4*>(q.ktail[row.dst] + dst) =
+          *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, false) + col);
+      *reinterpret_cast<uint4*>(q.vtail[row.dst] + dst) =
+          *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, true) + col);
+    }
+    // the first nsink new tokens -> sink rows [sink0, sink0 + nsink)
+    const int schunks = row.nsink * (D / 8);
+    for (int c = tid; c < schunks; c += blockDim.x) {
+      const int r = c / (D / 8);
+      const int col = (c % (D / 8)) * 8;
+      const size_t src = (static_cast<size_t>(p) * q.new_stride + r) * D + col;
+      const size_t dst = (static_cast<size_t>(p) * q.g.NSK + row.sink0 + r) * D + col;
+      *reinterpret_cast<uint4*>(q.ksink + dst) = *reinterpret_cast<const uint4*>(q.knew + src);
+      *reinterpret_cast<uint4*>(q.vsink + dst) = *reinterpret_cast<const uint4*>(q.vnew + src);
     }
     return;
   }
@@ -176,14 +188,14 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
     const int col = (c % (D / 8)) * 8;
     const int jc = x * G + j;
     *reinterpret_cast<uint4*>(xk + j * XP + col) =
-        *reinterpret_cast<const uint4*>(combined_row(q, p, jc) + col);
+        *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, false) + col);
     *reinterpret_cast<uint4*>(xv + j * XP + col) =
-        *reinterpret_cast<const uint4*>(combined_row_v(q, p, jc) + col);
+        *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, true) + col);
   }
   __syncthreads();
 
   uint8_t* blk = q.g.blocks +
-                 (static_cast<size_t>(p) * q.g.NB + q.first_block + x) * q.g.block_bytes;
+                 (static_cast<size_t>(p) * q.g.NB + row.first_block + x) * q.g.block_bytes;
   __half2* kmeta = reinterpret_cast<__half2*>(blk + q.g.off_km);
   __half2* vmeta = reinterpret_cast<__half2*>(blk + q.g.off_vm);
 
@@ -314,6 +326,15 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const QuantPara
   }
 }
 
+// A uniform cache (RAGGED = false) reads row 0's record at a fixed parameter
+// offset; a ragged one indexes the rows by the pair's batch row.
+template <int BK, int BV, bool RAGGED>
+__global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const __grid_constant__ QuantParams q) {
+  const int x = blockIdx.x;
+  const int p = blockIdx.y;
+  quantize_block<BK, BV>(q, q.rows[RAGGED ? p / q.hkv : 0], x, p);
+}
+
 __global__ void __launch_bounds__(kQuantThreads) dequantize_kernel(const DequantParams q) {
   const int i = blockIdx.x;
   const int p = blockIdx.y;
@@ -355,9 +376,10 @@ size_t quantize_smem_bytes(int D, int G) {
 
 namespace {
 using QuantFn = void (*)(const QuantParams);
-QuantFn quant_fn(int bk, int bv) {
+QuantFn quant_fn(int bk, int bv, bool ragged) {
 #define KVQ_Q(BK_, BV_) \
-  if (bk == BK_ && bv == BV_) return quantize_kernel<BK_, BV_>;
+  if (bk == BK_ && bv == BV_)    \
+    return ragged ? quantize_kernel<BK_, BV_, true> : quantize_kernel<BK_, BV_, false>;
   KVQ_Q(2, 2) KVQ_Q(2, 4) KVQ_Q(2, 8)
   KVQ_Q(4, 2) KVQ_Q(4, 4) KVQ_Q(4, 8)
   KVQ_Q(8, 2) KVQ_Q(8, 4) KVQ_Q(8, 8)
@@ -371,20 +393,25 @@ QuantFn quant_fn(int bk, int bv) {
 cudaError_t prepare_quantize() {
   const int bits[3] = {2, 4, 8};
   for (int a : bits)
-    for (int b : bits) {
-      cudaError_t e = cudaFuncSetAttribute(quant_fn(a, b), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(quantize_smem_bytes(128, 128)));
-      if (e != cudaSuccess) return e;
-    }
+    for (int b : bits)
+      for (int rg = 0; rg < 2; ++rg) {
+        cudaError_t e =
+            cudaFuncSetAttribute(quant_fn(a, b, rg != 0), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(quantize_smem_bytes(128, 128)));
+        if (e != cudaSuccess) return e;
+      }
   return cudaSuccess;
 }
 
 cudaError_t launch_quantize(const QuantParams& q, cudaStream_t stream) {
   const size_t smem = quantize_smem_bytes(q.g.D, q.g.G);
-  QuantFn fn = quant_fn(q.g.bk, q.g.bv);
+  QuantFn fn = quant_fn(q.g.bk, q.g.bv, q.ragged != 0);
   if (fn == nullptr) return cudaErrorInvalidValue;
-  dim3 grid(q.nflush + 1, q.g.P);
-  fn<<<grid, kQuantThreads, q.nflush > 0 ? smem : 0, stream>>>(q);
+  int mx = 0;  // most blocks any row flushes
+  const int nrows = q.ragged ? q.g.P / q.hkv : 1;
+  for (int b = 0; b < nrows; ++b) mx = q.rows[b].nflush > mx ? q.rows[b].nflush : mx;
+  dim3 grid(mx + 1, q.g.P);
+  fn<<<grid, kQuantThreads, mx > 0 ? smem : 0, stream>>>(q);
   return cudaGetLastError();
 }
 

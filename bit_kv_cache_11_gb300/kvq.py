@@ -48,7 +48,8 @@ class kvq_buffers(ctypes.Structure):
                 ("blocks_per_pair", ctypes.c_int), ("n_pairs", ctypes.c_int), ("T_q", ctypes.c_int),
                 ("T_tail", ctypes.c_int), ("code_order_k", ctypes.c_int), ("code_order_v", ctypes.c_int),
                 ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p), ("T_sink", ctypes.c_int),
-                ("tail_rows", ctypes.c_int)]
+                ("tail_rows", ctypes.c_int), ("k_tail_buffer", ctypes.c_void_p * 2),
+                ("v_tail_buffer", ctypes.c_void_p * 2), ("ragged", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -63,6 +64,9 @@ _sigs = {
     "kvq_destroy": (_S, [_P]),
     "kvq_quantize_prefill": (_S, [_P, _P, _P, _I, _P]),
     "kvq_append": (_S, [_P, _P, _P, _I, _P]),
+    "kvq_quantize_prefill_ragged": (_S, [_P, _P, _P, ctypes.POINTER(_I), _I, _P]),
+    "kvq_append_ragged": (_S, [_P, _P, _P, ctypes.POINTER(_I), _I, _P]),
+    "kvq_get_row_state": (_S, [_P, _I] + [ctypes.POINTER(_I)] * 4),
     "kvq_decode_attention": (_S, [_P, _P, _P, ctypes.c_float, _P]),
     "kvq_append_decode": (_S, [_P, _P, _P, _I, _P, _P, ctypes.c_float, _P]),
     "kvq_dequantize": (_S, [_P, _P, _P, _P]),
@@ -147,6 +151,37 @@ def kvq_quantize_prefill(handle, k, v, T: int | None = None, stream=None) -> Non
         T = k.shape[-2]
     _check(_lib.kvq_quantize_prefill(handle, _ptr(k), _ptr(v), int(T), _stream(stream)),
            "kvq_quantize_prefill")
+
+
+def _ints(values):
+    vals = [int(x) for x in values]
+    return (_I * max(len(vals), 1))(*vals)
+
+
+def kvq_quantize_prefill_ragged(handle, k, v, lengths, T_stride: int | None = None,
+                                stream=None) -> None:
+    """k, v: [batch][n_kv_heads][T_stride][head_dim]; row b holds lengths[b] tokens."""
+    if T_stride is None:
+        T_stride = k.shape[-2]
+    _check(_lib.kvq_quantize_prefill_ragged(handle, _ptr(k), _ptr(v), _ints(lengths),
+                                            int(T_stride), _stream(stream)),
+           "kvq_quantize_prefill_ragged")
+
+
+def kvq_append_ragged(handle, k, v, n_rows, n_stride: int | None = None, stream=None) -> None:
+    """k, v: [batch][n_kv_heads][n_stride][head_dim]; row b appends n_rows[b] tokens."""
+    if n_stride is None:
+        n_stride = k.shape[-2]
+    _check(_lib.kvq_append_ragged(handle, _ptr(k), _ptr(v), _ints(n_rows), int(n_stride),
+                                  _stream(stream)), "kvq_append_ragged")
+
+
+def kvq_get_row_state(handle, row: int) -> tuple[int, int, int, int]:
+    """(T_sink, T_q, T_tail, tail_buffer) of batch row `row`."""
+    vals = [_I(0) for _ in range(4)]
+    _check(_lib.kvq_get_row_state(handle, int(row), *[ctypes.byref(x) for x in vals]),
+           "kvq_get_row_state")
+    return tuple(x.value for x in vals)
 
 
 def kvq_append(handle, k, v, n: int | None = None, stream=None) -> None:
@@ -247,6 +282,16 @@ class KVCache:
     def prefill(self, k, v, stream=None):
         kvq_quantize_prefill(self.handle, k, v, k.shape[-2], stream)
 
+    def prefill_ragged(self, k, v, lengths, stream=None):
+        kvq_quantize_prefill_ragged(self.handle, k, v, lengths, k.shape[-2], stream)
+
+    def append_ragged(self, k, v, n_rows, stream=None):
+        kvq_append_ragged(self.handle, k, v, n_rows, k.shape[-2], stream)
+
+    def row_state(self, row: int) -> tuple[int, int, int, int]:
+        """(T_sink, T_q, T_tail, tail_buffer) of batch row `row`."""
+        return kvq_get_row_state(self.handle, row)
+
     def append(self, k, v, stream=None):
         kvq_append(self.handle, k, v, k.shape[-2], stream)
 
@@ -298,6 +343,16 @@ class KVCache:
         shape = (b.n_pairs, b.tail_rows, self.cfg.head_dim)
         k = device_view(b.k_tail, shape, "<f2")
         v = device_view(b.v_tail, shape, "<f2")
+        return k, v
+
+    def row_tail_views(self, row: int):
+        """fp16 [n_kv_heads][tail_rows][D] views of row `row`'s K and V tails."""
+        b = self.buffers()
+        buf = self.row_state(row)[3]
+        shape = (b.n_pairs, b.tail_rows, self.cfg.head_dim)
+        h = self.cfg.n_kv_heads
+        k = device_view(b.k_tail_buffer[buf], shape, "<f2")[row * h:(row + 1) * h]
+        v = device_view(b.v_tail_buffer[buf], shape, "<f2")[row * h:(row + 1) * h]
         return k, v
 
     def sink_views(self):

@@ -181,6 +181,10 @@ typedef struct {
   void* v_sink;                /* V sink window, same                           */
   int T_sink;                  /* sink tokens per pair, <= n_sink               */
   int tail_rows;               /* rows per pair of each tail buffer (residual + G) */
+  void* k_tail_buffer[2];      /* the two K tail buffers (kvq_get_row_state says  */
+  void* v_tail_buffer[2];      /*   which one holds a row's tail)               */
+  int ragged;                  /* 1: rows hold different lengths; the T_* fields
+                                  and k_tail / v_tail above describe row 0      */
 } kvq_buffers;
 
 /* Validates a config on the host (no GPU needed).  Returns KVQ_OK,
@@ -210,6 +214,20 @@ KVQ_API kvq_status kvq_destroy(kvq_cache* cache);
 KVQ_API kvq_status kvq_quantize_prefill(kvq_cache* cache, const void* k,
                                         const void* v, int T, void* stream);
 
+/* Prefill of a batch whose rows hold different numbers of tokens (ragged
+ * lengths, a serving batch): resets the cache, then stores lengths[b] tokens
+ * into every pair of row b exactly as kvq_quantize_prefill does for one
+ * length.  k, v: device fp16 [batch][n_kv_heads][T_stride][head_dim]; row b
+ * reads tokens [0, lengths[b]) of its pairs.  lengths: host int [batch], each
+ * in [1, T_stride] (KVQ_ERR_INVALID_ARG otherwise; > max_ctx ->
+ * KVQ_ERR_CAPACITY).  A ragged cache needs batch <= 64 (KVQ_ERR_UNSUPPORTED
+ * otherwise); equal lengths give a uniform cache.  Decode, append and
+ * append-decode then work per row; kvq_dequantize and kvq_get_state return
+ * KVQ_ERR_UNSUPPORTED for a ragged cache (kvq_get_row_state reports lengths). */
+KVQ_API kvq_status kvq_quantize_prefill_ragged(kvq_cache* cache, const void* k,
+                                               const void* v, const int* lengths,
+                                               int T_stride, void* stream);
+
 /* Decode-time append of n tokens per pair.  New tokens first fill the sink
  * window (while T_sink < n_sink); the others join the tail, which with them
  * forms one sequence: while it holds at least residual + G tokens, its oldest
@@ -219,6 +237,15 @@ KVQ_API kvq_status kvq_quantize_prefill(kvq_cache* cache, const void* k,
  * no-op.  T_sink + T_q + T_tail + n > max_ctx -> KVQ_ERR_CAPACITY. */
 KVQ_API kvq_status kvq_append(kvq_cache* cache, const void* k, const void* v,
                               int n, void* stream);
+
+/* Append of n_rows[b] tokens to every pair of row b (0 allowed: the row
+ * does not advance).  k, v: device fp16 [batch][n_kv_heads][n_stride][head_dim];
+ * n_rows: host int [batch], each in [0, n_stride].  Rows follow kvq_append's
+ * rules one by one; unequal counts make the cache ragged (batch <= 64,
+ * KVQ_ERR_UNSUPPORTED otherwise).  KVQ_ERR_CAPACITY when a row would exceed
+ * max_ctx. */
+KVQ_API kvq_status kvq_append_ragged(kvq_cache* cache, const void* k, const void* v,
+                                     const int* n_rows, int n_stride, void* stream);
 
 /* Split-K decode attention of one query token per head over every cached
  * token (T_sink fp16 sink tokens, T_q dequantized tokens, T_tail fp16 tail
@@ -295,9 +322,16 @@ KVQ_API kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const voi
                                                 float softmax_scale, int* device_error,
                                                 void* stream);
 
-/* Host-side lengths: quantized tokens and tail tokens per pair. */
+/* Host-side lengths: quantized tokens and tail tokens per pair
+ * (KVQ_ERR_UNSUPPORTED for a ragged cache). */
 KVQ_API kvq_status kvq_get_state(const kvq_cache* cache, int* T_q,
                                  int* T_tail);
+
+/* Lengths of batch row `row`: sink, quantized and tail tokens of each of its
+ * pairs, and which tail buffer (0 or 1 of kvq_buffers.k_tail_buffer) holds
+ * the tail rows. */
+KVQ_API kvq_status kvq_get_row_state(const kvq_cache* cache, int row, int* T_sink,
+                                     int* T_q, int* T_tail, int* tail_buffer);
 
 /* Device addresses and geometry (see the layout above). */
 KVQ_API kvq_status kvq_get_buffers(const kvq_cache* cache, kvq_buffers* out);
