@@ -42,11 +42,13 @@ def decode_bytes(w, T_q, T_t):
     return codes + meta + tail + qo
 
 
-def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, fp8=False):
+def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, fp8=False,
+                lengths=None):
     """The same decode step on a variant of the cache: fp16 windows (the first
-    n_sink tokens and `residual` recent tokens kept in fp16) or the FP8 (E4M3)
-    format (w with 8-bit sides).  Algorithmic bytes count sink rows like tail
-    rows; the single-launch steps are averaged, as for the main line."""
+    n_sink tokens and `residual` recent tokens kept in fp16), the FP8 (E4M3)
+    format (w with 8-bit sides), or a ragged batch (row b holds lengths[b]
+    tokens).  Algorithmic bytes count sink rows like tail rows, per row; the
+    single-launch steps are averaged, as for the main line."""
     import torch
     from bit_kv_cache_11_gb300 import kvq
     caches, steps_dev = [], []
@@ -57,7 +59,11 @@ def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, f
                         head_dim=w.head_dim, max_ctx=w.T + warmup + steps + 32, bits_k=w.bits_k,
                         bits_v=w.bits_v, group=w.group, axis_k=w.axis_k, axis_v=w.axis_v,
                         n_sink=n_sink, residual=residual, fp8=fp8)
-        c.prefill(torch.from_numpy(case["K"]).to(dev), torch.from_numpy(case["V"]).to(dev))
+        if lengths is None:
+            c.prefill(torch.from_numpy(case["K"]).to(dev), torch.from_numpy(case["V"]).to(dev))
+        else:
+            c.prefill_ragged(torch.from_numpy(case["K"]).to(dev), torch.from_numpy(case["V"]).to(dev),
+                             lengths)
         st = synth.make_decode_steps(w, warmup + steps, seed=seed + 500, outliers=case["outliers"])
         steps_dev.append([{k: torch.from_numpy(v).to(dev) for k, v in x.items()} for x in st])
         caches.append(c)
@@ -72,16 +78,17 @@ def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, f
     for i in range(warmup, warmup + steps):
         for layer in range(n_layers):
             s = steps_dev[layer][i]
-            b0 = caches[layer].buffers()
-            fused = b0.T_sink == n_sink and b0.T_tail + 1 < residual + w.group
+            rows = [caches[layer].row_state(b) for b in range(w.batch)]
+            fused = all(ts == n_sink and tt + 1 < residual + w.group for ts, _, tt, _ in rows)
             a = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
             a.record(stream)
             caches[layer].append_decode(s["k"], s["v"], s["q"], outs[layer], w.scale)
             e.record(stream)
-            tq, tt = caches[layer].state
+            rows = [caches[layer].row_state(b) for b in range(w.batch)]
+            nb = sum(decode_bytes(w.with_(batch=1), tq, tt + ts) for ts, tq, tt, _ in rows)
             if fused:
-                timed.append((a, e, decode_bytes(w, tq, tt + n_sink)))
+                timed.append((a, e, nb))
     torch.cuda.synchronize()
     for c in caches:
         c.check()
@@ -90,8 +97,14 @@ def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, f
     nb = statistics.mean(b for _, _, b in timed)
     peak, src = load_peaks()
     gbs = nb / (ms * 1e-3) / 1e9
-    name = w.name.replace("-2bit", "-fp8") if fp8 else f"{w.name}-sink{n_sink}-res{residual}"
-    return {"workload": name, "n_sink": n_sink, "residual": residual, "fp8": fp8, "GB/s": gbs, "frac": gbs / peak, "peak_source": f"hbm_gbs of {src}",
+    if fp8:
+        name = w.name.replace("-2bit", "-fp8")
+    elif lengths is not None:
+        name = w.name.replace("-t4113", f"-ragged-t{min(lengths)}..{max(lengths)}")
+    else:
+        name = f"{w.name}-sink{n_sink}-res{residual}"
+    return {"workload": name, "n_sink": n_sink, "residual": residual, "fp8": fp8,
+            "lengths": lengths, "GB/s": gbs, "frac": gbs / peak, "peak_source": f"hbm_gbs of {src}",
             "ms_per_launch": ms, "bytes_per_launch": nb, "launches_timed": len(timed)}
 
 
@@ -430,11 +443,13 @@ def run_gpu(args, w):
                   "cpu_oracle_Mtok_s": (t_cpu_tokens / w4.n_kv_heads / t_cpu / 1e6) if t_cpu else None}
         del K4, V4, flush
 
-    win_line = fp8_line = None
+    win_line = fp8_line = rag_line = None
     if rank == 0 and not args.skip_windows:
         win_line = variant_leg(w, dev, stream, L, 3, min(args.steps, 10), n_sink=4, residual=128)
         fp8_line = variant_leg(w.with_(bits_k=8, bits_v=8), dev, stream, L, 3, min(args.steps, 10),
                                fp8=True)
+        rag = [int(x) for x in np.linspace(1024, w.T, w.batch)]
+        rag_line = variant_leg(w, dev, stream, L, 3, min(args.steps, 10), lengths=rag)
 
     if rank != 0:
         if ws > 1:
@@ -479,6 +494,7 @@ def run_gpu(args, w):
         "quantize": q_line,
         "windows": win_line,
         "fp8": fp8_line,
+        "ragged": rag_line,
         "frac_of_8tbs_spec": achieved / 8000.0,
     }
     print(json.dumps(line), flush=True)
