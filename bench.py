@@ -74,22 +74,41 @@ def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, f
             s = steps_dev[layer][i]
             caches[layer].append_decode(s["k"], s["v"], s["q"], outs[layer], w.scale)
     torch.cuda.synchronize()
-    timed = []
+    # row lengths before the timed steps; the timed loop makes no host query
+    # (it would let the GPU run dry and time the host)
+    lens = [[list(caches[layer].row_state(b)[:3]) for b in range(w.batch)]
+            for layer in range(n_layers)]
+    ev = []
     for i in range(warmup, warmup + steps):
         for layer in range(n_layers):
             s = steps_dev[layer][i]
-            rows = [caches[layer].row_state(b) for b in range(w.batch)]
-            fused = all(ts == n_sink and tt + 1 < residual + w.group for ts, _, tt, _ in rows)
             a = torch.cuda.Event(enable_timing=True)
             e = torch.cuda.Event(enable_timing=True)
             a.record(stream)
             caches[layer].append_decode(s["k"], s["v"], s["q"], outs[layer], w.scale)
             e.record(stream)
-            rows = [caches[layer].row_state(b) for b in range(w.batch)]
-            nb = sum(decode_bytes(w.with_(batch=1), tq, tt + ts) for ts, tq, tt, _ in rows)
-            if fused:
-                timed.append((a, e, nb))
+            ev.append((layer, a, e))
     torch.cuda.synchronize()
+    # replay each row's lengths through the append rule (one token per row and
+    # step): the step runs as one launch when every row's token goes to its
+    # tail without a flush
+    timed = []
+    for layer, a, e in ev:
+        rows = lens[layer]
+        fused = all(ts == n_sink and tt + 1 < residual + w.group for ts, _, tt in rows)
+        for r in rows:
+            if r[0] < n_sink:
+                r[0] += 1
+            else:
+                r[2] += 1
+                if r[2] >= residual + w.group:
+                    r[1] += w.group
+                    r[2] -= w.group
+        nb = sum(decode_bytes(w.with_(batch=1), tq, tt + ts) for ts, tq, tt in rows)
+        if fused:
+            timed.append((a, e, nb))
+    for layer in range(n_layers):
+        assert [list(caches[layer].row_state(b)[:3]) for b in range(w.batch)] == lens[layer]
     for c in caches:
         c.check()
         c.close()

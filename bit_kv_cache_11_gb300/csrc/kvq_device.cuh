@@ -259,25 +259,29 @@ __host__ __device__ inline void set_row_units(UnitMap& m, int b, int tch) {
   m.upp[b] = m.Tq[b] / 32 + m.ntu[b] + fp16_units(m.Ts[b], tch);
 }
 
+// Units and pairs fit in 31 bits (kvq_create checks the unit count), so the
+// lookups below divide in 32 bits.
 __host__ __device__ inline int row_of(const UnitMap& m, long long pr) {
   if (!m.ragged) return 0;
-  return static_cast<int>(pr / m.hkv);
+  return static_cast<int>(pr) / m.hkv;
 }
 
 __host__ __device__ inline int units_of_row(const UnitMap& m, int b) { return m.upp[b]; }
 
 __host__ __device__ inline long long first_unit(const UnitMap& m, long long pr) {
-  if (!m.ragged) return pr * m.upp[0];
-  const int b = static_cast<int>(pr / m.hkv);
-  return m.uoff[b] + (pr - static_cast<long long>(b) * m.hkv) * m.upp[b];
+  const int p = static_cast<int>(pr);
+  if (!m.ragged) return static_cast<long long>(p) * m.upp[0];
+  const int b = p / m.hkv;
+  return m.uoff[b] + static_cast<long long>(p - b * m.hkv) * m.upp[b];
 }
 
 // The pair that owns unit u (u < the total).
 __host__ __device__ inline long long pair_of_unit(const UnitMap& m, long long u) {
-  if (!m.ragged) return u / m.upp[0];
+  const int ui = static_cast<int>(u);
+  if (!m.ragged) return ui / m.upp[0];
   int b = 0;
-  while (m.uoff[b + 1] <= u) ++b;
-  return static_cast<long long>(b) * m.hkv + (u - m.uoff[b]) / m.upp[b];
+  while (m.uoff[b + 1] <= ui) ++b;
+  return b * m.hkv + (ui - m.uoff[b]) / m.upp[b];
 }
 
 // Split-K decode launch.  Warp w of the grid processes units [w*U/W,
