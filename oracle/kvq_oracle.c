@@ -286,11 +286,11 @@ void kvo_block_offsets(int D, int G, int bk, int bv, size_t* offsets) {
 }
 
 /* Which order a side's codes are stored in: 1 = fragment order, used when
- * keys are grouped per channel, values per token, G = 32, D is 64 or 128 and
- * the side has 2 or 4 bits; 0 = sequential order otherwise. */
+ * keys are grouped per channel, values per token, G = 32 and D is 64 or 128
+ * (any bit width); 0 = sequential order otherwise. */
 int kvo_code_order(int D, int G, int bits, int ak, int av) {
   return (ak == 0 && av == 1 && G == 32 && (D == 64 || D == 128) &&
-          (bits == 2 || bits == 4)) ? 1 : 0;
+          (bits == 2 || bits == 4 || bits == 8)) ? 1 : 0;
 }
 
 /* Fragment order of one 32-token code region, seen as a tile of rows x cols
@@ -301,6 +301,7 @@ int kvo_code_order(int D, int G, int bits, int ak, int av) {
  * the code belongs to lane l = 4*g + t, in that lane's word
  *   w = mt*(cols/32) + ks/2   at bit 16*e + F2[hr][2*(ks%2) + kh]   (2 bits)
  *   w = mt*(cols/16) + ks     at bit 16*e + 8*kh + 4*hr             (4 bits)
+ *   w = 2*(mt*(cols/16) + ks) + kh   at bit 8*(2*hr + e)            (8 bits)
  * with F2[0] = {0, 10, 12, 14} and F2[1] = {2, 4, 6, 8}, and word w of lane
  * l is word ((w/4)*32 + l)*4 + w%4 of the region. */
 static void frag_position(int row, int col, int cols, int bits, size_t* word,
@@ -313,9 +314,12 @@ static void frag_position(int row, int col, int cols, int bits, size_t* word,
   if (bits == 2) {
     w = mt * (cols / 32) + ks / 2;
     *bit = 16 * e + F2[hr][2 * (ks % 2) + kh];
-  } else {
+  } else if (bits == 4) {
     w = mt * (cols / 16) + ks;
     *bit = 16 * e + 8 * kh + 4 * hr;
+  } else {
+    w = 2 * (mt * (cols / 16) + ks) + kh;
+    *bit = 8 * (2 * hr + e);
   }
   *word = ((size_t)(w / 4) * 32 + (size_t)lane) * 4 + (size_t)(w % 4);
 }

@@ -201,11 +201,11 @@ def test_packed_words(oracle_mod, row):
 
 def test_code_order_rule(oracle_mod):
     # fragment order only for keys per channel + values per token, G = 32,
-    # D in {64, 128}, 2/4 bits
+    # D in {64, 128}, every bit width
     for D in (64, 128):
         assert oracle_mod.code_order(D, 32, 2, 0, 1) == 1
         assert oracle_mod.code_order(D, 32, 4, 0, 1) == 1
-        assert oracle_mod.code_order(D, 32, 8, 0, 1) == 0
+        assert oracle_mod.code_order(D, 32, 8, 0, 1) == 1
         assert oracle_mod.code_order(D, 128, 2, 0, 1) == 0
         assert oracle_mod.code_order(D, 64, 4, 0, 1) == 0
         for ak, av in ((0, 0), (1, 0), (1, 1)):
