@@ -15,15 +15,16 @@
 // columns n = 2*r + h: query head r of the GQA group, h = 0/1 the high/low
 // fp16 halves of an fp32 operand (hi + lo keeps ~22 bits).
 //
-// A operand.  2- and 4-bit codes are stored in fragment order (include/kvq.h):
+// A operand.  Codes are stored in fragment order (include/kvq.h); for 2 and 4 bits
 // each lane's codes sit in its own words, placed so that an AND mask leaves
 // two codes c at bits p and p + 16 of a register -- an fp16 subnormal pair of
 // value c * 2^(p - 24), exact, with no constant to remove.  2-bit words give
 // their eight registers from the word and the word shifted right by 8 (p = 0,
 // 2, 4, 6 for the first row of a register pair, p + 2 for the row 8 below),
-// 4-bit words their four (p = 0 and 4).  8-bit codes stay in sequential order
-// and become exact fp16 values through a byte permute (1024 + c) and one
-// half2 subtraction of 1024.
+// 4-bit words their four (p = 0 and 4).  8-bit words hold two fp16-operand
+// byte pairs each (rows g and g+8); integer codes become exact fp16 values
+// through a byte permute (1024 + c) and one half2 subtraction of 1024, E4M3
+// codes through the fp8-pair conversion.
 // B operand.  The fp32 value (q_c * s_c for scores, p_j * s_j for values)
 // times 2^(24 - p) for its k-slot, times a power of two that keeps it inside
 // fp16's range, split into hi + lo.  Rows 8 below (p + 2, or p + 4 for 4-bit
@@ -86,53 +87,51 @@ __device__ __forceinline__ void frag_a4(uint32_t w, uint32_t& a0, uint32_t& a1, 
   a3 = y & 0x00F000F0u;  // p 4 (word bits 12-15)
 }
 
-// 8-bit codes in sequential order -> fp16 operand registers of one
-// 16-element slice.  x0 covers fragment columns (2t, 2t+1), x2 covers
-// (2t+8, 2t+9); element e sits in lane lane_t(e), register reg(e).  Integer
-// codes become exact fp16 values through 1024 + c; E4M3 codes (F8) through
-// the fp8-pair conversion, also exact.
-struct Frag8 {
-  static constexpr int PARTNER = 1;  // element sharing lane and register, other half
-  __device__ static __forceinline__ int base(int i) { return 2 * i; }
-  template <bool F8>
-  __device__ static __forceinline__ void get(const uint32_t* w, int t, uint32_t& x0, uint32_t& x2) {
-    const uint32_t v = w[t];
-    if constexpr (F8) {
-      x0 = e4m3x2_to_half2(v);        // elements 4t, 4t+1
-      x2 = e4m3x2_to_half2(v >> 16);  // elements 4t+2, 4t+3
-      return;
-    }
+// 8-bit fragment-order words -> A registers of one k-step: word x.x holds
+// row g (bytes 0-1) and row g+8 (bytes 2-3) at columns 2t, 2t+1; word x.y the
+// same at columns 2t+8, 2t+9.  Integer codes become exact fp16 values through
+// 1024 + c; E4M3 codes (F8) through the fp8-pair conversion, also exact.
+template <bool F8>
+__device__ __forceinline__ void frag_a8(uint2 x, uint32_t& a0, uint32_t& a1, uint32_t& a2,
+                                        uint32_t& a3) {
+  if constexpr (F8) {
+    a0 = e4m3x2_to_half2(x.x);
+    a1 = e4m3x2_to_half2(x.x >> 16);
+    a2 = e4m3x2_to_half2(x.y);
+    a3 = e4m3x2_to_half2(x.y >> 16);
+  } else {
     const __half2 k1024 = __float2half2_rn(1024.0f);
-    uint32_t p0 = __byte_perm(v, 0x64646464u, 0x4140u);  // 1024 + byte0, 1024 + byte1
-    uint32_t p2 = __byte_perm(v, 0x64646464u, 0x4342u);  // 1024 + byte2, 1024 + byte3
-    __half2 h0 = __hsub2(*reinterpret_cast<__half2*>(&p0), k1024);
-    __half2 h2 = __hsub2(*reinterpret_cast<__half2*>(&p2), k1024);
-    x0 = *reinterpret_cast<uint32_t*>(&h0);  // elements 4t, 4t+1 (exact codes)
-    x2 = *reinterpret_cast<uint32_t*>(&h2);  // elements 4t+2, 4t+3
+    auto pair = [&](uint32_t v, uint32_t sel) -> uint32_t {
+      uint32_t b = __byte_perm(v, 0x64646464u, sel);  // 1024 + byte, 1024 + byte
+      __half2 h = __hsub2(*reinterpret_cast<__half2*>(&b), k1024);
+      return *reinterpret_cast<uint32_t*>(&h);
+    };
+    a0 = pair(x.x, 0x4140u);
+    a1 = pair(x.x, 0x4342u);
+    a2 = pair(x.y, 0x4140u);
+    a3 = pair(x.y, 0x4342u);
   }
-  __device__ static __forceinline__ int lane_t(int e) { return e >> 2; }
-  __device__ static __forceinline__ int reg(int e) { return (e & 3) >= 2 ? 1 : 0; }
-};
+}
+
+// The two 8-bit words of (m-tile mt, k-step ks) of lane `lane` in a region of
+// KSN k-steps per m-tile: words 2*(mt*KSN + ks) and the next, adjacent.
+template <int KSN>
+__device__ __forceinline__ uint2 words8(const uint32_t* region, int mt, int ks, int lane) {
+  const int w = 2 * (mt * KSN + ks);
+  return *reinterpret_cast<const uint2*>(region + ((w >> 2) * 32 + lane) * 4 + (w & 3));
+}
 
 // B-operand slot of channel/token pair P (two adjacent k of one register):
 // k-step ks, register rg (0: k 2t.., 1: k 2t+8..), lane slot_t, first
-// element k0, and the factor 2^(24 - p) of its codes (1 for 8-bit codes).
+// element k0, and the factor 2^(24 - p) of its codes (1 for 8-bit codes,
+// which are exact fp16 values).
 template <int BITS>
 __device__ __forceinline__ void b_slot(int P, int& ks, int& rg, int& slot_t, int& k0, float& f) {
-  if constexpr (BITS == 8) {
-    const int e0 = Frag8::base(P & 7);
-    ks = P >> 3;
-    rg = Frag8::reg(e0);
-    slot_t = Frag8::lane_t(e0);
-    k0 = 16 * ks + e0;
-    f = 1.f;
-  } else {
-    ks = P >> 3;
-    rg = (P >> 2) & 1;
-    slot_t = P & 3;
-    k0 = 16 * ks + 8 * rg + 2 * slot_t;
-    f = BITS == 2 ? pow2i(24 - 2 * (2 * (ks & 1) + rg)) : 16777216.f;
-  }
+  ks = P >> 3;
+  rg = (P >> 2) & 1;
+  slot_t = P & 3;
+  k0 = 16 * ks + 8 * rg + 2 * slot_t;
+  f = BITS == 2 ? pow2i(24 - 2 * (2 * (ks & 1) + rg)) : (BITS == 4 ? 16777216.f : 1.f);
 }
 
 template <int D, int BK, int BV, int R, bool ROPE>
@@ -141,8 +140,6 @@ struct MmaCfg {
   static constexpr int NG = D / 32;               // value channel groups
   static constexpr int MTV = D / 16;              // value m-tiles
   static constexpr int CPL = D / 32;              // output channels per lane
-  static constexpr bool KFRAG = BK <= 4;          // key codes in fragment order
-  static constexpr bool VFRAG = BV <= 4;          // value codes in fragment order
   static constexpr int NT = (2 * R + 7) / 8;      // n-tiles = query groups of 4
   static constexpr int KS = D / 16;               // key k-steps
   static constexpr int KWL = D * BK / 32;         // key words per lane / per row
@@ -174,8 +171,8 @@ struct MmaCfg {
   static constexpr int CS_BYTES = ROPE ? (D / 2) * 32 * 8 : 0;
   static constexpr int SMEM = kDecodeWarps * WARP_BYTES + CS_BYTES;
   static_assert(2 * TCH * D * 2 == STAGE, "a tail chunk fills one stage");
-  static_assert(!KFRAG || KWL % 4 == 0, "lane words are read as 16-byte vectors");
-  static_assert(!VFRAG || VWL % 4 == 0, "lane words are read as 16-byte vectors");
+  static_assert(KWL % 4 == 0, "lane words are read as 16-byte vectors");
+  static_assert(VWL % 4 == 0, "lane words are read as 16-byte vectors");
 };
 
 // uint2 slot of lane l in B-operand block blk (BL lanes per block): XOR-swizzled
@@ -472,7 +469,20 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       for (int b = 0; b < NT; ++b)
 #pragma unroll
         for (int k = 0; k < 4; ++k) sc[a][b][k] = 0.f;
-    if constexpr (C::KFRAG) {
+    if constexpr (BK == 8) {
+#pragma unroll
+      for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          frag_a8<F8>(words8<KS>(kc, mt, ks, lane), a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
+            mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+          }
+        }
+    } else {
       uint32_t kw[C::KWL];
 #pragma unroll
       for (int q = 0; q < C::KWL / 4; ++q) {
@@ -492,25 +502,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
             mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
-    } else {
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) {
-        const uint32_t* r0 = kc + (16 * mt + g) * C::KWL;
-        const uint32_t* r1 = r0 + 8 * C::KWL;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          Frag8::get<F8>(r0 + ks * 4, t, a0, a2);
-          Frag8::get<F8>(r1 + ks * 4, t, a1, a3);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
-            mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
-          }
-        }
-      }
     }
-
   };
 
   auto softmax_scores = [&](float (&sc)[2][NT][4], const float (&kz)[R], float ek2,
@@ -634,7 +626,22 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   auto v_mma = [&](const uint8_t* st) {
     const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + C::KC_S + C::KM_S);
     // ---- values: O[c][2r+h] += sum_tok A_V[c][tok] * B_V[tok][2r+h]
-    if constexpr (C::VFRAG) {
+    if constexpr (BV == 8) {
+#pragma unroll
+      for (int mt = 0; mt < MTV; ++mt) {
+        const int gp = mt >> 1;
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          frag_a8<F8>(words8<2>(vc, mt, ks, lane), a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
+            mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+          }
+        }
+      }
+    } else {
       uint32_t vw[C::VWL];
 #pragma unroll
       for (int q = 0; q < C::VWL / 4; ++q) {
@@ -649,24 +656,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           uint32_t a0, a1, a2, a3;
           if constexpr (BV == 2) frag_a2(vw[mt], ks, a0, a1, a2, a3);
           else frag_a4(vw[2 * mt + ks], a0, a1, a2, a3);
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
-            mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
-          }
-        }
-      }
-    } else {
-#pragma unroll
-      for (int mt = 0; mt < MTV; ++mt) {
-        const int gp = mt >> 1;
-        const uint32_t* c0 = vc + (16 * mt + g) * BV;
-        const uint32_t* c1 = c0 + 8 * BV;
-#pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          Frag8::get<F8>(c0 + ks * 4, t, a0, a2);
-          Frag8::get<F8>(c1 + ks * 4, t, a1, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
@@ -708,15 +697,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
         }
       }
       __syncwarp();
-      // lane = token: its key codes.  Fragment order: token 16 mt + 8 hr + g2
-      // sits in lanes 4 g2 + t of the words of m-tile mt; sequential order:
-      // one row of KWL words.
-      constexpr int NKR = C::KFRAG ? 4 * (C::KWL / 2) : C::KWL;
+      // lane = token: its key codes.  Token 16 mt + 8 hr + g2 sits in lanes
+      // 4 g2 + t of the words of m-tile mt (fragment order): 2- and 4-bit
+      // words are held in registers, 8-bit codes are read as bytes.
+      constexpr int NKR = BK == 8 ? 1 : 4 * (C::KWL / 2);
       uint32_t kr[NKR];
-      int hr = 0;
-      if constexpr (C::KFRAG) {
-        const int mt = lane >> 4, g2 = lane & 7;
-        hr = (lane >> 3) & 1;
+      const int mt = lane >> 4, g2 = lane & 7, hr = (lane >> 3) & 1;
+      if constexpr (BK != 8) {
         constexpr int WPM = C::KWL / 2;  // words per m-tile
 #pragma unroll
         for (int ww = 0; ww < WPM; ++ww)
@@ -725,28 +712,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
             const int w = mt * WPM + ww;
             kr[ww * 4 + tq] = kc[((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)];
           }
-      } else {
-        const uint4* row = reinterpret_cast<const uint4*>(kc + lane * C::KWL);
-#pragma unroll
-        for (int v = 0; v < C::KWL / 4; ++v) {
-          const uint4 w4 = row[v];
-          kr[4 * v] = w4.x; kr[4 * v + 1] = w4.y; kr[4 * v + 2] = w4.z; kr[4 * v + 3] = w4.w;
-        }
       }
       // bit of the 2-bit field of (row half hr, pi = 2 (ks % 2) + kh)
       int sh2[4];
 #pragma unroll
       for (int pi = 0; pi < 4; ++pi) sh2[pi] = hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0);
       auto kcode = [&](int d) -> uint32_t {
-        if constexpr (C::KFRAG) {
-          const int ks = d >> 4, kh = (d >> 3) & 1, tq = (d >> 1) & 3, e = d & 1;
-          if constexpr (BK == 2)
-            return (kr[(ks >> 1) * 4 + tq] >> (16 * e + sh2[2 * (ks & 1) + kh])) & 3u;
-          else
-            return (kr[ks * 4 + tq] >> (16 * e + 8 * kh + 4 * hr)) & 15u;
+        const int ks = d >> 4, kh = (d >> 3) & 1, tq = (d >> 1) & 3, e = d & 1;
+        if constexpr (BK == 2) {
+          return (kr[(ks >> 1) * 4 + tq] >> (16 * e + sh2[2 * (ks & 1) + kh])) & 3u;
+        } else if constexpr (BK == 4) {
+          return (kr[ks * 4 + tq] >> (16 * e + 8 * kh + 4 * hr)) & 15u;
         } else {
-          constexpr int KPER = 32 / BK;
-          return (kr[d / KPER] >> ((d % KPER) * BK)) & ((1u << BK) - 1u);
+          const int w = 2 * (mt * KS + ks) + kh;
+          const uint8_t* kb = reinterpret_cast<const uint8_t*>(kc);
+          return kb[(((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)) * 4 + 2 * hr + e];
         }
       };
       float sc[R];

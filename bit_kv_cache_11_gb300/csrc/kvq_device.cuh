@@ -136,10 +136,11 @@ __host__ __device__ inline bool mma_geometry(int G, int ak, int av) {
 }
 
 // Code order of one side (include/kvq.h, "Code order of a side"): fragment
-// order for 2- and 4-bit codes in the tensor-core geometry with D = 64 or
-// 128, sequential order otherwise.
+// order for every bit width in the tensor-core geometry with D = 64 or 128,
+// sequential order otherwise.
 __host__ __device__ inline bool fragment_order(int D, int G, int bits, int ak, int av) {
-  return mma_geometry(G, ak, av) && (D == 64 || D == 128) && (bits == 2 || bits == 4);
+  return mma_geometry(G, ak, av) && (D == 64 || D == 128) &&
+         (bits == 2 || bits == 4 || bits == 8);
 }
 
 // Fragment order: word (within the side's 32-token region) and bit of tile
@@ -154,9 +155,12 @@ __host__ __device__ inline void frag_position(int row, int col, int cols, int bi
     const int pi = 2 * (ks & 1) + kh;  // F2[0] = {0, 10, 12, 14}, F2[1] = {2, 4, 6, 8}
     w = mt * (cols >> 5) + (ks >> 1);
     *bit = 16 * e + (hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0));
-  } else {
+  } else if (bits == 4) {
     w = mt * (cols >> 4) + ks;
     *bit = 16 * e + 8 * kh + 4 * hr;
+  } else {
+    w = 2 * (mt * (cols >> 4) + ks) + kh;
+    *bit = 8 * (2 * hr + e);
   }
   *word = ((w >> 2) * 32 + 4 * g + t) * 4 + (w & 3);
 }

@@ -266,7 +266,8 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
   // chunks, channel-major.  Fragment order (G = 32): word w of lane l = 4g + t
   // collects, per (hr, kh) and k-step, the two codes of tile row
   // 16 mt + 8 hr + g at columns 16 ks + 8 kh + 2 t + {0, 1} -- two adjacent
-  // bytes of the code tile, spread to bits b and b + 16.
+  // bytes of the code tile, spread to bits b and b + 16 (2 and 4 bits), or
+  // kept as bytes 0-1 (row g) and 2-3 (row g + 8) of the word (8 bits).
   auto frag_word = [&](const uint8_t* tile, int pitch, int cols, int bits, int w) -> uint32_t {
     const int l = (w >> 2) & 31, lw = ((w >> 7) << 2) | (w & 3);
     const int g = l >> 2, t = l & 3;
@@ -282,7 +283,7 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
           const int b = hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0);
           word |= __byte_perm(two, 0u, 0x7170) << b;  // bytes 0, 1 -> bits 0 and 16
         }
-    } else {
+    } else if (bits == 4) {
       const int mt = lw / (cols >> 4), ks = lw - mt * (cols >> 4);
 #pragma unroll
       for (int hr = 0; hr < 2; ++hr)
@@ -292,6 +293,13 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
           const uint32_t two = *reinterpret_cast<const uint16_t*>(tile + (16 * mt + 8 * hr + g) * pitch + col);
           word |= __byte_perm(two, 0u, 0x7170) << (8 * kh + 4 * hr);
         }
+    } else {  // 8 bits: rows g and g + 8 at columns 2t, 2t + 1 of one k-half
+      const int kh = lw & 1, q2 = lw >> 1;
+      const int mt = q2 / (cols >> 4), ks = q2 - mt * (cols >> 4);
+      const int col = 16 * ks + 8 * kh + 2 * t;
+      const uint32_t lo = *reinterpret_cast<const uint16_t*>(tile + (16 * mt + g) * pitch + col);
+      const uint32_t hi = *reinterpret_cast<const uint16_t*>(tile + (16 * mt + 8 + g) * pitch + col);
+      word = lo | (hi << 16);
     }
     return word;
   };

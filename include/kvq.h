@@ -81,8 +81,8 @@
  *
  *   Code order of a side (kvq_buffers.code_order_k / code_order_v):
  *   FRAGMENT order when keys are grouped per channel, values per token,
- *   G = 32, D is 64 or 128 and the side has 2 or 4 bits; SEQUENTIAL order
- *   otherwise.
+ *   G = 32 and D is 64 or 128 (2, 4 or 8 bits, FP8 included); SEQUENTIAL
+ *   order otherwise.
  *     Sequential.  K: token-major, token j's row is D*bk/32 words; channel d
  *       sits in word d/(32/bk) at bit (d % (32/bk))*bk.  V: 32-token chunks
  *       c = j/32; inside a chunk, channel-major: channel d owns bv words at
@@ -98,6 +98,7 @@
  *       The code belongs to lane l = 4*g + t, in that lane's word
  *         w = mt*(cols/32) + ks/2  at bit 16*e + F2[hr][2*(ks%2) + kh]  (2 bits)
  *         w = mt*(cols/16) + ks    at bit 16*e + 8*kh + 4*hr            (4 bits)
+ *         w = 2*(mt*(cols/16) + ks) + kh   at bit 8*(2*hr + e)          (8 bits)
  *       with F2[0] = {0, 10, 12, 14}, F2[1] = {2, 4, 6, 8}; word w of lane l
  *       is word ((w/4)*32 + l)*4 + w%4 of the region.
  *
