@@ -42,6 +42,21 @@ def decode_bytes(w, T_q, T_t):
     return codes + meta + tail + qo
 
 
+def append_one(row, n_sink, residual, group):
+    """Row lengths [T_sink, T_q, T_tail] after one appended token: it fills
+    the sink window first, then the tail; a group of `group` tokens is
+    quantized once it leaves `residual` newer tail tokens (the cache's append
+    rule, used to account the bytes of steps timed without host queries)."""
+    ts, tq, tt = row
+    if ts < n_sink:
+        return [ts + 1, tq, tt]
+    tt += 1
+    if tt >= residual + group:
+        tq += group
+        tt -= group
+    return [ts, tq, tt]
+
+
 def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, fp8=False,
                 lengths=None):
     """The same decode step on a variant of the cache: fp16 windows (the first
@@ -96,14 +111,8 @@ def variant_leg(w, dev, stream, n_layers, warmup, steps, n_sink=0, residual=0, f
     for layer, a, e in ev:
         rows = lens[layer]
         fused = all(ts == n_sink and tt + 1 < residual + w.group for ts, _, tt in rows)
-        for r in rows:
-            if r[0] < n_sink:
-                r[0] += 1
-            else:
-                r[2] += 1
-                if r[2] >= residual + w.group:
-                    r[1] += w.group
-                    r[2] -= w.group
+        for i_r, r in enumerate(rows):
+            rows[i_r] = append_one(r, n_sink, residual, w.group)
         nb = sum(decode_bytes(w.with_(batch=1), tq, tt + ts) for ts, tq, tt in rows)
         if fused:
             timed.append((a, e, nb))

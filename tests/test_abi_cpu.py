@@ -119,3 +119,36 @@ def test_null_handles_are_rejected_on_host(lib_path):
     assert lib.kvq_destroy(None) == k.KVQ_OK
     T = ctypes.c_int(0)
     assert lib.kvq_get_state(None, ctypes.byref(T), ctypes.byref(T)) == k.KVQ_ERR_INVALID_ARG
+
+
+def test_ctypes_structs_match_the_header(lib_path, tmp_path):
+    """The binding's kvq_config and kvq_buffers have the C layout of
+    include/kvq.h: every field at the same offset, the same sizes (a C program
+    built against the header prints them)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    k = _kvq(lib_path)
+    structs = {"kvq_config": k.kvq_config, "kvq_buffers": k.kvq_buffers}
+    lines = []
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "kvq.h"\nint main(void) {\n'
+                   + "\n".join(lines) + "\nreturn 0;\n}\n")
+    exe = tmp_path / "layout"
+    include = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    subprocess.check_call(["gcc", "-std=c99", "-I", include, str(src), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)], text=True).split("\n")
+    got = {}
+    for line in out:
+        if line:
+            struct, field, value = line.split()
+            got[(struct, field)] = int(value)
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert got[(name, field)] == getattr(cls, field).offset, (name, field)
