@@ -152,3 +152,17 @@ def test_ctypes_structs_match_the_header(lib_path, tmp_path):
         assert got[(name, "size")] == ctypes.sizeof(cls), name
         for field, _ in cls._fields_:
             assert got[(name, field)] == getattr(cls, field).offset, (name, field)
+
+
+def test_noalloc_refuses_windows_on_host(lib_path):
+    """kvq_decode_attention_noalloc takes no sink or residual buffers: a config
+    with either window is refused before any device work (no GPU needed)."""
+    k = _kvq(lib_path)
+    for kw in (dict(n_sink=4), dict(residual=32), dict(keys_pre_rope=True)):
+        cfg = k.make_config(2, 8, 8, 128, 256, **kw)
+        status = k._lib.kvq_decode_attention_noalloc(ctypes.byref(cfg), None, None, None, 0, 0,
+                                                    None, None, 0.1, None, None)
+        assert status == k.KVQ_ERR_UNSUPPORTED, kw
+    bad = k.make_config(2, 8, 8, 128, 256, fp8=True, bits_k=8, bits_v=4)
+    assert k._lib.kvq_decode_attention_noalloc(ctypes.byref(bad), None, None, None, 0, 0, None,
+                                               None, 0.1, None, None) == k.KVQ_ERR_INVALID_ARG
