@@ -678,3 +678,25 @@ def test_fp8_dequantize_is_value_times_scale(oracle_mod):
         e8 = oracle_mod.rel_fro(got, X.astype(np.float32))
         e4 = oracle_mod.rel_fro(oracle_mod.dequantize_tensor(c4, s4, z4, 32, axis), X.astype(np.float32))
         assert e8 < e4
+
+
+def test_fp8_cache_error_is_small_next_to_low_bit_codes(oracle_mod):
+    """On the Llama-2-7B-shaped recipe (outlier key channels, sink tokens) an
+    FP8 cache keeps the attention output much closer to the fp16 result than
+    4- and 2-bit integer codes on the same groups: the pages' case for trying
+    FP8 first (direction only)."""
+    from bit_kv_cache_11_gb300 import synth
+    w = synth.small(synth.WORKLOADS[2], batch=1, n_kv_heads=4, T=300)
+    case = synth.make_case(w, seed=2025)
+    err = {}
+    for name, bits, fp8 in (("fp8", 8, True), ("int4", 4, False), ("int2", 2, False)):
+        oe = []
+        for h in range(w.n_kv_heads):
+            K, V, q = case["K"][0, h], case["V"][0, h], case["q"][0, h:h + 1]
+            st = oracle_mod.build_pair(K, V, 32, bits, bits, 0, 1, fp8=fp8)
+            out = oracle_mod.decode_pair(st, q, w.scale)
+            ref = oracle_mod.reference_pair(K, V, q, w.scale)
+            oe.append(oracle_mod.rel_fro(out, ref))
+        err[name] = np.mean(oe)
+    assert err["fp8"] < 0.6 * err["int4"]
+    assert err["fp8"] < 0.1 * err["int2"]
