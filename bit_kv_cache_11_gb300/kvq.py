@@ -252,7 +252,24 @@ def device_view(ptr: int, shape, typestr: str = "|u1"):
 
 
 class KVCache:
-    """One layer's packed KV cache on the current CUDA device."""
+    """One layer's packed KV cache on the current CUDA device.
+
+    Keyword arguments are those of ``make_config`` (the fields of
+    ``kvq_config``): batch, n_q_heads, n_kv_heads, head_dim, max_ctx,
+    bits_k / bits_v (2, 4, 8), group (32, 64, 128), axis_k / axis_v,
+    keys_pre_rope / rope_base, n_sink and residual (fp16 windows), fp8 (E4M3
+    codes, 8-bit sides).  A typical decode loop::
+
+        cache = KVCache(batch=8, n_q_heads=32, n_kv_heads=32, head_dim=128,
+                        max_ctx=8192, bits_k=2, bits_v=2)
+        cache.prefill(k, v)                    # [B][Hkv][T][D] fp16 on the GPU
+        for step in range(n):
+            out = cache.append_decode(k1, v1, q)   # [B][Hkv][1][D], [B][Hq][D]
+
+    ``prefill_ragged`` / ``append_ragged`` take per-row lengths (a serving
+    batch of sequences of different lengths, batch <= 64); ``row_state``
+    reports each row's sink, quantized and tail counts.
+    """
 
     def __init__(self, **cfg_kw):
         self.cfg = make_config(**cfg_kw)
