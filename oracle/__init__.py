@@ -22,7 +22,17 @@ Sources (page titles and sections):
     Keys";
   * attention output and the error metrics (relative Frobenius norm, the
     plainest reading of the pages' unnamed error measures): same page, "Keys"
-    and "Values" sections.
+    and "Values" sections;
+  * fp16 windows (``window_lengths``): the residual window from "The Systems
+    Tax, and Why It Is Not a Detail" (a sliding window of recent tokens kept
+    in full precision), the sink window from "Where the Work Is Headed"
+    (high-precision windows for attention-sink tokens);
+  * FP8 cache (``e4m3_value``, ``e4m3_encode``, ``quantize_group_fp8``):
+    "Rotate, Then Round: The Geometry of KV-Cache Compression", "Key
+    takeaway"; the E4M3 format as the OCP 8-bit floating-point specification
+    defines it.
+A batch of rows with different lengths is checked row by row: each row is
+its own sequence (``build_pair`` of that row's tokens).
 """
 from __future__ import annotations
 

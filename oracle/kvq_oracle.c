@@ -20,6 +20,8 @@
  *   RoPE after dequant GEOMETRY "Rotary Embeddings Complicate the Keys"
  *   attention ........ GEOMETRY "Values: Where the Intuition Breaks" (softmax
  *                      weighted sum of value vectors), evaluated in fp64.
+ *   FP8 (E4M3) ....... "Rotate, Then Round: The Geometry of KV-Cache
+ *                      Compression", "Key takeaway"; the OCP E4M3 format.
  *
  * Every function works on ONE (batch, kv-head) pair; loops are plain and in
  * the order of the definition.  Parity pins for every function live in the
