@@ -5,6 +5,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
@@ -28,8 +29,38 @@ namespace {
 
 // Most warps a decode launch uses; the partial workspace is sized for it.
 constexpr long long kMaxDecodeWarps = 4096;
+// Virtual units charged after every pair in the tensor-core kernel's split.
+constexpr int kPairCost = 2;
 
 std::atomic<uint64_t> g_launches{0};
+
+// Fault injection (kvq_debug_fail_allocations): after g_alloc_pass more
+// successful device allocations, the next g_alloc_fail ones fail as if the
+// device were out of memory.
+std::mutex g_alloc_mu;
+int g_alloc_pass = 0;
+int g_alloc_fail = 0;
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  {
+    std::lock_guard<std::mutex> lock(g_alloc_mu);
+    if (g_alloc_fail > 0) {
+      if (g_alloc_pass > 0) {
+        --g_alloc_pass;
+      } else {
+        --g_alloc_fail;
+        *p = nullptr;
+        return cudaErrorMemoryAllocation;
+      }
+    }
+  }
+  return cudaMalloc(p, bytes);
+}
+
+template <typename T>
+bool alloc_ok(T** p, size_t bytes) {
+  return dev_alloc(reinterpret_cast<void**>(p), bytes) == cudaSuccess;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -73,9 +104,9 @@ kvq_status derive(const kvq_config* c, Derived* d) {
   if (P > 65535) return KVQ_ERR_UNSUPPORTED;  // grid.y of the quantize launch
   if (c->max_ctx > (1 << 26)) return KVQ_ERR_UNSUPPORTED;
   // decode units (32-token sub-blocks, tail and sink chunks of at least six
-  // tokens) are counted in int
-  if (P * (static_cast<long long>(c->max_ctx) / 32 + (c->n_sink + c->residual + c->group) / 6 + 2) >=
-      (1LL << 31))
+  // tokens) and their split costs (plus kPairCost per pair) are counted in int
+  if (P * (static_cast<long long>(c->max_ctx) / 32 + (c->n_sink + c->residual + c->group) / 6 + 2 +
+           kPairCost) >= (1LL << 31))
     return KVQ_ERR_UNSUPPORTED;
   d->P = static_cast<int>(P);
   d->R = R;
@@ -147,6 +178,7 @@ struct kvq_cache {
   float2* lvl_ml;
   int* tickets2; // [P*R] two-level merge counters, zero between launches
   bool mma;      // decode runs the tensor-core kernel (which can merge in place)
+  uint32_t wait_limit;  // try_wait rounds of a decode kernel's bounded waits
   // Token counts per batch row: sink, quantized, tail, and the row's active
   // tail buffer.  A uniform cache keeps every entry equal to row 0; a ragged
   // cache (rows of different lengths, batch <= kMaxRows) one entry per row.
@@ -322,6 +354,7 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   c->dv = d;
   c->ops = ops;
   c->mma = mma;
+  c->wait_limit = kWaitLimit;
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) !=
           cudaSuccess ||
@@ -334,22 +367,18 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
     delete c;
     return KVQ_ERR_UNSUPPORTED;
   }
-  bool ok = cudaMalloc(&c->blocks, d.blocks_bytes > 0 ? d.blocks_bytes : 16) == cudaSuccess;
-  for (int i = 0; i < 2 && ok; ++i) {
-    ok = cudaMalloc(&c->ktail[i], d.tail_bytes) == cudaSuccess &&
-         cudaMalloc(&c->vtail[i], d.tail_bytes) == cudaSuccess;
-  }
-  if (ok && d.sink_bytes)
-    ok = cudaMalloc(&c->ksink, d.sink_bytes) == cudaSuccess &&
-         cudaMalloc(&c->vsink, d.sink_bytes) == cudaSuccess;
-  if (ok && d.rope_bytes) ok = cudaMalloc(&c->rope, d.rope_bytes) == cudaSuccess;
-  if (ok) ok = cudaMalloc(&c->part_o, d.part_o_bytes) == cudaSuccess;
-  if (ok) ok = cudaMalloc(&c->part_ml, d.part_ml_bytes) == cudaSuccess;
-  if (ok) ok = cudaMalloc(&c->err, sizeof(int)) == cudaSuccess;
-  if (ok) ok = cudaMalloc(&c->tickets, sizeof(int) * d.P) == cudaSuccess;
-  if (ok) ok = cudaMalloc(&c->lvl_o, d.lvl_o_bytes) == cudaSuccess;
-  if (ok) ok = cudaMalloc(&c->lvl_ml, d.lvl_ml_bytes) == cudaSuccess;
-  if (ok) ok = cudaMalloc(&c->tickets2, sizeof(int) * d.P * d.R) == cudaSuccess;
+  bool ok = alloc_ok(&c->blocks, d.blocks_bytes > 0 ? d.blocks_bytes : 16);
+  for (int i = 0; i < 2 && ok; ++i)
+    ok = alloc_ok(&c->ktail[i], d.tail_bytes) && alloc_ok(&c->vtail[i], d.tail_bytes);
+  if (ok && d.sink_bytes) ok = alloc_ok(&c->ksink, d.sink_bytes) && alloc_ok(&c->vsink, d.sink_bytes);
+  if (ok && d.rope_bytes) ok = alloc_ok(&c->rope, d.rope_bytes);
+  if (ok) ok = alloc_ok(&c->part_o, d.part_o_bytes);
+  if (ok) ok = alloc_ok(&c->part_ml, d.part_ml_bytes);
+  if (ok) ok = alloc_ok(&c->err, sizeof(int));
+  if (ok) ok = alloc_ok(&c->tickets, sizeof(int) * d.P);
+  if (ok) ok = alloc_ok(&c->lvl_o, d.lvl_o_bytes);
+  if (ok) ok = alloc_ok(&c->lvl_ml, d.lvl_ml_bytes);
+  if (ok) ok = alloc_ok(&c->tickets2, sizeof(int) * d.P * d.R);
   if (!ok) {
     cudaGetLastError();
     free_all(c);
@@ -516,28 +545,22 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
     set_row_units(m, b, tch);
     if (c->act[b]) p.act |= 1ull << b;
   }
-  long long U;
+  m.rows = nr;
   int max_upp = 0;
-  if (m.ragged) {
-    m.uoff[0] = 0;
-    for (int b = 0; b < nr; ++b) {
-      m.uoff[b + 1] = m.uoff[b] + m.hkv * units_of_row(m, b);
-      max_upp = std::max(max_upp, units_of_row(m, b));
-    }
-    U = m.uoff[nr];
-  } else {
-    max_upp = units_of_row(m, 0);
-    U = static_cast<long long>(d.P) * max_upp;
-  }
+  for (int b = 0; b < nr; ++b) max_upp = std::max(max_upp, units_of_row(m, b));
+  long long target = static_cast<long long>(c->sm_count) * c->decode_ctas_per_sm * kDecodeWarps;
+  if (target > kMaxDecodeWarps) target = kMaxDecodeWarps;
+  // Leaving a pair (its partial, the merge, the next pair's query and its
+  // fp16 tail units) costs the tensor-core kernel about kPairCost units of
+  // block work: the split charges each pair that much extra.
+  const long long W = finish_map(m, d.P, c->mma ? kPairCost : 0, target);
+  const long long U = m.U;
   if (U == 0) {  // an empty cache (n_new is 0 here)
     if (cudaMemsetAsync(out, 0, static_cast<size_t>(d.P) * d.R * d.D * sizeof(float), st) !=
         cudaSuccess)
       return KVQ_ERR_CUDA;
     return KVQ_OK;
   }
-  long long target = static_cast<long long>(c->sm_count) * c->decode_ctas_per_sm * kDecodeWarps;
-  if (target > kMaxDecodeWarps) target = kMaxDecodeWarps;
-  const long long W = U < target ? U : target;
 
   p.g = geom_of(c);
   for (int i = 0; i < 2; ++i) {
@@ -551,7 +574,6 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   p.vnew = static_cast<const __half*>(vnew);
   p.lg_G = d.G == 32 ? 5 : (d.G == 64 ? 6 : 7);
   p.lg_sub = p.lg_G - 5;
-  p.U = U;
   p.n_warps = static_cast<int>(W);
   p.rope = c->cfg.keys_pre_rope;
   p.rope_tab = c->rope;
@@ -561,10 +583,11 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   p.part_o = c->part_o;
   p.part_ml = c->part_ml;
   p.err = c->err;
+  p.wait_limit = c->wait_limit;
   // Merge in place when every pair has few partials; the separate merge
   // kernel otherwise (few pairs over many warps, e.g. one long sequence).
-  // A pair's units [x, x + upp) touch at most upp * W / U + 2 warps.
-  const long long max_seg = static_cast<long long>(max_upp) * W / U + 2;
+  // A pair's costs touch at most (upp + vcost) * W / C + 2 warps.
+  const long long max_seg = static_cast<long long>(max_upp + m.vcost) * W / m.C + 2;
   p.fused = (c->mma && max_seg <= 64) ? 1 : 0;
   p.tickets = c->tickets;
   p.out = static_cast<float*>(out);
@@ -581,8 +604,6 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   mp.tickets = c->tickets2;
   mp.out = static_cast<float*>(out);
   mp.map = m;
-  mp.U = U;
-  mp.n_warps = static_cast<int>(W);
   mp.R = d.R;
   mp.D = d.D;
   // chunks of CS partial slots, at most C2max chunks per (pair, query)
@@ -724,6 +745,32 @@ kvq_status kvq_check_device_error(kvq_cache* c, void* stream) {
 }
 
 uint64_t kvq_launch_count(void) { return g_launches.load(); }
+
+kvq_status kvq_debug_fail_allocations(int after, int n) {
+  if (after < 0 || n < 0) return KVQ_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_alloc_mu);
+  g_alloc_pass = after;
+  g_alloc_fail = n;
+  return KVQ_OK;
+}
+
+kvq_status kvq_debug_set_device_error(kvq_cache* c, int value) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARG;
+  DeviceGuard g(c->device);
+  if (!g.ok) return KVQ_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(c->err, &value, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_ERR_CUDA;
+  }
+  return KVQ_OK;
+}
+
+kvq_status kvq_debug_set_wait_limit(kvq_cache* c, int limit) {
+  if (c == nullptr) return KVQ_ERR_INVALID_ARG;
+  c->wait_limit = limit < 0 ? kWaitLimit : static_cast<uint32_t>(limit);
+  return KVQ_OK;
+}
 
 const char* kvq_status_string(kvq_status s) {
   switch (s) {

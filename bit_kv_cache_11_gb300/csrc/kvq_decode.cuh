@@ -8,9 +8,11 @@
 // Is Where This Bites"), so the kernel is built to stream HBM.
 //
 // Work decomposition.  Units are (pair, 32-token sub-block) plus one fp16
-// unit per pair for the tail and one for the sink window (when present); warp w of the grid owns units [w*U/W, (w+1)*U/W) — a
-// contiguous range, so every warp streams contiguous memory and all warps get
-// the same amount of work whatever the batch/head/context shape.  A warp keeps
+// unit per pair for the tail and one for the sink window (when present); warp
+// w of the grid owns a contiguous range of units (kvq_device.cuh, UnitMap: an
+// equal share of the cost, where every pair adds a few virtual units for the
+// work of leaving it), so every warp streams contiguous memory and all warps
+// get the same amount of work whatever the batch/head/context shape.  A warp keeps
 // one online-softmax state (m, l, o) per query head of the GQA group and
 // writes it as a partial for every pair its range touches; the merge kernel
 // combines the partials of a pair.
@@ -88,8 +90,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
   const int lgG = p.lg_G;
   const int ng = D >> lgG;     // channel groups per token (token axis); 0 if G > D
   const int sub_mask = (1 << p.lg_sub) - 1;
-  const long long ua = gw * p.U / p.n_warps;
-  const long long ub = (gw + 1) * p.U / p.n_warps;
+  int ua_i, ub_i;
+  warp_units(p.map, static_cast<int>(gw), &ua_i, &ub_i);
+  const long long ua = ua_i, ub = ub_i;
 
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
@@ -435,7 +438,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
       continue;
     }
     const int s = qi % NS;
-    if (!mbar_wait_bounded(&bars[s], static_cast<uint32_t>((qi / NS) & 1))) {
+    if (!mbar_wait_bounded(&bars[s], static_cast<uint32_t>((qi / NS) & 1), p.wait_limit)) {
       // Give up: record the error, wait (bounded) for this warp's copies in
       // flight so no bulk copy lands after the CTA exits, and return.
       if (lane == 0) atomicExch(p.err, kDevErrWait);

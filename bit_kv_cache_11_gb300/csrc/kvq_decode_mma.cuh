@@ -3,10 +3,14 @@
 // configuration "Your KV cache doesn't have a bit problem, it has a geometry
 // problem" recommends, section "What to Do with This").
 //
-// Work split, partials, merge and fp16 tail are those of decode_split_kernel
-// (kvq_decode.cuh).  With G = 32 a sub-block is a whole block, so one bulk
-// copy of block_bytes moves a unit into a stage; tail units stream their fp16
-// rows through the same stages (mma_tail_chunk tokens per unit).
+// Work split, partials and merge follow decode_split_kernel (kvq_decode.cuh):
+// every warp streams a contiguous range of units (an equal share of the cost,
+// where each pair adds virtual units for the work of leaving it).  With
+// G = 32 a sub-block is a whole block, so one bulk copy of block_bytes moves a
+// unit into a stage; tail units stream their fp16 rows through the same
+// stages (mma_tail_chunk tokens per unit).  The first unit a warp loads for a
+// pair also brings that pair's fp16 queries into a per-stage slot, so a warp
+// never waits on a global load when it enters a pair.
 //
 // Scores and value sums run on mma.sync m16n8k16 (fp16 inputs, fp32
 // accumulation) with the packed codes themselves as the A operand:
@@ -26,11 +30,17 @@
 // through a byte permute (1024 + c) and one half2 subtraction of 1024, E4M3
 // codes through the fp8-pair conversion.
 // B operand.  The fp32 value (q_c * s_c for scores, p_j * s_j for values)
-// times 2^(24 - p) for its k-slot, times a power of two that keeps it inside
-// fp16's range, split into hi + lo.  Rows 8 below (p + 2, or p + 4 for 4-bit
-// codes) come out 4x (16x) and are scaled back once.
+// times 2^(24 - p) for its k-slot (folded into the query once per pair, and
+// into the probabilities as they are stored), times a power of two that keeps
+// it inside fp16's range, split into hi + lo.  Rows 8 below (p + 2, or p + 4
+// for 4-bit codes) come out 4x (16x) and are scaled back once.
 //
-// Scores are in log2 units (the query carries scale * log2 e).
+// Online softmax.  Scores are in log2 units (the query carries scale * log2
+// e).  The running maximum m is raised only when a block holds a score more
+// than kLazyMax above it (and at a pair's first block); otherwise the block's
+// weights exp2(s - m) are used as they are (at most 2^kLazyMax), which keeps
+// the block maximum and its cross-lane reduction off the common path.  The
+// merge weighs partials by their own m, so the result is the same softmax.
 #pragma once
 
 #include "kvq_decode.cuh"
@@ -121,17 +131,21 @@ __device__ __forceinline__ uint2 words8(const uint32_t* region, int mt, int ks, 
   return *reinterpret_cast<const uint2*>(region + ((w >> 2) * 32 + lane) * 4 + (w & 3));
 }
 
-// B-operand slot of channel/token pair P (two adjacent k of one register):
-// k-step ks, register rg (0: k 2t.., 1: k 2t+8..), lane slot_t, first
-// element k0, and the factor 2^(24 - p) of its codes (1 for 8-bit codes,
-// which are exact fp16 values).
-template <int BITS>
-__device__ __forceinline__ void b_slot(int P, int& ks, int& rg, int& slot_t, int& k0, float& f) {
-  ks = P >> 3;
-  rg = (P >> 2) & 1;
-  slot_t = P & 3;
-  k0 = 16 * ks + 8 * rg + 2 * slot_t;
-  f = BITS == 2 ? pow2i(24 - 2 * (2 * (ks & 1) + rg)) : (BITS == 4 ? 16777216.f : 1.f);
+// Largest value of the warp for non-negative finite x: the bit patterns of
+// such floats order as unsigned integers, so one redux.sync finds it.
+__device__ __forceinline__ float warp_max_nonneg(float x) {
+  return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(x)));
+}
+
+// Weights exp2(s - m) of a block may reach 2^kLazyMax before m is raised.
+constexpr float kLazyMax = 8.0f;
+
+// log2 of the factor 2^(24 - p) of a value code at token tau (B_V operand):
+// 2-bit codes sit at p = 2 (2 ((tau >> 4) & 1) + ((tau >> 3) & 1)), 4-bit codes
+// at p = 0, 8-bit codes are exact fp16 values (factor 1).
+template <int BV>
+__host__ __device__ constexpr int vcode_log2(int tau) {
+  return BV == 2 ? 24 - 2 * (2 * ((tau >> 4) & 1) + ((tau >> 3) & 1)) : (BV == 4 ? 24 : 0);
 }
 
 template <int D, int BK, int BV, int R, bool ROPE>
@@ -142,6 +156,8 @@ struct MmaCfg {
   static constexpr int CPL = D / 32;              // output channels per lane
   static constexpr int NT = (2 * R + 7) / 8;      // n-tiles = query groups of 4
   static constexpr int KS = D / 16;               // key k-steps
+  static constexpr int KP = D / 64;               // key channel pairs per lane
+  static constexpr int VJ = NG / 2;               // value items per lane
   static constexpr int KWL = D * BK / 32;         // key words per lane / per row
   static constexpr int VWL = D * BV / 32;         // value words per lane (fragment)
   // rows 8 below come out this many times too large (fragment order)
@@ -154,14 +170,20 @@ struct MmaCfg {
   static constexpr int STAGE = KC_S + KM_S + VC_S + VM_S;  // one block
   static constexpr int NS = ROPE ? 2 : (STAGE <= 4096 ? 3 : 2);
   static constexpr int TCH = mma_tail_chunk(BK, BV);
-  static constexpr int OFF_BAR = NS * STAGE;
+  static constexpr int QB = R * D * 2;            // one pair's fp16 queries
   // B-operand blocks hold only the lanes whose columns exist: BL lanes
-  // (columns < 2R of a single n-tile live in lanes < 8R).
+  // (columns < 2R of a single n-tile live in lanes < 8R), padded to BSTR
+  // uint2 so that the lanes filling one column of several blocks at once hit
+  // distinct banks (the block stride in words is an odd multiple of 8 banks
+  // apart for the four blocks a store instruction touches).
   static constexpr int BL = NT == 1 ? (8 * R < 32 ? 8 * R : 32) : 32;
-  static constexpr int OFF_KB = OFF_BAR + 64;                       // [KS][NT][BL] uint2
-  static constexpr int KB_BYTES = ROPE ? 0 : KS * NT * BL * 8;
-  static constexpr int OFF_VB = OFF_KB + KB_BYTES;                  // [NG][2][NT][BL] uint2
-  static constexpr int VB_BYTES = NG * 2 * NT * BL * 8;
+  static constexpr int BSTR = NT == 1 ? BL + 4 : BL + 2;
+  static constexpr int OFF_BAR = NS * STAGE;
+  static constexpr int OFF_QS = OFF_BAR + 64;                       // [NS][QB] query slots
+  static constexpr int OFF_KB = OFF_QS + NS * QB;                   // [KS*NT][BSTR] uint2
+  static constexpr int KB_BYTES = ROPE ? 0 : KS * NT * BSTR * 8;
+  static constexpr int OFF_VB = OFF_KB + KB_BYTES;                  // [NG*2*NT][BSTR] uint2
+  static constexpr int VB_BYTES = NG * 2 * NT * BSTR * 8;
   static constexpr int OFF_PB = OFF_VB + VB_BYTES;                  // [R][32] float
   static constexpr int OFF_OS = OFF_PB + R * 32 * 4;                // [R][D] float
   // RoPE: per-warp key coefficients [R][D/2][8] floats; per-CTA table of
@@ -173,14 +195,14 @@ struct MmaCfg {
   static_assert(2 * TCH * D * 2 == STAGE, "a tail chunk fills one stage");
   static_assert(KWL % 4 == 0, "lane words are read as 16-byte vectors");
   static_assert(VWL % 4 == 0, "lane words are read as 16-byte vectors");
+  static_assert(QB % 16 == 0 && OFF_QS % 16 == 0, "query slots are bulk-copy targets");
 };
 
-// uint2 slot of lane l in B-operand block blk (BL lanes per block): XOR-swizzled
-// so that the lanes storing one column set into several blocks at once hit
-// distinct banks.
-template <int BL>
-__device__ __forceinline__ int bslot(int blk, int l) {
-  return blk * BL + (l ^ (BL == 8 ? 4 * ((blk >> 1) & 1) : 4 * (blk & 3)));
+// Word offset, inside a B-operand region, of column n relative to column 0
+// of the same lane slot (the slot's base holds its block, lane and register).
+template <int BSTR>
+__host__ __device__ constexpr int bcol(int n) {
+  return (n >> 3) * BSTR * 2 + (n & 7) * 8;
 }
 
 template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false>
@@ -188,13 +210,14 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   using C = MmaCfg<D, BK, BV, R, ROPE>;
   constexpr int NS = C::NS, NT = C::NT, NG = C::NG, MTV = C::MTV, CPL = C::CPL, TCH = C::TCH,
-                STAGE = C::STAGE, KS = C::KS, BL = C::BL;
+                STAGE = C::STAGE, KS = C::KS, BL = C::BL, BSTR = C::BSTR, KP = C::KP,
+                VJ = C::VJ, QB = C::QB;
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const long long gw = static_cast<long long>(blockIdx.x) * kDecodeWarps + warp;
+  const int gw = blockIdx.x * kDecodeWarps + warp;
   // Launched as a programmatic dependent: wait until the preceding grid in
   // the stream has completed (and its writes are visible) before touching
   // global memory, and let the next grid launch while this one runs.
@@ -233,6 +256,10 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     }
   }
   if (gw >= p.n_warps) return;
+  // ---- this warp's units [ua, ub)
+  int ua, ub;
+  warp_units(p.map, gw, &ua, &ub);
+  if (ua >= ub) return;
 
   uint8_t* ws = smem + warp * C::WARP_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ws + C::OFF_BAR);
@@ -242,70 +269,69 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   const uint2* vbv = reinterpret_cast<const uint2*>(ws + C::OFF_VB);
   float* pb = reinterpret_cast<float*>(ws + C::OFF_PB);
   float* os = reinterpret_cast<float*>(ws + C::OFF_OS);
-
-  // Operand buffers (every entry is rewritten each sub-block; lanes >= BL
-  // read zero columns without touching memory).
-  for (int i = lane; i < (C::OFF_PB - C::OFF_KB) / 4; i += 32) kb32[i] = 0u;
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
   }
   __syncwarp();
 
-  // ---- this warp's units [ua, ub) and the load cursor, NS units ahead
-  const int ua = static_cast<int>(gw * p.U / p.n_warps);
-  const int ub = static_cast<int>((gw + 1) * p.U / p.n_warps);
+  // ---- the load cursor (unit lj of pair lpr), NS units ahead of compute
   int lu = ua;
   int lpr = static_cast<int>(pair_of_unit(p.map, ua));
   int lj = ua - static_cast<int>(first_unit(p.map, lpr));
-  int lnsub = pair_nsub(p, lpr), lupp = pair_upp(p, lpr);  // the load cursor's pair
-  int pr = lpr, j = lj;             // the compute cursor (unit j of pair pr)
-  int cnsub = lnsub, cupp = lupp;
+  int lnsub = pair_nsub(p, lpr), lupp = pair_upp(p, lpr);
+  bool lfirst = true;  // the next load is this warp's first unit of its pair
   const uint8_t* lbase = p.g.blocks + static_cast<size_t>(lpr) * p.g.NB * STAGE;
-  auto issue = [&](int s) {  // lane 0: unit (lpr, lj) -> stage s
+  // Lane 0: unit (lpr, lj) -> stage s, plus the pair's queries into the
+  // stage's query slot when it is the warp's first unit of the pair.
+  auto issue = [&](int s) {
     uint8_t* st = ws + s * STAGE;
+    const uint32_t qb = lfirst ? static_cast<uint32_t>(QB) : 0u;
     if (lj < lnsub) {
-      mbar_arrive_expect_tx(&bars[s], STAGE);
+      mbar_arrive_expect_tx(&bars[s], STAGE + qb);
       bulk_g2s(st, lbase + static_cast<size_t>(lj) * STAGE, STAGE, &bars[s]);
-      return;
-    }
-    const PairLens ll = pair_lens(p, lpr);
-    if (lj >= ll.nsub + ll.ntu) {
-      // sink rows [t0, t1): K rows, then V rows, one copy each
-      const int t0 = (lj - ll.nsub - ll.ntu) * TCH;
-      const int t1 = min(t0 + TCH, ll.Ts);
-      const uint32_t bytes = static_cast<uint32_t>(t1 - t0) * D * 2;
-      const size_t row = static_cast<size_t>(lpr) * p.g.NSK + t0;
-      mbar_arrive_expect_tx(&bars[s], 2 * bytes);
-      bulk_g2s(st, p.ksink + row * D, bytes, &bars[s]);
-      bulk_g2s(st + TCH * D * 2, p.vsink + row * D, bytes, &bars[s]);
     } else {
-      // tail rows [t0, t1): those below t_old from the tail buffer, the rest
-      // (tokens appended by this call) from knew / vnew
-      const int t0 = (lj - ll.nsub) * TCH;
-      const int t1 = min(t0 + TCH, ll.Tt);
-      const int tm = max(t0, min(t1, ll.t_old));
-      mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(t1 - t0) * D * 4);
-      if (tm > t0) {
-        const uint32_t bytes = static_cast<uint32_t>(tm - t0) * D * 2;
-        const size_t row = static_cast<size_t>(lpr) * p.g.TC + t0;
-        bulk_g2s(st, p.ktail[ll.buf] + row * D, bytes, &bars[s]);
-        bulk_g2s(st + TCH * D * 2, p.vtail[ll.buf] + row * D, bytes, &bars[s]);
-      }
-      if (t1 > tm) {
-        const int n_new = p.n_new;
-        const uint32_t bytes = static_cast<uint32_t>(t1 - tm) * D * 2;
-        const size_t row = static_cast<size_t>(lpr) * n_new + (tm - ll.t_old);
-        bulk_g2s(st + (tm - t0) * D * 2, p.knew + row * D, bytes, &bars[s]);
-        bulk_g2s(st + (TCH + tm - t0) * D * 2, p.vnew + row * D, bytes, &bars[s]);
+      const PairLens ll = pair_lens(p, lpr);
+      if (lj >= ll.nsub + ll.ntu) {
+        // sink rows [t0, t1): K rows, then V rows, one copy each
+        const int t0 = (lj - ll.nsub - ll.ntu) * TCH;
+        const int t1 = min(t0 + TCH, ll.Ts);
+        const uint32_t bytes = static_cast<uint32_t>(t1 - t0) * D * 2;
+        const size_t row = static_cast<size_t>(lpr) * p.g.NSK + t0;
+        mbar_arrive_expect_tx(&bars[s], 2 * bytes + qb);
+        bulk_g2s(st, p.ksink + row * D, bytes, &bars[s]);
+        bulk_g2s(st + TCH * D * 2, p.vsink + row * D, bytes, &bars[s]);
+      } else {
+        // tail rows [t0, t1): those below t_old from the tail buffer, the rest
+        // (tokens appended by this call) from knew / vnew
+        const int t0 = (lj - ll.nsub) * TCH;
+        const int t1 = min(t0 + TCH, ll.Tt);
+        const int tm = max(t0, min(t1, ll.t_old));
+        mbar_arrive_expect_tx(&bars[s], static_cast<uint32_t>(t1 - t0) * D * 4 + qb);
+        if (tm > t0) {
+          const uint32_t bytes = static_cast<uint32_t>(tm - t0) * D * 2;
+          const size_t row = static_cast<size_t>(lpr) * p.g.TC + t0;
+          bulk_g2s(st, p.ktail[ll.buf] + row * D, bytes, &bars[s]);
+          bulk_g2s(st + TCH * D * 2, p.vtail[ll.buf] + row * D, bytes, &bars[s]);
+        }
+        if (t1 > tm) {
+          const int n_new = p.n_new;
+          const uint32_t bytes = static_cast<uint32_t>(t1 - tm) * D * 2;
+          const size_t row = static_cast<size_t>(lpr) * n_new + (tm - ll.t_old);
+          bulk_g2s(st + (tm - t0) * D * 2, p.knew + row * D, bytes, &bars[s]);
+          bulk_g2s(st + (TCH + tm - t0) * D * 2, p.vnew + row * D, bytes, &bars[s]);
+        }
       }
     }
+    if (qb) bulk_g2s(ws + C::OFF_QS + s * QB, p.q + static_cast<size_t>(lpr) * R * D, QB, &bars[s]);
   };
   auto advance_load = [&]() {
     ++lu;
+    lfirst = false;
     if (++lj == lupp) {
       lj = 0;
       ++lpr;
+      lfirst = true;
       lbase += static_cast<size_t>(p.g.NB) * STAGE;
       if (lu < ub) {
         lnsub = pair_nsub(p, lpr);
@@ -318,41 +344,88 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     advance_load();
   }
 
+  // ---- per-lane constants of the B operands
+  // Keys: channel pairs P = lane + 32 i (k-step ks = P >> 3, register
+  // rg = (P >> 2) & 1, lane slot t); channels kch[i], kch[i] + 1.
+  const int rg = (lane >> 2) & 1;
+  int kch[KP], kbo[KP];
+#pragma unroll
+  for (int i = 0; i < KP; ++i) {
+    const int ks = (lane >> 3) + 4 * i;
+    kch[i] = 16 * ks + 8 * rg + 2 * t;
+    kbo[i] = ks * NT * BSTR * 2 + 2 * t + rg;
+  }
+  // code factor 2^(24 - p) of the lane's key slots (the same for every i)
+  const int klog = BK == 2 ? 24 - 2 * (2 * ((lane >> 3) & 1) + rg) : (BK == 4 ? 24 : 0);
+  const float kf = pow2i(klog), kfinv = pow2i(-klog);
+  // Values: items J = lane + 32 i: token pair J & 15 (tokens tau0, tau0 + 1),
+  // channel group (lane >> 4) + 2 i.
+  const int ksv = (lane >> 3) & 1;
+  const int tau0 = 16 * ksv + 8 * rg + 2 * t;
+  int vbo[VJ];
+#pragma unroll
+  for (int i = 0; i < VJ; ++i) vbo[i] = (((lane >> 4) + 2 * i) * 2 + ksv) * NT * BSTR * 2 + 2 * t + rg;
+  const float vfinv = pow2i(-vcode_log2<BV>(tau0));  // the lane's items' code factor, inverted
+  const float vfl = pow2i(vcode_log2<BV>(lane));      // code factor of token `lane`
+
+  // Operand buffers: columns that no query fills stay zero (lanes >= BL read
+  // zero columns without touching memory).
+  for (int i = lane; i < (C::OFF_PB - C::OFF_KB) / 4; i += 32) kb32[i] = 0u;
+  __syncwarp();
+
   // ---- state of the current pair
-  // Key channel pairs of this lane (B_K slots): pairs P = lane + 32 i.
-  constexpr int KP = D / 64;
-  constexpr int VJ = 2;  // value token pairs of this lane: J = lane + 32 i
-  float qreg[R][KP][2];  // q * scale * log2(e) of this lane's key channels
-  float m[R], l[R];      // online softmax, identical in all lanes
+  float qf[R][KP][2];    // q * scale * log2(e) * 2^klog of this lane's key channels
+  float m[R];            // running maximum (log2 units), identical in all lanes
+  float mlk[NT][4];      // m of the lane's query minus log2 f of its four score tokens
+  float lq[R];           // this lane's share of the softmax denominators
   float acc[MTV][NT][4];
-  float corr[R][VJ];     // value zero-point sums of this lane's items
+  float corr[R][VJ];     // value zero-point sums of this lane's items (in units of the code factor)
   float acct[R][CPL];    // fp16-tail contributions, channels lane*CPL + c
   int ev = -126;         // value operand exponent: B_V = p * s * f * 2^-ev
   int cur = -1;
 
-  auto enter_pair = [&](int pr) {
-    const __half* qp = p.q + static_cast<size_t>(pr) * R * D;
+  // value of f for this lane's query column (query 4*nt + t), 1 if none
+  auto lane_factor = [&](const float (&f)[R], int nt) -> float {
+    float v = 1.f;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (r == 4 * nt + t) v = f[r];
+    return v;
+  };
+
+  auto set_mlk = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float mq = lane_factor(m, nt);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) mlk[nt][k] = mq - static_cast<float>(vcode_log2<BV>(8 * k));
+    }
+  };
+
+  // New pair: its queries from the query slot of stage s.
+  auto enter_pair = [&](int s) {
+    const __half* qp = reinterpret_cast<const __half*>(ws + C::OFF_QS + s * QB);
     if constexpr (!ROPE) {
 #pragma unroll
-      for (int i = 0; i < KP; ++i) {
-        int ks, rg, slot_t, k0;
-        float f;
-        b_slot<BK>(lane + 32 * i, ks, rg, slot_t, k0, f);
+      for (int i = 0; i < KP; ++i)
 #pragma unroll
-        for (int r = 0; r < R; ++r)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) qreg[r][i][h] = __half2float(qp[r * D + k0 + h]) * p.qscale;
-      }
+        for (int r = 0; r < R; ++r) {
+          const float2 q2 = __half22float2(*reinterpret_cast<const __half2*>(qp + r * D + kch[i]));
+          const float sc = p.qscale * kf;
+          qf[r][i][0] = q2.x * sc;
+          qf[r][i][1] = q2.y * sc;
+        }
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       m[r] = -INFINITY;
-      l[r] = 0.f;
+      lq[r] = 0.f;
 #pragma unroll
       for (int k = 0; k < VJ; ++k) corr[r][k] = 0.f;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) acct[r][c] = 0.f;
     }
+    set_mlk();
 #pragma unroll
     for (int a = 0; a < MTV; ++a)
 #pragma unroll
@@ -365,24 +438,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     __syncwarp();
   };
 
-  // value of f for this lane's query column (query 4*nt + t), 1 if none
-  auto lane_factor = [&](const float (&f)[R], int nt) -> float {
-    float v = 1.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r)
-      if (r == 4 * nt + t) v = f[r];
-    return v;
-  };
-
-  // Multiplies the value accumulators and corrections by per-query factors.
-  auto rescale = [&](const float (&f)[R], float fv) {
-    bool any = fv != 1.f;
-#pragma unroll
-    for (int r = 0; r < R; ++r) any |= f[r] != 1.f;
-    if (!any) return;  // warp-uniform
+  // The running maximum rose: multiply everything accumulated by alpha.
+  auto rescale_all = [&](const float (&alpha)[R]) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float lf = lane_factor(f, nt) * fv;
+      const float lf = lane_factor(alpha, nt);
 #pragma unroll
       for (int a = 0; a < MTV; ++a)
 #pragma unroll
@@ -390,73 +450,75 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     }
 #pragma unroll
     for (int r = 0; r < R; ++r) {
+      lq[r] *= alpha[r];
 #pragma unroll
-      for (int k = 0; k < VJ; ++k) corr[r][k] *= f[r];
+      for (int k = 0; k < VJ; ++k) corr[r][k] *= alpha[r];
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) acct[r][c] *= f[r];
+      for (int c = 0; c < CPL; ++c) acct[r][c] *= alpha[r];
     }
   };
 
-  auto softmax_merge = [&](const float (&mx)[R], float (&alpha)[R], float (&mnew)[R]) {
+  // Eager update of the running maximum to the block maxima mx; rescales
+  // when it rises.
+  auto raise_max = [&](const float (&mx)[R]) {
+    float alpha[R];
+    bool any = false;
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      mnew[r] = fmaxf(m[r], mx[r]);
-      alpha[r] = fast_exp2(m[r] - mnew[r]);
-      m[r] = mnew[r];
+      const float mn = fmaxf(m[r], mx[r]);
+      any |= mn != m[r];
+      alpha[r] = fast_exp2(m[r] - mn);
+      m[r] = mn;
+    }
+    if (any) {  // warp-uniform
+      rescale_all(alpha);
+      set_mlk();
     }
   };
-
 
   // ---- pieces of a sub-block (keys stored after RoPE), so that the main
   // loop can put the key mma of one block and the value mma of the previous
   // block in one basic block (two independent instruction streams).
   auto k_prep = [&](const uint8_t* st, float (&kz)[R], float& ek2) {
-    const __half2* km = reinterpret_cast<const __half2*>(st + C::KC_S);
     // ---- key operand: B_K[c][2r+h] = hi/lo of q_r[c] s_c f_c 2^-ek
     float qh[R][KP][2];
+    float kzl[R];
     float amax = 0.f;
 #pragma unroll
-    for (int r = 0; r < R; ++r) kz[r] = 0.f;
+    for (int r = 0; r < R; ++r) kzl[r] = 0.f;
 #pragma unroll
     for (int i = 0; i < KP; ++i) {
-      int ks, rg, slot_t, k0;
-      float f;
-      b_slot<BK>(lane + 32 * i, ks, rg, slot_t, k0, f);
-      const float2 s0 = __half22float2(km[k0]);
-      const float2 s1 = __half22float2(km[k0 + 1]);
+      // {scale, zero} of channels kch[i] and kch[i] + 1
+      const uint2 mm = *reinterpret_cast<const uint2*>(st + C::KC_S + 4 * kch[i]);
+      const float2 s0 = __half22float2(*reinterpret_cast<const __half2*>(&mm.x));
+      const float2 s1 = __half22float2(*reinterpret_cast<const __half2*>(&mm.y));
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        qh[r][i][0] = qreg[r][i][0] * s0.x * f;
-        qh[r][i][1] = qreg[r][i][1] * s1.x * f;
-        kz[r] = fmaf(qreg[r][i][0], s0.y, fmaf(qreg[r][i][1], s1.y, kz[r]));
+        qh[r][i][0] = qf[r][i][0] * s0.x;
+        qh[r][i][1] = qf[r][i][1] * s1.x;
+        kzl[r] = fmaf(qf[r][i][0], s0.y, fmaf(qf[r][i][1], s1.y, kzl[r]));
         amax = fmaxf(amax, fmaxf(fabsf(qh[r][i][0]), fabsf(qh[r][i][1])));
       }
     }
-    amax = warp_max(amax);
+    amax = warp_max_nonneg(amax);
     // |B| < 2^14: one exponent for the sub-block
     const int ek = min(max(ilog2f(amax) - 13, -120), 120);
     const float sk = pow2i(-ek);
     ek2 = pow2i(ek);
 #pragma unroll
     for (int i = 0; i < KP; ++i) {
-      int ks, rg, slot_t, k0;
-      float f;
-      b_slot<BK>(lane + 32 * i, ks, rg, slot_t, k0, f);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const float v0 = qh[r][i][0] * sk, v1 = qh[r][i][1] * sk;
         const __half2 hi = __floats2half2_rn(v0, v1);
         const float2 hf = __half22float2(hi);
         const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-        const int n0 = 2 * r, n1 = 2 * r + 1;
-        kb32[bslot<BL>(ks * NT + (n0 >> 3), (n0 & 7) * 4 + slot_t) * 2 + rg] =
-            *reinterpret_cast<const uint32_t*>(&hi);
-        kb32[bslot<BL>(ks * NT + (n1 >> 3), (n1 & 7) * 4 + slot_t) * 2 + rg] =
-            *reinterpret_cast<const uint32_t*>(&lo);
+        kb32[kbo[i] + bcol<BSTR>(2 * r)] = *reinterpret_cast<const uint32_t*>(&hi);
+        kb32[kbo[i] + bcol<BSTR>(2 * r + 1)] = *reinterpret_cast<const uint32_t*>(&lo);
       }
     }
 #pragma unroll
-    for (int r = 0; r < R; ++r) kz[r] = warp_sum(kz[r]);
+    for (int r = 0; r < R; ++r) kz[r] = warp_sum(kzl[r] * kfinv);
     __syncwarp();
   };
 
@@ -478,7 +540,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           frag_a8<F8>(words8<KS>(kc, mt, ks, lane), a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
+            const uint2 b = lane < BL ? kbv[(ks * NT + nt) * BSTR + lane] : make_uint2(0u, 0u);
             mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -498,18 +560,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           else frag_a4(kw[mt * KS + ks], a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? kbv[bslot<BL>(ks * NT + nt, lane)] : make_uint2(0u, 0u);
+            const uint2 b = lane < BL ? kbv[(ks * NT + nt) * BSTR + lane] : make_uint2(0u, 0u);
             mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
     }
   };
 
-  auto softmax_scores = [&](float (&sc)[2][NT][4], const float (&kz)[R], float ek2,
-                            float (&alpha)[R]) {
-    // ---- online softmax (log2 units); lane holds query 4*nt + t
+  // Scores -> weights of the block (lazy maximum), stored in pb with each
+  // token's value code factor folded in; the lane's shares of l grow.
+  auto softmax_scores = [&](float (&sc)[2][NT][4], const float (&kz)[R], float ek2) {
+    // lane holds query 4*nt + t, tokens g, g + 8, g + 16, g + 24 (s4[nt][k])
     float s4[NT][4];
-    float mx[R], mxl[NT];
+    float dmax = -INFINITY;
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float z = lane_factor(kz, nt);
@@ -518,106 +581,99 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
         s4[nt][2 * mt] = fmaf(ek2, sc[mt][nt][0] + sc[mt][nt][1], z);
         s4[nt][2 * mt + 1] = fmaf(ek2 * C::RK, sc[mt][nt][2] + sc[mt][nt][3], z);
       }
-      float v = fmaxf(fmaxf(s4[nt][0], s4[nt][1]), fmaxf(s4[nt][2], s4[nt][3]));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
-      v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
-      mxl[nt] = v;
+      if (4 * nt + t < R) {
+        const float bm = fmaxf(fmaxf(s4[nt][0], s4[nt][1]), fmaxf(s4[nt][2], s4[nt][3]));
+        // vcode_log2(0) is the offset of token g; mlk[nt][0] = m - that
+        dmax = fmaxf(dmax, bm - (mlk[nt][0] + static_cast<float>(vcode_log2<BV>(0))));
+      }
     }
+    if (__any_sync(0xffffffffu, dmax > kLazyMax)) {
+      // rare: the pair's first block, or a score far above the maximum
+      float mxl[NT], mx[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) mx[r] = __shfl_sync(0xffffffffu, mxl[r >> 2], r & 3);
-    float mnew[R];
-    softmax_merge(mx, alpha, mnew);
-    float ps[NT];
+      for (int nt = 0; nt < NT; ++nt) {
+        float v = fmaxf(fmaxf(s4[nt][0], s4[nt][1]), fmaxf(s4[nt][2], s4[nt][3]));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+        mxl[nt] = v;
+      }
+#pragma unroll
+      for (int r = 0; r < R; ++r) mx[r] = __shfl_sync(0xffffffffu, mxl[r >> 2], r & 3);
+      raise_max(mx);
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float mm = lane_factor(mnew, nt);
-      float sum = 0.f;
+      float pf[4];
+      float lp = 0.f;
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
-        s4[nt][k] = fast_exp2(s4[nt][k] - mm);
-        sum += s4[nt][k];
+        pf[k] = fast_exp2(s4[nt][k] - mlk[nt][k]);
+        lp = fmaf(pf[k], pow2i(-vcode_log2<BV>(8 * k)), lp);
       }
-      sum += __shfl_xor_sync(0xffffffffu, sum, 4);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 8);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 16);
-      ps[nt] = sum;
       const int r = 4 * nt + t;
       if (r < R) {
-        pb[r * 32 + g] = s4[nt][0];
-        pb[r * 32 + g + 8] = s4[nt][1];
-        pb[r * 32 + g + 16] = s4[nt][2];
-        pb[r * 32 + g + 24] = s4[nt][3];
+        pb[r * 32 + g] = pf[0];
+        pb[r * 32 + g + 8] = pf[1];
+        pb[r * 32 + g + 16] = pf[2];
+        pb[r * 32 + g + 24] = pf[3];
       }
-    }
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-      l[r] = l[r] * alpha[r] + __shfl_sync(0xffffffffu, ps[r >> 2], r & 3);
+      for (int rr = 4 * nt; rr < 4 * nt + 4 && rr < R; ++rr)
+        if (t == rr - 4 * nt) lq[rr] += lp;
+    }
     __syncwarp();
   };
 
-  auto v_prep = [&](const uint8_t* st, const float (&alpha)[R]) {
+  // Value operand from the weights in pb (which carry the code factor):
+  // items (token pair, group) -> raw pf * s, exponent ev, hi/lo.
+  auto v_prep = [&](const uint8_t* st) {
     const __half2* vm = reinterpret_cast<const __half2*>(st + C::KC_S + C::KM_S + C::VC_S);
-    // ---- value operand: items (token pair, group) -> raw p * s * f
     float raw[R][VJ][2];
-    float zz[R][VJ];
     float vmax = 0.f;
+    float2 pp[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) pp[r] = *reinterpret_cast<const float2*>(pb + r * 32 + tau0);
 #pragma unroll
     for (int i = 0; i < VJ; ++i) {
-      const int J = lane + 32 * i;
-      const int gp = J >> 4;
-      int ks, rg, slot_t, tau0;
-      float f;
-      b_slot<BV>(J & 15, ks, rg, slot_t, tau0, f);
-      const int tau1 = tau0 + 1;
-      const bool valid = gp < NG;
-      const float2 m0 = valid ? __half22float2(vm[tau0 * NG + gp]) : make_float2(0.f, 0.f);
-      const float2 m1 = valid ? __half22float2(vm[tau1 * NG + gp]) : make_float2(0.f, 0.f);
+      const int gp = (lane >> 4) + 2 * i;
+      const float2 m0 = __half22float2(vm[tau0 * NG + gp]);
+      const float2 m1 = __half22float2(vm[(tau0 + 1) * NG + gp]);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const float p0 = pb[r * 32 + tau0], p1 = pb[r * 32 + tau1];
-        raw[r][i][0] = p0 * m0.x * f;
-        raw[r][i][1] = p1 * m1.x * f;
-        zz[r][i] = fmaf(p0, m0.y, p1 * m1.y);
+        raw[r][i][0] = pp[r].x * m0.x;
+        raw[r][i][1] = pp[r].y * m1.x;
+        corr[r][i] = fmaf(pp[r].x, m0.y, fmaf(pp[r].y, m1.y, corr[r][i]));
         vmax = fmaxf(vmax, fmaxf(raw[r][i][0], raw[r][i][1]));
       }
     }
     // B_V = raw * 2^-ev must stay below 2^14; a trip (the first sub-block of a
     // pair, or larger weights/scales later) raises ev and rescales exactly.
-    float fv = 1.f;
-    if (__any_sync(0xffffffffu, vmax * pow2i(min(-ev, 127)) >= 16384.f)) {
-      const float va = warp_max(vmax);
+    const float va = warp_max_nonneg(vmax);
+    if (va * pow2i(min(-ev, 127)) >= 16384.f) {
       const int evn = ilog2f(va) - 13;
       if (evn > ev) {
-        fv = pow2i(max(ev - evn, -126));
+        const float fv = pow2i(max(ev - evn, -126));
+#pragma unroll
+        for (int a = 0; a < MTV; ++a)
+#pragma unroll
+          for (int b = 0; b < NT; ++b)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[a][b][k] *= fv;
         ev = evn;
       }
     }
-    rescale(alpha, fv);
-    {
-      const float sv = pow2i(min(-ev, 127));
+    const float sv = pow2i(min(-ev, 127));
 #pragma unroll
-      for (int i = 0; i < VJ; ++i) {
-        const int J = lane + 32 * i;
-        const int gp = J >> 4;
-        int ks, rg, slot_t, tau0;
-        float f;
-        b_slot<BV>(J & 15, ks, rg, slot_t, tau0, f);
-        if (gp < NG) {
+    for (int i = 0; i < VJ; ++i) {
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const float v0 = raw[r][i][0] * sv, v1 = raw[r][i][1] * sv;
-            const __half2 hi = __floats2half2_rn(v0, v1);
-            const float2 hf = __half22float2(hi);
-            const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
-            corr[r][i] += zz[r][i];
-            const int n0 = 2 * r, n1 = 2 * r + 1;
-            vb32[bslot<BL>((gp * 2 + ks) * NT + (n0 >> 3), (n0 & 7) * 4 + slot_t) * 2 + rg] =
-                *reinterpret_cast<const uint32_t*>(&hi);
-            vb32[bslot<BL>((gp * 2 + ks) * NT + (n1 >> 3), (n1 & 7) * 4 + slot_t) * 2 + rg] =
-                *reinterpret_cast<const uint32_t*>(&lo);
-          }
-        }
+      for (int r = 0; r < R; ++r) {
+        const float v0 = raw[r][i][0] * sv, v1 = raw[r][i][1] * sv;
+        const __half2 hi = __floats2half2_rn(v0, v1);
+        const float2 hf = __half22float2(hi);
+        const __half2 lo = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+        vb32[vbo[i] + bcol<BSTR>(2 * r)] = *reinterpret_cast<const uint32_t*>(&hi);
+        vb32[vbo[i] + bcol<BSTR>(2 * r + 1)] = *reinterpret_cast<const uint32_t*>(&lo);
       }
     }
     __syncwarp();
@@ -636,7 +692,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           frag_a8<F8>(words8<2>(vc, mt, ks, lane), a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
+            const uint2 b =
+                lane < BL ? vbv[((gp * 2 + ks) * NT + nt) * BSTR + lane] : make_uint2(0u, 0u);
             mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -658,7 +715,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           else frag_a4(vw[2 * mt + ks], a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? vbv[bslot<BL>((gp * 2 + ks) * NT + nt, lane)] : make_uint2(0u, 0u);
+            const uint2 b =
+                lane < BL ? vbv[((gp * 2 + ks) * NT + nt) * BSTR + lane] : make_uint2(0u, 0u);
             mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -666,117 +724,109 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     }
   };
 
-  // One 32-token sub-block (sub-block ju of the pair) in stage `st`, all parts
-  // in order (keys stored before RoPE; and the pipelined loop's edges).
-  auto process_sub = [&](const uint8_t* st, int ju) {
+  // Keys stored before RoPE: one 32-token sub-block (sub-block ju of the
+  // pair) in stage `st`, scores on CUDA cores (lane = token), then the value
+  // operand and mma.
+  auto process_sub_rope = [&](const uint8_t* st, int ju) {
     const __half2* km = reinterpret_cast<const __half2*>(st + C::KC_S);
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
-    (void)km;
-    (void)kc;
-    float alpha[R];
-    if constexpr (ROPE) {
-      // ---- rotated keys (CUDA cores).  Sub-block positions p0 + j, p0 = 32*ju:
-      // q . R(p0 + j) k_j = q' . R(j) k_j with q' = R(-p0) q, and with
-      // k = s*c + z per channel, for the pair (i, i+D/2):
-      //   cos(j th_i) (a c_i + b c_i2 + e) + sin(j th_i) (f c_i - g c_i2 + h).
-      constexpr int H = D / 2;
-      float* cf = reinterpret_cast<float*>(ws + C::OFF_CF);
-      const int p0 = p.map.Ts[row_of(p.map, pr)] + ju * 32;
-      for (int i = lane; i < H; i += 32) {
-        const float2 cs = p.rope_tab[static_cast<size_t>(p0) * H + i];
-        const float2 m0 = __half22float2(km[i]), m1 = __half22float2(km[i + H]);
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float qi = os[r * D + i], qh = os[r * D + i + H];
-          const float ui = fmaf(qi, cs.x, qh * cs.y);   // q'_i
-          const float uh = fmaf(qh, cs.x, -qi * cs.y);  // q'_{i+H}
-          float* c = cf + (r * H + i) * 8;
-          *reinterpret_cast<float4*>(c) =
-              make_float4(ui * m0.x, uh * m1.x, fmaf(ui, m0.y, uh * m1.y), uh * m0.x);
-          *reinterpret_cast<float2*>(c + 4) = make_float2(ui * m1.x, fmaf(uh, m0.y, -ui * m1.y));
-        }
-      }
-      __syncwarp();
-      // lane = token: its key codes.  Token 16 mt + 8 hr + g2 sits in lanes
-      // 4 g2 + t of the words of m-tile mt (fragment order): 2- and 4-bit
-      // words are held in registers, 8-bit codes are read as bytes.
-      constexpr int NKR = BK == 8 ? 1 : 4 * (C::KWL / 2);
-      uint32_t kr[NKR];
-      const int mt = lane >> 4, g2 = lane & 7, hr = (lane >> 3) & 1;
-      if constexpr (BK != 8) {
-        constexpr int WPM = C::KWL / 2;  // words per m-tile
-#pragma unroll
-        for (int ww = 0; ww < WPM; ++ww)
-#pragma unroll
-          for (int tq = 0; tq < 4; ++tq) {
-            const int w = mt * WPM + ww;
-            kr[ww * 4 + tq] = kc[((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)];
-          }
-      }
-      // bit of the 2-bit field of (row half hr, pi = 2 (ks % 2) + kh)
-      int sh2[4];
-#pragma unroll
-      for (int pi = 0; pi < 4; ++pi) sh2[pi] = hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0);
-      auto kcode = [&](int d) -> uint32_t {
-        const int ks = d >> 4, kh = (d >> 3) & 1, tq = (d >> 1) & 3, e = d & 1;
-        if constexpr (BK == 2) {
-          return (kr[(ks >> 1) * 4 + tq] >> (16 * e + sh2[2 * (ks & 1) + kh])) & 3u;
-        } else if constexpr (BK == 4) {
-          return (kr[ks * 4 + tq] >> (16 * e + 8 * kh + 4 * hr)) & 15u;
-        } else {
-          const int w = 2 * (mt * KS + ks) + kh;
-          const uint8_t* kb = reinterpret_cast<const uint8_t*>(kc);
-          return kb[(((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)) * 4 + 2 * hr + e];
-        }
-      };
-      float sc[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) sc[r] = 0.f;
-#pragma unroll
-      for (int i = 0; i < H; ++i) {
-        const float c0 = code_value<F8>(kcode(i));
-        const float c1 = code_value<F8>(kcode(i + H));
-        const float2 cs = cs_tab[i * 32 + lane];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-          const float4 ab = *reinterpret_cast<const float4*>(cf + (r * H + i) * 8);
-          const float2 gh = *reinterpret_cast<const float2*>(cf + (r * H + i) * 8 + 4);
-          const float A = fmaf(ab.x, c0, fmaf(ab.y, c1, ab.z));
-          const float B = fmaf(ab.w, c0, fmaf(-gh.x, c1, gh.y));
-          sc[r] = fmaf(cs.x, A, fmaf(cs.y, B, sc[r]));
-        }
-      }
-      float mx[R], mnew[R];
-#pragma unroll
-      for (int r = 0; r < R; ++r) mx[r] = warp_max(sc[r]);
-      softmax_merge(mx, alpha, mnew);
+    // ---- rotated keys (CUDA cores).  Sub-block positions p0 + j, p0 = 32*ju:
+    // q . R(p0 + j) k_j = q' . R(j) k_j with q' = R(-p0) q, and with
+    // k = s*c + z per channel, for the pair (i, i+D/2):
+    //   cos(j th_i) (a c_i + b c_i2 + e) + sin(j th_i) (f c_i - g c_i2 + h).
+    constexpr int H = D / 2;
+    float* cf = reinterpret_cast<float*>(ws + C::OFF_CF);
+    const int p0 = p.map.Ts[row_of(p.map, cur)] + ju * 32;
+    for (int i = lane; i < H; i += 32) {
+      const float2 cs = p.rope_tab[static_cast<size_t>(p0) * H + i];
+      const float2 m0 = __half22float2(km[i]), m1 = __half22float2(km[i + H]);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const float pj = fast_exp2(sc[r] - mnew[r]);
-        l[r] = l[r] * alpha[r] + warp_sum(pj);
-        pb[r * 32 + lane] = pj;
+        const float qi = os[r * D + i], qh = os[r * D + i + H];
+        const float ui = fmaf(qi, cs.x, qh * cs.y);   // q'_i
+        const float uh = fmaf(qh, cs.x, -qi * cs.y);  // q'_{i+H}
+        float* c = cf + (r * H + i) * 8;
+        *reinterpret_cast<float4*>(c) =
+            make_float4(ui * m0.x, uh * m1.x, fmaf(ui, m0.y, uh * m1.y), uh * m0.x);
+        *reinterpret_cast<float2*>(c + 4) = make_float2(ui * m1.x, fmaf(uh, m0.y, -ui * m1.y));
       }
-      __syncwarp();
-    } else {
-      float kz[R], ek2, sc[2][NT][4];
-      k_prep(st, kz, ek2);
-      k_mma(st, sc);
-      softmax_scores(sc, kz, ek2, alpha);
     }
-    v_prep(st, alpha);
+    __syncwarp();
+    // lane = token: its key codes.  Token 16 mt + 8 hr + g2 sits in lanes
+    // 4 g2 + t of the words of m-tile mt (fragment order): 2- and 4-bit
+    // words are held in registers, 8-bit codes are read as bytes.
+    constexpr int NKR = BK == 8 ? 1 : 4 * (C::KWL / 2);
+    uint32_t kr[NKR];
+    const int mt = lane >> 4, g2 = lane & 7, hr = (lane >> 3) & 1;
+    if constexpr (BK != 8) {
+      constexpr int WPM = C::KWL / 2;  // words per m-tile
+#pragma unroll
+      for (int ww = 0; ww < WPM; ++ww)
+#pragma unroll
+        for (int tq = 0; tq < 4; ++tq) {
+          const int w = mt * WPM + ww;
+          kr[ww * 4 + tq] = kc[((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)];
+        }
+    }
+    // bit of the 2-bit field of (row half hr, pi = 2 (ks % 2) + kh)
+    int sh2[4];
+#pragma unroll
+    for (int pi = 0; pi < 4; ++pi) sh2[pi] = hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0);
+    auto kcode = [&](int d) -> uint32_t {
+      const int ks = d >> 4, kh = (d >> 3) & 1, tq = (d >> 1) & 3, e = d & 1;
+      if constexpr (BK == 2) {
+        return (kr[(ks >> 1) * 4 + tq] >> (16 * e + sh2[2 * (ks & 1) + kh])) & 3u;
+      } else if constexpr (BK == 4) {
+        return (kr[ks * 4 + tq] >> (16 * e + 8 * kh + 4 * hr)) & 15u;
+      } else {
+        const int w = 2 * (mt * KS + ks) + kh;
+        const uint8_t* kb = reinterpret_cast<const uint8_t*>(kc);
+        return kb[(((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)) * 4 + 2 * hr + e];
+      }
+    };
+    float sc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) sc[r] = 0.f;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      const float c0 = code_value<F8>(kcode(i));
+      const float c1 = code_value<F8>(kcode(i + H));
+      const float2 cs = cs_tab[i * 32 + lane];
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const float4 ab = *reinterpret_cast<const float4*>(cf + (r * H + i) * 8);
+        const float2 gh = *reinterpret_cast<const float2*>(cf + (r * H + i) * 8 + 4);
+        const float A = fmaf(ab.x, c0, fmaf(ab.y, c1, ab.z));
+        const float B = fmaf(ab.w, c0, fmaf(-gh.x, c1, gh.y));
+        sc[r] = fmaf(cs.x, A, fmaf(cs.y, B, sc[r]));
+      }
+    }
+    float mx[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) mx[r] = warp_max(sc[r]);
+    raise_max(mx);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float pj = fast_exp2(sc[r] - m[r]);
+      lq[r] += pj;
+      pb[r * 32 + lane] = pj * vfl;
+    }
+    __syncwarp();
+    v_prep(st);
     v_mma(st);
     __syncwarp();
   };
 
-
   // fp16 chunk of n <= TCH rows (tail or sink window; its K rows then its V
   // rows in the stage), row j at position pos0 + j.  Lane l holds channels
   // [l*CPL, (l+1)*CPL) (rotated keys: the frequency pairs (i, i + D/2),
-  // i = l + 32f); a token's score is the warp sum of the lanes' dot products.
-  // The scaled query sits in `os` (free until the pair's partial is written).
+  // i = l + 32f); a token's score is the warp sum of the lanes' dot products,
+  // JB tokens at a time so that their reductions overlap.  The scaled query
+  // sits in `os` (free until the pair's partial is written).
   auto process_chunk = [&](const uint8_t* st, int n, int pos0) {
     const __half* kt = reinterpret_cast<const __half*>(st);
     const __half* vt = kt + TCH * D;
+    constexpr int JB = R >= 8 ? 1 : 8 / R;
     if constexpr (ROPE) {
       // key of row j at absolute position pos0 + j, rotated after
       // dequantization: (k_i cos - k_{i+H} sin, k_{i+H} cos + k_i sin)
@@ -790,28 +840,34 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           qb[r][f] = os[r * D + lane + 32 * f + H];
         }
 #pragma unroll
-      for (int j = 0; j < TCH; ++j) {
-        if (j < n) {
-          const float2* cs = p.rope_tab + static_cast<size_t>(pos0 + j) * H + lane;
-          float v[R];
+      for (int j0 = 0; j0 < TCH; j0 += JB) {
+        float v[JB][R];
 #pragma unroll
-          for (int r = 0; r < R; ++r) v[r] = 0.f;
+        for (int jj = 0; jj < JB; ++jj) {
+          const int j = j0 + jj;
 #pragma unroll
-          for (int f = 0; f < FPL; ++f) {
-            const float2 c = cs[32 * f];
-            const float k0 = __half2float(kt[j * D + lane + 32 * f]);
-            const float k1 = __half2float(kt[j * D + lane + 32 * f + H]);
-            const float r0 = k0 * c.x - k1 * c.y;
-            const float r1 = k1 * c.x + k0 * c.y;
+          for (int r = 0; r < R; ++r) v[jj][r] = 0.f;
+          if (j < TCH) {
+            const float2* cs = p.rope_tab + static_cast<size_t>(pos0 + min(j, n - 1)) * H + lane;
 #pragma unroll
-            for (int r = 0; r < R; ++r) v[r] = fmaf(qa[r][f], r0, fmaf(qb[r][f], r1, v[r]));
-          }
+            for (int f = 0; f < FPL; ++f) {
+              const float2 c = cs[32 * f];
+              const float k0 = __half2float(kt[j * D + lane + 32 * f]);
+              const float k1 = __half2float(kt[j * D + lane + 32 * f + H]);
+              const float r0 = k0 * c.x - k1 * c.y;
+              const float r1 = k1 * c.x + k0 * c.y;
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            const float sj = warp_sum(v[r]);
-            if (lane == j) pb[r * 32 + j] = sj;
+              for (int r = 0; r < R; ++r) v[jj][r] = fmaf(qa[r][f], r0, fmaf(qb[r][f], r1, v[jj][r]));
+            }
           }
         }
+#pragma unroll
+        for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float sj = warp_sum(v[jj][r]);
+            if (lane == j0 + jj) pb[r * 32 + lane] = sj;
+          }
       }
     } else {
       float qc[R][CPL];
@@ -820,43 +876,53 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
 #pragma unroll
         for (int c = 0; c < CPL; ++c) qc[r][c] = os[r * D + lane * CPL + c];
 #pragma unroll
-      for (int j = 0; j < TCH; ++j) {
-        if (j < n) {
-          float kk[CPL];
-          const __half* kr = kt + j * D + lane * CPL;
-          if constexpr (CPL == 4) {
-            const uint2 x = *reinterpret_cast<const uint2*>(kr);
-            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
-            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
-            kk[0] = a.x; kk[1] = a.y; kk[2] = b.x; kk[3] = b.y;
-          } else {
+      for (int j0 = 0; j0 < TCH; j0 += JB) {
+        float v[JB][R];
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) kk[c] = __half2float(kr[c]);
-          }
+        for (int jj = 0; jj < JB; ++jj) {
+          const int j = j0 + jj;
 #pragma unroll
-          for (int r = 0; r < R; ++r) {
-            float v = 0.f;
+          for (int r = 0; r < R; ++r) v[jj][r] = 0.f;
+          if (j < TCH) {
+            float kk[CPL];
+            const __half* kr = kt + j * D + lane * CPL;
+            if constexpr (CPL == 4) {
+              const uint2 x = *reinterpret_cast<const uint2*>(kr);
+              const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&x.x));
+              const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&x.y));
+              kk[0] = a.x; kk[1] = a.y; kk[2] = b.x; kk[3] = b.y;
+            } else {
 #pragma unroll
-            for (int c = 0; c < CPL; ++c) v = fmaf(qc[r][c], kk[c], v);
-            const float sj = warp_sum(v);
-            if (lane == j) pb[r * 32 + j] = sj;
+              for (int c = 0; c < CPL; ++c) kk[c] = __half2float(kr[c]);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r)
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) v[jj][r] = fmaf(qc[r][c], kk[c], v[jj][r]);
           }
         }
+#pragma unroll
+        for (int jj = 0; jj < JB; ++jj)
+#pragma unroll
+          for (int r = 0; r < R; ++r) {
+            const float sj = warp_sum(v[jj][r]);
+            if (lane == j0 + jj) pb[r * 32 + lane] = sj;
+          }
       }
     }
     __syncwarp();
-    float sc[R], mx[R], alpha[R], mnew[R];
+    // rows >= n hold stale stage bytes: their scores are dropped here
+    float sc[R], mx[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
       sc[r] = lane < n ? pb[r * 32 + lane] : -INFINITY;
       mx[r] = warp_max(sc[r]);
     }
-    softmax_merge(mx, alpha, mnew);
-    rescale(alpha, 1.f);
+    raise_max(mx);
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const float pj = fast_exp2(sc[r] - mnew[r]);
-      l[r] = l[r] * alpha[r] + warp_sum(pj);
+      const float pj = fast_exp2(sc[r] - m[r]);
+      lq[r] += pj;
       pb[r * 32 + lane] = pj;
     }
     __syncwarp();
@@ -885,10 +951,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     __syncwarp();
   };
 
-
   // unit j >= nsub of a pair: a chunk of its tail, then of its sink window
   auto process_fp16_unit = [&](const uint8_t* st, int j) {
-    const PairLens cl = pair_lens(p, pr);
+    const PairLens cl = pair_lens(p, cur);
     const int k = j - cl.nsub;
     if (k < cl.ntu) {
       const int t0 = k * TCH;
@@ -899,17 +964,17 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     }
   };
 
-  auto write_partial = [&](int prr) {
-    const long long pr = prr;
-    const long long slot = gw + pr;
+  auto write_partial = [&](int pr) {
+    const long long slot = static_cast<long long>(gw) + pr;
     const float e2 = pow2i(ev);
     // zero-point sums: item i of lane L is in group 2 i + (L >> 4); this
     // lane's output channels lie in group go = (lane * CPL) >> 5
     const int go = (lane * CPL) >> 5;
-    float ct[R];
+    float ct[R], lsum[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      float s0 = corr[r][0], s1 = corr[r][1];
+      float s0 = corr[r][0] * vfinv;
+      float s1 = VJ > 1 ? corr[r][VJ - 1] * vfinv : 0.f;
 #pragma unroll
       for (int o = 1; o < 16; o <<= 1) {
         s0 += __shfl_xor_sync(0xffffffffu, s0, o);
@@ -918,6 +983,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       const float a = __shfl_sync(0xffffffffu, s0, 16 * (go & 1));
       const float b = __shfl_sync(0xffffffffu, s1, 16 * (go & 1));
       ct[r] = go < 2 ? a : b;
+      lsum[r] = warp_sum(lq[r]);
     }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -933,7 +999,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     __syncwarp();
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      if (lane == 0) p.part_ml[slot * R + r] = make_float2(m[r], l[r]);
+      if (lane == 0) p.part_ml[slot * R + r] = make_float2(m[r], lsum[r]);
       float* o = p.part_o + (slot * R + r) * D + lane * CPL;
 #pragma unroll
       for (int c = 0; c < CPL; ++c) o[c] = os[r * D + lane * CPL + c] + ct[r] + acct[r][c];
@@ -944,43 +1010,59 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       // (it never waits for the others: the ticket tells it they are done).
       __threadfence();
       __syncwarp();
-      const long long x0 = first_unit(p.map, pr);
-      const long long w0 = owner_warp(x0, p.U, p.n_warps);
-      const long long w1 =
-          owner_warp(x0 + units_of_row(p.map, row_of(p.map, pr)) - 1, p.U, p.n_warps);
+      int w0, w1;
+      pair_warps(p.map, pr, &w0, &w1);
       int last = 0;
-      if (lane == 0) last = atomicAdd(&p.tickets[pr], 1) == static_cast<int>(w1 - w0);
+      if (lane == 0) last = atomicAdd(&p.tickets[pr], 1) == w1 - w0;
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence();
-        // Lane i weighs partials i and i + 32; the partial rows are loaded
-        // eight at a time before they are summed (one L2 round trip each).
-        const int nseg = static_cast<int>(w1 - w0 + 1);  // <= 64 when fused
+        // Lane i weighs partials i and i + 32.  The first eight partial rows
+        // are loaded together with the weights (one L2 round trip).
+        const int nseg = w1 - w0 + 1;  // <= 64 when fused
+        constexpr int RB = 8;
 #pragma unroll 1
         for (int r = 0; r < R; ++r) {
+          float v[RB][CPL];
+#pragma unroll
+          for (int u = 0; u < RB; ++u) {
+            const long long w = w0 + min(u, nseg - 1);
+            const float* src = p.part_o + ((w + pr) * R + r) * D + lane * CPL;
+            if constexpr (CPL == 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else {
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) v[u][c] = __ldcg(src + c);
+            }
+          }
           float2 a = make_float2(-INFINITY, 0.f), b = a;
           if (lane < nseg) a = __ldcg(&p.part_ml[(w0 + lane + pr) * R + r]);
           if (lane + 32 < nseg) b = __ldcg(&p.part_ml[(w0 + lane + 32 + pr) * R + r]);
           const float ms = warp_max(fmaxf(a.x, b.x));
-          const float fa = fast_exp2(a.x - ms), fb = fast_exp2(b.x - ms);
+          const float mb = ms == -INFINITY ? 0.f : ms;  // every partial empty
+          const float fa = fast_exp2(a.x - mb), fb = fast_exp2(b.x - mb);
           const float L = warp_sum(fmaf(fa, a.y, fb * b.y));
           float o[CPL];
 #pragma unroll
           for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+#pragma unroll
+          for (int u = 0; u < RB; ++u) {
+            const float f = __shfl_sync(0xffffffffu, fa, u);
+            if (u < nseg) {
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) o[c] = fmaf(f, v[u][c], o[c]);
+            }
+          }
 #pragma unroll 1
-          for (int wb = 0; wb < nseg; wb += 8) {
-            float v[8][CPL];
+          for (int wb = RB; wb < nseg; wb += 8) {
+            float x8[8][CPL];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
               const long long w = w0 + min(wb + u, nseg - 1);
               const float* src = p.part_o + ((w + pr) * R + r) * D + lane * CPL;
-              if constexpr (CPL == 4) {
-                const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-                v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-              } else {
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) v[u][c] = __ldcg(src + c);
-              }
+              for (int c = 0; c < CPL; ++c) x8[u][c] = __ldcg(src + c);
             }
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
@@ -988,12 +1070,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
               const float f = __shfl_sync(0xffffffffu, w < 32 ? fa : fb, w & 31);
               if (w < nseg) {
 #pragma unroll
-                for (int c = 0; c < CPL; ++c) o[c] = fmaf(f, v[u][c], o[c]);
+                for (int c = 0; c < CPL; ++c) o[c] = fmaf(f, x8[u][c], o[c]);
               }
             }
           }
-          const float inv = 1.f / L;
-          float* dst = p.out + (pr * R + r) * D + lane * CPL;
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          float* dst = p.out + (static_cast<long long>(pr) * R + r) * D + lane * CPL;
 #pragma unroll
           for (int c = 0; c < CPL; ++c) dst[c] = o[c] * inv;
         }
@@ -1003,6 +1085,9 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   };
 
   // ---- main loop: unit n = u - ua sits in stage n % NS, phase (n / NS) & 1
+  int pr = static_cast<int>(pair_of_unit(p.map, ua));  // the compute cursor (unit j of pair pr)
+  int j = ua - static_cast<int>(first_unit(p.map, pr));
+  int cnsub = pair_nsub(p, pr), cupp = pair_upp(p, pr);
   int s = 0;
   uint32_t ph = 0u;
   // the next unit to load goes into `stage` (lane 0 issues the copy)
@@ -1015,7 +1100,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   // stage of the previous sub-block when its value mma is still pending
   int pend = -1;
   for (int u = ua; u < ub; ++u) {
-    if (pr != cur) {
+    const bool newp = pr != cur;
+    if (newp) {
       if constexpr (!ROPE) {
         if (pend >= 0) {
           v_mma(ws + pend * STAGE);
@@ -1025,10 +1111,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
         }
       }
       if (cur >= 0) write_partial(cur);
-      enter_pair(pr);
-      cur = pr;
     }
-    if (!mbar_wait_bounded(&bars[s], ph)) {
+    if (!mbar_wait_bounded(&bars[s], ph, p.wait_limit)) {
       // Give up: record the error, wait (bounded) for this warp's copies in
       // flight so no bulk copy lands after the CTA exits, and return.
       if (lane == 0) atomicExch(p.err, kDevErrWait);
@@ -1037,9 +1121,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       return;
     }
     const uint8_t* st = ws + s * STAGE;
+    if (newp) {
+      cur = pr;
+      enter_pair(s);
+    }
     if constexpr (ROPE) {
       if (j < cnsub)
-        process_sub(st, j);
+        process_sub_rope(st, j);
       else
         process_fp16_unit(st, j);
       refill(s);
@@ -1048,7 +1136,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
         // keys of this block, then its key mma beside the value mma of the
         // previous block (independent), then softmax and this block's value
         // operand; its value mma waits for the next iteration
-        float kz[R], ek2, alpha[R], sc[2][NT][4];
+        float kz[R], ek2, sc[2][NT][4];
         k_prep(st, kz, ek2);
         if (pend >= 0) {
           k_mma(st, sc);
@@ -1059,8 +1147,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           k_mma(st, sc);
           __syncwarp();
         }
-        softmax_scores(sc, kz, ek2, alpha);
-        v_prep(st, alpha);
+        softmax_scores(sc, kz, ek2);
+        v_prep(st);
         pend = s;
       } else {
         if (pend >= 0) {

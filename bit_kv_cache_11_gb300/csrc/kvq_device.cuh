@@ -62,10 +62,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on phase `parity` of `bar`.  Returns false when the limit ran
-// out (the caller records the error and stops).
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitLimit; ++i) {
+// Bounded wait on phase `parity` of `bar`: at most `limit` try_wait rounds.
+// Returns false when the limit ran out (the caller records the error and
+// stops).  A limit of 0 gives up at once (the fault-injection hook of the
+// host API uses it; the drain of copies in flight always uses kWaitLimit).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint32_t limit = kWaitLimit) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
   }
   return false;
@@ -245,15 +248,28 @@ __host__ __device__ inline int fp16_units(int rows, int tch) {
 // quantized sub-blocks, then its fp16 tail units, then its fp16 sink units.
 // Token positions (RoPE): sink row t at t, quantized token i at Ts + i, tail
 // row t at Ts + Tq + t.
+//
+// Warps split the work by cost: a pair costs its units plus `vcost` virtual
+// units placed after its last unit, which stand for the work of leaving a
+// pair (its partial, the merge, the next pair's query).  Warp w takes the
+// costs [start(w), start(w+1)), start(w) = floor(w * C / W), and processes the
+// real units among them; a warp whose costs are all virtual has no work.
 struct UnitMap {
   int ragged;              // 0: row 0's counts hold for every row
   int hkv;                 // pairs per row
+  int rows;                // row records in use (1 when uniform)
+  int vcost;               // virtual cost units after every pair
+  int U;                   // units of all pairs
+  int C;                   // cost of all pairs (U + P * vcost)
+  int W;                   // warps the costs are split over
+  int cq, cr;              // C / W and C % W
   int Ts[kMaxRows];        // sink tokens of each row
   int Tq[kMaxRows];        // quantized tokens
   int Tt[kMaxRows];        // tail tokens, including those a fused append adds
   int ntu[kMaxRows];       // fp16 tail units of a pair of the row
   int upp[kMaxRows];       // units of a pair of the row
   int uoff[kMaxRows + 1];  // ragged: first unit of each row
+  int coff[kMaxRows + 1];  // ragged: first cost of each row
 };
 
 // Fills ntu and upp of row b from its token counts (tch: fp16 rows per unit,
@@ -263,8 +279,38 @@ __host__ __device__ inline void set_row_units(UnitMap& m, int b, int tch) {
   m.upp[b] = m.Tq[b] / 32 + m.ntu[b] + fp16_units(m.Ts[b], tch);
 }
 
-// Units and pairs fit in 31 bits (kvq_create checks the unit count), so the
-// lookups below divide in 32 bits.
+// Host side, after set_row_units of every row record: the row offsets and
+// totals for P = hkv * (ragged ? rows : batch) pairs, and the split over at
+// most W warps (W is lowered to the unit count when that is smaller).
+// Returns the warp count used.
+inline int finish_map(UnitMap& m, int n_pairs, int vcost, long long W) {
+  m.vcost = vcost;
+  long long U = 0, C = 0;
+  if (m.ragged) {
+    m.uoff[0] = 0;
+    m.coff[0] = 0;
+    for (int b = 0; b < m.rows; ++b) {
+      m.uoff[b + 1] = m.uoff[b] + m.hkv * m.upp[b];
+      m.coff[b + 1] = m.coff[b] + m.hkv * (m.upp[b] + vcost);
+    }
+    U = m.uoff[m.rows];
+    C = m.coff[m.rows];
+  } else {
+    U = static_cast<long long>(n_pairs) * m.upp[0];
+    C = static_cast<long long>(n_pairs) * (m.upp[0] + vcost);
+  }
+  if (W > U) W = U;
+  if (W < 1) W = 1;
+  m.U = static_cast<int>(U);
+  m.C = static_cast<int>(C);
+  m.W = static_cast<int>(W);
+  m.cq = static_cast<int>(C / W);
+  m.cr = static_cast<int>(C % W);
+  return m.W;
+}
+
+// Units, costs and pairs fit in 31 bits (kvq_create checks the cost of a
+// full cache), so the lookups below divide in 32 bits.
 __host__ __device__ inline int row_of(const UnitMap& m, long long pr) {
   if (!m.ragged) return 0;
   return static_cast<int>(pr) / m.hkv;
@@ -288,9 +334,57 @@ __host__ __device__ inline long long pair_of_unit(const UnitMap& m, long long u)
   return b * m.hkv + (ui - m.uoff[b]) / m.upp[b];
 }
 
-// Split-K decode launch.  Warp w of the grid processes units [w*U/W,
-// (w+1)*U/W) of the unit map and writes one partial (m, l, o) per pair it
-// touches into slot (w + p).
+// The cost of the first unit of pair pr.
+__host__ __device__ inline int first_cost(const UnitMap& m, long long pr) {
+  const int p = static_cast<int>(pr);
+  if (!m.ragged) return p * (m.upp[0] + m.vcost);
+  const int b = p / m.hkv;
+  return m.coff[b] + (p - b * m.hkv) * (m.upp[b] + m.vcost);
+}
+
+// The first real unit at or after cost c (0 <= c <= C): the unit of cost c,
+// the next pair's first unit when c is one of a pair's virtual costs, U at C.
+__host__ __device__ inline int unit_at_cost(const UnitMap& m, int c) {
+  int b = 0, c0 = 0, u0 = 0;
+  if (m.ragged) {
+    while (b + 1 < m.rows && m.coff[b + 1] <= c) ++b;
+    c0 = m.coff[b];
+    u0 = m.uoff[b];
+  }
+  const int upp = m.upp[b];
+  const int k = (c - c0) / (upp + m.vcost);
+  const int j = c - c0 - k * (upp + m.vcost);
+  return u0 + k * upp + (j < upp ? j : upp);
+}
+
+// First cost of warp w: floor(w * C / W), in 32-bit arithmetic.
+__host__ __device__ inline int warp_cost(const UnitMap& m, int w) {
+  return w * m.cq + (w * m.cr) / m.W;
+}
+
+// The real units [*ua, *ub) of warp w.
+__host__ __device__ inline void warp_units(const UnitMap& m, int w, int* ua, int* ub) {
+  *ua = unit_at_cost(m, warp_cost(m, w));
+  *ub = unit_at_cost(m, warp_cost(m, w + 1));
+}
+
+// The warp that processes the unit of cost c: the largest w with
+// start(w) <= c  <=>  w * C < (c + 1) * W.
+__host__ __device__ __forceinline__ int owner_warp(const UnitMap& m, int c) {
+  return static_cast<int>(((static_cast<long long>(c) + 1) * m.W - 1) / m.C);
+}
+
+// The warps [*w0, *w1] whose ranges hold units of pair pr (each writes one
+// partial of the pair, into slot w + pr).
+__host__ __device__ inline void pair_warps(const UnitMap& m, long long pr, int* w0, int* w1) {
+  const int c0 = first_cost(m, pr);
+  *w0 = owner_warp(m, c0);
+  *w1 = owner_warp(m, c0 + units_of_row(m, row_of(m, pr)) - 1);
+}
+
+// Split-K decode launch.  Warp w of the grid processes its units of the unit
+// map (warp_units) and writes one partial (m, l, o) per pair it touches into
+// slot (w + p).
 struct DecodeParams {
   CacheGeom g;
   UnitMap map;
@@ -307,8 +401,7 @@ struct DecodeParams {
   const __half* vnew;
   int lg_G;             // log2(G)
   int lg_sub;           // log2(G / 32): 32-token sub-blocks per block
-  long long U;          // total units
-  int n_warps;          // W
+  int n_warps;          // warps of the launch (map.W)
   int rope;             // rotate keys after dequantization
   const float2* rope_tab;  // [max_ctx][D/2] {cos, sin}
   int rope_rows;        // rows of rope_tab (max_ctx)
@@ -317,6 +410,7 @@ struct DecodeParams {
   float* part_o;        // [W + P][R][D]
   float2* part_ml;      // [W + P][R] {m, l} (m in log2 units)
   int* err;
+  uint32_t wait_limit;  // try_wait rounds of a main-loop wait (kWaitLimit normally)
   // Fused merge: the last warp to finish a pair merges its partials into
   // `out` (ticket counters, one per pair, start and end at zero).
   int fused;
@@ -388,9 +482,7 @@ struct MergeParams {
   const float* part_o;
   const float2* part_ml;
   float* out;  // [P][R][D]
-  UnitMap map;
-  long long U;
-  int n_warps;
+  UnitMap map;  // the decode launch's units and split
   int R, D;
 };
 
@@ -405,18 +497,11 @@ struct Merge2Params {
   float2* lvl_ml;  // [P*R*C2]
   int* tickets;    // [P*R], zero between launches
   float* out;      // [P][R][D]
-  UnitMap map;
-  long long U;
-  int n_warps;
+  UnitMap map;     // the decode launch's units and split
   int R, D;
   int C2;          // level-1 chunks per (pair, query)
   int CS;          // partial slots per chunk
 };
 
-// Largest warp whose unit range starts at or before unit x (the warp that
-// owns unit x): start(w) = floor(w*U/W) <= x  <=>  w*U < (x+1)*W.
-__host__ __device__ __forceinline__ long long owner_warp(long long x, long long U, long long W) {
-  return ((x + 1) * W - 1) / U;
-}
 
 }  // namespace kvq

@@ -69,21 +69,22 @@ DecodeOps decode_ops(int D, int R, int bk, int bv) {
 __global__ void merge_kernel(const MergeParams mp) {
   const long long pr = blockIdx.x;
   const int d = threadIdx.x;
-  const long long x0 = first_unit(mp.map, pr);
-  const int upp = units_of_row(mp.map, row_of(mp.map, pr));
-  const long long w0 = owner_warp(x0, mp.U, mp.n_warps);
-  const long long w1 = owner_warp(x0 + upp - 1, mp.U, mp.n_warps);
+  int w0, w1;
+  pair_warps(mp.map, pr, &w0, &w1);
   for (int r = 0; r < mp.R; ++r) {
     float ms = -INFINITY;
     for (long long w = w0; w <= w1; ++w) ms = fmaxf(ms, mp.part_ml[(w + pr) * mp.R + r].x);
+    // Partials that saw no token (m = -inf, l = 0) weigh 0; if all of them
+    // are empty the output is 0.
+    const float mb = ms == -INFINITY ? 0.f : ms;
     float L = 0.f, o = 0.f;
     for (long long w = w0; w <= w1; ++w) {
       const float2 ml = mp.part_ml[(w + pr) * mp.R + r];
-      const float f = exp2f(ml.x - ms);
+      const float f = exp2f(ml.x - mb);
       L = fmaf(f, ml.y, L);
       o = fmaf(f, mp.part_o[((w + pr) * mp.R + r) * mp.D + d], o);
     }
-    mp.out[(pr * mp.R + r) * mp.D + d] = o / L;
+    mp.out[(pr * mp.R + r) * mp.D + d] = L > 0.f ? o / L : 0.f;
   }
 }
 
@@ -95,10 +96,8 @@ __global__ void merge2_kernel(const Merge2Params mp) {
   const int r = pq % mp.R;
   const long long pr = pq / mp.R;
   const int d = threadIdx.x;
-  const long long x0 = first_unit(mp.map, pr);
-  const int upp = units_of_row(mp.map, row_of(mp.map, pr));
-  const long long w0 = owner_warp(x0, mp.U, mp.n_warps);
-  const long long w1 = owner_warp(x0 + upp - 1, mp.U, mp.n_warps);
+  int w0, w1;
+  pair_warps(mp.map, pr, &w0, &w1);
   const long long s0 = w0 + static_cast<long long>(mp.CS) * c;
   const long long s1 = s0 + mp.CS - 1 < w1 ? s0 + mp.CS - 1 : w1;
   float ms = -INFINITY;

@@ -155,6 +155,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   UnitMap map;
   map.ragged = 0;
   map.hkv = cfg->n_kv_heads;
+  map.rows = 1;
   map.Ts[0] = 0;
   map.Tq[0] = T_q;
   map.Tt[0] = T_tail;
@@ -174,7 +175,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     long long W = static_cast<long long>(ds.sm_count) * ctas_per_sm * kDecodeWarps;
     if (W > kMaxWarps) W = kMaxWarps;
     if (W > max_slots - P) W = max_slots - P;
-    if (W > U) W = U;
+    W = finish_map(map, static_cast<int>(P), 0, W);
 
     DecodeParams p;
     p.g.blocks = static_cast<uint8_t*>(const_cast<void*>(blocks));
@@ -208,7 +209,6 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.vnew = nullptr;
     p.lg_G = G == 32 ? 5 : (G == 64 ? 6 : 7);
     p.lg_sub = p.lg_G - 5;
-    p.U = U;
     p.n_warps = static_cast<int>(W);
     p.rope = 0;
     p.rope_tab = nullptr;
@@ -218,6 +218,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.part_o = part_o;
     p.part_ml = part_ml;
     p.err = err;
+    p.wait_limit = kWaitLimit;
     p.fused = 0;
     p.tickets = nullptr;
     p.out = nullptr;
@@ -227,8 +228,6 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     mp.part_ml = part_ml;
     mp.out = static_cast<float*>(out);
     mp.map = map;
-    mp.U = U;
-    mp.n_warps = static_cast<int>(W);
     mp.R = R;
     mp.D = D;
     if (launch_merge(mp, static_cast<int>(P), st) != cudaSuccess) return KVQ_ERR_CUDA;

@@ -75,6 +75,9 @@ _sigs = {
     "kvq_get_buffers": (_S, [_P, ctypes.POINTER(kvq_buffers)]),
     "kvq_check_device_error": (_S, [_P, _P]),
     "kvq_launch_count": (ctypes.c_uint64, []),
+    "kvq_debug_fail_allocations": (_S, [_I, _I]),
+    "kvq_debug_set_device_error": (_S, [_P, _I]),
+    "kvq_debug_set_wait_limit": (_S, [_P, _I]),
     "kvq_status_string": (ctypes.c_char_p, [_S]),
 }
 for _name, (_res, _args) in _sigs.items():
@@ -234,6 +237,18 @@ def kvq_check_device_error(handle, stream=None) -> int:
 
 def kvq_launch_count() -> int:
     return int(_lib.kvq_launch_count())
+
+
+def kvq_debug_fail_allocations(after: int, n: int) -> None:
+    _check(_lib.kvq_debug_fail_allocations(after, n), "kvq_debug_fail_allocations")
+
+
+def kvq_debug_set_device_error(handle, value: int) -> None:
+    _check(_lib.kvq_debug_set_device_error(handle, value), "kvq_debug_set_device_error")
+
+
+def kvq_debug_set_wait_limit(handle, limit: int) -> None:
+    _check(_lib.kvq_debug_set_wait_limit(handle, limit), "kvq_debug_set_wait_limit")
 
 
 # ---- convenience -------------------------------------------------------------

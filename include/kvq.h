@@ -344,6 +344,28 @@ KVQ_API kvq_status kvq_check_device_error(kvq_cache* cache, void* stream);
 /* Number of kernels this library has launched in this process. */
 KVQ_API uint64_t kvq_launch_count(void);
 
+/* Fault-injection hooks for tests of the failure paths (host side; none of
+ * them makes a kernel fault or hang).
+ *
+ * kvq_debug_fail_allocations: after `after` more successful device
+ *   allocations, the next n the library makes fail as if the device were out
+ *   of memory (kvq_create then returns KVQ_ERR_OOM, frees what it had
+ *   allocated and leaves *out NULL).  n = 0 turns the injection off; a
+ *   negative argument -> KVQ_ERR_INVALID_ARG.  Process-wide.
+ * kvq_debug_set_device_error: synchronizes the device and writes `value`
+ *   into the cache's device error word, as a kernel whose bounded wait ran
+ *   out would (kvq_check_device_error then reports KVQ_ERR_DEVICE_CHECK and
+ *   clears the word).
+ * kvq_debug_set_wait_limit: the number of try_wait rounds each main-loop
+ *   wait of this cache's decode kernels makes before it gives up (records
+ *   the error word, waits with the normal limit for its own copies in flight,
+ *   and leaves the launch).  0 gives up at the first wait, so a decode
+ *   records the error without writing `out`; limit < 0 restores the normal
+ *   limit.  Applies to launches enqueued afterwards. */
+KVQ_API kvq_status kvq_debug_fail_allocations(int after, int n);
+KVQ_API kvq_status kvq_debug_set_device_error(kvq_cache* cache, int value);
+KVQ_API kvq_status kvq_debug_set_wait_limit(kvq_cache* cache, int limit);
+
 /* Static description of a status code. */
 KVQ_API const char* kvq_status_string(kvq_status s);
 

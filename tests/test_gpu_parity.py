@@ -282,8 +282,13 @@ def _sample_pairs(w, k, seed):
     return sorted(picks)
 
 
-@pytest.mark.parametrize("cfg,bits", [(2, 2), (3, 2), (3, 4)], ids=["llama7b-b8", "llama13b-2bit", "llama13b-4bit"])
+@pytest.mark.parametrize("cfg,bits", [(1, 2), (2, 2), (3, 2), (3, 4)],
+                         ids=["tiny-b1-h2-d64-t256", "llama7b-b8", "llama13b-2bit", "llama13b-4bit"])
 def test_full_size_decode_sampled(kvq, orc, cfg, bits):
+    """The workloads at their stated sizes (the tiny case exactly as stated:
+    batch 1, 2 heads, head_dim 64, 256 tokens, x50 outliers on channels
+    {3, 17}; every pair checked), in the launch configuration the bench
+    uses."""
     w = synth.WORKLOADS[cfg].with_(bits_k=bits, bits_v=bits)
     c = synth.make_case(w)
     pairs = _sample_pairs(w, 6, cfg)
@@ -291,6 +296,9 @@ def test_full_size_decode_sampled(kvq, orc, cfg, bits):
         cache.prefill(dev(c["K"]), dev(c["V"]))
         torch.cuda.synchronize()
         check_state(orc, cache, w, c["K"], c["V"], pairs)
+        if cfg == 1:
+            assert pairs == [0, 1]
+            check_dequant(orc, cache, w, c["K"], c["V"], pairs)
         check_decode(orc, cache, w, c["K"], c["V"], c["q"], pairs)
         cache.check()
 

@@ -1,0 +1,314 @@
+"""The CUDA quantizer on crafted groups, bit for bit against the CPU oracle.
+
+The seeded N(0, 1) workloads almost never produce the inputs where a fast
+quantizer can part from the definition ("Your KV cache doesn't have a bit
+problem, it has a geometry problem", section "What Quantization Error Is
+Actually Made Of": zero point = minimum, step = range / (2^B - 1), round to
+the nearest step; ties to even, the stored fp16 step codes the group).  The
+CUDA kernel multiplies by the reciprocal of the step and falls back to the
+IEEE divide near a rounding tie, and has separate paths for a zero step, a
+-0 minimum and the clamp at the top level; the FP8 format saturates at 448
+and has subnormal codes.  This file builds groups that land exactly on those
+cases and places them as key groups (G tokens of one channel) and value
+groups (G channels of one token) of a cache, on both axis assignments:
+
+  * every row of tests/golden/quantizer_cases.txt;
+  * exact ties at every level of 2-, 4- and 8-bit groups, at normal and
+    subnormal steps;
+  * quotients within 2^-11 (and 2^-13) of a tie, found by scanning fp16
+    values: input selection only, the expected codes come from the oracle;
+  * constant groups, steps that round to fp16 zero, subnormal steps, -0 and
+    +0 minima, top-level clamps at 8 bits;
+  * FP8: quotients at and beyond 448, E4M3 ties, subnormal quotients, zero
+    and subnormal scales.
+
+Bars: packed blocks and fp16 tails bit-exact and dequantized values
+bit-exact, through the C ABI, on every group.  Decode within 2e-3 max abs /
+1e-3 relative L2 of the oracle's fp64 attention on the groups whose values
+stay within |x| <= 16 (the absolute bar is set for N(0, 1)-scale values; the
+widest groups reach 65504).
+"""
+import os
+import zlib
+
+import numpy as np
+import pytest
+
+from bit_kv_cache_11_gb300 import synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATOL = 2e-3
+RTOL_L2 = 1e-3
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_kv_cache_11_gb300 import kvq as k
+    return k
+
+
+@pytest.fixture(scope="module")
+def orc():
+    import oracle
+    oracle.build()
+    return oracle
+
+
+def dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).cuda()
+
+
+F16 = np.float16
+F32 = np.float32
+
+
+def _fill(vals, G, rng):
+    """A group of G fp16 values holding `vals` (repeated to length G) in a
+    seeded order; repeats leave the minimum and maximum unchanged."""
+    v = np.asarray(vals, dtype=F16)
+    out = np.resize(v, G)
+    return out[rng.permutation(G)]
+
+
+def golden_groups(G, rng):
+    groups = []
+    with open(os.path.join(HERE, "golden", "quantizer_cases.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            bits, vals, _, _ = [x.strip() for x in line.split("|")]
+            groups.append((int(bits), _fill([float(x) for x in vals.split()], G, rng)))
+    return groups
+
+
+def tie_groups(bits, G, rng):
+    """Exact ties at every level: minimum m, step 2^e, x = m + (k + 1/2) 2^e
+    (all fp16 values, so every quotient is exactly k + 1/2)."""
+    L = (1 << bits) - 1
+    out = []
+    for e in (-22, -16, -13, -6, 0, 3):
+        if (2 * L - 1) * 2.0 ** (e - 1) > 60000:
+            continue
+        for m in (0.0, -L * 2.0 ** e):
+            ks = np.arange(L) if L <= G - 2 else rng.choice(L, G - 2, replace=False)
+            vals = [m, m + L * 2.0 ** e] + [m + (k + 0.5) * 2.0 ** e for k in ks]
+            assert all(float(F16(x)) == x for x in vals)
+            out.append(_fill(vals, G, rng))
+    return out
+
+
+def near_tie_groups(bits, G, rng, count=24):
+    """Groups [m, m + R, x...] whose quotients (x - m) / fp16(R / L),
+    evaluated in IEEE fp32, lie within 2^-10 of a half-integer without being
+    one, the closest such values first.  With fp16 inputs a nonzero distance
+    stays above about 2^-12 unless x - m itself rounds in fp32 (a minimum
+    with low-order bits far below the other values), so half of the groups
+    take a subnormal negative minimum.  Input selection only: the expected
+    codes come from the oracle."""
+    L = (1 << bits) - 1
+    allf = np.arange(0, 0x7c00, dtype=np.uint16).view(F16)  # every finite non-negative fp16
+    out = []
+    tries = 0
+    while len(out) < count and tries < 2000:
+        tries += 1
+        R = F16(rng.uniform(0.01, 3000.0))
+        m = F32(0.0) if len(out) % 2 == 0 else -F32(F16(rng.integers(1, 1024) * 2.0 ** -24))
+        hi = F32(m) + F32(R)
+        s = F32(F16((hi - m) / F32(L)))
+        if s == 0 or float(F16(hi)) != float(hi):
+            continue
+        xs = allf[allf <= F16(hi)].astype(F32)
+        q = (xs - m) / s
+        d = np.abs(q - (np.floor(q) + F32(0.5)))
+        ok = (d > 0) & (d < 2.0 ** -10)
+        if not ok.any():
+            continue
+        order = np.argsort(d[ok])
+        pick = xs[ok][order[: G - 2]]
+        out.append(_fill([float(m), float(hi)] + [float(x) for x in pick], G, rng))
+    assert len(out) >= count // 2, "too few near-tie groups found"
+    return out
+
+
+def special_groups(bits, G, rng):
+    L = (1 << bits) - 1
+    g = []
+    g.append(_fill([2.5], G, rng))                                   # range 0
+    g.append(_fill([-3.0], G, rng))
+    g.append(_fill([-0.0, 0.0], G, rng))                             # range -0 / +0
+    g.append(_fill([-0.0, 1.0, 0.25, 0.5], G, rng))                  # -0 minimum
+    g.append(_fill([0.0, -0.0, 7.0, 3.0], G, rng))
+    g.append(_fill([0.0, 2.0 ** -24], G, rng))                       # step rounds to 0 (8-bit), subnormal
+    g.append(_fill([1.0, 1.0 + 2.0 ** -10], G, rng))                 # range one ulp
+    g.append(_fill([0.0, L * 2.0 ** -20, 2.0 ** -20, 3 * 2.0 ** -21], G, rng))  # subnormal step
+    g.append(_fill([0.0, L * 2.0 ** -15 * 1.5], G, rng))            # step near the normal boundary
+    g.append(_fill([-65504.0, 65504.0, 0.0, 1.0], G, rng))           # widest range
+    g.append(_fill([60000.0, 65504.0, 61234.0], G, rng))
+    # the top level: ranges whose fp16 step rounds below range / L, so that
+    # range / step exceeds L and the clamp decides
+    for _ in range(6):
+        R = F16(rng.uniform(1.0, 1000.0))
+        g.append(_fill([0.0, float(R), float(R) * 0.999, float(R) * 0.5], G, rng))
+    return g
+
+
+def fp8_groups(G, rng):
+    g = []
+    # scale 1 (max 448): E4M3 ties between neighbours, subnormal ties, signs
+    ties = [1.0625, 1.1875, 3.0 * 2 ** -10, 2.0 ** -10, 5.0 * 2 ** -10, 17.0, 19.0, 400.0, 432.0]
+    g.append(_fill([448.0] + ties + [-x for x in ties], G, rng))
+    # scales below max / 448 after fp16 rounding: the largest quotient exceeds
+    # 448 and saturates
+    for _ in range(6):
+        a = F16(rng.uniform(100.0, 60000.0))
+        g.append(_fill([float(a), -float(a) * 0.75, float(a) * 0.999, 1.0, -2.5], G, rng))
+    g.append(_fill([2.0 ** -24, -(2.0 ** -24)], G, rng))            # scale rounds to 0
+    g.append(_fill([1e-3, -7e-4, 2e-5], G, rng))                    # subnormal scale
+    g.append(_fill([0.0, -0.0], G, rng))
+    g.append(_fill([5.0], G, rng))
+    g.append(_fill([448.0, 2.0 ** -9, 2.0 ** -8, 2.0 ** -7, 1.5 * 2.0 ** -9, 2.0 ** -6], G, rng))
+    return g
+
+
+def crafted_groups(bits, G, fp8, rng):
+    if fp8:
+        gs = fp8_groups(G, rng)
+        gs += [x for b, x in golden_groups(G, rng)]
+        gs += tie_groups(8, G, rng)
+        return gs
+    gs = [x for b, x in golden_groups(G, rng) if b == bits]
+    gs += [x for b, x in golden_groups(G, rng) if b != bits]   # same values, other level counts
+    gs += tie_groups(bits, G, rng)
+    gs += near_tie_groups(bits, G, rng)
+    gs += special_groups(bits, G, rng)
+    return gs
+
+
+def layout(groups, P, T, D, G, ak, av, rng):
+    """K, V fp16 [P][T][D] whose groups (per the axes) are the crafted groups,
+    cycled; the last T % G tokens form the fp16 tail and carry crafted values
+    too.  Key group (block, channel) on the channel axis = K[block rows, c];
+    on the token axis = K[t, g*G:(g+1)*G]."""
+    K = np.empty((P, T, D), dtype=F16)
+    V = np.empty((P, T, D), dtype=F16)
+    it = 0
+
+    def nxt():
+        nonlocal it
+        x = groups[it % len(groups)]
+        it += 1
+        return x
+
+    nb = (T + G - 1) // G
+    for X, axis in ((K, ak), (V, av)):
+        for p in range(P):
+            if axis == 0:
+                for b in range(nb):
+                    rows = min(G, T - b * G)
+                    for c in range(D):
+                        X[p, b * G:b * G + rows, c] = nxt()[:rows]
+            else:
+                for t in range(T):
+                    for g0 in range(0, D, G):
+                        X[p, t, g0:g0 + G] = nxt()
+    return K, V
+
+
+CASES = [
+    # name, D, R, bits, G, ak, av, fp8
+    ("pages-2bit", 128, 1, 2, 32, 0, 1, False),
+    ("pages-4bit-gqa4", 128, 4, 4, 32, 0, 1, False),
+    ("pages-8bit-d64", 64, 2, 8, 32, 0, 1, False),
+    ("flipped-2bit", 128, 1, 2, 32, 1, 0, False),
+    ("flipped-8bit-g128", 128, 4, 8, 128, 1, 0, False),
+    ("both-channel-4bit-g64", 64, 1, 4, 64, 0, 0, False),
+    ("pages-fp8", 128, 1, 8, 32, 0, 1, True),
+    ("flipped-fp8-g128", 128, 2, 8, 128, 1, 0, True),
+]
+
+
+def run_case(kvq, orc, case, moderate):
+    name, D, R, bits, G, ak, av, fp8 = case
+    rng = np.random.default_rng(zlib.crc32(name.encode()) % 100000 + moderate)
+    groups = crafted_groups(bits, G, fp8, rng)
+    if moderate:
+        groups = [g for g in groups if np.abs(g.astype(F32)).max() <= 16.0]
+    B, H = 1, 3
+    P = B * H
+    T = 5 * G + 7
+    K, V = layout(groups, P, T, D, G, ak, av, rng)
+    K = K.reshape(B, H, T, D)
+    V = V.reshape(B, H, T, D)
+    q = (0.25 * rng.standard_normal((B, H * R, D), dtype=np.float32)).astype(F16)
+    scale = 1.0 / np.sqrt(D)
+    with kvq.KVCache(batch=B, n_q_heads=H * R, n_kv_heads=H, head_dim=D, max_ctx=T + 32,
+                     bits_k=bits, bits_v=bits, group=G, axis_k=ak, axis_v=av, fp8=fp8) as cache:
+        cache.prefill(dev(K), dev(V))
+        torch.cuda.synchronize()
+        tq, tt = cache.state
+        assert (tq, tt) == (5 * G, 7)
+        blocks = cache.block_bytes_view().cpu().numpy()
+        kt, vt = cache.tail_views()
+        kh, vh = cache.dequantize()
+        out = cache.decode(dev(q), softmax_scale=scale)
+        torch.cuda.synchronize()
+        out = out.cpu().numpy().astype(np.float64)
+        got_all, want_all = [], []
+        for p in range(P):
+            b, h = divmod(p, H)
+            st = orc.build_pair(K[b, h], V[b, h], G, bits, bits, ak, av, fp8=fp8)
+            want = orc.pack_pair(st)
+            assert np.array_equal(blocks[p, :tq // G], want), f"pair {p}: packed blocks differ"
+            assert np.array_equal(kt[p, :tt].cpu().numpy().view(np.uint16), st["ktail"].view(np.uint16))
+            assert np.array_equal(vt[p, :tt].cpu().numpy().view(np.uint16), st["vtail"].view(np.uint16))
+            okh, ovh = orc.dequantize_pair(st)
+            assert np.array_equal(kh[b, h].cpu().numpy().view(np.uint32), okh.view(np.uint32))
+            assert np.array_equal(vh[b, h].cpu().numpy().view(np.uint32), ovh.view(np.uint32))
+            if moderate:
+                ref = orc.decode_pair(st, q[b, h * R:(h + 1) * R], scale)
+                got_all.append(out[b, h * R:(h + 1) * R])
+                want_all.append(ref)
+        cache.check()
+    if moderate:
+        got_all, want_all = np.stack(got_all), np.stack(want_all)
+        assert np.isfinite(got_all).all()
+        err = np.abs(got_all - want_all).max()
+        rel = np.linalg.norm(got_all - want_all) / max(np.linalg.norm(want_all), 1e-300)
+        assert err <= ATOL, f"max abs {err:.3e}"
+        assert rel <= RTOL_L2, f"rel L2 {rel:.3e}"
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_crafted_groups_bit_exact(kvq, orc, case):
+    run_case(kvq, orc, case, moderate=False)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_crafted_groups_decode(kvq, orc, case):
+    run_case(kvq, orc, case, moderate=True)
+
+
+def test_near_tie_groups_are_near_ties():
+    """Input selection check: every near-tie group holds quotients within
+    2^-10 of a half-integer, and the subnormal-minimum groups reach within
+    2^-12 (where a reciprocal product can round the other way)."""
+    rng = np.random.default_rng(3)
+    for bits in (2, 4, 8):
+        L = (1 << bits) - 1
+        best = 1.0
+        for g in near_tie_groups(bits, 32, rng):
+            g32 = g.astype(F32)
+            m, hi = g32.min(), g32.max()
+            s = F32(F16((hi - m) / F32(L)))
+            q = (g32 - m) / s
+            d = np.abs(q - (np.floor(q) + F32(0.5)))
+            d = d[d > 0]
+            assert d.min() < 2.0 ** -10
+            best = min(best, float(d.min()))
+        assert best < 2.0 ** -12, (bits, best)
