@@ -30,7 +30,14 @@ Sources (page titles and sections):
   * FP8 cache (``e4m3_value``, ``e4m3_encode``, ``quantize_group_fp8``):
     "Rotate, Then Round: The Geometry of KV-Cache Compression", "Key
     takeaway"; the E4M3 format as the OCP 8-bit floating-point specification
-    defines it.
+    defines it;
+  * dense-and-sparse outlier isolation (``select_outliers``,
+    ``quantize_tensor_sparse``, ``apply_outliers``): KVQuant's "isolating a
+    small fraction of outliers" in "Why KV Cache Geometry Matters More Than
+    Bit Precision", "KV Cache Size, GPU Memory Efficiency, and the Shift to
+    Geometry-Aware Quantization"; the selection rule and the format are a
+    reading (the pages give neither): the n largest-magnitude elements of
+    every block side, kept in fp16 with their positions.
 A batch of rows with different lengths is checked row by row: each row is
 its own sequence (``build_pair`` of that row's tokens).
 """
@@ -93,6 +100,16 @@ def _load():
     lib.kvo_block_offsets.argtypes = [I, I, I, I, P]
     lib.kvo_pack_pair.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P]
     lib.kvo_unpack_pair.argtypes = [I, I, I, I, I, I, I, P, P, P, P, P, P, P]
+    lib.kvo_quantize_group_masked.argtypes = [P, L, I, I, P, L, P, P, P]
+    lib.kvo_select_outliers.argtypes = [P, I, I, I, P]
+    lib.kvo_quantize_tensor_sparse.restype = I
+    lib.kvo_quantize_tensor_sparse.argtypes = [I, I, I, I, I, I, P, P, P, P, P]
+    lib.kvo_apply_outliers.argtypes = [I, I, I, I, P, P]
+    lib.kvo_block_bytes_n.restype = ctypes.c_size_t
+    lib.kvo_block_bytes_n.argtypes = [I, I, I, I, I]
+    lib.kvo_block_offsets_n.argtypes = [I, I, I, I, I, P]
+    lib.kvo_pack_pair_n.argtypes = [I, I, I, I, I, I, I, I] + [P] * 9
+    lib.kvo_unpack_pair_n.argtypes = [I, I, I, I, I, I, I, I] + [P] * 9
     lib.kvo_rope.argtypes = [P, I, L, D]
     lib.kvo_attention_pair.argtypes = [I, I, I, I, P, P, P, P, P, D, I, D, P, P]
     _lib = lib
@@ -185,6 +202,49 @@ def quantize_tensor(X_f16: np.ndarray, G: int, bits: int, axis: int, fp8: bool =
     return Tq, codes, scale, zero
 
 
+def select_outliers(tile_f16: np.ndarray, n: int) -> np.ndarray:
+    """Positions j*D + d (ascending) of the n elements of largest magnitude in
+    a G x D fp16 tile (ties: lower position)."""
+    G, D = tile_f16.shape
+    assert 0 <= n <= G * D
+    x = bits_of(tile_f16)
+    pos = np.zeros(max(n, 1), np.int32)
+    _load().kvo_select_outliers(_p(x), G, D, n, _p(pos))
+    return pos[:n]
+
+
+def quantize_group_masked(x_f16: np.ndarray, bits: int, skip: np.ndarray):
+    """One group over its elements with skip == 0: (scale bits, zero bits,
+    codes); skipped elements get code 0."""
+    x = bits_of(x_f16).reshape(-1)
+    m = _c(skip, np.uint8).reshape(-1)
+    s = np.zeros(1, np.uint16)
+    z = np.zeros(1, np.uint16)
+    codes = np.zeros(x.size, np.uint8)
+    _load().kvo_quantize_group_masked(_p(x), 1, x.size, bits, _p(m), 1, _p(s), _p(z), _p(codes))
+    return int(s[0]), int(z[0]), codes
+
+
+def quantize_tensor_sparse(X_f16: np.ndarray, G: int, bits: int, axis: int, n_out: int):
+    """quantize_tensor with n_out outliers isolated per G-token block.
+    Returns (Tq, codes, scale bits, zero bits, outliers uint32 [Tq/G][n_out]):
+    each outlier entry holds the kept fp16 value in bits 0-15 and its
+    position j*D + d in the block in bits 16-31."""
+    T, D = X_f16.shape
+    assert 0 <= n_out <= G * D
+    Tq = (T // G) * G
+    x = bits_of(X_f16)
+    codes = np.zeros((Tq, D), np.uint8)
+    mshape = (Tq // G, D) if axis == 0 else (Tq, D // G)
+    scale = np.zeros(mshape, np.uint16)
+    zero = np.zeros(mshape, np.uint16)
+    outl = np.zeros((Tq // G, max(n_out, 1)), np.uint32)
+    got = _load().kvo_quantize_tensor_sparse(T, D, G, bits, axis, n_out, _p(x), _p(codes),
+                                             _p(scale), _p(zero), _p(outl))
+    assert got == Tq
+    return Tq, codes, scale, zero, outl[:, :n_out]
+
+
 def dequantize_tensor(codes, scale, zero, G: int, axis: int, fp8: bool = False) -> np.ndarray:
     Tq, D = codes.shape
     out = np.zeros((Tq, D), np.float32)
@@ -200,13 +260,19 @@ def code_order(D: int, G: int, bits: int, ak: int, av: int) -> int:
     return int(_load().kvo_code_order(D, G, bits, ak, av))
 
 
-def block_bytes(D: int, G: int, bk: int, bv: int) -> int:
-    return int(_load().kvo_block_bytes(D, G, bk, bv))
+def block_bytes(D: int, G: int, bk: int, bv: int, n_out: int = 0) -> int:
+    return int(_load().kvo_block_bytes_n(D, G, bk, bv, n_out))
 
 
-def block_offsets(D: int, G: int, bk: int, bv: int):
-    off = np.zeros(4, np.uint64)
-    _load().kvo_block_offsets(D, G, bk, bv, _p(off))
+def block_offsets(D: int, G: int, bk: int, bv: int, n_out: int | None = None):
+    """[K codes, K meta, V codes, V meta] offsets; with n_out given, the six
+    offsets [K codes, K meta, K outliers, V codes, V meta, V outliers]."""
+    if n_out is None:
+        off = np.zeros(4, np.uint64)
+        _load().kvo_block_offsets(D, G, bk, bv, _p(off))
+    else:
+        off = np.zeros(6, np.uint64)
+        _load().kvo_block_offsets_n(D, G, bk, bv, n_out, _p(off))
     return [int(v) for v in off]
 
 
@@ -214,27 +280,38 @@ def pack_pair(st: dict) -> np.ndarray:
     """Packs one pair's quantized state into its blocks: uint8 [Tq/G][block_bytes]."""
     Tq, D = st["kcodes"].shape
     G, bk, bv, ak, av = st["G"], st["bk"], st["bv"], st["ak"], st["av"]
-    bb = block_bytes(D, G, bk, bv)
+    n = st.get("n_out", 0)
+    bb = block_bytes(D, G, bk, bv, n)
     out = np.zeros((Tq // G, bb), np.uint8)
     arrs = [_c(st["kcodes"], np.uint8), _c(st["kscale"], np.uint16), _c(st["kzero"], np.uint16),
             _c(st["vcodes"], np.uint8), _c(st["vscale"], np.uint16), _c(st["vzero"], np.uint16)]
-    _load().kvo_pack_pair(Tq, D, G, bk, bv, ak, av, *[_p(a) for a in arrs], _p(out))
+    empty = np.zeros((max(Tq // G, 1), 1), np.uint32)
+    kout = _c(st["kout"], np.uint32) if n else empty
+    vout = _c(st["vout"], np.uint32) if n else empty
+    _load().kvo_pack_pair_n(Tq, D, G, bk, bv, ak, av, n, *[_p(a) for a in arrs], _p(kout),
+                            _p(vout), _p(out))
     return out
 
 
-def unpack_pair(blocks: np.ndarray, D: int, G: int, bk: int, bv: int, ak: int, av: int) -> dict:
+def unpack_pair(blocks: np.ndarray, D: int, G: int, bk: int, bv: int, ak: int, av: int,
+                n_out: int = 0) -> dict:
     nb = blocks.shape[0]
     Tq = nb * G
     km = (nb, D) if ak == 0 else (Tq, D // G)
     vm = (nb, D) if av == 0 else (Tq, D // G)
-    st = dict(G=G, bk=bk, bv=bv, ak=ak, av=av,
+    st = dict(G=G, bk=bk, bv=bv, ak=ak, av=av, n_out=n_out,
               kcodes=np.zeros((Tq, D), np.uint8), kscale=np.zeros(km, np.uint16),
               kzero=np.zeros(km, np.uint16), vcodes=np.zeros((Tq, D), np.uint8),
-              vscale=np.zeros(vm, np.uint16), vzero=np.zeros(vm, np.uint16))
+              vscale=np.zeros(vm, np.uint16), vzero=np.zeros(vm, np.uint16),
+              kout=np.zeros((nb, max(n_out, 1)), np.uint32),
+              vout=np.zeros((nb, max(n_out, 1)), np.uint32))
     blk = _c(blocks, np.uint8)
-    _load().kvo_unpack_pair(Tq, D, G, bk, bv, ak, av, _p(blk),
-                            _p(st["kcodes"]), _p(st["kscale"]), _p(st["kzero"]),
-                            _p(st["vcodes"]), _p(st["vscale"]), _p(st["vzero"]))
+    _load().kvo_unpack_pair_n(Tq, D, G, bk, bv, ak, av, n_out, _p(blk),
+                              _p(st["kcodes"]), _p(st["kscale"]), _p(st["kzero"]),
+                              _p(st["vcodes"]), _p(st["vscale"]), _p(st["vzero"]),
+                              _p(st["kout"]), _p(st["vout"]))
+    st["kout"] = st["kout"][:, :n_out]
+    st["vout"] = st["vout"][:, :n_out]
     return st
 
 
@@ -260,20 +337,29 @@ def window_lengths(T: int, G: int, n_sink: int = 0, residual: int = 0):
 
 def build_pair(K_f16: np.ndarray, V_f16: np.ndarray, G: int, bk: int, bv: int,
                ak: int = 0, av: int = 1, n_sink: int = 0, residual: int = 0,
-               fp8: bool = False) -> dict:
+               fp8: bool = False, n_outliers: int = 0) -> dict:
     """The cache state of one pair after its T tokens arrived (any mix of
     prefill and appends): the sink tokens in fp16, then the quantized groups,
     then the fp16 tail (window_lengths gives the three counts).  The state
     does not depend on how the tokens were split into calls, because every
     flush leaves the same G-aligned boundary.  fp8: both sides stored as E4M3
-    with absmax scales (bk = bv = 8)."""
+    with absmax scales (bk = bv = 8).  n_outliers: the elements of largest
+    magnitude kept apart in every block of each side (dense-and-sparse
+    isolation, quantize_tensor_sparse)."""
     T, D = K_f16.shape
     assert not fp8 or bk == bv == 8
+    assert not (fp8 and n_outliers)
     Ts, Tq, Tt = window_lengths(T, G, n_sink, residual)
-    Tq_, kc, ks, kz = quantize_tensor(K_f16[Ts:Ts + Tq], G, bk, ak, fp8)
-    _, vc, vs, vz = quantize_tensor(V_f16[Ts:Ts + Tq], G, bv, av, fp8)
+    kout = vout = np.zeros((Tq // G, 0), np.uint32)
+    if n_outliers:
+        Tq_, kc, ks, kz, kout = quantize_tensor_sparse(K_f16[Ts:Ts + Tq], G, bk, ak, n_outliers)
+        _, vc, vs, vz, vout = quantize_tensor_sparse(V_f16[Ts:Ts + Tq], G, bv, av, n_outliers)
+    else:
+        Tq_, kc, ks, kz = quantize_tensor(K_f16[Ts:Ts + Tq], G, bk, ak, fp8)
+        _, vc, vs, vz = quantize_tensor(V_f16[Ts:Ts + Tq], G, bv, av, fp8)
     assert Tq_ == Tq
     return dict(G=G, bk=bk, bv=bv, ak=ak, av=av, fp8=fp8, Ts=Ts, Tq=Tq, Tt=Tt,
+                n_out=n_outliers, kout=kout, vout=vout,
                 kcodes=kc, kscale=ks, kzero=kz, vcodes=vc, vscale=vs, vzero=vz,
                 ksink=np.ascontiguousarray(K_f16[:Ts], np.float16),
                 vsink=np.ascontiguousarray(V_f16[:Ts], np.float16),
@@ -281,10 +367,22 @@ def build_pair(K_f16: np.ndarray, V_f16: np.ndarray, G: int, bk: int, bv: int,
                 vtail=np.ascontiguousarray(V_f16[Ts + Tq:], np.float16))
 
 
+def apply_outliers(xhat: np.ndarray, outliers: np.ndarray, G: int) -> np.ndarray:
+    """Dequantized values with every block's kept outliers put back."""
+    Tq, D = xhat.shape
+    out = np.array(xhat, np.float32, copy=True)
+    o = _c(outliers, np.uint32)
+    _load().kvo_apply_outliers(Tq, D, G, o.shape[1] if o.ndim == 2 else 0, _p(o), _p(out))
+    return out
+
+
 def dequantize_pair(st: dict):
     f8 = st.get("fp8", False)
     kh = dequantize_tensor(st["kcodes"], st["kscale"], st["kzero"], st["G"], st["ak"], f8)
     vh = dequantize_tensor(st["vcodes"], st["vscale"], st["vzero"], st["G"], st["av"], f8)
+    if st.get("n_out", 0):
+        kh = apply_outliers(kh, st["kout"], st["G"])
+        vh = apply_outliers(vh, st["vout"], st["G"])
     return kh, vh
 
 

@@ -22,6 +22,10 @@
  *                      weighted sum of value vectors), evaluated in fp64.
  *   FP8 (E4M3) ....... "Rotate, Then Round: The Geometry of KV-Cache
  *                      Compression", "Key takeaway"; the OCP E4M3 format.
+ *   outlier isolation  "Why KV Cache Geometry Matters More Than Bit
+ *                      Precision", "KV Cache Size, GPU Memory Efficiency, and
+ *                      the Shift to Geometry-Aware Quantization" (KVQuant);
+ *                      GEOMETRY "Rotary Embeddings Complicate the Keys".
  *
  * Every function works on ONE (batch, kv-head) pair; loops are plain and in
  * the order of the definition.  Parity pins for every function live in the
@@ -236,6 +240,142 @@ void kvo_dequantize_tensor(int Tq, int D, int G, int axis, int fp8,
   }
 }
 
+/* ---- dense-and-sparse outlier isolation -----------------------------------
+ * KVQuant's third ingredient besides per-channel keys and pre-RoPE keys
+ * ("Why KV Cache Geometry Matters More Than Bit Precision", section "KV
+ * Cache Size, GPU Memory Efficiency, and the Shift to Geometry-Aware
+ * Quantization"; "Your KV cache doesn't have a bit problem, it has a geometry
+ * problem", section "Rotary Embeddings Complicate the Keys"): a small
+ * fraction of extreme values is kept apart, so that it does not widen the
+ * step of its group ("Inside the Attention Equation": one very large
+ * activation makes every element of its group coarser).  The pages give no
+ * selection rule and no storage format.  Reading: in every G-token block of
+ * a side, the n elements of largest magnitude (ties: lower token, then lower
+ * channel) are kept exactly, in fp16, with their positions; every group
+ * takes its minimum and maximum over its remaining elements (scale 0 and
+ * zero +0 when none remain); the kept positions get code 0 and dequantize to
+ * their kept value. */
+
+/* kvo_quantize_group over the elements i with skip[i * skip_stride] == 0;
+ * skipped elements get code 0. */
+void kvo_quantize_group_masked(const uint16_t* x, long stride, int n, int bits,
+                               const uint8_t* skip, long skip_stride,
+                               uint16_t* scale_out, uint16_t* zero_out,
+                               uint8_t* codes) {
+  int any = 0;
+  float mn = 0.0f, mx = 0.0f;
+  for (int i = 0; i < n; ++i) {
+    if (skip[(long)i * skip_stride]) continue;
+    float v = kvo_h2f(x[(long)i * stride]);
+    if (!any || v < mn) mn = v;
+    if (!any || v > mx) mx = v;
+    any = 1;
+  }
+  if (!any) {
+    *scale_out = 0;
+    *zero_out = 0;
+    for (int i = 0; i < n; ++i) codes[i] = 0;
+    return;
+  }
+  int levels = (1 << bits) - 1;
+  float step = (mx - mn) / (float)levels;
+  uint16_t s_h = kvo_f2h(step);
+  float s = kvo_h2f(s_h);
+  *scale_out = s_h;
+  *zero_out = kvo_f2h(mn + 0.0f);
+  for (int i = 0; i < n; ++i) {
+    int c = 0;
+    if (!skip[(long)i * skip_stride] && s != 0.0f) {
+      float r = rintf((kvo_h2f(x[(long)i * stride]) - mn) / s);
+      if (!(r >= 0.0f)) r = 0.0f;
+      if (r > (float)levels) r = (float)levels;
+      c = (int)r;
+    }
+    codes[i] = (uint8_t)c;
+  }
+}
+
+/* Ordering of the selection: larger magnitude first, then lower position. */
+static const uint16_t* g_sel_x;
+static int by_magnitude(const void* a, const void* b) {
+  int32_t i = *(const int32_t*)a, j = *(const int32_t*)b;
+  float xi = fabsf(kvo_h2f(g_sel_x[i])), xj = fabsf(kvo_h2f(g_sel_x[j]));
+  if (xi != xj) return xi > xj ? -1 : 1;
+  return i < j ? -1 : (i > j ? 1 : 0);
+}
+static int ascending(const void* a, const void* b) {
+  int32_t i = *(const int32_t*)a, j = *(const int32_t*)b;
+  return i < j ? -1 : (i > j ? 1 : 0);
+}
+
+/* Positions (j*D + d) of the n elements of largest |x| in the G x D fp16
+ * tile X (row stride D), in ascending order.  n <= G * D. */
+void kvo_select_outliers(const uint16_t* X, int G, int D, int n, int32_t* pos) {
+  int32_t* idx = (int32_t*)malloc(sizeof(int32_t) * (size_t)G * D);
+  for (int i = 0; i < G * D; ++i) idx[i] = i;
+  g_sel_x = X;
+  qsort(idx, (size_t)G * D, sizeof(int32_t), by_magnitude);
+  for (int k = 0; k < n; ++k) pos[k] = idx[k];
+  qsort(pos, (size_t)n, sizeof(int32_t), ascending);
+  free(idx);
+}
+
+/* kvo_quantize_tensor with n_out outliers isolated in every G-token block
+ * (integer codes only).  outliers: [Tq/G][n_out] entries, each a uint32 with
+ * the kept fp16 value in bits 0-15 and the position j*D + d inside the
+ * block in bits 16-31, ascending by position.  Returns Tq. */
+int kvo_quantize_tensor_sparse(int T, int D, int G, int bits, int axis, int n_out,
+                               const uint16_t* X, uint8_t* codes, uint16_t* scale,
+                               uint16_t* zero, uint32_t* outliers) {
+  int Tq = (T / G) * G;
+  uint8_t* skip = (uint8_t*)malloc((size_t)G * D);
+  int32_t* pos = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n_out > 0 ? n_out : 1));
+  uint8_t* tmp = (uint8_t*)malloc((size_t)G);
+  int ng = D / G;
+  for (int i = 0; i < Tq / G; ++i) {
+    const uint16_t* tile = X + (size_t)i * G * D;
+    memset(skip, 0, (size_t)G * D);
+    kvo_select_outliers(tile, G, D, n_out, pos);
+    for (int k = 0; k < n_out; ++k) {
+      skip[pos[k]] = 1;
+      outliers[(size_t)i * n_out + k] = (uint32_t)tile[pos[k]] | ((uint32_t)pos[k] << 16);
+    }
+    if (axis == 0) {
+      for (int d = 0; d < D; ++d) {
+        kvo_quantize_group_masked(tile + d, D, G, bits, skip + d, D, &scale[(size_t)i * D + d],
+                                  &zero[(size_t)i * D + d], tmp);
+        for (int j = 0; j < G; ++j) codes[(size_t)(i * G + j) * D + d] = tmp[j];
+      }
+    } else {
+      for (int j = 0; j < G; ++j) {
+        for (int g = 0; g < ng; ++g) {
+          size_t t = (size_t)i * G + j;
+          kvo_quantize_group_masked(tile + (size_t)j * D + (size_t)g * G, 1, G, bits,
+                                    skip + (size_t)j * D + (size_t)g * G, 1,
+                                    &scale[t * ng + g], &zero[t * ng + g], tmp);
+          for (int e = 0; e < G; ++e) codes[t * D + (size_t)g * G + e] = tmp[e];
+        }
+      }
+    }
+  }
+  free(tmp);
+  free(pos);
+  free(skip);
+  return Tq;
+}
+
+/* Dequantized values of the kept elements: out[i*G + pos / D][pos % D] =
+ * their fp16 value, for every block i and entry. */
+void kvo_apply_outliers(int Tq, int D, int G, int n_out, const uint32_t* outliers, float* out) {
+  for (int i = 0; i < Tq / G; ++i) {
+    for (int k = 0; k < n_out; ++k) {
+      uint32_t e = outliers[(size_t)i * n_out + k];
+      uint32_t p = e >> 16;
+      out[((size_t)i * G + p / D) * D + p % D] = kvo_h2f((uint16_t)(e & 0xffff));
+    }
+  }
+}
+
 /* ---- the packed byte layout ---------------------------------------------- */
 
 static void put_bits(uint8_t* base, size_t word_index, int bit, int bits,
@@ -275,16 +415,33 @@ static void get_meta(const uint8_t* base, size_t entry, uint16_t* s,
   *z = (uint16_t)(e[2] | (e[3] << 8));
 }
 
-size_t kvo_block_bytes(int D, int G, int bk, int bv) {
-  return (size_t)G * D * (bk + bv) / 8 + 8 * (size_t)D;
+/* A block: [K codes | K meta (4 D) | K outliers (4 n) | V codes | V meta
+ * (4 D) | V outliers (4 n)], n the outliers kept per block side (0: no
+ * outlier sections). */
+size_t kvo_block_bytes_n(int D, int G, int bk, int bv, int n) {
+  return (size_t)G * D * (bk + bv) / 8 + 8 * (size_t)D + 8 * (size_t)n;
 }
 
-/* offsets[0..3] = K codes, K meta, V codes, V meta */
-void kvo_block_offsets(int D, int G, int bk, int bv, size_t* offsets) {
+size_t kvo_block_bytes(int D, int G, int bk, int bv) { return kvo_block_bytes_n(D, G, bk, bv, 0); }
+
+/* offsets[0..5] = K codes, K meta, K outliers, V codes, V meta, V outliers */
+void kvo_block_offsets_n(int D, int G, int bk, int bv, int n, size_t* offsets) {
   offsets[0] = 0;
   offsets[1] = (size_t)G * D * bk / 8;
   offsets[2] = offsets[1] + 4 * (size_t)D;
-  offsets[3] = offsets[2] + (size_t)G * D * bv / 8;
+  offsets[3] = offsets[2] + 4 * (size_t)n;
+  offsets[4] = offsets[3] + (size_t)G * D * bv / 8;
+  offsets[5] = offsets[4] + 4 * (size_t)D;
+}
+
+/* offsets[0..3] = K codes, K meta, V codes, V meta (no outlier sections) */
+void kvo_block_offsets(int D, int G, int bk, int bv, size_t* offsets) {
+  size_t o[6];
+  kvo_block_offsets_n(D, G, bk, bv, 0, o);
+  offsets[0] = o[0];
+  offsets[1] = o[1];
+  offsets[2] = o[3];
+  offsets[3] = o[4];
 }
 
 /* Which order a side's codes are stored in: 1 = fragment order, used when
@@ -354,15 +511,29 @@ static void value_position(int D, int G, int bv, int ak, int av, int j, int d,
   }
 }
 
-/* Writes the Tq/G blocks of one pair into `blocks` (Tq/G * block_bytes). */
-void kvo_pack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
-                   const uint8_t* kcodes, const uint16_t* kscale,
-                   const uint16_t* kzero, const uint8_t* vcodes,
-                   const uint16_t* vscale, const uint16_t* vzero,
-                   uint8_t* blocks) {
-  size_t bb = kvo_block_bytes(D, G, bk, bv);
-  size_t off[4];
-  kvo_block_offsets(D, G, bk, bv, off);
+static void put_u32(uint8_t* base, size_t entry, uint32_t v) {
+  uint8_t* e = base + entry * 4;
+  e[0] = (uint8_t)(v & 0xff);
+  e[1] = (uint8_t)((v >> 8) & 0xff);
+  e[2] = (uint8_t)((v >> 16) & 0xff);
+  e[3] = (uint8_t)((v >> 24) & 0xff);
+}
+
+static uint32_t get_u32(const uint8_t* base, size_t entry) {
+  const uint8_t* e = base + entry * 4;
+  return (uint32_t)e[0] | ((uint32_t)e[1] << 8) | ((uint32_t)e[2] << 16) | ((uint32_t)e[3] << 24);
+}
+
+/* Writes the Tq/G blocks of one pair into `blocks` (Tq/G * block bytes);
+ * kout / vout: [Tq/G][n] outlier entries of each side (unused when n = 0). */
+void kvo_pack_pair_n(int Tq, int D, int G, int bk, int bv, int ak, int av, int n,
+                     const uint8_t* kcodes, const uint16_t* kscale,
+                     const uint16_t* kzero, const uint8_t* vcodes,
+                     const uint16_t* vscale, const uint16_t* vzero,
+                     const uint32_t* kout, const uint32_t* vout, uint8_t* blocks) {
+  size_t bb = kvo_block_bytes_n(D, G, bk, bv, n);
+  size_t off[6];
+  kvo_block_offsets_n(D, G, bk, bv, n, off);
   memset(blocks, 0, (size_t)(Tq / G) * bb);
   for (int i = 0; i < Tq / G; ++i) {
     uint8_t* blk = blocks + (size_t)i * bb;
@@ -381,7 +552,7 @@ void kvo_pack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
         size_t word;
         int bit;
         value_position(D, G, bv, ak, av, j, d, &word, &bit);
-        put_bits(blk + off[2], word, bit, bv, vcodes[(size_t)(i * G + j) * D + d]);
+        put_bits(blk + off[3], word, bit, bv, vcodes[(size_t)(i * G + j) * D + d]);
       }
     }
     /* metadata: D entries each */
@@ -391,19 +562,33 @@ void kvo_pack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
       size_t vm = (av == 0) ? (size_t)i * D + e
                             : (size_t)(i * G + e / (D / G)) * (D / G) + e % (D / G);
       put_meta(blk + off[1], e, kscale[km], kzero[km]);
-      put_meta(blk + off[3], e, vscale[vm], vzero[vm]);
+      put_meta(blk + off[4], e, vscale[vm], vzero[vm]);
+    }
+    /* outliers: n entries each */
+    for (int k = 0; k < n; ++k) {
+      put_u32(blk + off[2], k, kout[(size_t)i * n + k]);
+      put_u32(blk + off[5], k, vout[(size_t)i * n + k]);
     }
   }
 }
 
-/* Inverse of kvo_pack_pair. */
-void kvo_unpack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
-                     const uint8_t* blocks, uint8_t* kcodes, uint16_t* kscale,
-                     uint16_t* kzero, uint8_t* vcodes, uint16_t* vscale,
-                     uint16_t* vzero) {
-  size_t bb = kvo_block_bytes(D, G, bk, bv);
-  size_t off[4];
-  kvo_block_offsets(D, G, bk, bv, off);
+void kvo_pack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
+                   const uint8_t* kcodes, const uint16_t* kscale,
+                   const uint16_t* kzero, const uint8_t* vcodes,
+                   const uint16_t* vscale, const uint16_t* vzero,
+                   uint8_t* blocks) {
+  kvo_pack_pair_n(Tq, D, G, bk, bv, ak, av, 0, kcodes, kscale, kzero, vcodes, vscale, vzero,
+                  NULL, NULL, blocks);
+}
+
+/* Inverse of kvo_pack_pair_n. */
+void kvo_unpack_pair_n(int Tq, int D, int G, int bk, int bv, int ak, int av, int n,
+                       const uint8_t* blocks, uint8_t* kcodes, uint16_t* kscale,
+                       uint16_t* kzero, uint8_t* vcodes, uint16_t* vscale,
+                       uint16_t* vzero, uint32_t* kout, uint32_t* vout) {
+  size_t bb = kvo_block_bytes_n(D, G, bk, bv, n);
+  size_t off[6];
+  kvo_block_offsets_n(D, G, bk, bv, n, off);
   for (int i = 0; i < Tq / G; ++i) {
     const uint8_t* blk = blocks + (size_t)i * bb;
     for (int j = 0; j < G; ++j) {
@@ -413,7 +598,7 @@ void kvo_unpack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
         key_position(D, G, bk, ak, av, j, d, &word, &bit);
         kcodes[(size_t)(i * G + j) * D + d] = (uint8_t)get_bits(blk + off[0], word, bit, bk);
         value_position(D, G, bv, ak, av, j, d, &word, &bit);
-        vcodes[(size_t)(i * G + j) * D + d] = (uint8_t)get_bits(blk + off[2], word, bit, bv);
+        vcodes[(size_t)(i * G + j) * D + d] = (uint8_t)get_bits(blk + off[3], word, bit, bv);
       }
     }
     for (int e = 0; e < D; ++e) {
@@ -422,9 +607,21 @@ void kvo_unpack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
       size_t vm = (av == 0) ? (size_t)i * D + e
                             : (size_t)(i * G + e / (D / G)) * (D / G) + e % (D / G);
       get_meta(blk + off[1], e, &kscale[km], &kzero[km]);
-      get_meta(blk + off[3], e, &vscale[vm], &vzero[vm]);
+      get_meta(blk + off[4], e, &vscale[vm], &vzero[vm]);
+    }
+    for (int k = 0; k < n; ++k) {
+      kout[(size_t)i * n + k] = get_u32(blk + off[2], k);
+      vout[(size_t)i * n + k] = get_u32(blk + off[5], k);
     }
   }
+}
+
+void kvo_unpack_pair(int Tq, int D, int G, int bk, int bv, int ak, int av,
+                     const uint8_t* blocks, uint8_t* kcodes, uint16_t* kscale,
+                     uint16_t* kzero, uint8_t* vcodes, uint16_t* vscale,
+                     uint16_t* vzero) {
+  kvo_unpack_pair_n(Tq, D, G, bk, bv, ak, av, 0, blocks, kcodes, kscale, kzero, vcodes, vscale,
+                    vzero, NULL, NULL);
 }
 
 /* ---- RoPE (fp64) --------------------------------------------------------- */
