@@ -15,7 +15,7 @@
 #include "kvq_device.cuh"
 
 namespace kvq {
-size_t quantize_smem_bytes(int D, int G);
+size_t quantize_smem_bytes(int D, int G, int nout);
 cudaError_t prepare_quantize();
 cudaError_t launch_quantize(const QuantParams& q, cudaStream_t stream);
 cudaError_t launch_dequantize(const DequantParams& q, cudaStream_t stream);
@@ -72,7 +72,8 @@ struct Derived {
   int frag_k, frag_v;  // code order of each side (1 fragment, 0 sequential)
   bool mma_geom;       // geometry of the tensor-core decode kernel
   int C2max;  // level-1 chunks per (pair, query) of the two-level merge
-  size_t block_bytes, off_kc, off_km, off_vc, off_vm;
+  int n_out;           // outliers kept per block and side
+  size_t block_bytes, off_kc, off_km, off_ko, off_vc, off_vm, off_vo;
   size_t blocks_bytes, tail_bytes, sink_bytes, rope_bytes, part_o_bytes, part_ml_bytes;
   size_t lvl_o_bytes, lvl_ml_bytes;
 };
@@ -94,12 +95,19 @@ kvq_status derive(const kvq_config* c, Derived* d) {
     return KVQ_ERR_INVALID_ARG;
   if (c->fp8 != 0 && c->fp8 != 1) return KVQ_ERR_INVALID_ARG;
   if (c->fp8 && (c->bits_k != 8 || c->bits_v != 8)) return KVQ_ERR_INVALID_ARG;
+  if (c->n_outliers < 0 || c->n_outliers > 64 || c->n_outliers % 4 != 0) return KVQ_ERR_INVALID_ARG;
   if ((c->axis_k == 1 || c->axis_v == 1) && c->head_dim % c->group != 0)
     return KVQ_ERR_INVALID_ARG;
   const int R = c->n_q_heads / c->n_kv_heads;
   if (R != 1 && R != 2 && R != 4 && R != 8) return KVQ_ERR_UNSUPPORTED;
   if (c->head_dim != 64 && c->head_dim != 128) return KVQ_ERR_UNSUPPORTED;
   if (c->group != 32 && c->group != 64 && c->group != 128) return KVQ_ERR_UNSUPPORTED;
+  // outlier isolation: the tensor-core geometry with 2- or 4-bit integer
+  // sides, keys stored after RoPE
+  if (c->n_outliers > 0 &&
+      (!mma_geometry(c->group, c->axis_k, c->axis_v) || c->fp8 || c->keys_pre_rope ||
+       (c->bits_k != 2 && c->bits_k != 4) || (c->bits_v != 2 && c->bits_v != 4)))
+    return KVQ_ERR_UNSUPPORTED;
   const long long P = static_cast<long long>(c->batch) * c->n_kv_heads;
   if (P > 65535) return KVQ_ERR_UNSUPPORTED;  // grid.y of the quantize launch
   if (c->max_ctx > (1 << 26)) return KVQ_ERR_UNSUPPORTED;
@@ -119,12 +127,15 @@ kvq_status derive(const kvq_config* c, Derived* d) {
   d->residual = c->residual;
   d->TC = c->residual + c->group;
   d->NB = c->max_ctx / c->group;
-  const size_t D = c->head_dim, G = c->group;
+  const size_t D = c->head_dim, G = c->group, n = c->n_outliers;
+  d->n_out = c->n_outliers;
   d->off_kc = 0;
   d->off_km = G * D * c->bits_k / 8;
-  d->off_vc = d->off_km + 4 * D;
+  d->off_ko = d->off_km + 4 * D;
+  d->off_vc = d->off_ko + 4 * n;
   d->off_vm = d->off_vc + G * D * c->bits_v / 8;
-  d->block_bytes = d->off_vm + 4 * D;
+  d->off_vo = d->off_vm + 4 * D;
+  d->block_bytes = d->off_vo + 4 * n;
   d->blocks_bytes = static_cast<size_t>(P) * d->NB * d->block_bytes;
   d->tail_bytes = static_cast<size_t>(P) * d->TC * D * 2;  // one fp16 [P][TC][D] buffer
   d->sink_bytes = static_cast<size_t>(P) * d->NSK * D * 2;  // one fp16 [P][NSK][D] buffer
@@ -231,6 +242,9 @@ static CacheGeom geom_of(const kvq_cache* c) {
   g.fp8 = c->cfg.fp8;
   g.TC = c->dv.TC;
   g.NSK = c->dv.NSK;
+  g.nout = c->dv.n_out;
+  g.off_ko = static_cast<int>(c->dv.off_ko);
+  g.off_vo = static_cast<int>(c->dv.off_vo);
   return g;
 }
 
@@ -342,7 +356,7 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   // (an FP8 cache dispatches on the E4M3 tag instead of its 8 bits)
   const int bk = cfg->fp8 ? kBitsE4M3 : cfg->bits_k, bv = cfg->fp8 ? kBitsE4M3 : cfg->bits_v;
   DecodeOps ops{nullptr, nullptr};
-  if (d.mma_geom) ops = decode_mma_ops(d.D, d.R, bk, bv, cfg->keys_pre_rope != 0);
+  if (d.mma_geom) ops = decode_mma_ops(d.D, d.R, bk, bv, cfg->keys_pre_rope != 0, d.n_out > 0);
   const bool mma = ops.launch != nullptr;
   if ((d.frag_k || d.frag_v) && !mma) return KVQ_ERR_UNSUPPORTED;
   if (ops.launch == nullptr) ops = decode_ops(d.D, d.R, bk, bv);
@@ -721,6 +735,9 @@ kvq_status kvq_get_buffers(const kvq_cache* c, kvq_buffers* out) {
     out->v_tail_buffer[i] = c->vtail[i];
   }
   out->ragged = c->ragged ? 1 : 0;
+  out->off_ko = c->dv.off_ko;
+  out->off_vo = c->dv.off_vo;
+  out->n_outliers = c->dv.n_out;
   return KVQ_OK;
 }
 

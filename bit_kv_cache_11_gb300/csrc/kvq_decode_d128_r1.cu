@@ -8,5 +8,5 @@
 
 namespace kvq {
 DecodeOps decode_ops_d128_r1(int bk, int bv) { return decode_ops_for<128, 1>(bk, bv); }
-DecodeOps decode_mma_ops_d128_r1(int bk, int bv) { return decode_mma_ops_for<128, 1, false>(bk, bv); }
+DecodeOps decode_mma_ops_d128_r1(int bk, int bv, bool out) { return decode_mma_ops_for<128, 1, false>(bk, bv, out); }
 }  // namespace kvq

@@ -8,5 +8,5 @@
 
 namespace kvq {
 DecodeOps decode_ops_d64_r8(int bk, int bv) { return decode_ops_for<64, 8>(bk, bv); }
-DecodeOps decode_mma_ops_d64_r8(int bk, int bv) { return decode_mma_ops_for<64, 8, false>(bk, bv); }
+DecodeOps decode_mma_ops_d64_r8(int bk, int bv, bool out) { return decode_mma_ops_for<64, 8, false>(bk, bv, out); }
 }  // namespace kvq

@@ -148,7 +148,7 @@ __host__ __device__ constexpr int vcode_log2(int tau) {
   return BV == 2 ? 24 - 2 * (2 * ((tau >> 4) & 1) + ((tau >> 3) & 1)) : (BV == 4 ? 24 : 0);
 }
 
-template <int D, int BK, int BV, int R, bool ROPE>
+template <int D, int BK, int BV, int R, bool ROPE, bool OUT = false>
 struct MmaCfg {
   static constexpr int G = 32;
   static constexpr int NG = D / 32;               // value channel groups
@@ -167,7 +167,12 @@ struct MmaCfg {
   static constexpr int KM_S = 4 * D;
   static constexpr int VC_S = 4 * D * BV;
   static constexpr int VM_S = 4 * D;
-  static constexpr int STAGE = KC_S + KM_S + VC_S + VM_S;  // one block
+  // Dense-and-sparse blocks (OUT) carry up to kMaxOut outlier entries per
+  // side after each side's metadata: the stage holds the largest block and
+  // the value sections sit 4 * nout bytes further (a runtime offset).
+  static constexpr int kMaxOut = 64;
+  static constexpr int BLK = KC_S + KM_S + VC_S + VM_S;    // a block without outliers
+  static constexpr int STAGE = BLK + (OUT ? 8 * kMaxOut : 0);
   static constexpr int NS = ROPE ? 2 : (STAGE <= 4096 ? 3 : 2);
   static constexpr int TCH = mma_tail_chunk(BK, BV);
   static constexpr int QB = R * D * 2;            // one pair's fp16 queries
@@ -189,10 +194,14 @@ struct MmaCfg {
   // RoPE: per-warp key coefficients [R][D/2][8] floats; per-CTA table of
   // cos/sin(j * theta_i), j < 32, stored [D/2][32] float2.
   static constexpr int OFF_CF = OFF_OS + R * D * 4;
-  static constexpr int WARP_BYTES = round_up(OFF_CF + (ROPE ? R * (D / 2) * 32 : 0), 128);
+  // OUT: score corrections [R][32] and value corrections [R][D] (floats)
+  static constexpr int OFF_KX = OFF_CF + (ROPE ? R * (D / 2) * 32 : 0);
+  static constexpr int OFF_VX = OFF_KX + (OUT ? R * 32 * 4 : 0);
+  static constexpr int WARP_BYTES = round_up(OFF_VX + (OUT ? R * D * 4 : 0), 128);
   static constexpr int CS_BYTES = ROPE ? (D / 2) * 32 * 8 : 0;
   static constexpr int SMEM = kDecodeWarps * WARP_BYTES + CS_BYTES;
-  static_assert(2 * TCH * D * 2 == STAGE, "a tail chunk fills one stage");
+  static_assert(2 * TCH * D * 2 == BLK, "a tail chunk fills a block's stage");
+  static_assert(!(OUT && ROPE), "outlier corrections are applied to post-RoPE keys");
   static_assert(KWL % 4 == 0, "lane words are read as 16-byte vectors");
   static_assert(VWL % 4 == 0, "lane words are read as 16-byte vectors");
   static_assert(QB % 16 == 0 && OFF_QS % 16 == 0, "query slots are bulk-copy targets");
@@ -205,10 +214,10 @@ __host__ __device__ constexpr int bcol(int n) {
   return (n >> 3) * BSTR * 2 + (n & 7) * 8;
 }
 
-template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false>
+template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false, bool OUT = false>
 __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (R <= 4 ? 3 : 1))
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
-  using C = MmaCfg<D, BK, BV, R, ROPE>;
+  using C = MmaCfg<D, BK, BV, R, ROPE, OUT>;
   constexpr int NS = C::NS, NT = C::NT, NG = C::NG, MTV = C::MTV, CPL = C::CPL, TCH = C::TCH,
                 STAGE = C::STAGE, KS = C::KS, BL = C::BL, BSTR = C::BSTR, KP = C::KP,
                 VJ = C::VJ, QB = C::QB;
@@ -269,6 +278,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   const uint2* vbv = reinterpret_cast<const uint2*>(ws + C::OFF_VB);
   float* pb = reinterpret_cast<float*>(ws + C::OFF_PB);
   float* os = reinterpret_cast<float*>(ws + C::OFF_OS);
+  float* kx = reinterpret_cast<float*>(ws + C::OFF_KX);  // OUT: score corrections [R][32]
+  float* vx = reinterpret_cast<float*>(ws + C::OFF_VX);  // OUT: value corrections [R][D]
+  // a block's bytes, and where its value sections start in a stage
+  const int nout = OUT ? p.g.nout : 0;
+  const uint32_t blk_bytes = OUT ? static_cast<uint32_t>(p.g.block_bytes) : static_cast<uint32_t>(STAGE);
+  const int voff = C::KC_S + C::KM_S + 4 * nout;
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
     fence_barrier_init();
@@ -281,15 +296,15 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   int lj = ua - static_cast<int>(first_unit(p.map, lpr));
   int lnsub = pair_nsub(p, lpr), lupp = pair_upp(p, lpr);
   bool lfirst = true;  // the next load is this warp's first unit of its pair
-  const uint8_t* lbase = p.g.blocks + static_cast<size_t>(lpr) * p.g.NB * STAGE;
+  const uint8_t* lbase = p.g.blocks + static_cast<size_t>(lpr) * p.g.NB * blk_bytes;
   // Lane 0: unit (lpr, lj) -> stage s, plus the pair's queries into the
   // stage's query slot when it is the warp's first unit of the pair.
   auto issue = [&](int s) {
     uint8_t* st = ws + s * STAGE;
     const uint32_t qb = lfirst ? static_cast<uint32_t>(QB) : 0u;
     if (lj < lnsub) {
-      mbar_arrive_expect_tx(&bars[s], STAGE + qb);
-      bulk_g2s(st, lbase + static_cast<size_t>(lj) * STAGE, STAGE, &bars[s]);
+      mbar_arrive_expect_tx(&bars[s], blk_bytes + qb);
+      bulk_g2s(st, lbase + static_cast<size_t>(lj) * blk_bytes, blk_bytes, &bars[s]);
     } else {
       const PairLens ll = pair_lens(p, lpr);
       if (lj >= ll.nsub + ll.ntu) {
@@ -332,7 +347,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       lj = 0;
       ++lpr;
       lfirst = true;
-      lbase += static_cast<size_t>(p.g.NB) * STAGE;
+      lbase += static_cast<size_t>(p.g.NB) * blk_bytes;
       if (lu < ub) {
         lnsub = pair_nsub(p, lpr);
         lupp = pair_upp(p, lpr);
@@ -368,9 +383,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   const float vfinv = pow2i(-vcode_log2<BV>(tau0));  // the lane's items' code factor, inverted
   const float vfl = pow2i(vcode_log2<BV>(lane));      // code factor of token `lane`
 
-  // Operand buffers: columns that no query fills stay zero (lanes >= BL read
-  // zero columns without touching memory).
+  // Operand buffers: columns that no query fills stay zero; lanes >= BL
+  // (no column of theirs exists) read the zeroed padding slots of a block.
   for (int i = lane; i < (C::OFF_PB - C::OFF_KB) / 4; i += 32) kb32[i] = 0u;
+  static_assert(BL == 32 || BSTR >= BL + 4, "padding slots for the lanes beyond BL");
+  const int blane = lane < BL ? lane : BL + (lane & 3);
   __syncwarp();
 
   // ---- state of the current pair
@@ -435,6 +452,8 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     ev = -126;
     // the scaled query, all channels (rotated-key sub-blocks and the tail)
     for (int i = lane; i < R * D; i += 32) os[i] = __half2float(qp[i]) * p.qscale;
+    if constexpr (OUT)
+      for (int i = lane; i < R * D; i += 32) vx[i] = 0.f;
     __syncwarp();
   };
 
@@ -455,6 +474,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       for (int k = 0; k < VJ; ++k) corr[r][k] *= alpha[r];
 #pragma unroll
       for (int c = 0; c < CPL; ++c) acct[r][c] *= alpha[r];
+      if constexpr (OUT) {
+        __syncwarp();
+        for (int i = lane; i < D; i += 32) vx[r * D + i] *= alpha[r];
+        __syncwarp();
+      }
     }
   };
 
@@ -540,7 +564,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           frag_a8<F8>(words8<KS>(kc, mt, ks, lane), a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? kbv[(ks * NT + nt) * BSTR + lane] : make_uint2(0u, 0u);
+            const uint2 b = kbv[(ks * NT + nt) * BSTR + blane];
             mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -560,7 +584,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           else frag_a4(kw[mt * KS + ks], a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b = lane < BL ? kbv[(ks * NT + nt) * BSTR + lane] : make_uint2(0u, 0u);
+            const uint2 b = kbv[(ks * NT + nt) * BSTR + blane];
             mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -569,10 +593,28 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
 
   // Scores -> weights of the block (lazy maximum), stored in pb with each
   // token's value code factor folded in; the lane's shares of l grow.
-  auto softmax_scores = [&](float (&sc)[2][NT][4], const float (&kz)[R], float ek2) {
+  auto softmax_scores = [&](const uint8_t* st, float (&sc)[2][NT][4], const float (&kz)[R],
+                            float ek2) {
     // lane holds query 4*nt + t, tokens g, g + 8, g + 16, g + 24 (s4[nt][k])
     float s4[NT][4];
     float dmax = -INFINITY;
+    if constexpr (OUT) {
+      // kept key outliers: the dense path scored them as their group's zero
+      // point; token j gains q_c (x - z_c) for each kept (j, c)
+      const __half2* km = reinterpret_cast<const __half2*>(st + C::KC_S);
+      const uint32_t* ko = reinterpret_cast<const uint32_t*>(st + C::KC_S + C::KM_S);
+      for (int i = lane; i < R * 32; i += 32) kx[i] = 0.f;
+      __syncwarp();
+      for (int e = lane; e < nout; e += 32) {
+        const uint32_t en = ko[e];
+        const int pos = static_cast<int>(en >> 16), j = pos / D, c = pos % D;
+        const float x = __half2float(__ushort_as_half(static_cast<unsigned short>(en & 0xffffu)));
+        const float dz = x - __high2float(km[c]);
+#pragma unroll
+        for (int r = 0; r < R; ++r) atomicAdd(&kx[r * 32 + j], os[r * D + c] * dz);
+      }
+      __syncwarp();
+    }
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float z = lane_factor(kz, nt);
@@ -580,6 +622,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       for (int mt = 0; mt < 2; ++mt) {
         s4[nt][2 * mt] = fmaf(ek2, sc[mt][nt][0] + sc[mt][nt][1], z);
         s4[nt][2 * mt + 1] = fmaf(ek2 * C::RK, sc[mt][nt][2] + sc[mt][nt][3], z);
+      }
+      if constexpr (OUT) {
+        const int r = 4 * nt + t;
+        if (r < R) {
+#pragma unroll
+          for (int k = 0; k < 4; ++k) s4[nt][k] += kx[r * 32 + g + 8 * k];
+        }
       }
       if (4 * nt + t < R) {
         const float bm = fmaxf(fmaxf(s4[nt][0], s4[nt][1]), fmaxf(s4[nt][2], s4[nt][3]));
@@ -628,7 +677,21 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   // Value operand from the weights in pb (which carry the code factor):
   // items (token pair, group) -> raw pf * s, exponent ev, hi/lo.
   auto v_prep = [&](const uint8_t* st) {
-    const __half2* vm = reinterpret_cast<const __half2*>(st + C::KC_S + C::KM_S + C::VC_S);
+    const __half2* vm = reinterpret_cast<const __half2*>(st + voff + C::VC_S);
+    if constexpr (OUT) {
+      // kept value outliers: the dense path weighed them as their group's
+      // zero point; channel c gains p_j (x - z_jg) for each kept (j, c)
+      const uint32_t* vo = reinterpret_cast<const uint32_t*>(st + voff + C::VC_S + C::VM_S);
+      for (int e = lane; e < nout; e += 32) {
+        const uint32_t en = vo[e];
+        const int pos = static_cast<int>(en >> 16), j = pos / D, c = pos % D;
+        const float x = __half2float(__ushort_as_half(static_cast<unsigned short>(en & 0xffffu)));
+        const float dz = x - __high2float(vm[j * NG + (c >> 5)]);
+        const float fj = pow2i(-vcode_log2<BV>(j));
+#pragma unroll
+        for (int r = 0; r < R; ++r) atomicAdd(&vx[r * D + c], pb[r * 32 + j] * fj * dz);
+      }
+    }
     float raw[R][VJ][2];
     float vmax = 0.f;
     float2 pp[R];
@@ -680,7 +743,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   };
 
   auto v_mma = [&](const uint8_t* st) {
-    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + C::KC_S + C::KM_S);
+    const uint32_t* vc = reinterpret_cast<const uint32_t*>(st + voff);
     // ---- values: O[c][2r+h] += sum_tok A_V[c][tok] * B_V[tok][2r+h]
     if constexpr (BV == 8) {
 #pragma unroll
@@ -692,8 +755,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           frag_a8<F8>(words8<2>(vc, mt, ks, lane), a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b =
-                lane < BL ? vbv[((gp * 2 + ks) * NT + nt) * BSTR + lane] : make_uint2(0u, 0u);
+            const uint2 b = vbv[((gp * 2 + ks) * NT + nt) * BSTR + blane];
             mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -715,8 +777,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           else frag_a4(vw[2 * mt + ks], a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
-            const uint2 b =
-                lane < BL ? vbv[((gp * 2 + ks) * NT + nt) * BSTR + lane] : make_uint2(0u, 0u);
+            const uint2 b = vbv[((gp * 2 + ks) * NT + nt) * BSTR + blane];
             mma_16816(acc[mt][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
@@ -1002,7 +1063,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       if (lane == 0) p.part_ml[slot * R + r] = make_float2(m[r], lsum[r]);
       float* o = p.part_o + (slot * R + r) * D + lane * CPL;
 #pragma unroll
-      for (int c = 0; c < CPL; ++c) o[c] = os[r * D + lane * CPL + c] + ct[r] + acct[r][c];
+      for (int c = 0; c < CPL; ++c) {
+        float v = os[r * D + lane * CPL + c] + ct[r] + acct[r][c];
+        if constexpr (OUT) v += vx[r * D + lane * CPL + c];
+        o[c] = v;
+      }
     }
     __syncwarp();
     if (p.fused) {
@@ -1147,7 +1212,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           k_mma(st, sc);
           __syncwarp();
         }
-        softmax_scores(sc, kz, ek2);
+        softmax_scores(st, sc, kz, ek2);
         v_prep(st);
         pend = s;
       } else {
@@ -1183,19 +1248,19 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   if (cur >= 0) write_partial(cur);
 }
 
-template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false>
+template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false, bool OUT = false>
 cudaError_t decode_mma_prepare(int* ctas_per_sm) {
-  using C = MmaCfg<D, BK, BV, R, ROPE>;
-  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BK, BV, R, ROPE, F8>,
+  using C = MmaCfg<D, BK, BV, R, ROPE, OUT>;
+  cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BK, BV, R, ROPE, F8, OUT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
   return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, decode_mma_kernel<D, BK, BV, R, ROPE, F8>, kDecodeWarps * 32, C::SMEM);
+      ctas_per_sm, decode_mma_kernel<D, BK, BV, R, ROPE, F8, OUT>, kDecodeWarps * 32, C::SMEM);
 }
 
-template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false>
+template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false, bool OUT = false>
 cudaError_t decode_mma_launch(const DecodeParams& p, cudaStream_t stream) {
-  using C = MmaCfg<D, BK, BV, R, ROPE>;
+  using C = MmaCfg<D, BK, BV, R, ROPE, OUT>;
   // programmatic stream serialization: the grid may start while the previous
   // kernel of the stream finishes; it waits for it before any global access
   cudaLaunchConfig_t cfg = {};
@@ -1208,13 +1273,26 @@ cudaError_t decode_mma_launch(const DecodeParams& p, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BK, BV, R, ROPE, F8>, p);
+  return cudaLaunchKernelEx(&cfg, decode_mma_kernel<D, BK, BV, R, ROPE, F8, OUT>, p);
 }
 
 // Every (bits_k, bits_v) pair of the geometry (G = 32, keys per channel,
-// values per token).
+// values per token); with `out`, the dense-and-sparse variant (2- and 4-bit
+// sides, keys stored after RoPE).
 template <int D, int R, bool ROPE>
-DecodeOps decode_mma_ops_for(int bk, int bv) {
+DecodeOps decode_mma_ops_for(int bk, int bv, bool out) {
+  if constexpr (!ROPE) {
+    if (out) {
+#define KVQ_CASE(BK_, BV_)                                                              \
+  if (bk == BK_ && bv == BV_)                                                           \
+    return DecodeOps{decode_mma_prepare<D, BK_, BV_, R, false, false, true>,            \
+                     decode_mma_launch<D, BK_, BV_, R, false, false, true>};
+      KVQ_CASE(2, 2) KVQ_CASE(2, 4) KVQ_CASE(4, 2) KVQ_CASE(4, 4)
+#undef KVQ_CASE
+      return DecodeOps{nullptr, nullptr};
+    }
+  }
+  if (out) return DecodeOps{nullptr, nullptr};
 #define KVQ_CASE(BK_, BV_)                                                              \
   if (bk == BK_ && bv == BV_)                                                           \
     return DecodeOps{decode_mma_prepare<D, BK_, BV_, R, ROPE>,                          \
@@ -1231,6 +1309,6 @@ DecodeOps decode_mma_ops_for(int bk, int bv) {
 
 // Dispatch over the per-(D, R) translation units (kvq_merge.cu);
 // {nullptr, nullptr} when no tensor-core instantiation exists.
-DecodeOps decode_mma_ops(int D, int R, int bk, int bv, bool rope);
+DecodeOps decode_mma_ops(int D, int R, int bk, int bv, bool rope, bool out = false);
 
 }  // namespace kvq

@@ -4,5 +4,5 @@
 #include "kvq_decode_mma.cuh"
 
 namespace kvq {
-DecodeOps decode_mma_rope_ops_d128_r4(int bk, int bv) { return decode_mma_ops_for<128, 4, true>(bk, bv); }
+DecodeOps decode_mma_rope_ops_d128_r4(int bk, int bv) { return decode_mma_ops_for<128, 4, true>(bk, bv, false); }
 }  // namespace kvq

@@ -180,6 +180,8 @@ struct CacheGeom {
   int fp8;             // 1: both sides hold E4M3 codes with absmax scales
   int TC;              // rows per pair of a tail buffer (residual + G)
   int NSK;             // rows per pair of the sink window (n_sink)
+  int nout;            // outliers kept per block and side (0: none)
+  int off_ko, off_vo;  // the K and V outlier sections of a block
 };
 
 // ---------------------------------------------------------------- batch rows

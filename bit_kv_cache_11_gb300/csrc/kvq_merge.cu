@@ -18,14 +18,14 @@ DecodeOps decode_ops_d128_r2(int, int);
 DecodeOps decode_ops_d128_r4(int, int);
 DecodeOps decode_ops_d128_r8(int, int);
 
-DecodeOps decode_mma_ops_d64_r1(int, int);
-DecodeOps decode_mma_ops_d64_r2(int, int);
-DecodeOps decode_mma_ops_d64_r4(int, int);
-DecodeOps decode_mma_ops_d64_r8(int, int);
-DecodeOps decode_mma_ops_d128_r1(int, int);
-DecodeOps decode_mma_ops_d128_r2(int, int);
-DecodeOps decode_mma_ops_d128_r4(int, int);
-DecodeOps decode_mma_ops_d128_r8(int, int);
+DecodeOps decode_mma_ops_d64_r1(int, int, bool);
+DecodeOps decode_mma_ops_d64_r2(int, int, bool);
+DecodeOps decode_mma_ops_d64_r4(int, int, bool);
+DecodeOps decode_mma_ops_d64_r8(int, int, bool);
+DecodeOps decode_mma_ops_d128_r1(int, int, bool);
+DecodeOps decode_mma_ops_d128_r2(int, int, bool);
+DecodeOps decode_mma_ops_d128_r4(int, int, bool);
+DecodeOps decode_mma_ops_d128_r8(int, int, bool);
 DecodeOps decode_mma_rope_ops_d64_r1(int, int);
 DecodeOps decode_mma_rope_ops_d64_r2(int, int);
 DecodeOps decode_mma_rope_ops_d64_r4(int, int);
@@ -35,17 +35,17 @@ DecodeOps decode_mma_rope_ops_d128_r2(int, int);
 DecodeOps decode_mma_rope_ops_d128_r4(int, int);
 DecodeOps decode_mma_rope_ops_d128_r8(int, int);
 
-DecodeOps decode_mma_ops(int D, int R, int bk, int bv, bool rope) {
+DecodeOps decode_mma_ops(int D, int R, int bk, int bv, bool rope, bool out) {
   if (D == 64) {
-    if (R == 1) return rope ? decode_mma_rope_ops_d64_r1(bk, bv) : decode_mma_ops_d64_r1(bk, bv);
-    if (R == 2) return rope ? decode_mma_rope_ops_d64_r2(bk, bv) : decode_mma_ops_d64_r2(bk, bv);
-    if (R == 4) return rope ? decode_mma_rope_ops_d64_r4(bk, bv) : decode_mma_ops_d64_r4(bk, bv);
-    if (R == 8) return rope ? decode_mma_rope_ops_d64_r8(bk, bv) : decode_mma_ops_d64_r8(bk, bv);
+    if (R == 1) return rope ? decode_mma_rope_ops_d64_r1(bk, bv) : decode_mma_ops_d64_r1(bk, bv, out);
+    if (R == 2) return rope ? decode_mma_rope_ops_d64_r2(bk, bv) : decode_mma_ops_d64_r2(bk, bv, out);
+    if (R == 4) return rope ? decode_mma_rope_ops_d64_r4(bk, bv) : decode_mma_ops_d64_r4(bk, bv, out);
+    if (R == 8) return rope ? decode_mma_rope_ops_d64_r8(bk, bv) : decode_mma_ops_d64_r8(bk, bv, out);
   } else if (D == 128) {
-    if (R == 1) return rope ? decode_mma_rope_ops_d128_r1(bk, bv) : decode_mma_ops_d128_r1(bk, bv);
-    if (R == 2) return rope ? decode_mma_rope_ops_d128_r2(bk, bv) : decode_mma_ops_d128_r2(bk, bv);
-    if (R == 4) return rope ? decode_mma_rope_ops_d128_r4(bk, bv) : decode_mma_ops_d128_r4(bk, bv);
-    if (R == 8) return rope ? decode_mma_rope_ops_d128_r8(bk, bv) : decode_mma_ops_d128_r8(bk, bv);
+    if (R == 1) return rope ? decode_mma_rope_ops_d128_r1(bk, bv) : decode_mma_ops_d128_r1(bk, bv, out);
+    if (R == 2) return rope ? decode_mma_rope_ops_d128_r2(bk, bv) : decode_mma_ops_d128_r2(bk, bv, out);
+    if (R == 4) return rope ? decode_mma_rope_ops_d128_r4(bk, bv) : decode_mma_ops_d128_r4(bk, bv, out);
+    if (R == 8) return rope ? decode_mma_rope_ops_d128_r8(bk, bv) : decode_mma_ops_d128_r8(bk, bv, out);
   }
   return DecodeOps{nullptr, nullptr};
 }
@@ -132,7 +132,7 @@ __global__ void merge2_kernel(const Merge2Params mp) {
     L = fmaf(f, ml.y, L);
     o = fmaf(f, __ldcg(&mp.lvl_o[(base + k) * mp.D + d]), o);
   }
-  mp.out[(pr * mp.R + r) * mp.D + d] = o / L;
+  mp.out[(pr * mp.R + r) * mp.D + d] = L > 0.f ? o / L : 0.f;
   if (d == 0) mp.tickets[pq] = 0;
 }
 

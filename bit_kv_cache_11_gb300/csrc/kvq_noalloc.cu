@@ -104,6 +104,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
   if (cs != KVQ_OK) return cs;
   if (cfg->keys_pre_rope) return KVQ_ERR_UNSUPPORTED;  // the RoPE table would need memory
   if (cfg->n_sink != 0 || cfg->residual != 0) return KVQ_ERR_UNSUPPORTED;  // no window buffers
+  if (cfg->n_outliers != 0) return KVQ_ERR_UNSUPPORTED;  // its corrections need the cache's kernels
   const int D = cfg->head_dim, G = cfg->group;
   const int R = cfg->n_q_heads / cfg->n_kv_heads;
   const long long P = static_cast<long long>(cfg->batch) * cfg->n_kv_heads;
@@ -196,6 +197,9 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     p.g.fp8 = cfg->fp8;
     p.g.TC = G;
     p.g.NSK = 0;
+    p.g.nout = 0;
+    p.g.off_ko = p.g.off_km + 4 * D;
+    p.g.off_vo = p.g.off_vm + 4 * D;
     p.map = map;
     for (int i = 0; i < 2; ++i) {  // the caller's one tail, read only
       p.ktail[i] = static_cast<__half*>(const_cast<void*>(k_tail));

@@ -139,6 +139,132 @@ __device__ __forceinline__ uint32_t pack_word<8>(const uint8_t* b) {
 
 }  // namespace
 
+// Shared ints of the outlier selection: two histograms (256 + 128), four
+// results and a block scan's kQuantThreads / 32 + 1 slots.
+constexpr int kSelectScratch = 256 + 128 + 4 + kQuantThreads / 32 + 1;
+
+// Exclusive prefix sum of v over the CTA's kQuantThreads threads (tot: the
+// sum of all); scratch holds kQuantThreads / 32 + 1 ints.  Ends with a CTA
+// barrier, so scratch may be reused right after.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* scratch, int* tot) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[wid] = x;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int w = 0; w < kQuantThreads / 32; ++w) {
+      const int t = scratch[w];
+      scratch[w] = acc;
+      acc += t;
+    }
+    scratch[kQuantThreads / 32] = acc;
+  }
+  __syncthreads();
+  const int r = scratch[wid] + x - v;
+  *tot = scratch[kQuantThreads / 32];
+  __syncthreads();
+  return r;
+}
+
+// The bucket b (searching from the top) where the running count of hist[]
+// reaches `need` (need >= 1, sum(hist) >= need), and the count of elements
+// in the buckets above b; one warp, nb buckets (a multiple of 32).
+__device__ __forceinline__ void top_bucket(const int* hist, int nb, int need, int* b_out,
+                                           int* above_out) {
+  const int lane = threadIdx.x & 31;
+  const int per = nb / 32;
+  // lane l owns buckets [nb - (l+1) per, nb - l per): lane 0 the highest
+  int sum = 0;
+  for (int i = 0; i < per; ++i) sum += hist[nb - 1 - lane * per - i];
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  const unsigned hit = __ballot_sync(0xffffffffu, incl >= need);
+  const int l = __ffs(hit) - 1;  // first lane whose prefix reaches need
+  const int before = __shfl_sync(0xffffffffu, incl - sum, l);
+  if (lane == l) {
+    int acc = before;
+    for (int i = 0; i < per; ++i) {
+      const int b = nb - 1 - lane * per - i;
+      if (acc + hist[b] >= need) {
+        *b_out = b;
+        *above_out = acc;
+        break;
+      }
+      acc += hist[b];
+    }
+  }
+}
+
+// Dense-and-sparse isolation of one side of a block (G x D fp16 tile X, row
+// pitch XP): the n elements of largest magnitude (ties: lower position
+// j*D + d) get skip[pos] = 1 and an entry (fp16 bits | pos << 16), written
+// in ascending position order to `entries` (global).  Every thread owns
+// G*D / kQuantThreads consecutive positions.  sh: kSelectScratch ints of
+// shared scratch.  Starts and ends with the CTA in step.
+__device__ void select_outliers(const __half* X, int XP, int G, int D, int n, uint8_t* skip,
+                                uint32_t* entries, int* sh) {
+  const int tid = threadIdx.x;
+  const int per = G * D / kQuantThreads;
+  const int pos0 = tid * per;
+  int* hist1 = sh;          // key >> 7
+  int* hist2 = sh + 256;    // key & 127 within the chosen high bucket
+  int* misc = sh + 384;     // [0] high bucket, [1] above it, [2] low bucket, [3] above it,
+                            // [4, 4 + kQuantThreads / 32] the scans' scratch
+  for (int i = tid; i < 384; i += kQuantThreads) sh[i] = 0;
+  __syncthreads();
+  auto key_at = [&](int pos) -> int {
+    const int j = pos / D, d = pos - j * D;
+    return __half_as_ushort(X[j * XP + d]) & 0x7fff;
+  };
+  for (int i = 0; i < per; ++i) atomicAdd(&hist1[key_at(pos0 + i) >> 7], 1);
+  __syncthreads();
+  if (tid < 32) top_bucket(hist1, 256, n, &misc[0], &misc[1]);
+  __syncthreads();
+  const int b1 = misc[0];
+  for (int i = 0; i < per; ++i) {
+    const int k = key_at(pos0 + i);
+    if ((k >> 7) == b1) atomicAdd(&hist2[k & 127], 1);
+  }
+  __syncthreads();
+  if (tid < 32) top_bucket(hist2, 128, n - misc[1], &misc[2], &misc[3]);
+  __syncthreads();
+  const int T = (b1 << 7) | misc[2];       // the n-th largest key
+  const int need = n - misc[1] - misc[3];  // how many elements equal to T are kept
+  int eq = 0;
+  for (int i = 0; i < per; ++i) eq += key_at(pos0 + i) == T;
+  int tot;
+  int rank = block_exclusive_scan(eq, misc + 4, &tot);
+  int kept = 0;
+  for (int i = 0; i < per; ++i) {
+    const int k = key_at(pos0 + i);
+    bool keep = k > T;
+    if (k == T) keep = rank++ < need;
+    skip[pos0 + i] = keep ? 1 : 0;
+    kept += keep;
+  }
+  const int base = block_exclusive_scan(kept, misc + 4, &tot);
+  int e = base;
+  for (int i = 0; i < per; ++i) {
+    const int pos = pos0 + i;
+    if (skip[pos]) {
+      const int j = pos / D, d = pos - j * D;
+      entries[e++] = static_cast<uint32_t>(__half_as_ushort(X[j * XP + d])) |
+                     (static_cast<uint32_t>(pos) << 16);
+    }
+  }
+  __syncthreads();
+}
+
 // CTA x of pair p, whose row record is `row` (see QuantParams).
 template <int BK, int BV>
 __device__ __forceinline__ void quantize_block(const QuantParams& q, const QuantRow& row, int x,
@@ -180,6 +306,11 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
   __half* xv = xk + G * XP;
   uint8_t* kcode = reinterpret_cast<uint8_t*>(xv + G * XP);  // [G][KP] token-major
   uint8_t* vcode = kcode + G * KP;                            // [D][VP] channel-major
+  // outlier isolation: skip masks [G*D] per side and selection scratch
+  const int nout = q.g.nout;
+  uint8_t* kskip = vcode + D * VP;
+  uint8_t* vskip = kskip + G * D;
+  int* osh = reinterpret_cast<int*>(vskip + G * D);
 
   // 1. the block's rows (combined index x*G + j), 16-byte loads
   const int chunks = G * (D / 8);
@@ -199,6 +330,13 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
   __half2* kmeta = reinterpret_cast<__half2*>(blk + q.g.off_km);
   __half2* vmeta = reinterpret_cast<__half2*>(blk + q.g.off_vm);
 
+  // 1b. dense-and-sparse isolation: the nout elements of largest magnitude
+  //     of each side are kept apart (skip masks) and stored as entries
+  if (nout > 0) {
+    select_outliers(xk, XP, G, D, nout, kskip, reinterpret_cast<uint32_t*>(blk + q.g.off_ko), osh);
+    select_outliers(xv, XP, G, D, nout, vskip, reinterpret_cast<uint32_t*>(blk + q.g.off_vo), osh);
+  }
+
   // 2. one thread per group: statistics, then the group's codes as bytes.
   //    Every block has D key groups and D value groups whatever the axis.
   int lgG = 5;
@@ -215,12 +353,49 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
     const int bits = isv ? BV : BK;
     const float top = static_cast<float>((1 << bits) - 1);
     const __half* X = isv ? xv : xk;
-    if (axis == 0) {  // channel ee over the G tokens
+    const uint8_t* skip = isv ? vskip : kskip;
+    if (axis == 0 && nout > 0) {  // channel ee, its kept outliers excluded
+      float mn = 0.f, mx = 0.f;
+      bool any = false;
+      for (int j = 0; j < G; ++j) {
+        if (skip[j * D + ee]) continue;
+        const float v = __half2float(X[j * XP + ee]);
+        mn = any ? fminf(mn, v) : v;
+        mx = any ? fmaxf(mx, v) : v;
+        any = true;
+      }
+      const Stat st = stat_of(mn, mx, bits, f8, (isv ? vmeta : kmeta) + ee);
+      for (int j = 0; j < G; ++j) {
+        const uint8_t c = skip[j * D + ee] ? 0 : code(__half2float(X[j * XP + ee]), st, top);
+        if (isv) vcode[ee * VP + j] = c;
+        else kcode[j * KP + ee] = c;
+      }
+    } else if (axis == 0) {  // channel ee over the G tokens
       const Stat st = group_stat(X + ee, XP, G, bits, f8, (isv ? vmeta : kmeta) + ee);
       for (int j = 0; j < G; ++j) {
         const uint8_t c = code(__half2float(X[j * XP + ee]), st, top);
         if (isv) vcode[ee * VP + j] = c;
         else kcode[j * KP + ee] = c;
+      }
+    } else if (nout > 0) {  // token j, channels [g*G, (g+1)*G), kept outliers excluded
+      const int j = ee & (G - 1), g = ee >> lgG;
+      const __half* row = X + j * XP + (g << lgG);
+      const uint8_t* sk = skip + j * D + (g << lgG);
+      float mn = 0.f, mx = 0.f;
+      bool any = false;
+      for (int i = 0; i < G; ++i) {
+        if (sk[i]) continue;
+        const float v = __half2float(row[i]);
+        mn = any ? fminf(mn, v) : v;
+        mx = any ? fmaxf(mx, v) : v;
+        any = true;
+      }
+      const Stat st = stat_of(mn, mx, bits, f8, (isv ? vmeta : kmeta) + j * ng + g);
+      for (int i = 0; i < G; ++i) {
+        const int d = (g << lgG) + i;
+        const uint8_t c = sk[i] ? 0 : code(__half2float(row[i]), st, top);
+        if (isv) vcode[d * VP + j] = c;
+        else kcode[j * KP + d] = c;
       }
     } else {          // token j, channels [g*G, (g+1)*G); consecutive threads: consecutive j
       // the group's G contiguous values, 16 bytes at a time (row pitch 16 mod
@@ -375,11 +550,28 @@ __global__ void __launch_bounds__(kQuantThreads) dequantize_kernel(const Dequant
       q.vout[o] = fmaf(q.g.fp8 ? e4m3_value(c) : static_cast<float>(c), sz.x, sz.y);
     }
   }
+  // kept outliers replace their positions
+  if (q.g.nout > 0) {
+    __syncthreads();
+    const uint32_t* ko = reinterpret_cast<const uint32_t*>(blk + q.g.off_ko);
+    const uint32_t* vo = reinterpret_cast<const uint32_t*>(blk + q.g.off_vo);
+    for (int k = threadIdx.x; k < 2 * q.g.nout; k += blockDim.x) {
+      const bool isv = k >= q.g.nout;
+      const uint32_t e = isv ? vo[k - q.g.nout] : ko[k];
+      const int pos = static_cast<int>(e >> 16);
+      const size_t o = (static_cast<size_t>(p) * q.T_q + static_cast<size_t>(i) * G + pos / D) * D +
+                       pos % D;
+      const float v = __half2float(__ushort_as_half(static_cast<unsigned short>(e & 0xffffu)));
+      (isv ? q.vout : q.kout)[o] = v;
+    }
+  }
 }
 
-size_t quantize_smem_bytes(int D, int G) {
-  return static_cast<size_t>(2) * G * xpitch(D) * sizeof(__half) +
-         static_cast<size_t>(G) * kpitch(D) + static_cast<size_t>(D) * vpitch(G);
+size_t quantize_smem_bytes(int D, int G, int nout) {
+  size_t b = static_cast<size_t>(2) * G * xpitch(D) * sizeof(__half) +
+             static_cast<size_t>(G) * kpitch(D) + static_cast<size_t>(D) * vpitch(G);
+  if (nout > 0) b += static_cast<size_t>(2) * G * D + sizeof(int) * kSelectScratch;
+  return b;
 }
 
 namespace {
@@ -405,14 +597,14 @@ cudaError_t prepare_quantize() {
       for (int rg = 0; rg < 2; ++rg) {
         cudaError_t e =
             cudaFuncSetAttribute(quant_fn(a, b, rg != 0), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(quantize_smem_bytes(128, 128)));
+                                 static_cast<int>(quantize_smem_bytes(128, 128, 0)));
         if (e != cudaSuccess) return e;
       }
   return cudaSuccess;
 }
 
 cudaError_t launch_quantize(const QuantParams& q, cudaStream_t stream) {
-  const size_t smem = quantize_smem_bytes(q.g.D, q.g.G);
+  const size_t smem = quantize_smem_bytes(q.g.D, q.g.G, q.g.nout);
   QuantFn fn = quant_fn(q.g.bk, q.g.bv, q.ragged != 0);
   if (fn == nullptr) return cudaErrorInvalidValue;
   int mx = 0;  // most blocks any row flushes

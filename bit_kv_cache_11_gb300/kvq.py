@@ -38,7 +38,8 @@ class kvq_config(ctypes.Structure):
                 ("head_dim", ctypes.c_int), ("max_ctx", ctypes.c_int), ("bits_k", ctypes.c_int),
                 ("bits_v", ctypes.c_int), ("group", ctypes.c_int), ("axis_k", ctypes.c_int),
                 ("axis_v", ctypes.c_int), ("keys_pre_rope", ctypes.c_int), ("rope_base", ctypes.c_float),
-                ("n_sink", ctypes.c_int), ("residual", ctypes.c_int), ("fp8", ctypes.c_int)]
+                ("n_sink", ctypes.c_int), ("residual", ctypes.c_int), ("fp8", ctypes.c_int),
+                ("n_outliers", ctypes.c_int)]
 
 
 class kvq_buffers(ctypes.Structure):
@@ -49,7 +50,9 @@ class kvq_buffers(ctypes.Structure):
                 ("T_tail", ctypes.c_int), ("code_order_k", ctypes.c_int), ("code_order_v", ctypes.c_int),
                 ("k_sink", ctypes.c_void_p), ("v_sink", ctypes.c_void_p), ("T_sink", ctypes.c_int),
                 ("tail_rows", ctypes.c_int), ("k_tail_buffer", ctypes.c_void_p * 2),
-                ("v_tail_buffer", ctypes.c_void_p * 2), ("ragged", ctypes.c_int)]
+                ("v_tail_buffer", ctypes.c_void_p * 2), ("ragged", ctypes.c_int),
+                ("off_ko", ctypes.c_size_t), ("off_vo", ctypes.c_size_t),
+                ("n_outliers", ctypes.c_int)]
 
 
 _P = ctypes.c_void_p
@@ -116,11 +119,11 @@ def _stream(stream) -> int | None:
 
 def make_config(batch, n_q_heads, n_kv_heads, head_dim, max_ctx, bits_k=2, bits_v=2, group=32,
                 axis_k=KVQ_AXIS_CHANNEL, axis_v=KVQ_AXIS_TOKEN, keys_pre_rope=False,
-                rope_base=10000.0, n_sink=0, residual=0, fp8=False) -> kvq_config:
+                rope_base=10000.0, n_sink=0, residual=0, fp8=False, n_outliers=0) -> kvq_config:
     return kvq_config(int(batch), int(n_q_heads), int(n_kv_heads), int(head_dim), int(max_ctx),
                       int(bits_k), int(bits_v), int(group), int(axis_k), int(axis_v),
                       1 if keys_pre_rope else 0, float(rope_base), int(n_sink), int(residual),
-                      1 if fp8 else 0)
+                      1 if fp8 else 0, int(n_outliers))
 
 
 # ---- the C calls, same names ------------------------------------------------
@@ -273,7 +276,8 @@ class KVCache:
     ``kvq_config``): batch, n_q_heads, n_kv_heads, head_dim, max_ctx,
     bits_k / bits_v (2, 4, 8), group (32, 64, 128), axis_k / axis_v,
     keys_pre_rope / rope_base, n_sink and residual (fp16 windows), fp8 (E4M3
-    codes, 8-bit sides).  A typical decode loop::
+    codes, 8-bit sides), n_outliers (elements kept in fp16 per block and
+    side).  A typical decode loop::
 
         cache = KVCache(batch=8, n_q_heads=32, n_kv_heads=32, head_dim=128,
                         max_ctx=8192, bits_k=2, bits_v=2)

@@ -68,16 +68,30 @@
  * bk, bv = bits of K and V; words are little-endian uint32):
  *
  *   block (p, i) starts at byte (p * NB + i) * block_bytes, where
- *   block_bytes = G*D*(bk+bv)/8 + 8*D, and holds tokens [i*G, (i+1)*G):
+ *   block_bytes = G*D*(bk+bv)/8 + 8*D + 8*n (n = n_outliers), and holds
+ *   tokens [i*G, (i+1)*G):
  *     [off_kc, +G*D*bk/8)  K codes, in the side's code order (below).
  *     [off_km, +4*D)       K metadata: D entries {fp16 scale, fp16 zero}
  *                          (scale at the lower address).  Channel axis:
  *                          entry d is channel d's group.  Token axis: entry
  *                          j*(D/G) + g is token j, channels [g*G, (g+1)*G).
+ *     [off_ko, +4*n)       K outliers: n uint32 entries, the kept fp16 value
+ *                          in bits 0-15 and its position j*D + d in the block
+ *                          in bits 16-31, ascending by position.
  *     [off_vc, +G*D*bv/8)  V codes, in the side's code order (below).
  *     [off_vm, +4*D)       V metadata, indexed as for K by V's axis.
- *   off_kc = 0, off_km = G*D*bk/8, off_vc = off_km + 4*D,
- *   off_vm = off_vc + G*D*bv/8.
+ *     [off_vo, +4*n)       V outliers, as for K.
+ *   off_kc = 0, off_km = G*D*bk/8, off_ko = off_km + 4*D,
+ *   off_vc = off_ko + 4*n, off_vm = off_vc + G*D*bv/8, off_vo = off_vm + 4*D.
+ *
+ *   Outliers (dense-and-sparse isolation, n > 0; KVQuant's "isolating a small
+ *   fraction of outliers", "Why KV Cache Geometry Matters More Than Bit
+ *   Precision", section "KV Cache Size, GPU Memory Efficiency, and the Shift
+ *   to Geometry-Aware Quantization"): in every block and side the n elements
+ *   of largest magnitude (ties: lower position j*D + d) are kept exactly;
+ *   every group takes its min and max over its other elements (scale 0 and
+ *   zero +0 when none remain); kept positions hold code 0 and dequantize to
+ *   their kept value.
  *
  *   Code order of a side (kvq_buffers.code_order_k / code_order_v):
  *   FRAGMENT order when keys are grouped per channel, values per token,
@@ -160,6 +174,11 @@ typedef struct {
                         group; 0..4096 (0: the tail holds < G tokens)         */
   int fp8;           /* 1: FP8 cache (requires bits_k = bits_v = 8): codes are
                         E4M3, scale = fp16(max|x| / 448), zero = 0            */
+  int n_outliers;    /* dense-and-sparse isolation: elements of largest
+                        magnitude kept in fp16 per block and side; 0..64, a
+                        multiple of 4.  Nonzero needs keys per channel, values
+                        per token, G = 32, 2- or 4-bit sides, no FP8 and keys
+                        stored after RoPE (KVQ_ERR_UNSUPPORTED otherwise)    */
 } kvq_config;
 
 typedef struct kvq_cache kvq_cache; /* opaque */
@@ -186,6 +205,8 @@ typedef struct {
   void* v_tail_buffer[2];      /*   which one holds a row's tail)               */
   int ragged;                  /* 1: rows hold different lengths; the T_* fields
                                   and k_tail / v_tail above describe row 0      */
+  size_t off_ko, off_vo;       /* K and V outlier sections (n_outliers entries) */
+  int n_outliers;
 } kvq_buffers;
 
 /* Validates a config on the host (no GPU needed).  Returns KVQ_OK,
@@ -297,9 +318,10 @@ KVQ_API kvq_status kvq_dequantize(kvq_cache* cache, void* k_out, void* v_out,
  * the layout described at the top of this header, this call decodes it
  * without a kvq_cache (whose creation allocates) and calls no allocating
  * routine.
- *   cfg            the cache's geometry; keys_pre_rope, n_sink and residual
- *                  must be 0 (KVQ_ERR_UNSUPPORTED otherwise: the RoPE table
- *                  would need memory; this call has no window buffers).
+ *   cfg            the cache's geometry; keys_pre_rope, n_sink, residual
+ *                  and n_outliers must be 0 (KVQ_ERR_UNSUPPORTED otherwise:
+ *                  the RoPE table would need memory; this call has no window
+ *                  buffers and no outlier corrections).
  *   blocks         device, [P][max_ctx/G][block_bytes] packed blocks.
  *   k_tail, v_tail device, fp16 [P][G][D]; rows [0, T_tail) are read.  May be
  *                  NULL when T_tail = 0.

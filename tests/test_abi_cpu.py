@@ -72,6 +72,11 @@ def test_config_check_on_host(lib_path):
         (dict(fp8=True, bits_k=8, bits_v=4), k.KVQ_ERR_INVALID_ARG),
         (dict(fp8=True, bits_k=8, bits_v=8), k.KVQ_OK),
         (dict(fp8=True, bits_k=8, bits_v=8, axis_k=1, group=128), k.KVQ_OK),
+        (dict(n_outliers=32), k.KVQ_OK),
+        (dict(n_outliers=30), k.KVQ_ERR_INVALID_ARG),              # a multiple of 4
+        (dict(n_outliers=128), k.KVQ_ERR_INVALID_ARG),             # at most 64
+        (dict(n_outliers=32, bits_k=8), k.KVQ_ERR_UNSUPPORTED),
+        (dict(n_outliers=32, group=64), k.KVQ_ERR_UNSUPPORTED),
     ]
     base = dict(batch=8, n_q_heads=32, n_kv_heads=32, head_dim=128, max_ctx=8192)
     for over, status in cases:
