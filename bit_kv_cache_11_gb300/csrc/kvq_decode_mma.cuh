@@ -172,7 +172,9 @@ struct MmaCfg {
   // the value sections sit 4 * nout bytes further (a runtime offset).
   static constexpr int kMaxOut = 64;
   static constexpr int BLK = KC_S + KM_S + VC_S + VM_S;    // a block without outliers
-  static constexpr int STAGE = BLK + (OUT ? 8 * kMaxOut : 0);
+  // RoPE stages also carry the cos/sin row (D/2 float2) of the block's first
+  // position, copied with the block.
+  static constexpr int STAGE = BLK + (OUT ? 8 * kMaxOut : 0) + (ROPE ? 4 * D : 0);
   static constexpr int NS = ROPE ? 2 : (STAGE <= 4096 ? 3 : 2);
   static constexpr int TCH = mma_tail_chunk(BK, BV);
   static constexpr int QB = R * D * 2;            // one pair's fp16 queries
@@ -191,14 +193,16 @@ struct MmaCfg {
   static constexpr int VB_BYTES = NG * 2 * NT * BSTR * 8;
   static constexpr int OFF_PB = OFF_VB + VB_BYTES;                  // [R][32] float
   static constexpr int OFF_OS = OFF_PB + R * 32 * 4;                // [R][D] float
-  // RoPE: per-warp key coefficients [R][D/2][8] floats; per-CTA table of
-  // cos/sin(j * theta_i), j < 32, stored [D/2][32] float2.
+  // RoPE: per-warp key coefficients, six per frequency pair, stored for
+  // pairs (2f, 2f + 1) as three float4 [R][D/4][3]; per-CTA table of
+  // cos/sin(j * theta_i), j < 32, stored [D/4][32] float4 {cos_2f, cos_2f+1,
+  // sin_2f, sin_2f+1} so that lane j reads its own row conflict-free.
   static constexpr int OFF_CF = OFF_OS + R * D * 4;
   // OUT: score corrections [R][32] and value corrections [R][D] (floats)
-  static constexpr int OFF_KX = OFF_CF + (ROPE ? R * (D / 2) * 32 : 0);
+  static constexpr int OFF_KX = OFF_CF + (ROPE ? R * (D / 4) * 48 : 0);
   static constexpr int OFF_VX = OFF_KX + (OUT ? R * 32 * 4 : 0);
   static constexpr int WARP_BYTES = round_up(OFF_VX + (OUT ? R * D * 4 : 0), 128);
-  static constexpr int CS_BYTES = ROPE ? (D / 2) * 32 * 8 : 0;
+  static constexpr int CS_BYTES = ROPE ? (D / 4) * 32 * 16 : 0;
   static constexpr int SMEM = kDecodeWarps * WARP_BYTES + CS_BYTES;
   static_assert(2 * TCH * D * 2 == BLK, "a tail chunk fills a block's stage");
   static_assert(!(OUT && ROPE), "outlier corrections are applied to post-RoPE keys");
@@ -233,14 +237,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   asm volatile("griddepcontrol.wait;" ::: "memory");
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // RoPE: cos/sin(j * theta_i) for the 32 token offsets of a sub-block (table
-  // rows 0..31), transposed so lane j reads its own column conflict-free.
-  // Loaded before any warp of the CTA can leave.
-  float2* cs_tab = reinterpret_cast<float2*>(smem + kDecodeWarps * C::WARP_BYTES);
+  // rows 0..31), transposed so lane j reads its own column conflict-free, two
+  // frequency pairs per entry.  Loaded before any warp of the CTA can leave.
+  float4* cs_tab = reinterpret_cast<float4*>(smem + kDecodeWarps * C::WARP_BYTES);
   if constexpr (ROPE) {
-    for (int idx = threadIdx.x; idx < (D / 2) * 32; idx += blockDim.x) {
-      const int i = idx >> 5, j = idx & 31;
-      cs_tab[idx] = j < p.rope_rows ? p.rope_tab[static_cast<size_t>(j) * (D / 2) + i]
-                                    : make_float2(1.f, 0.f);
+    for (int idx = threadIdx.x; idx < (D / 4) * 32; idx += blockDim.x) {
+      const int f = idx >> 5, j = idx & 31;
+      const bool in = j < p.rope_rows;
+      const float2 a = in ? p.rope_tab[static_cast<size_t>(j) * (D / 2) + 2 * f] : make_float2(1.f, 0.f);
+      const float2 b = in ? p.rope_tab[static_cast<size_t>(j) * (D / 2) + 2 * f + 1] : make_float2(1.f, 0.f);
+      cs_tab[idx] = make_float4(a.x, b.x, a.y, b.y);
     }
     __syncthreads();
   }
@@ -282,7 +288,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   float* vx = reinterpret_cast<float*>(ws + C::OFF_VX);  // OUT: value corrections [R][D]
   // a block's bytes, and where its value sections start in a stage
   const int nout = OUT ? p.g.nout : 0;
-  const uint32_t blk_bytes = OUT ? static_cast<uint32_t>(p.g.block_bytes) : static_cast<uint32_t>(STAGE);
+  const uint32_t blk_bytes = OUT ? static_cast<uint32_t>(p.g.block_bytes) : static_cast<uint32_t>(C::BLK);
   const int voff = C::KC_S + C::KM_S + 4 * nout;
   if (lane == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(&bars[s], 1);
@@ -303,8 +309,12 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     uint8_t* st = ws + s * STAGE;
     const uint32_t qb = lfirst ? static_cast<uint32_t>(QB) : 0u;
     if (lj < lnsub) {
-      mbar_arrive_expect_tx(&bars[s], blk_bytes + qb);
+      mbar_arrive_expect_tx(&bars[s], blk_bytes + qb + (ROPE ? 4 * D : 0));
       bulk_g2s(st, lbase + static_cast<size_t>(lj) * blk_bytes, blk_bytes, &bars[s]);
+      if constexpr (ROPE) {
+        const int p0 = p.map.Ts[row_of(p.map, lpr)] + 32 * lj;
+        bulk_g2s(st + C::BLK, p.rope_tab + static_cast<size_t>(p0) * (D / 2), 4 * D, &bars[s]);
+      }
     } else {
       const PairLens ll = pair_lens(p, lpr);
       if (lj >= ll.nsub + ll.ntu) {
@@ -794,22 +804,38 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
     // ---- rotated keys (CUDA cores).  Sub-block positions p0 + j, p0 = 32*ju:
     // q . R(p0 + j) k_j = q' . R(j) k_j with q' = R(-p0) q, and with
     // k = s*c + z per channel, for the pair (i, i+D/2):
-    //   cos(j th_i) (a c_i + b c_i2 + e) + sin(j th_i) (f c_i - g c_i2 + h).
-    constexpr int H = D / 2;
+    //   cos(j th_i) (al c_i + be c_i2 + ze) + sin(j th_i) (ga c_i + de c_i2 + et).
+    // Integer codes are read as x = 1 + c 2^-BK (the code in the mantissa of
+    // 1.0, no conversion instruction): the coefficients are scaled by 2^BK
+    // and the constant terms absorb the 1s.  Two frequency pairs travel
+    // together through packed fp32x2 FMAs.
+    constexpr int H = D / 2, F = D / 4;
+    constexpr bool MANT = !F8 && BK != 8;
+    constexpr float KSC = MANT ? static_cast<float>(1 << BK) : 1.f;
     float* cf = reinterpret_cast<float*>(ws + C::OFF_CF);
-    const int p0 = p.map.Ts[row_of(p.map, cur)] + ju * 32;
+    const float2* rrow = reinterpret_cast<const float2*>(st + C::BLK);  // cos/sin(p0 th_i)
     for (int i = lane; i < H; i += 32) {
-      const float2 cs = p.rope_tab[static_cast<size_t>(p0) * H + i];
+      const float2 cs = rrow[i];
       const float2 m0 = __half22float2(km[i]), m1 = __half22float2(km[i + H]);
 #pragma unroll
       for (int r = 0; r < R; ++r) {
         const float qi = os[r * D + i], qh = os[r * D + i + H];
         const float ui = fmaf(qi, cs.x, qh * cs.y);   // q'_i
         const float uh = fmaf(qh, cs.x, -qi * cs.y);  // q'_{i+H}
-        float* c = cf + (r * H + i) * 8;
-        *reinterpret_cast<float4*>(c) =
-            make_float4(ui * m0.x, uh * m1.x, fmaf(ui, m0.y, uh * m1.y), uh * m0.x);
-        *reinterpret_cast<float2*>(c + 4) = make_float2(ui * m1.x, fmaf(uh, m0.y, -ui * m1.y));
+        const float al = ui * m0.x * KSC, be = uh * m1.x * KSC;
+        const float ga = uh * m0.x * KSC, de = -ui * m1.x * KSC;
+        float ze = fmaf(ui, m0.y, uh * m1.y), et = fmaf(uh, m0.y, -ui * m1.y);
+        if constexpr (MANT) {
+          ze -= al + be;
+          et -= ga + de;
+        }
+        float* c = cf + (r * F + (i >> 1)) * 12 + (i & 1);
+        c[0] = al;
+        c[2] = be;
+        c[4] = ze;
+        c[6] = ga;
+        c[8] = de;
+        c[10] = et;
       }
     }
     __syncwarp();
@@ -829,39 +855,57 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
           kr[ww * 4 + tq] = kc[((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)];
         }
     }
-    // bit of the 2-bit field of (row half hr, pi = 2 (ks % 2) + kh)
-    int sh2[4];
+    // right rotation that brings the code field of (e, row half hr,
+    // pi = 2 (ks % 2) + kh) to the mantissa bits [23 - BK, 23)
+    int rot[2][4];
 #pragma unroll
-    for (int pi = 0; pi < 4; ++pi) sh2[pi] = hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0);
-    auto kcode = [&](int d) -> uint32_t {
+    for (int e = 0; e < 2; ++e)
+#pragma unroll
+      for (int pi = 0; pi < 4; ++pi) {
+        const int bit = BK == 2 ? 16 * e + (hr ? 2 + 2 * pi : (pi ? 8 + 2 * pi : 0))
+                                : 16 * e + 8 * (pi & 1) + 4 * hr;
+        rot[e][pi] = (bit - (23 - BK)) & 31;
+      }
+    // the code of channel d as a float: 1 + c 2^-BK (MANT), else its value
+    auto kval = [&](int d) -> float {
       const int ks = d >> 4, kh = (d >> 3) & 1, tq = (d >> 1) & 3, e = d & 1;
       if constexpr (BK == 2) {
-        return (kr[(ks >> 1) * 4 + tq] >> (16 * e + sh2[2 * (ks & 1) + kh])) & 3u;
+        const uint32_t w = kr[(ks >> 1) * 4 + tq];
+        return __uint_as_float((__funnelshift_r(w, w, rot[e][2 * (ks & 1) + kh]) & (3u << 21)) |
+                               0x3F800000u);
       } else if constexpr (BK == 4) {
-        return (kr[ks * 4 + tq] >> (16 * e + 8 * kh + 4 * hr)) & 15u;
+        const uint32_t w = kr[ks * 4 + tq];
+        return __uint_as_float((__funnelshift_r(w, w, rot[e][kh]) & (15u << 19)) | 0x3F800000u);
       } else {
         const int w = 2 * (mt * KS + ks) + kh;
         const uint8_t* kb = reinterpret_cast<const uint8_t*>(kc);
-        return kb[(((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)) * 4 + 2 * hr + e];
+        return code_value<F8>(kb[(((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)) * 4 + 2 * hr + e]);
       }
     };
-    float sc[R];
+    float2 sc2[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r) sc[r] = 0.f;
+    for (int r = 0; r < R; ++r) sc2[r] = make_float2(0.f, 0.f);
+    const float4* cf4 = reinterpret_cast<const float4*>(cf);
 #pragma unroll
-    for (int i = 0; i < H; ++i) {
-      const float c0 = code_value<F8>(kcode(i));
-      const float c1 = code_value<F8>(kcode(i + H));
-      const float2 cs = cs_tab[i * 32 + lane];
+    for (int f = 0; f < F; ++f) {
+      const float2 x0 = make_float2(kval(2 * f), kval(2 * f + 1));
+      const float2 x1 = make_float2(kval(2 * f + H), kval(2 * f + 1 + H));
+      const float4 cs = cs_tab[f * 32 + lane];
 #pragma unroll
       for (int r = 0; r < R; ++r) {
-        const float4 ab = *reinterpret_cast<const float4*>(cf + (r * H + i) * 8);
-        const float2 gh = *reinterpret_cast<const float2*>(cf + (r * H + i) * 8 + 4);
-        const float A = fmaf(ab.x, c0, fmaf(ab.y, c1, ab.z));
-        const float B = fmaf(ab.w, c0, fmaf(-gh.x, c1, gh.y));
-        sc[r] = fmaf(cs.x, A, fmaf(cs.y, B, sc[r]));
+        const float4 c0 = cf4[(r * F + f) * 3];      // al, be
+        const float4 c1 = cf4[(r * F + f) * 3 + 1];  // ze, ga
+        const float4 c2 = cf4[(r * F + f) * 3 + 2];  // de, et
+        const float2 A = __ffma2_rn(make_float2(c0.x, c0.y), x0,
+                                    __ffma2_rn(make_float2(c0.z, c0.w), x1, make_float2(c1.x, c1.y)));
+        const float2 B = __ffma2_rn(make_float2(c1.z, c1.w), x0,
+                                    __ffma2_rn(make_float2(c2.x, c2.y), x1, make_float2(c2.z, c2.w)));
+        sc2[r] = __ffma2_rn(make_float2(cs.x, cs.y), A, __ffma2_rn(make_float2(cs.z, cs.w), B, sc2[r]));
       }
     }
+    float sc[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) sc[r] = sc2[r].x + sc2[r].y;
     float mx[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) mx[r] = warp_max(sc[r]);
