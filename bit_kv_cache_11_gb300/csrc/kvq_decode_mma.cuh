@@ -175,7 +175,9 @@ struct MmaCfg {
   // RoPE stages also carry the cos/sin row (D/2 float2) of the block's first
   // position, copied with the block.
   static constexpr int STAGE = BLK + (OUT ? 8 * kMaxOut : 0) + (ROPE ? 4 * D : 0);
-  static constexpr int NS = ROPE ? 2 : (STAGE <= 4096 ? 3 : 2);
+  // Two stages where shared memory would otherwise limit the CTAs per SM
+  // (RoPE tables, four or more query heads): more resident warps instead.
+  static constexpr int NS = (ROPE || R >= 4) ? 2 : (STAGE <= 4096 ? 3 : 2);
   static constexpr int TCH = mma_tail_chunk(BK, BV);
   static constexpr int QB = R * D * 2;            // one pair's fp16 queries
   // B-operand blocks hold only the lanes whose columns exist: BL lanes

@@ -95,6 +95,21 @@ __device__ __forceinline__ uint32_t code_of(float x, const Stat& st, float top) 
   return __float_as_uint(r + 8388608.0f) & 0xffu;  // exact: r is an integer in [0, 255]
 }
 
+// code_of for two elements at once (packed fp32x2 subtract and multiply),
+// each with its own minimum, reciprocal and step; the codes come back at
+// bits 0 and 16.
+__device__ __forceinline__ uint32_t code_pair(float2 x, float4 st, float2 s, float top) {
+  const float2 d = __fadd2_rn(x, make_float2(-st.x, -st.y));
+  const float2 q = __fmul2_rn(d, make_float2(st.z, st.w));
+  float r0 = rintf(q.x), r1 = rintf(q.y);
+  const float2 t = __fadd2_rn(q, make_float2(-r0, -r1));
+  if (fabsf(t.x) > 0.5f - 0.000244140625f) r0 = rintf(__fdiv_rn(d.x, s.x));
+  if (fabsf(t.y) > 0.5f - 0.000244140625f) r1 = rintf(__fdiv_rn(d.y, s.y));
+  const float2 m = __fadd2_rn(make_float2(fminf(r0, top), fminf(r1, top)),
+                              make_float2(8388608.0f, 8388608.0f));
+  return (__float_as_uint(m.x) & 0xffu) | ((__float_as_uint(m.y) & 0xffu) << 16);
+}
+
 // Row jc of pair p's combined sequence (its row's tail rows, then the new
 // tokens that follow the sink window's share), K or V.
 __device__ __forceinline__ const __half* combined_row(const QuantParams& q, const QuantRow& r,
@@ -266,6 +281,105 @@ __device__ void select_outliers(const __half* X, int XP, int G, int D, int n, ui
 }
 
 // CTA x of pair p, whose row record is `row` (see QuantParams).
+// Steps 2 and 3 for the pages' geometry (keys per channel, values per token,
+// G = 32, fragment order on both sides, 2- or 4-bit codes, no outliers):
+//   2. statistics only: thread c < D/2 takes key channels 2c, 2c+1 (fp16
+//      min/max over the 32 rows), the next 32 * D/32 threads one value group
+//      each; {min, 1/step} and the step go to shared memory, {scale, zero}
+//      to the block;
+//   3. one thread per output word computes its codes straight from the fp16
+//      tile, two at a time (code_pair), and stores the word: no byte tile.
+// The codes equal code_of's, element by element.
+template <int BK, int BV>
+__device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv, float* sts,
+                                              uint32_t* kc, __half2* kmeta, uint32_t* vc,
+                                              __half2* vmeta, int D) {
+  constexpr int G = 32;
+  const int XP = xpitch(D);
+  const int tid = threadIdx.x;
+  const int NG = D / G;
+  float4* kst = reinterpret_cast<float4*>(sts);   // [D/2] {mn, mn', rcp, rcp'}
+  float2* kss = reinterpret_cast<float2*>(kst + D / 2);          // [D/2] {s, s'}
+  float4* vst = reinterpret_cast<float4*>(kss + D / 2);          // [NG][16]
+  float2* vss = reinterpret_cast<float2*>(vst + NG * 16);        // [NG][16]
+  if (tid < D / 2) {
+    const __half2* col = reinterpret_cast<const __half2*>(xk) + tid;
+    __half2 lo = col[0], hi = lo;
+    for (int j = 1; j < G; ++j) {
+      const __half2 h = col[j * (XP / 2)];
+      lo = __hmin2(lo, h);
+      hi = __hmax2(hi, h);
+    }
+    const Stat a = stat_of(__low2float(lo), __low2float(hi), BK, false, kmeta + 2 * tid);
+    const Stat b = stat_of(__high2float(lo), __high2float(hi), BK, false, kmeta + 2 * tid + 1);
+    kst[tid] = make_float4(a.mn, b.mn, a.rcp, b.rcp);
+    kss[tid] = make_float2(a.s, b.s);
+  } else if (tid < D / 2 + G * NG) {
+    const int u = tid - D / 2, j = u & (G - 1), g = u >> 5;
+    const __half* row = xv + j * XP + g * G;
+    __half2 lo = *reinterpret_cast<const __half2*>(row), hi = lo;
+#pragma unroll
+    for (int i = 0; i < G; i += 8) {
+      const uint4 v = *reinterpret_cast<const uint4*>(row + i);
+      const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        lo = __hmin2(lo, h[k]);
+        hi = __hmax2(hi, h[k]);
+      }
+    }
+    const Stat st = stat_of(fminf(__low2float(lo), __high2float(lo)),
+                            fmaxf(__low2float(hi), __high2float(hi)), BV, false, vmeta + j * NG + g);
+    float* f = reinterpret_cast<float*>(vst + g * 16 + (j >> 1));
+    f[j & 1] = st.mn;
+    f[2 + (j & 1)] = st.rcp;
+    reinterpret_cast<float*>(vss + g * 16 + (j >> 1))[j & 1] = st.s;
+  }
+  __syncthreads();
+
+  const float topk = static_cast<float>((1 << BK) - 1), topv = static_cast<float>((1 << BV) - 1);
+  const int nk = D * BK, nv = D * BV;  // words per side
+  for (int w = tid; w < nk + nv; w += blockDim.x) {
+    const bool isv = w >= nk;
+    const int wi = isv ? w - nk : w;
+    const int l = (wi >> 2) & 31, lw = ((wi >> 7) << 2) | (wi & 3);
+    const int g = l >> 2, t = l & 3;
+    const int bits = isv ? BV : BK;
+    const int cols = isv ? G : D;         // tile columns: K channels, V tokens
+    const int kpr = bits == 2 ? cols >> 5 : cols >> 4;  // lane words per 16 tile rows
+    const int mt = lw / kpr, kk = lw - mt * kpr;
+    const int r0 = 16 * mt + g, r1 = r0 + 8;  // tile rows: K tokens, V channels
+    uint32_t word = 0;
+#pragma unroll
+    for (int sl = 0; sl < 4; ++sl) {
+      if (bits == 4 && sl >= 2) break;
+      // slot sl: k-step and half, bit offsets of rows r0 and r1
+      const int ks = bits == 2 ? 2 * kk + (sl >> 1) : kk;
+      const int kh = bits == 2 ? (sl & 1) : sl;
+      const int b0 = bits == 2 ? (sl ? 8 + 2 * sl : 0) : 8 * sl;
+      const int b1 = bits == 2 ? 2 + 2 * sl : 8 * sl + 4;
+      const int col = 16 * ks + 8 * kh + 2 * t;
+      if (!isv) {
+        const float4 st = kst[col >> 1];
+        const float2 ss = kss[col >> 1];
+        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(xk + r0 * XP + col));
+        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(xk + r1 * XP + col));
+        word |= code_pair(a, st, ss, topk) << b0;
+        word |= code_pair(b, st, ss, topk) << b1;
+      } else {
+        const int gv = r0 >> 5;  // rows r0 and r1 share a channel group
+        const float4 st = vst[gv * 16 + (col >> 1)];
+        const float2 ss = vss[gv * 16 + (col >> 1)];
+        const float2 a = make_float2(__half2float(xv[col * XP + r0]), __half2float(xv[(col + 1) * XP + r0]));
+        const float2 b = make_float2(__half2float(xv[col * XP + r1]), __half2float(xv[(col + 1) * XP + r1]));
+        word |= code_pair(a, st, ss, topv) << b0;
+        word |= code_pair(b, st, ss, topv) << b1;
+      }
+    }
+    (isv ? vc : kc)[wi] = word;
+  }
+}
+
 template <int BK, int BV>
 __device__ __forceinline__ void quantize_block(const QuantParams& q, const QuantRow& row, int x,
                                                int p) {
@@ -329,6 +443,14 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
                  (static_cast<size_t>(p) * q.g.NB + row.first_block + x) * q.g.block_bytes;
   __half2* kmeta = reinterpret_cast<__half2*>(blk + q.g.off_km);
   __half2* vmeta = reinterpret_cast<__half2*>(blk + q.g.off_vm);
+
+  if constexpr (BK != 8 && BV != 8) {
+    if (q.g.frag_k && q.g.frag_v && nout == 0) {
+      quantize_frag<BK, BV>(xk, xv, reinterpret_cast<float*>(kcode), reinterpret_cast<uint32_t*>(blk),
+                            kmeta, reinterpret_cast<uint32_t*>(blk + q.g.off_vc), vmeta, D);
+      return;
+    }
+  }
 
   // 1b. dense-and-sparse isolation: the nout elements of largest magnitude
   //     of each side are kept apart (skip masks) and stored as entries
