@@ -369,17 +369,20 @@ def decode_roofline(torch, kvq, w, caches, qs, outs, stream, n_regions=64):
 
 
 def variant_leg(torch, kvq, w, dev, stream, n_layers, steps, n_sink=0, residual=0, fp8=False,
-                lengths=None):
+                lengths=None, n_outliers=0):
     """The decode step on a variant of the cache: fp16 windows (the first
     n_sink tokens and `residual` recent tokens kept in fp16), the FP8 (E4M3)
-    format (w with 8-bit sides), or a ragged batch (row b holds lengths[b]
-    tokens).  Algorithmic bytes count sink rows like tail rows, per row.  The
-    decode kernel is timed as regions of one kvq_decode_attention per layer."""
+    format (w with 8-bit sides), a ragged batch (row b holds lengths[b]
+    tokens), or dense-and-sparse blocks (n_outliers kept per block side).
+    Algorithmic bytes count sink rows like tail rows, per row, and the
+    outlier sections (8 n bytes per block).  The decode kernel is timed as
+    regions of one kvq_decode_attention per layer."""
     caches, qs = [], []
     for layer in range(n_layers):
         seed = rank_seed(w.config_id, 0, layer) + 7
         case = synth.make_case(w, seed=seed)
-        c = make_cache(kvq, w, w.T + 32, n_sink=n_sink, residual=residual, fp8=fp8)
+        c = make_cache(kvq, w, w.T + 32, n_sink=n_sink, residual=residual, fp8=fp8,
+                       n_outliers=n_outliers)
         if lengths is None:
             c.prefill(torch.from_numpy(case["K"]).to(dev), torch.from_numpy(case["V"]).to(dev))
         else:
@@ -398,6 +401,7 @@ def variant_leg(torch, kvq, w, dev, stream, n_layers, steps, n_sink=0, residual=
     for b in range(w.batch):
         ts, tq, tt, _ = caches[0].row_state(b)
         nb += decode_bytes(w.with_(batch=1), tq, tt + ts)
+        nb += w.n_kv_heads * (tq // w.group) * 8 * n_outliers
     for c in caches:
         c.check()
         c.close()
@@ -408,10 +412,12 @@ def variant_leg(torch, kvq, w, dev, stream, n_layers, steps, n_sink=0, residual=
         name = w.name.replace("-2bit", "-fp8")
     elif lengths is not None:
         name = w.name.replace("-t4113", f"-ragged-t{min(lengths)}..{max(lengths)}")
+    elif n_outliers:
+        name = f"{w.name}-outliers{n_outliers}"
     else:
         name = f"{w.name}-sink{n_sink}-res{residual}"
     return {"workload": name, "n_sink": n_sink, "residual": residual, "fp8": fp8,
-            "lengths": lengths, "GB/s": gbs, "frac": gbs / peak, "peak_source": f"hbm_gbs of {src}",
+            "lengths": lengths, "n_outliers": n_outliers, "GB/s": gbs, "frac": gbs / peak, "peak_source": f"hbm_gbs of {src}",
             "bytes_per_launch": nb, **sp}
 
 
@@ -714,6 +720,7 @@ def run_gpu(args, w):
                                   fp8=True)
         rag = [int(x) for x in np.linspace(1024, w.T, w.batch)]
         legs["ragged"] = variant_leg(torch, kvq, w, dev, stream, L, 16, lengths=rag)
+        legs["outliers"] = variant_leg(torch, kvq, w, dev, stream, L, 16, n_outliers=32)
         legs["rope"] = rope_leg(torch, kvq, dev, stream)
         legs["long_context"] = long_context_leg(torch, kvq, dev, stream, case4)
         legs["sweep"] = sweep_leg(torch, kvq, dev, stream)

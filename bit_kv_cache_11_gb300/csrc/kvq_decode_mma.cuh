@@ -233,50 +233,13 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
   const int gw = blockIdx.x * kDecodeWarps + warp;
-  // Launched as a programmatic dependent: wait until the preceding grid in
-  // the stream has completed (and its writes are visible) before touching
-  // global memory, and let the next grid launch while this one runs.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // RoPE: cos/sin(j * theta_i) for the 32 token offsets of a sub-block (table
-  // rows 0..31), transposed so lane j reads its own column conflict-free, two
-  // frequency pairs per entry.  Loaded before any warp of the CTA can leave.
-  float4* cs_tab = reinterpret_cast<float4*>(smem + kDecodeWarps * C::WARP_BYTES);
-  if constexpr (ROPE) {
-    for (int idx = threadIdx.x; idx < (D / 4) * 32; idx += blockDim.x) {
-      const int f = idx >> 5, j = idx & 31;
-      const bool in = j < p.rope_rows;
-      const float2 a = in ? p.rope_tab[static_cast<size_t>(j) * (D / 2) + 2 * f] : make_float2(1.f, 0.f);
-      const float2 b = in ? p.rope_tab[static_cast<size_t>(j) * (D / 2) + 2 * f + 1] : make_float2(1.f, 0.f);
-      cs_tab[idx] = make_float4(a.x, b.x, a.y, b.y);
-    }
-    __syncthreads();
-  }
-  // Fused append: store the new tokens into the tail for later calls (no
-  // access of this launch reads those tail rows).
-  if (p.n_new > 0) {
-    const int n_new = p.n_new;
-    const long long chunks = static_cast<long long>(p.g.P) * n_new * (D / 8);
-    for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
-         c += static_cast<long long>(gridDim.x) * blockDim.x) {
-      const long long rowi = c / (D / 8);
-      const int col = static_cast<int>(c - rowi * (D / 8)) * 8;
-      const long long pr = rowi / n_new;
-      const int r = static_cast<int>(rowi - pr * n_new);
-      const int b = row_of(p.map, pr);
-      const int buf = static_cast<int>((p.act >> b) & 1ull);
-      const size_t dst = (static_cast<size_t>(pr) * p.g.TC + (p.map.Tt[b] - n_new) + r) * D + col;
-      *reinterpret_cast<uint4*>(p.ktail[buf] + dst) =
-          *reinterpret_cast<const uint4*>(p.knew + rowi * D + col);
-      *reinterpret_cast<uint4*>(p.vtail[buf] + dst) =
-          *reinterpret_cast<const uint4*>(p.vnew + rowi * D + col);
-    }
-  }
-  if (gw >= p.n_warps) return;
-  // ---- this warp's units [ua, ub)
-  int ua, ub;
-  warp_units(p.map, gw, &ua, &ub);
-  if (ua >= ub) return;
+  // Everything up to griddepcontrol.wait below touches no global memory, so
+  // it runs while the preceding grid in the stream finishes: this warp's
+  // units [ua, ub), its barriers, load cursor and per-lane constants.
+  int ua = 0, ub = 0;
+  if (gw < p.n_warps) warp_units(p.map, gw, &ua, &ub);
+  const bool active = ua < ub;
+  if (!active) ua = ub = 0;
 
   uint8_t* ws = smem + warp * C::WARP_BYTES;
   uint64_t* bars = reinterpret_cast<uint64_t*>(ws + C::OFF_BAR);
@@ -366,11 +329,6 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
       }
     }
   };
-  for (int s = 0; s < NS && lu < ub; ++s) {
-    if (lane == 0) issue(s);
-    advance_load();
-  }
-
   // ---- per-lane constants of the B operands
   // Keys: channel pairs P = lane + 32 i (k-step ks = P >> 3, register
   // rg = (P >> 2) & 1, lane slot t); channels kch[i], kch[i] + 1.
@@ -401,6 +359,51 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   static_assert(BL == 32 || BSTR >= BL + 4, "padding slots for the lanes beyond BL");
   const int blane = lane < BL ? lane : BL + (lane & 3);
   __syncwarp();
+
+  // Launched as a programmatic dependent: wait until the preceding grid in
+  // the stream has completed (and its writes are visible) before touching
+  // global memory, and let the next grid launch while this one runs.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // RoPE: cos/sin(j * theta_i) for the 32 token offsets of a sub-block (table
+  // rows 0..31), transposed so lane j reads its own column conflict-free, two
+  // frequency pairs per entry.  Loaded before any warp of the CTA can leave.
+  float4* cs_tab = reinterpret_cast<float4*>(smem + kDecodeWarps * C::WARP_BYTES);
+  if constexpr (ROPE) {
+    for (int idx = threadIdx.x; idx < (D / 4) * 32; idx += blockDim.x) {
+      const int f = idx >> 5, j = idx & 31;
+      const bool in = j < p.rope_rows;
+      const float2 a = in ? p.rope_tab[static_cast<size_t>(j) * (D / 2) + 2 * f] : make_float2(1.f, 0.f);
+      const float2 b = in ? p.rope_tab[static_cast<size_t>(j) * (D / 2) + 2 * f + 1] : make_float2(1.f, 0.f);
+      cs_tab[idx] = make_float4(a.x, b.x, a.y, b.y);
+    }
+    __syncthreads();
+  }
+  // Fused append: store the new tokens into the tail for later calls (no
+  // access of this launch reads those tail rows).
+  if (p.n_new > 0) {
+    const int n_new = p.n_new;
+    const long long chunks = static_cast<long long>(p.g.P) * n_new * (D / 8);
+    for (long long c = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; c < chunks;
+         c += static_cast<long long>(gridDim.x) * blockDim.x) {
+      const long long rowi = c / (D / 8);
+      const int col = static_cast<int>(c - rowi * (D / 8)) * 8;
+      const long long pr = rowi / n_new;
+      const int r = static_cast<int>(rowi - pr * n_new);
+      const int b = row_of(p.map, pr);
+      const int buf = static_cast<int>((p.act >> b) & 1ull);
+      const size_t dst = (static_cast<size_t>(pr) * p.g.TC + (p.map.Tt[b] - n_new) + r) * D + col;
+      *reinterpret_cast<uint4*>(p.ktail[buf] + dst) =
+          *reinterpret_cast<const uint4*>(p.knew + rowi * D + col);
+      *reinterpret_cast<uint4*>(p.vtail[buf] + dst) =
+          *reinterpret_cast<const uint4*>(p.vnew + rowi * D + col);
+    }
+  }
+  if (!active) return;
+  for (int s = 0; s < NS && lu < ub; ++s) {
+    if (lane == 0) issue(s);
+    advance_load();
+  }
 
   // ---- state of the current pair
   float qf[R][KP][2];    // q * scale * log2(e) * 2^klog of this lane's key channels
@@ -560,24 +563,28 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
 
   auto k_mma = [&](const uint8_t* st, float (&sc)[2][NT][4]) {
     const uint32_t* kc = reinterpret_cast<const uint32_t*>(st);
-    // ---- scores: tokens 16*mt + g (c0,c1) and 16*mt + g + 8 (c2,c3)
+    // ---- scores: tokens 16*mt + g (c0,c1) and 16*mt + g + 8 (c2,c3); even
+    // and odd k-steps accumulate apart (four independent mma chains), then add
+    float sa[2][2][NT][4];
 #pragma unroll
     for (int a = 0; a < 2; ++a)
 #pragma unroll
-      for (int b = 0; b < NT; ++b)
+      for (int h = 0; h < 2; ++h)
 #pragma unroll
-        for (int k = 0; k < 4; ++k) sc[a][b][k] = 0.f;
+        for (int b = 0; b < NT; ++b)
+#pragma unroll
+          for (int k = 0; k < 4; ++k) sa[a][h][b][k] = 0.f;
     if constexpr (BK == 8) {
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
+        for (int mt = 0; mt < 2; ++mt) {
           uint32_t a0, a1, a2, a3;
           frag_a8<F8>(words8<KS>(kc, mt, ks, lane), a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const uint2 b = kbv[(ks * NT + nt) * BSTR + blane];
-            mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+            mma_16816(sa[mt][ks & 1][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
     } else {
@@ -588,19 +595,25 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
         kw[4 * q] = x.x; kw[4 * q + 1] = x.y; kw[4 * q + 2] = x.z; kw[4 * q + 3] = x.w;
       }
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
+        for (int mt = 0; mt < 2; ++mt) {
           uint32_t a0, a1, a2, a3;
           if constexpr (BK == 2) frag_a2(kw[mt * (KS / 2) + (ks >> 1)], ks & 1, a0, a1, a2, a3);
           else frag_a4(kw[mt * KS + ks], a0, a1, a2, a3);
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
             const uint2 b = kbv[(ks * NT + nt) * BSTR + blane];
-            mma_16816(sc[mt][nt], a0, a1, a2, a3, b.x, b.y);
+            mma_16816(sa[mt][ks & 1][nt], a0, a1, a2, a3, b.x, b.y);
           }
         }
     }
+#pragma unroll
+    for (int a = 0; a < 2; ++a)
+#pragma unroll
+      for (int b = 0; b < NT; ++b)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) sc[a][b][k] = sa[a][0][b][k] + sa[a][1][b][k];
   };
 
   // Scores -> weights of the block (lazy maximum), stored in pb with each
