@@ -173,7 +173,7 @@ struct kvq_cache {
   Derived dv;
   int device;
   int sm_count;
-  int decode_ctas_per_sm;
+  int decode_warps_per_sm;  // resident warps of the decode kernel per SM
   DecodeOps ops;
   uint8_t* blocks;
   __half* ktail[2];
@@ -372,12 +372,12 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   if (cudaGetDevice(&c->device) != cudaSuccess ||
       cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device) !=
           cudaSuccess ||
-      ops.prepare(&c->decode_ctas_per_sm) != cudaSuccess || prepare_quantize() != cudaSuccess) {
+      ops.prepare(&c->decode_warps_per_sm) != cudaSuccess || prepare_quantize() != cudaSuccess) {
     cudaGetLastError();
     delete c;
     return KVQ_ERR_CUDA;
   }
-  if (c->decode_ctas_per_sm < 1) {
+  if (c->decode_warps_per_sm < 1) {
     delete c;
     return KVQ_ERR_UNSUPPORTED;
   }
@@ -562,7 +562,7 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   m.rows = nr;
   int max_upp = 0;
   for (int b = 0; b < nr; ++b) max_upp = std::max(max_upp, units_of_row(m, b));
-  long long target = static_cast<long long>(c->sm_count) * c->decode_ctas_per_sm * kDecodeWarps;
+  long long target = static_cast<long long>(c->sm_count) * c->decode_warps_per_sm;
   if (target > kMaxDecodeWarps) target = kMaxDecodeWarps;
   // Leaving a pair (its partial, the merge, the next pair's query and its
   // fp16 tail units) costs the tensor-core kernel about kPairCost units of

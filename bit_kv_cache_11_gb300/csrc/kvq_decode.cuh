@@ -460,13 +460,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
 
 // Host-side entry points of one instantiation.
 template <int D, int BK, int BV, int R, bool F8 = false>
-cudaError_t decode_prepare(int* ctas_per_sm) {
+cudaError_t decode_prepare(int* warps_per_sm) {
   using C = DecodeCfg<D, BK, BV, R>;
   cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D, BK, BV, R, F8>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, decode_split_kernel<D, BK, BV, R, F8>, kDecodeWarps * 32, C::SMEM);
+  int ctas = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &ctas, decode_split_kernel<D, BK, BV, R, F8>, kDecodeWarps * 32, C::SMEM);
+  *warps_per_sm = ctas * kDecodeWarps;
+  return e;
 }
 
 template <int D, int BK, int BV, int R, bool F8 = false>
@@ -478,7 +481,7 @@ cudaError_t decode_launch(const DecodeParams& p, cudaStream_t stream) {
 }
 
 struct DecodeOps {
-  cudaError_t (*prepare)(int* ctas_per_sm);
+  cudaError_t (*prepare)(int* warps_per_sm);  // opt-ins; resident warps per SM
   cudaError_t (*launch)(const DecodeParams& p, cudaStream_t stream);
 };
 

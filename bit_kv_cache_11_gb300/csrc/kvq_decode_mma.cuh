@@ -205,7 +205,11 @@ struct MmaCfg {
   static constexpr int OFF_VX = OFF_KX + (OUT ? R * 32 * 4 : 0);
   static constexpr int WARP_BYTES = round_up(OFF_VX + (OUT ? R * D * 4 : 0), 128);
   static constexpr int CS_BYTES = ROPE ? (D / 4) * 32 * 16 : 0;
-  static constexpr int SMEM = kDecodeWarps * WARP_BYTES + CS_BYTES;
+  // Warps per CTA, and CTAs per SM the registers allow (the register budget
+  // per thread is 65536 / (32 NW MINB)).
+  static constexpr int NW = 4;
+  static constexpr int MINB = R <= 4 ? 3 : 1;
+  static constexpr int SMEM = NW * WARP_BYTES + CS_BYTES;
   static_assert(2 * TCH * D * 2 == BLK, "a tail chunk fills a block's stage");
   static_assert(!(OUT && ROPE), "outlier corrections are applied to post-RoPE keys");
   static_assert(KWL % 4 == 0, "lane words are read as 16-byte vectors");
@@ -221,7 +225,8 @@ __host__ __device__ constexpr int bcol(int n) {
 }
 
 template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false, bool OUT = false>
-__global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (R <= 4 ? 3 : 1))
+__global__ void __launch_bounds__(MmaCfg<D, BK, BV, R, ROPE, OUT>::NW * 32,
+                                  MmaCfg<D, BK, BV, R, ROPE, OUT>::MINB)
     decode_mma_kernel(const __grid_constant__ DecodeParams p) {
   using C = MmaCfg<D, BK, BV, R, ROPE, OUT>;
   constexpr int NS = C::NS, NT = C::NT, NG = C::NG, MTV = C::MTV, CPL = C::CPL, TCH = C::TCH,
@@ -232,10 +237,11 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
-  const int gw = blockIdx.x * kDecodeWarps + warp;
-  // Everything up to griddepcontrol.wait below touches no global memory, so
-  // it runs while the preceding grid in the stream finishes: this warp's
-  // units [ua, ub), its barriers, load cursor and per-lane constants.
+  const int gw = blockIdx.x * C::NW + warp;
+  // Up to griddepcontrol.wait below nothing reads or writes what the
+  // preceding grid in the stream may still touch, so this runs while it
+  // finishes: this warp's units [ua, ub), its barriers, load cursor and
+  // per-lane constants.
   int ua = 0, ub = 0;
   if (gw < p.n_warps) warp_units(p.map, gw, &ua, &ub);
   const bool active = ua < ub;
@@ -368,7 +374,7 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
   // RoPE: cos/sin(j * theta_i) for the 32 token offsets of a sub-block (table
   // rows 0..31), transposed so lane j reads its own column conflict-free, two
   // frequency pairs per entry.  Loaded before any warp of the CTA can leave.
-  float4* cs_tab = reinterpret_cast<float4*>(smem + kDecodeWarps * C::WARP_BYTES);
+  float4* cs_tab = reinterpret_cast<float4*>(smem + C::NW * C::WARP_BYTES);
   if constexpr (ROPE) {
     for (int idx = threadIdx.x; idx < (D / 4) * 32; idx += blockDim.x) {
       const int f = idx >> 5, j = idx & 31;
@@ -1308,13 +1314,16 @@ __global__ void __launch_bounds__(kDecodeWarps * 32, R == 1 ? (ROPE ? 3 : 4) : (
 }
 
 template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false, bool OUT = false>
-cudaError_t decode_mma_prepare(int* ctas_per_sm) {
+cudaError_t decode_mma_prepare(int* warps_per_sm) {
   using C = MmaCfg<D, BK, BV, R, ROPE, OUT>;
   cudaError_t e = cudaFuncSetAttribute(decode_mma_kernel<D, BK, BV, R, ROPE, F8, OUT>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
   if (e != cudaSuccess) return e;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-      ctas_per_sm, decode_mma_kernel<D, BK, BV, R, ROPE, F8, OUT>, kDecodeWarps * 32, C::SMEM);
+  int ctas = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      &ctas, decode_mma_kernel<D, BK, BV, R, ROPE, F8, OUT>, C::NW * 32, C::SMEM);
+  *warps_per_sm = ctas * C::NW;
+  return e;
 }
 
 template <int D, int BK, int BV, int R, bool ROPE, bool F8 = false, bool OUT = false>
@@ -1323,8 +1332,8 @@ cudaError_t decode_mma_launch(const DecodeParams& p, cudaStream_t stream) {
   // programmatic stream serialization: the grid may start while the previous
   // kernel of the stream finishes; it waits for it before any global access
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((p.n_warps + kDecodeWarps - 1) / kDecodeWarps);
-  cfg.blockDim = dim3(kDecodeWarps * 32);
+  cfg.gridDim = dim3((p.n_warps + C::NW - 1) / C::NW);
+  cfg.blockDim = dim3(C::NW * 32);
   cfg.dynamicSmemBytes = C::SMEM;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];

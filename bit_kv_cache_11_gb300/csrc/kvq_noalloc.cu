@@ -48,7 +48,7 @@ DeviceSetup g_setup[kMaxDevices];
 struct OccEntry {
   int device;
   cudaError_t (*prepare)(int*);
-  int ctas_per_sm;
+  int warps_per_sm;
 };
 OccEntry g_occ[256];
 int g_n_occ = 0;
@@ -56,7 +56,7 @@ int g_n_occ = 0;
 // Once per device, with that device current: the scratch address and the SM
 // count.  Also the per-kernel shared-memory opt-in and occupancy, once per
 // (device, kernel).  None of these calls allocates device memory.
-kvq_status setup(int dev, const DecodeOps& ops, DeviceSetup* out, int* ctas_per_sm) {
+kvq_status setup(int dev, const DecodeOps& ops, DeviceSetup* out, int* warps_per_sm) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (dev < 0 || dev >= kMaxDevices) return KVQ_ERR_UNSUPPORTED;
   DeviceSetup& s = g_setup[dev];
@@ -73,7 +73,7 @@ kvq_status setup(int dev, const DecodeOps& ops, DeviceSetup* out, int* ctas_per_
   for (int i = 0; i < g_n_occ; ++i) {
     if (g_occ[i].device == dev && g_occ[i].prepare == ops.prepare) {
       *out = s;
-      *ctas_per_sm = g_occ[i].ctas_per_sm;
+      *warps_per_sm = g_occ[i].warps_per_sm;
       return KVQ_OK;
     }
   }
@@ -85,7 +85,7 @@ kvq_status setup(int dev, const DecodeOps& ops, DeviceSetup* out, int* ctas_per_
   if (n < 1) return KVQ_ERR_UNSUPPORTED;
   if (g_n_occ < 256) g_occ[g_n_occ++] = OccEntry{dev, ops.prepare, n};
   *out = s;
-  *ctas_per_sm = n;
+  *warps_per_sm = n;
   return KVQ_OK;
 }
 
@@ -148,8 +148,8 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     return KVQ_ERR_CUDA;
   }
   DeviceSetup ds;
-  int ctas_per_sm = 0;
-  const kvq_status ss = setup(dev, ops, &ds, &ctas_per_sm);
+  int warps_per_sm = 0;
+  const kvq_status ss = setup(dev, ops, &ds, &warps_per_sm);
   if (ss != KVQ_OK) return ss;
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -173,7 +173,7 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_config* cfg, const 
     if (cudaMemsetAsync(out, 0, static_cast<size_t>(P) * R * D * sizeof(float), st) != cudaSuccess)
       return KVQ_ERR_CUDA;
   } else {
-    long long W = static_cast<long long>(ds.sm_count) * ctas_per_sm * kDecodeWarps;
+    long long W = static_cast<long long>(ds.sm_count) * warps_per_sm;
     if (W > kMaxWarps) W = kMaxWarps;
     if (W > max_slots - P) W = max_slots - P;
     W = finish_map(map, static_cast<int>(P), 0, W);
