@@ -207,8 +207,10 @@ struct MmaCfg {
   static constexpr int CS_BYTES = ROPE ? (D / 4) * 32 * 16 : 0;
   // Warps per CTA, and CTAs per SM the registers allow (the register budget
   // per thread is 65536 / (32 NW MINB)).
-  static constexpr int NW = 4;
-  static constexpr int MINB = R <= 4 ? 3 : 1;
+  // 8-bit sides on both halves (two 9 KB stages per warp): 5 warps in each of
+  // two CTAs fill the shared memory (10 warps per SM instead of 8).
+  static constexpr int NW = (BK == 8 && BV == 8 && R == 1 && !ROPE) ? 5 : 4;
+  static constexpr int MINB = (BK == 8 && BV == 8 && R == 1 && !ROPE) ? 2 : (R <= 4 ? 3 : 1);
   static constexpr int SMEM = NW * WARP_BYTES + CS_BYTES;
   static_assert(2 * TCH * D * 2 == BLK, "a tail chunk fills a block's stage");
   static_assert(!(OUT && ROPE), "outlier corrections are applied to post-RoPE keys");

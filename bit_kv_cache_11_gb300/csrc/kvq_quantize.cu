@@ -426,16 +426,33 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
   uint8_t* vskip = kskip + G * D;
   int* osh = reinterpret_cast<int*>(vskip + G * D);
 
-  // 1. the block's rows (combined index x*G + j), 16-byte loads
+  // 1. the block's rows (combined index x*G + j), 16-byte loads; two chunks
+  // per side and thread are loaded before any is stored, so their latencies
+  // overlap (the stores could otherwise alias the next loads)
   const int chunks = G * (D / 8);
-  for (int c = tid; c < chunks; c += blockDim.x) {
-    const int j = c / (D / 8);
-    const int col = (c % (D / 8)) * 8;
-    const int jc = x * G + j;
-    *reinterpret_cast<uint4*>(xk + j * XP + col) =
-        *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, false) + col);
-    *reinterpret_cast<uint4*>(xv + j * XP + col) =
-        *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, true) + col);
+  for (int c0 = tid; c0 < chunks; c0 += 2 * blockDim.x) {
+    uint4 rk[2], rv[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c = c0 + k * blockDim.x;
+      if (c < chunks) {
+        const int j = c / (D / 8);
+        const int col = (c % (D / 8)) * 8;
+        const int jc = x * G + j;
+        rk[k] = *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, false) + col);
+        rv[k] = *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, true) + col);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c = c0 + k * blockDim.x;
+      if (c < chunks) {
+        const int j = c / (D / 8);
+        const int col = (c % (D / 8)) * 8;
+        *reinterpret_cast<uint4*>(xk + j * XP + col) = rk[k];
+        *reinterpret_cast<uint4*>(xv + j * XP + col) = rv[k];
+      }
+    }
   }
   __syncthreads();
 
