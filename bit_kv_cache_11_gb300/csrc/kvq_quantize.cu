@@ -86,11 +86,15 @@ __device__ __forceinline__ uint32_t code_fp8(float x, const Stat& st) {
 // computed as (x - mn) * (1/s): for codes below 2^9 that product is within
 // 2^-13 of the IEEE quotient, so unless it lies within 2^-12 of a rounding
 // tie both round to the same integer; near a tie the IEEE divide decides.
+// The near-tie case, out of line: a call taken only near a tie, instead of
+// an IEEE divide the compiler would predicate into every element.
+__device__ __noinline__ float tie_code(float d, float s) { return rintf(__fdiv_rn(d, s)); }
+
 __device__ __forceinline__ uint32_t code_of(float x, const Stat& st, float top) {
   const float d = __fsub_rn(x, st.mn);
   float r = rintf(__fmul_rn(d, st.rcp));
   const float t = __fsub_rn(__fmul_rn(d, st.rcp), r);
-  if (fabsf(t) > 0.5f - 0.000244140625f) r = rintf(__fdiv_rn(d, st.s));
+  if (fabsf(t) > 0.5f - 0.000244140625f) r = tie_code(d, st.s);
   r = fminf(r, top);  // d >= 0 and rcp >= 0, so r >= 0 (+0 when s == 0)
   return __float_as_uint(r + 8388608.0f) & 0xffu;  // exact: r is an integer in [0, 255]
 }
@@ -103,8 +107,10 @@ __device__ __forceinline__ uint32_t code_pair(float2 x, float4 st, float2 s, flo
   const float2 q = __fmul2_rn(d, make_float2(st.z, st.w));
   float r0 = rintf(q.x), r1 = rintf(q.y);
   const float2 t = __fadd2_rn(q, make_float2(-r0, -r1));
-  if (fabsf(t.x) > 0.5f - 0.000244140625f) r0 = rintf(__fdiv_rn(d.x, s.x));
-  if (fabsf(t.y) > 0.5f - 0.000244140625f) r1 = rintf(__fdiv_rn(d.y, s.y));
+  if (fmaxf(fabsf(t.x), fabsf(t.y)) > 0.5f - 0.000244140625f) {
+    if (fabsf(t.x) > 0.5f - 0.000244140625f) r0 = tie_code(d.x, s.x);
+    if (fabsf(t.y) > 0.5f - 0.000244140625f) r1 = tie_code(d.y, s.y);
+  }
   const float2 m = __fadd2_rn(make_float2(fminf(r0, top), fminf(r1, top)),
                               make_float2(8388608.0f, 8388608.0f));
   return (__float_as_uint(m.x) & 0xffu) | ((__float_as_uint(m.y) & 0xffu) << 16);
