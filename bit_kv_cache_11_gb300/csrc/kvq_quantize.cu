@@ -343,46 +343,57 @@ __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv
   }
   __syncthreads();
 
-  const float topk = static_cast<float>((1 << BK) - 1), topv = static_cast<float>((1 << BV) - 1);
-  const int nk = D * BK, nv = D * BV;  // words per side
-  for (int w = tid; w < nk + nv; w += blockDim.x) {
-    const bool isv = w >= nk;
-    const int wi = isv ? w - nk : w;
+  // K words (tile: 32 token rows x D channels), then V words (D channel
+  // rows x 32 tokens); bit widths are compile-time, lane words per 16 tile
+  // rows a power of two (shifts, no division)
+  constexpr float topk = static_cast<float>((1 << BK) - 1), topv = static_cast<float>((1 << BV) - 1);
+  const int lgk = (BK == 2 ? 0 : 1) + (D == 128 ? 2 : 1);  // log2(D * BK / 64)
+  constexpr int lgv = BV == 2 ? 0 : 1;
+  for (int wi = tid; wi < D * BK; wi += blockDim.x) {
     const int l = (wi >> 2) & 31, lw = ((wi >> 7) << 2) | (wi & 3);
     const int g = l >> 2, t = l & 3;
-    const int bits = isv ? BV : BK;
-    const int cols = isv ? G : D;         // tile columns: K channels, V tokens
-    const int kpr = bits == 2 ? cols >> 5 : cols >> 4;  // lane words per 16 tile rows
-    const int mt = lw / kpr, kk = lw - mt * kpr;
-    const int r0 = 16 * mt + g, r1 = r0 + 8;  // tile rows: K tokens, V channels
+    const int mt = lw >> lgk, kk = lw & ((1 << lgk) - 1);
+    const int r0 = 16 * mt + g, r1 = r0 + 8;
     uint32_t word = 0;
 #pragma unroll
-    for (int sl = 0; sl < 4; ++sl) {
-      if (bits == 4 && sl >= 2) break;
+    for (int sl = 0; sl < (BK == 2 ? 4 : 2); ++sl) {
       // slot sl: k-step and half, bit offsets of rows r0 and r1
-      const int ks = bits == 2 ? 2 * kk + (sl >> 1) : kk;
-      const int kh = bits == 2 ? (sl & 1) : sl;
-      const int b0 = bits == 2 ? (sl ? 8 + 2 * sl : 0) : 8 * sl;
-      const int b1 = bits == 2 ? 2 + 2 * sl : 8 * sl + 4;
+      const int ks = BK == 2 ? 2 * kk + (sl >> 1) : kk;
+      const int kh = BK == 2 ? (sl & 1) : sl;
+      const int b0 = BK == 2 ? (sl ? 8 + 2 * sl : 0) : 8 * sl;
+      const int b1 = BK == 2 ? 2 + 2 * sl : 8 * sl + 4;
       const int col = 16 * ks + 8 * kh + 2 * t;
-      if (!isv) {
-        const float4 st = kst[col >> 1];
-        const float2 ss = kss[col >> 1];
-        const float2 a = __half22float2(*reinterpret_cast<const __half2*>(xk + r0 * XP + col));
-        const float2 b = __half22float2(*reinterpret_cast<const __half2*>(xk + r1 * XP + col));
-        word |= code_pair(a, st, ss, topk) << b0;
-        word |= code_pair(b, st, ss, topk) << b1;
-      } else {
-        const int gv = r0 >> 5;  // rows r0 and r1 share a channel group
-        const float4 st = vst[gv * 16 + (col >> 1)];
-        const float2 ss = vss[gv * 16 + (col >> 1)];
-        const float2 a = make_float2(__half2float(xv[col * XP + r0]), __half2float(xv[(col + 1) * XP + r0]));
-        const float2 b = make_float2(__half2float(xv[col * XP + r1]), __half2float(xv[(col + 1) * XP + r1]));
-        word |= code_pair(a, st, ss, topv) << b0;
-        word |= code_pair(b, st, ss, topv) << b1;
-      }
+      const float4 st = kst[col >> 1];
+      const float2 ss = kss[col >> 1];
+      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(xk + r0 * XP + col));
+      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(xk + r1 * XP + col));
+      word |= code_pair(a, st, ss, topk) << b0;
+      word |= code_pair(b, st, ss, topk) << b1;
     }
-    (isv ? vc : kc)[wi] = word;
+    kc[wi] = word;
+  }
+  for (int wi = tid; wi < D * BV; wi += blockDim.x) {
+    const int l = (wi >> 2) & 31, lw = ((wi >> 7) << 2) | (wi & 3);
+    const int g = l >> 2, t = l & 3;
+    const int mt = lw >> lgv, kk = lw & ((1 << lgv) - 1);
+    const int r0 = 16 * mt + g, r1 = r0 + 8;
+    const int gv = r0 >> 5;  // rows r0 and r1 share a channel group
+    uint32_t word = 0;
+#pragma unroll
+    for (int sl = 0; sl < (BV == 2 ? 4 : 2); ++sl) {
+      const int ks = BV == 2 ? 2 * kk + (sl >> 1) : kk;
+      const int kh = BV == 2 ? (sl & 1) : sl;
+      const int b0 = BV == 2 ? (sl ? 8 + 2 * sl : 0) : 8 * sl;
+      const int b1 = BV == 2 ? 2 + 2 * sl : 8 * sl + 4;
+      const int col = 16 * ks + 8 * kh + 2 * t;  // token
+      const float4 st = vst[gv * 16 + (col >> 1)];
+      const float2 ss = vss[gv * 16 + (col >> 1)];
+      const float2 a = make_float2(__half2float(xv[col * XP + r0]), __half2float(xv[(col + 1) * XP + r0]));
+      const float2 b = make_float2(__half2float(xv[col * XP + r1]), __half2float(xv[(col + 1) * XP + r1]));
+      word |= code_pair(a, st, ss, topv) << b0;
+      word |= code_pair(b, st, ss, topv) << b1;
+    }
+    vc[wi] = word;
   }
 }
 
