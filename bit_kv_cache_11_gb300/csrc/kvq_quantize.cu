@@ -100,20 +100,21 @@ __device__ __forceinline__ uint32_t code_of(float x, const Stat& st, float top) 
 }
 
 // code_of for two elements at once (packed fp32x2 subtract and multiply),
-// each with its own minimum, reciprocal and step; the codes come back at
-// bits 0 and 16.
+// each with its own negated minimum (st.x, st.y), reciprocal (st.z, st.w)
+// and step; the codes come back at bits 0 and 16.
 __device__ __forceinline__ uint32_t code_pair(float2 x, float4 st, float2 s, float top) {
-  const float2 d = __fadd2_rn(x, make_float2(-st.x, -st.y));
+  const float2 d = __fadd2_rn(x, make_float2(st.x, st.y));  // x - min, exactly as __fsub_rn
   const float2 q = __fmul2_rn(d, make_float2(st.z, st.w));
   float r0 = rintf(q.x), r1 = rintf(q.y);
-  const float2 t = __fadd2_rn(q, make_float2(-r0, -r1));
+  const float2 t = __ffma2_rn(make_float2(r0, r1), make_float2(-1.f, -1.f), q);  // q - r
   if (fmaxf(fabsf(t.x), fabsf(t.y)) > 0.5f - 0.000244140625f) {
     if (fabsf(t.x) > 0.5f - 0.000244140625f) r0 = tie_code(d.x, s.x);
     if (fabsf(t.y) > 0.5f - 0.000244140625f) r1 = tie_code(d.y, s.y);
   }
   const float2 m = __fadd2_rn(make_float2(fminf(r0, top), fminf(r1, top)),
                               make_float2(8388608.0f, 8388608.0f));
-  return (__float_as_uint(m.x) & 0xffu) | ((__float_as_uint(m.y) & 0xffu) << 16);
+  // 2^23 + c has the code in byte 0 and a zero byte 1: bytes {c0, 0, c1, 0}
+  return __byte_perm(__float_as_uint(m.x), __float_as_uint(m.y), 0x1410);
 }
 
 // Row jc of pair p's combined sequence (its row's tail rows, then the new
@@ -304,7 +305,7 @@ __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv
   const int XP = xpitch(D);
   const int tid = threadIdx.x;
   const int NG = D / G;
-  float4* kst = reinterpret_cast<float4*>(sts);   // [D/2] {mn, mn', rcp, rcp'}
+  float4* kst = reinterpret_cast<float4*>(sts);   // [D/2] {-mn, -mn', rcp, rcp'}
   float2* kss = reinterpret_cast<float2*>(kst + D / 2);          // [D/2] {s, s'}
   float4* vst = reinterpret_cast<float4*>(kss + D / 2);          // [NG][16]
   float2* vss = reinterpret_cast<float2*>(vst + NG * 16);        // [NG][16]
@@ -318,7 +319,7 @@ __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv
     }
     const Stat a = stat_of(__low2float(lo), __low2float(hi), BK, false, kmeta + 2 * tid);
     const Stat b = stat_of(__high2float(lo), __high2float(hi), BK, false, kmeta + 2 * tid + 1);
-    kst[tid] = make_float4(a.mn, b.mn, a.rcp, b.rcp);
+    kst[tid] = make_float4(-a.mn, -b.mn, a.rcp, b.rcp);
     kss[tid] = make_float2(a.s, b.s);
   } else if (tid < D / 2 + G * NG) {
     const int u = tid - D / 2, j = u & (G - 1), g = u >> 5;
@@ -337,7 +338,7 @@ __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv
     const Stat st = stat_of(fminf(__low2float(lo), __high2float(lo)),
                             fmaxf(__low2float(hi), __high2float(hi)), BV, false, vmeta + j * NG + g);
     float* f = reinterpret_cast<float*>(vst + g * 16 + (j >> 1));
-    f[j & 1] = st.mn;
+    f[j & 1] = -st.mn;
     f[2 + (j & 1)] = st.rcp;
     reinterpret_cast<float*>(vss + g * 16 + (j >> 1))[j & 1] = st.s;
   }
