@@ -188,7 +188,6 @@ struct kvq_cache {
   float* lvl_o;  // two-level merge: level-2 partials
   float2* lvl_ml;
   int* tickets2; // [P*R] two-level merge counters, zero between launches
-  int* tickets1; // [P*C2max] chunk tickets of the in-kernel two-level merge
   bool mma;      // decode runs the tensor-core kernel (which can merge in place)
   uint32_t wait_limit;  // try_wait rounds of a decode kernel's bounded waits
   // Token counts per batch row: sink, quantized, tail, and the row's active
@@ -265,7 +264,6 @@ static void free_all(kvq_cache* c) {
   cudaFree(c->lvl_o);
   cudaFree(c->lvl_ml);
   cudaFree(c->tickets2);
-  cudaFree(c->tickets1);
 }
 
 // Appends to every pair of row b its n_rows[b] tokens (n_all for every row
@@ -341,7 +339,7 @@ kvq_status kvq_cache_bytes(const kvq_config* cfg, size_t* bytes) {
   if (s != KVQ_OK) return s;
   *bytes = d.blocks_bytes + 4 * d.tail_bytes + 2 * d.sink_bytes + d.rope_bytes + d.part_o_bytes +
            d.part_ml_bytes + d.lvl_o_bytes + d.lvl_ml_bytes + sizeof(int) +
-           sizeof(int) * static_cast<size_t>(d.P) * (1 + d.R + d.C2max);
+           sizeof(int) * static_cast<size_t>(d.P) * (1 + d.R);
   return KVQ_OK;
 }
 
@@ -395,7 +393,6 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   if (ok) ok = alloc_ok(&c->lvl_o, d.lvl_o_bytes);
   if (ok) ok = alloc_ok(&c->lvl_ml, d.lvl_ml_bytes);
   if (ok) ok = alloc_ok(&c->tickets2, sizeof(int) * d.P * d.R);
-  if (ok) ok = alloc_ok(&c->tickets1, sizeof(int) * d.P * d.C2max);
   if (!ok) {
     cudaGetLastError();
     free_all(c);
@@ -404,8 +401,7 @@ kvq_status kvq_create(const kvq_config* cfg, kvq_cache** out) {
   }
   bool init_ok = cudaMemset(c->err, 0, sizeof(int)) == cudaSuccess &&
                  cudaMemset(c->tickets, 0, sizeof(int) * d.P) == cudaSuccess &&
-                 cudaMemset(c->tickets2, 0, sizeof(int) * d.P * d.R) == cudaSuccess &&
-                 cudaMemset(c->tickets1, 0, sizeof(int) * d.P * d.C2max) == cudaSuccess;
+                 cudaMemset(c->tickets2, 0, sizeof(int) * d.P * d.R) == cudaSuccess;
   for (int i = 0; i < 2 && init_ok; ++i)
     init_ok = cudaMemset(c->ktail[i], 0, d.tail_bytes) == cudaSuccess &&
               cudaMemset(c->vtail[i], 0, d.tail_bytes) == cudaSuccess;
@@ -602,23 +598,12 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   p.part_ml = c->part_ml;
   p.err = c->err;
   p.wait_limit = c->wait_limit;
-  // The tensor-core kernel merges in place: in one level when every pair has
-  // few partials, in two (chunks of CS slots, then the chunks) otherwise
-  // (few pairs over many warps, e.g. one long sequence).  The CUDA-core
-  // kernel leaves its partials to the merge kernel.  A pair's costs touch at
-  // most (upp + vcost) * W / C + 2 warps.
+  // Merge in place when every pair has few partials; the separate merge
+  // kernel otherwise (few pairs over many warps, e.g. one long sequence).
+  // A pair's costs touch at most (upp + vcost) * W / C + 2 warps.
   const long long max_seg = static_cast<long long>(max_upp + m.vcost) * W / m.C + 2;
-  // chunks of CS partial slots, at most min(64, C2max) chunks per (pair, query)
-  const long long c2cap = std::min(64, d.C2max);
-  const int CS = static_cast<int>(std::max<long long>(16, (max_seg + c2cap - 1) / c2cap));
-  const int C2 = static_cast<int>((max_seg + CS - 1) / CS);
-  p.fused = c->mma ? (max_seg <= 64 ? 1 : (CS <= 64 ? 2 : 0)) : 0;
+  p.fused = (c->mma && max_seg <= 64) ? 1 : 0;
   p.tickets = c->tickets;
-  p.tickets1 = c->tickets1;
-  p.lvl_o = c->lvl_o;
-  p.lvl_ml = c->lvl_ml;
-  p.CS = CS;
-  p.C2 = C2;
   p.out = static_cast<float*>(out);
   if (c->ops.launch(p, st) != cudaSuccess) return KVQ_ERR_CUDA;
   if (p.fused) {
@@ -635,8 +620,9 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   mp.map = m;
   mp.R = d.R;
   mp.D = d.D;
-  mp.CS = CS;
-  mp.C2 = C2;
+  // chunks of CS partial slots, at most C2max chunks per (pair, query)
+  mp.CS = static_cast<int>(std::max<long long>(16, (max_seg + d.C2max - 1) / d.C2max));
+  mp.C2 = static_cast<int>((max_seg + mp.CS - 1) / mp.CS);
   if (launch_merge2(mp, d.P, st) != cudaSuccess) return KVQ_ERR_CUDA;
   g_launches.fetch_add(2);
   return KVQ_OK;
@@ -770,7 +756,6 @@ kvq_status kvq_check_device_error(kvq_cache* c, void* stream) {
     // A warp that gave up left its pair's ticket short: start clean.
     cudaMemset(c->tickets, 0, sizeof(int) * c->dv.P);
     cudaMemset(c->tickets2, 0, sizeof(int) * c->dv.P * c->dv.R);
-    cudaMemset(c->tickets1, 0, sizeof(int) * c->dv.P * c->dv.C2max);
     return KVQ_ERR_DEVICE_CHECK;
   }
   return KVQ_OK;

@@ -1092,74 +1092,6 @@ __global__ void __launch_bounds__(MmaCfg<D, BK, BV, R, ROPE, OUT>::NW * 32,
     }
   };
 
-  // Merges nseg (<= 64) partial rows of one query: row k holds o at
-  // o0 + k ostride (D floats) and {m, l} at ml0[k mlstride].  dst_ml null:
-  // dst = o / l, the output; else dst = o (unnormalised) and *dst_ml = {m, l}
-  // over the rows, a level-2 partial.  Lane i weighs rows i and i + 32; the
-  // first eight rows are loaded together with the weights (one L2 round trip).
-  auto merge_rows = [&](int nseg, const float* o0, long long ostride, const float2* ml0,
-                        long long mlstride, float* dst, float2* dst_ml) {
-    constexpr int RB = 8;
-    float v[RB][CPL];
-#pragma unroll
-    for (int u = 0; u < RB; ++u) {
-      const float* src = o0 + min(u, nseg - 1) * ostride + lane * CPL;
-      if constexpr (CPL == 4) {
-        const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
-        v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-      } else {
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) v[u][c] = __ldcg(src + c);
-      }
-    }
-    float2 a = make_float2(-INFINITY, 0.f), b = a;
-    if (lane < nseg) a = __ldcg(ml0 + lane * mlstride);
-    if (lane + 32 < nseg) b = __ldcg(ml0 + (lane + 32) * mlstride);
-    const float ms = warp_max(fmaxf(a.x, b.x));
-    const float mb = ms == -INFINITY ? 0.f : ms;  // every row empty
-    const float fa = fast_exp2(a.x - mb), fb = fast_exp2(b.x - mb);
-    const float L = warp_sum(fmaf(fa, a.y, fb * b.y));
-    float o[CPL];
-#pragma unroll
-    for (int c = 0; c < CPL; ++c) o[c] = 0.f;
-#pragma unroll
-    for (int u = 0; u < RB; ++u) {
-      const float f = __shfl_sync(0xffffffffu, fa, u);
-      if (u < nseg) {
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) o[c] = fmaf(f, v[u][c], o[c]);
-      }
-    }
-#pragma unroll 1
-    for (int wb = RB; wb < nseg; wb += 8) {
-      float x8[8][CPL];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float* src = o0 + min(wb + u, nseg - 1) * ostride + lane * CPL;
-#pragma unroll
-        for (int c = 0; c < CPL; ++c) x8[u][c] = __ldcg(src + c);
-      }
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int w = wb + u;
-        const float f = __shfl_sync(0xffffffffu, w < 32 ? fa : fb, w & 31);
-        if (w < nseg) {
-#pragma unroll
-          for (int c = 0; c < CPL; ++c) o[c] = fmaf(f, x8[u][c], o[c]);
-        }
-      }
-    }
-    if (dst_ml == nullptr) {
-      const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) dst[lane * CPL + c] = o[c] * inv;
-    } else {
-#pragma unroll
-      for (int c = 0; c < CPL; ++c) dst[lane * CPL + c] = o[c];
-      if (lane == 0) *dst_ml = make_float2(ms, L);
-    }
-  };
-
   auto write_partial = [&](int pr) {
     const long long slot = static_cast<long long>(gw) + pr;
     const float e2 = pow2i(ev);
@@ -1206,61 +1138,80 @@ __global__ void __launch_bounds__(MmaCfg<D, BK, BV, R, ROPE, OUT>::NW * 32,
     }
     __syncwarp();
     if (p.fused) {
-      // Publish this partial, take a ticket; the last warp to finish a set
-      // of partials merges it (it never waits for the others: the ticket
-      // tells it they are done).
+      // Publish this partial, take a ticket; the pair's last warp merges
+      // (it never waits for the others: the ticket tells it they are done).
       __threadfence();
       __syncwarp();
       int w0, w1;
       pair_warps(p.map, pr, &w0, &w1);
-      if (p.fused == 1) {
-        int last = 0;
-        if (lane == 0) last = atomicAdd(&p.tickets[pr], 1) == w1 - w0;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(&p.tickets[pr], 1) == w1 - w0;
+      last = __shfl_sync(0xffffffffu, last, 0);
+      if (last) {
+        __threadfence();
+        // Lane i weighs partials i and i + 32.  The first eight partial rows
+        // are loaded together with the weights (one L2 round trip).
+        const int nseg = w1 - w0 + 1;  // <= 64 when fused
+        constexpr int RB = 8;
 #pragma unroll 1
-          for (int r = 0; r < R; ++r)
-            merge_rows(w1 - w0 + 1, p.part_o + ((static_cast<long long>(w0) + pr) * R + r) * D,
-                       static_cast<long long>(R) * D,
-                       p.part_ml + (static_cast<long long>(w0) + pr) * R + r, R,
-                       p.out + (static_cast<long long>(pr) * R + r) * D, nullptr);
-          if (lane == 0) p.tickets[pr] = 0;
-        }
-      } else {
-        // Two levels: the pair's slots in chunks of CS, merged by the last
-        // warp of each chunk into a level-2 partial; the last chunk merger
-        // merges those.
-        const int k = (static_cast<int>(gw) - w0) / p.CS;
-        const int c0 = w0 + k * p.CS, c1 = min(c0 + p.CS - 1, w1);
-        const long long q0 = static_cast<long long>(pr) * R * p.C2;  // level-2 rows of the pair
-        int last = 0;
-        if (lane == 0) last = atomicAdd(&p.tickets1[static_cast<long long>(pr) * p.C2 + k], 1) == c1 - c0;
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
-#pragma unroll 1
-          for (int r = 0; r < R; ++r)
-            merge_rows(c1 - c0 + 1, p.part_o + ((static_cast<long long>(c0) + pr) * R + r) * D,
-                       static_cast<long long>(R) * D,
-                       p.part_ml + (static_cast<long long>(c0) + pr) * R + r, R,
-                       p.lvl_o + (q0 + r * p.C2 + k) * D, p.lvl_ml + q0 + r * p.C2 + k);
-          if (lane == 0) p.tickets1[static_cast<long long>(pr) * p.C2 + k] = 0;
-          __threadfence();
-          __syncwarp();
-          const int nch = (w1 - w0) / p.CS + 1;
-          int last2 = 0;
-          if (lane == 0) last2 = atomicAdd(&p.tickets[pr], 1) == nch - 1;
-          last2 = __shfl_sync(0xffffffffu, last2, 0);
-          if (last2) {
-            __threadfence();
-#pragma unroll 1
-            for (int r = 0; r < R; ++r)
-              merge_rows(nch, p.lvl_o + (q0 + r * p.C2) * D, D, p.lvl_ml + q0 + r * p.C2, 1,
-                         p.out + (static_cast<long long>(pr) * R + r) * D, nullptr);
-            if (lane == 0) p.tickets[pr] = 0;
+        for (int r = 0; r < R; ++r) {
+          float v[RB][CPL];
+#pragma unroll
+          for (int u = 0; u < RB; ++u) {
+            const long long w = w0 + min(u, nseg - 1);
+            const float* src = p.part_o + ((w + pr) * R + r) * D + lane * CPL;
+            if constexpr (CPL == 4) {
+              const float4 x = __ldcg(reinterpret_cast<const float4*>(src));
+              v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else {
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) v[u][c] = __ldcg(src + c);
+            }
           }
+          float2 a = make_float2(-INFINITY, 0.f), b = a;
+          if (lane < nseg) a = __ldcg(&p.part_ml[(w0 + lane + pr) * R + r]);
+          if (lane + 32 < nseg) b = __ldcg(&p.part_ml[(w0 + lane + 32 + pr) * R + r]);
+          const float ms = warp_max(fmaxf(a.x, b.x));
+          const float mb = ms == -INFINITY ? 0.f : ms;  // every partial empty
+          const float fa = fast_exp2(a.x - mb), fb = fast_exp2(b.x - mb);
+          const float L = warp_sum(fmaf(fa, a.y, fb * b.y));
+          float o[CPL];
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) o[c] = 0.f;
+#pragma unroll
+          for (int u = 0; u < RB; ++u) {
+            const float f = __shfl_sync(0xffffffffu, fa, u);
+            if (u < nseg) {
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) o[c] = fmaf(f, v[u][c], o[c]);
+            }
+          }
+#pragma unroll 1
+          for (int wb = RB; wb < nseg; wb += 8) {
+            float x8[8][CPL];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const long long w = w0 + min(wb + u, nseg - 1);
+              const float* src = p.part_o + ((w + pr) * R + r) * D + lane * CPL;
+#pragma unroll
+              for (int c = 0; c < CPL; ++c) x8[u][c] = __ldcg(src + c);
+            }
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+              const int w = wb + u;
+              const float f = __shfl_sync(0xffffffffu, w < 32 ? fa : fb, w & 31);
+              if (w < nseg) {
+#pragma unroll
+                for (int c = 0; c < CPL; ++c) o[c] = fmaf(f, x8[u][c], o[c]);
+              }
+            }
+          }
+          const float inv = L > 0.f ? 1.f / L : 0.f;
+          float* dst = p.out + (static_cast<long long>(pr) * R + r) * D + lane * CPL;
+#pragma unroll
+          for (int c = 0; c < CPL; ++c) dst[c] = o[c] * inv;
         }
+        if (lane == 0) p.tickets[pr] = 0;
       }
     }
   };

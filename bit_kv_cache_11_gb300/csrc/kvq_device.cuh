@@ -413,17 +413,10 @@ struct DecodeParams {
   float2* part_ml;      // [W + P][R] {m, l} (m in log2 units)
   int* err;
   uint32_t wait_limit;  // try_wait rounds of a main-loop wait (kWaitLimit normally)
-  // Fused merge (tensor-core kernel): 1 -- the last warp to finish a pair
-  // merges its partials into `out`; 2 -- the pair's slots in chunks of CS,
-  // each merged by its last warp into a level-2 partial (lvl_o, lvl_ml,
-  // C2 per pair and query), the last of those merged into `out`.  Ticket
-  // counters start and end at zero.
+  // Fused merge: the last warp to finish a pair merges its partials into
+  // `out` (ticket counters, one per pair, start and end at zero).
   int fused;
-  int* tickets;         // [P] pair tickets
-  int* tickets1;        // [P][C2] chunk tickets (fused == 2)
-  float* lvl_o;         // [P][R][C2][D] (fused == 2)
-  float2* lvl_ml;       // [P][R][C2]
-  int CS, C2;           // slots per chunk, chunks per pair (fused == 2)
+  int* tickets;         // [P]
   float* out;           // [P][R][D]
 };
 

@@ -126,7 +126,7 @@ def test_device_error_word_is_reported_and_cleared(kvq, orc):
 
 # name, G, axis_k, axis_v, T: the tensor-core kernel with its in-place merge,
 # the CUDA-core kernel with the two-level merge kernel, and a long context
-# whose pairs the tensor-core kernel merges in two levels in place
+# whose pairs go to the two-level merge in the tensor-core geometry
 WAIT_CASES = [
     ("tensor-core", 32, 0, 1, 7 * 32 + 9, 2),
     ("cuda-core", 128, 1, 0, 3 * 128 + 5, 2),
