@@ -623,6 +623,7 @@ static kvq_status enqueue_decode(kvq_cache* c, const void* q, void* out, float s
   // chunks of CS partial slots, at most C2max chunks per (pair, query)
   mp.CS = static_cast<int>(std::max<long long>(16, (max_seg + d.C2max - 1) / d.C2max));
   mp.C2 = static_cast<int>((max_seg + mp.CS - 1) / mp.CS);
+  if (mp.CS > kMerge2MaxRows || mp.C2 > kMerge2MaxRows) return KVQ_ERR_UNSUPPORTED;
   if (launch_merge2(mp, d.P, st) != cudaSuccess) return KVQ_ERR_CUDA;
   g_launches.fetch_add(2);
   return KVQ_OK;

@@ -492,6 +492,10 @@ struct MergeParams {
 // block (pair, query, chunk) merges at most CS partial slots into a level-2
 // partial; the last block of a (pair, query), found with a ticket, merges the
 // level-2 partials into the output.
+// Rows (partial slots of a chunk, or chunks of a pair) one merge2 block
+// merges at most (its shared-memory row table).
+constexpr int kMerge2MaxRows = 512;
+
 struct Merge2Params {
   const float* part_o;
   const float2* part_ml;

@@ -88,8 +88,48 @@ __global__ void merge_kernel(const MergeParams mp) {
   }
 }
 
+// Weighted sum over n rows (row k: {m, l} at ml[k mlstride], o at o0[k ostride]) of
+// this thread's channel, with the weights exp2(m_k - max m): the {m, l} go
+// through shared memory in one round of loads, the o values are loaded 16
+// rows at a time before any is used.  Returns the sum; *ms, *L the maximum
+// and the weighted l (-inf and 0 when every row is empty).
+__device__ __forceinline__ float merge_column(int n, const float2* ml, long long mlstride,
+                                              bool coherent, const float* o0, long long ostride,
+                                              float2* sml, float* ms_out, float* L_out) {
+  const int d = threadIdx.x;
+  __syncthreads();  // sml free (a previous use)
+  for (int k = d; k < n; k += blockDim.x)
+    sml[k] = coherent ? __ldcg(ml + k * mlstride) : ml[k * mlstride];
+  __syncthreads();
+  float ms = -INFINITY;
+  for (int k = 0; k < n; ++k) ms = fmaxf(ms, sml[k].x);
+  const float mb = ms == -INFINITY ? 0.f : ms;  // every row empty: weights 0
+  float L = 0.f, o = 0.f;
+  for (int k0 = 0; k0 < n; k0 += 16) {
+    float v[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      const int k = min(k0 + u, n - 1);
+      v[u] = coherent ? __ldcg(o0 + k * ostride) : o0[k * ostride];
+    }
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      if (k0 + u < n) {
+        const float2 m = sml[k0 + u];
+        const float f = exp2f(m.x - mb);
+        L = fmaf(f, m.y, L);
+        o = fmaf(f, v[u], o);
+      }
+    }
+  }
+  *ms_out = ms;
+  *L_out = L;
+  return o;
+}
+
 // grid = P * R * C2 blocks of D threads.
 __global__ void merge2_kernel(const Merge2Params mp) {
+  __shared__ float2 sml[kMerge2MaxRows];
   const int b = blockIdx.x;
   const int c = b % mp.C2;
   const int pq = b / mp.C2;
@@ -100,17 +140,11 @@ __global__ void merge2_kernel(const Merge2Params mp) {
   pair_warps(mp.map, pr, &w0, &w1);
   const long long s0 = w0 + static_cast<long long>(mp.CS) * c;
   const long long s1 = s0 + mp.CS - 1 < w1 ? s0 + mp.CS - 1 : w1;
-  float ms = -INFINITY;
-  for (long long w = s0; w <= s1; ++w) ms = fmaxf(ms, mp.part_ml[(w + pr) * mp.R + r].x);
-  // A chunk may hold only empty partials (m = -inf, l = 0): weigh them 0.
-  float mb = ms == -INFINITY ? 0.f : ms;
-  float L = 0.f, o = 0.f;
-  for (long long w = s0; w <= s1; ++w) {
-    const float2 ml = mp.part_ml[(w + pr) * mp.R + r];
-    const float f = exp2f(ml.x - mb);
-    L = fmaf(f, ml.y, L);
-    o = fmaf(f, mp.part_o[((w + pr) * mp.R + r) * mp.D + d], o);
-  }
+  // the chunk's partial slots s0 .. s1 (a chunk may hold only empty partials)
+  float ms, L;
+  const float o = merge_column(static_cast<int>(s1 - s0 + 1), mp.part_ml + (s0 + pr) * mp.R + r, mp.R,
+                               false, mp.part_o + ((s0 + pr) * mp.R + r) * mp.D + d,
+                               static_cast<long long>(mp.R) * mp.D, sml, &ms, &L);
   mp.lvl_o[static_cast<size_t>(b) * mp.D + d] = o;
   if (d == 0) mp.lvl_ml[b] = make_float2(ms, L);
   __threadfence();
@@ -121,18 +155,9 @@ __global__ void merge2_kernel(const Merge2Params mp) {
   if (!last) return;
   __threadfence();
   const size_t base = static_cast<size_t>(pq) * mp.C2;
-  ms = -INFINITY;
-  for (int k = 0; k < mp.C2; ++k) ms = fmaxf(ms, __ldcg(&mp.lvl_ml[base + k]).x);
-  mb = ms == -INFINITY ? 0.f : ms;
-  L = 0.f;
-  o = 0.f;
-  for (int k = 0; k < mp.C2; ++k) {
-    const float2 ml = __ldcg(&mp.lvl_ml[base + k]);
-    const float f = exp2f(ml.x - mb);  // 0 for an empty chunk (m = -inf)
-    L = fmaf(f, ml.y, L);
-    o = fmaf(f, __ldcg(&mp.lvl_o[(base + k) * mp.D + d]), o);
-  }
-  mp.out[(pr * mp.R + r) * mp.D + d] = L > 0.f ? o / L : 0.f;
+  const float o2 = merge_column(mp.C2, mp.lvl_ml + base, 1, true, mp.lvl_o + base * mp.D + d, mp.D,
+                                sml, &ms, &L);
+  mp.out[(pr * mp.R + r) * mp.D + d] = L > 0.f ? o2 / L : 0.f;
   if (d == 0) mp.tickets[pq] = 0;
 }
 
