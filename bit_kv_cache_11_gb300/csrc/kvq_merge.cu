@@ -136,6 +136,11 @@ __global__ void merge2_kernel(const Merge2Params mp) {
   const int r = pq % mp.R;
   const long long pr = pq / mp.R;
   const int d = threadIdx.x;
+  // Launched as a programmatic dependent of the decode grid: its blocks may
+  // become resident while that grid drains; wait for it (and its writes)
+  // before reading, and let the next grid of the stream launch meanwhile.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   int w0, w1;
   pair_warps(mp.map, pr, &w0, &w1);
   const long long s0 = w0 + static_cast<long long>(mp.CS) * c;
@@ -162,8 +167,16 @@ __global__ void merge2_kernel(const Merge2Params mp) {
 }
 
 cudaError_t launch_merge2(const Merge2Params& mp, int n_pairs, cudaStream_t stream) {
-  merge2_kernel<<<n_pairs * mp.R * mp.C2, mp.D, 0, stream>>>(mp);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_pairs * mp.R * mp.C2);
+  cfg.blockDim = dim3(mp.D);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, merge2_kernel, mp);
 }
 
 cudaError_t launch_merge(const MergeParams& mp, int n_pairs, cudaStream_t stream) {
