@@ -297,14 +297,14 @@ __device__ void select_outliers(const __half* X, int XP, int G, int D, int n, ui
 //   3. one thread per output word computes its codes straight from the fp16
 //      tile, two at a time (code_pair), and stores the word: no byte tile.
 // The codes equal code_of's, element by element.
-template <int BK, int BV>
+template <int BK, int BV, int D>
 __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv, float* sts,
                                               uint32_t* kc, __half2* kmeta, uint32_t* vc,
-                                              __half2* vmeta, int D) {
+                                              __half2* vmeta) {
   constexpr int G = 32;
-  const int XP = xpitch(D);
+  constexpr int XP = xpitch(D);
   const int tid = threadIdx.x;
-  const int NG = D / G;
+  constexpr int NG = D / G;
   float4* kst = reinterpret_cast<float4*>(sts);   // [D/2] {-mn, -mn', rcp, rcp'}
   float2* kss = reinterpret_cast<float2*>(kst + D / 2);          // [D/2] {s, s'}
   float4* vst = reinterpret_cast<float4*>(kss + D / 2);          // [NG][16]
@@ -348,9 +348,9 @@ __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv
   // rows x 32 tokens); bit widths are compile-time, lane words per 16 tile
   // rows a power of two (shifts, no division)
   constexpr float topk = static_cast<float>((1 << BK) - 1), topv = static_cast<float>((1 << BV) - 1);
-  const int lgk = (BK == 2 ? 0 : 1) + (D == 128 ? 2 : 1);  // log2(D * BK / 64)
+  constexpr int lgk = (BK == 2 ? 0 : 1) + (D == 128 ? 2 : 1);  // log2(D * BK / 64)
   constexpr int lgv = BV == 2 ? 0 : 1;
-  for (int wi = tid; wi < D * BK; wi += blockDim.x) {
+  for (int wi = tid; wi < D * BK; wi += kQuantThreads) {
     const int l = (wi >> 2) & 31, lw = ((wi >> 7) << 2) | (wi & 3);
     const int g = l >> 2, t = l & 3;
     const int mt = lw >> lgk, kk = lw & ((1 << lgk) - 1);
@@ -373,7 +373,7 @@ __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv
     }
     kc[wi] = word;
   }
-  for (int wi = tid; wi < D * BV; wi += blockDim.x) {
+  for (int wi = tid; wi < D * BV; wi += kQuantThreads) {
     const int l = (wi >> 2) & 31, lw = ((wi >> 7) << 2) | (wi & 3);
     const int g = l >> 2, t = l & 3;
     const int mt = lw >> lgv, kk = lw & ((1 << lgv) - 1);
@@ -398,12 +398,75 @@ __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv
   }
 }
 
+// combined_row with the head dimension known at compile time.
+template <int D>
+__device__ __forceinline__ const __half* combined_row_d(const QuantParams& q, const QuantRow& r,
+                                                        int p, int jc, bool isv) {
+  if (jc < r.T_t) {
+    const __half* t = isv ? (r.src ? q.vtail[1] : q.vtail[0]) : (r.src ? q.ktail[1] : q.ktail[0]);
+    return t + (static_cast<size_t>(p) * q.g.TC + jc) * D;
+  }
+  return (isv ? q.vnew : q.knew) +
+         (static_cast<size_t>(p) * q.new_stride + r.nsink + (jc - r.T_t)) * D;
+}
+
+// Block x (< row.nflush) of pair p in the pages' geometry (fragment order on
+// both sides, G = 32, 2- or 4-bit codes, no outliers), the head dimension a
+// compile-time constant: step 1 (the rows into shared memory) as in
+// quantize_block, then quantize_frag.
+template <int BK, int BV, int D>
+__device__ __forceinline__ void quantize_block_frag(const QuantParams& q, const QuantRow& row, int x,
+                                                    int p) {
+  constexpr int G = 32, XP = xpitch(D), CPR = D / 8;  // 16-byte chunks per row
+  const int tid = threadIdx.x;
+  extern __shared__ __align__(16) uint8_t smem[];
+  __half* xk = reinterpret_cast<__half*>(smem);
+  __half* xv = xk + G * XP;
+  float* sts = reinterpret_cast<float*>(xv + G * XP);
+  constexpr int chunks = G * CPR;
+  for (int c0 = tid; c0 < chunks; c0 += 2 * kQuantThreads) {
+    uint4 rk[2], rv[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c = c0 + k * kQuantThreads;
+      if (c < chunks) {
+        const int j = c / CPR, col = (c % CPR) * 8;
+        rk[k] = *reinterpret_cast<const uint4*>(combined_row_d<D>(q, row, p, x * G + j, false) + col);
+        rv[k] = *reinterpret_cast<const uint4*>(combined_row_d<D>(q, row, p, x * G + j, true) + col);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      const int c = c0 + k * kQuantThreads;
+      if (c < chunks) {
+        const int j = c / CPR, col = (c % CPR) * 8;
+        *reinterpret_cast<uint4*>(xk + j * XP + col) = rk[k];
+        *reinterpret_cast<uint4*>(xv + j * XP + col) = rv[k];
+      }
+    }
+  }
+  __syncthreads();
+  uint8_t* blk = q.g.blocks +
+                 (static_cast<size_t>(p) * q.g.NB + row.first_block + x) * q.g.block_bytes;
+  quantize_frag<BK, BV, D>(xk, xv, sts, reinterpret_cast<uint32_t*>(blk),
+                           reinterpret_cast<__half2*>(blk + q.g.off_km),
+                           reinterpret_cast<uint32_t*>(blk + q.g.off_vc),
+                           reinterpret_cast<__half2*>(blk + q.g.off_vm));
+}
+
 template <int BK, int BV>
 __device__ __forceinline__ void quantize_block(const QuantParams& q, const QuantRow& row, int x,
                                                int p) {
   const int D = q.g.D, G = q.g.G;
   const int tid = threadIdx.x;
   if (x > row.nflush) return;
+  if constexpr (BK != 8 && BV != 8) {
+    if (x < row.nflush && q.g.frag_k && q.g.frag_v && q.g.nout == 0) {
+      if (D == 128) quantize_block_frag<BK, BV, 128>(q, row, x, p);
+      else quantize_block_frag<BK, BV, 64>(q, row, x, p);
+      return;
+    }
+  }
 
   if (x == row.nflush) {
     // remainder -> tail rows [dst_row0, ...) of buffer dst
@@ -478,14 +541,6 @@ __device__ __forceinline__ void quantize_block(const QuantParams& q, const Quant
                  (static_cast<size_t>(p) * q.g.NB + row.first_block + x) * q.g.block_bytes;
   __half2* kmeta = reinterpret_cast<__half2*>(blk + q.g.off_km);
   __half2* vmeta = reinterpret_cast<__half2*>(blk + q.g.off_vm);
-
-  if constexpr (BK != 8 && BV != 8) {
-    if (q.g.frag_k && q.g.frag_v && nout == 0) {
-      quantize_frag<BK, BV>(xk, xv, reinterpret_cast<float*>(kcode), reinterpret_cast<uint32_t*>(blk),
-                            kmeta, reinterpret_cast<uint32_t*>(blk + q.g.off_vc), vmeta, D);
-      return;
-    }
-  }
 
   // 1b. dense-and-sparse isolation: the nout elements of largest magnitude
   //     of each side are kept apart (skip masks) and stored as entries
