@@ -99,22 +99,48 @@ __device__ __forceinline__ uint32_t code_of(float x, const Stat& st, float top) 
   return __float_as_uint(r + 8388608.0f) & 0xffu;  // exact: r is an integer in [0, 255]
 }
 
-// code_of for two elements at once (packed fp32x2 subtract and multiply),
-// each with its own negated minimum (st.x, st.y), reciprocal (st.z, st.w)
-// and step; the codes come back at bits 0 and 16.
-__device__ __forceinline__ uint32_t code_pair(float2 x, float4 st, float2 s, float top) {
-  const float2 d = __fadd2_rn(x, make_float2(st.x, st.y));  // x - min, exactly as __fsub_rn
-  const float2 q = __fmul2_rn(d, make_float2(st.z, st.w));
-  float r0 = rintf(q.x), r1 = rintf(q.y);
-  const float2 t = __ffma2_rn(make_float2(r0, r1), make_float2(-1.f, -1.f), q);  // q - r
-  if (fmaxf(fabsf(t.x), fabsf(t.y)) > 0.5f - 0.000244140625f) {
-    if (fabsf(t.x) > 0.5f - 0.000244140625f) r0 = tie_code(d.x, s.x);
-    if (fabsf(t.y) > 0.5f - 0.000244140625f) r1 = tie_code(d.y, s.y);
+// ldmatrix of four 8x8 fp16 matrices (lane i addresses row i % 8 of matrix
+// i / 8; 16-byte aligned rows): lane L receives row L / 4, columns 2 (L % 4)
+// and 2 (L % 4) + 1 of each matrix; .trans: rows 2 (L % 4), 2 (L % 4) + 1 of
+// column L / 4.
+__device__ __forceinline__ void ldsm_x4(uint32_t (&x)[4], const __half* row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+               : "r"(smem_addr(row)));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&x)[4], const __half* row) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(x[0]), "=r"(x[1]), "=r"(x[2]), "=r"(x[3])
+               : "r"(smem_addr(row)));
+}
+
+// code_of for the four elements of a slot (xa and xb: rows r0 and r1 at
+// the same two columns, so the same statistics): q + 1.5 * 2^23 rounds q to
+// the nearest integer, ties to even (rintf), into the low mantissa bits;
+// one near-tie test covers the four elements; the steps are read only on
+// that rare path.  Codes of xa come back in ca, of xb in cb (bits 0, 16).
+__device__ __forceinline__ void code_quad(float2 xa, float2 xb, float4 st, const float2* ss,
+                                          float top, uint32_t& ca, uint32_t& cb) {
+  constexpr float kM = 12582912.0f;
+  constexpr float kTie = 0.5f - 0.000244140625f;
+  const float2 mn = make_float2(st.x, st.y), rc = make_float2(st.z, st.w);
+  const float2 km = make_float2(kM, kM), nkm = make_float2(-kM, -kM), neg = make_float2(-1.f, -1.f);
+  const float2 da = __fadd2_rn(xa, mn), db = __fadd2_rn(xb, mn);  // x - min, exactly
+  const float2 qa = __fmul2_rn(da, rc), qb = __fmul2_rn(db, rc);
+  float2 ma = __fadd2_rn(qa, km), mb = __fadd2_rn(qb, km);         // kM + rint(q)
+  const float2 ta = __ffma2_rn(__fadd2_rn(ma, nkm), neg, qa);     // q - rint(q), exact
+  const float2 tb = __ffma2_rn(__fadd2_rn(mb, nkm), neg, qb);
+  if (fmaxf(fmaxf(fabsf(ta.x), fabsf(ta.y)), fmaxf(fabsf(tb.x), fabsf(tb.y))) > kTie) {
+    const float2 s = *ss;
+    if (fabsf(ta.x) > kTie) ma.x = tie_code(da.x, s.x) + kM;
+    if (fabsf(ta.y) > kTie) ma.y = tie_code(da.y, s.y) + kM;
+    if (fabsf(tb.x) > kTie) mb.x = tie_code(db.x, s.x) + kM;
+    if (fabsf(tb.y) > kTie) mb.y = tie_code(db.y, s.y) + kM;
   }
-  const float2 m = __fadd2_rn(make_float2(fminf(r0, top), fminf(r1, top)),
-                              make_float2(8388608.0f, 8388608.0f));
-  // 2^23 + c has the code in byte 0 and a zero byte 1: bytes {c0, 0, c1, 0}
-  return __byte_perm(__float_as_uint(m.x), __float_as_uint(m.y), 0x1410);
+  const float hi = kM + top;  // r <= top exactly when kM + r <= kM + top
+  // bytes {c0, 0, c1, 0}: kM + c has the code in byte 0 and a zero byte 1
+  ca = __byte_perm(__float_as_uint(fminf(ma.x, hi)), __float_as_uint(fminf(ma.y, hi)), 0x1410);
+  cb = __byte_perm(__float_as_uint(fminf(mb.x, hi)), __float_as_uint(fminf(mb.y, hi)), 0x1410);
 }
 
 // Row jc of pair p's combined sequence (its row's tail rows, then the new
@@ -294,8 +320,9 @@ __device__ void select_outliers(const __half* X, int XP, int G, int D, int n, ui
 //      min/max over the 32 rows), the next 32 * D/32 threads one value group
 //      each; {min, 1/step} and the step go to shared memory, {scale, zero}
 //      to the block;
-//   3. one thread per output word computes its codes straight from the fp16
-//      tile, two at a time (code_pair), and stores the word: no byte tile.
+//   3. one thread per output word, its lane the word's fragment lane: each
+//      k-step's fp16 pairs come from one ldmatrix (.trans for the values),
+//      the codes from code_quad, four at a time: no byte tile.
 // The codes equal code_of's, element by element.
 template <int BK, int BV, int D>
 __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv, float* sts,
@@ -345,56 +372,65 @@ __device__ __forceinline__ void quantize_frag(const __half* xk, const __half* xv
   __syncthreads();
 
   // K words (tile: 32 token rows x D channels), then V words (D channel
-  // rows x 32 tokens); bit widths are compile-time, lane words per 16 tile
-  // rows a power of two (shifts, no division)
+  // rows x 32 tokens).  Warp w takes lane words lw = w, w + 8, ...; its lane
+  // is the word's fragment lane, so one ldmatrix (.trans for the values,
+  // whose tile is stored token-major) hands every lane the fp16 pairs of a
+  // k-step: registers 0 and 1 rows r0 and r1 at columns 2t, 2t + 1, 2 and 3
+  // the same at columns 2t + 8, 2t + 9.  Bit widths are compile-time.
   constexpr float topk = static_cast<float>((1 << BK) - 1), topv = static_cast<float>((1 << BV) - 1);
   constexpr int lgk = (BK == 2 ? 0 : 1) + (D == 128 ? 2 : 1);  // log2(D * BK / 64)
   constexpr int lgv = BV == 2 ? 0 : 1;
-  for (int wi = tid; wi < D * BK; wi += kQuantThreads) {
-    const int l = (wi >> 2) & 31, lw = ((wi >> 7) << 2) | (wi & 3);
-    const int g = l >> 2, t = l & 3;
+  constexpr int NWARP = kQuantThreads / 32;
+  const int lane = tid & 31, warp = tid >> 5;
+  const int t = lane & 3;
+  const int lr = lane & 7, lm = lane >> 3;  // the row and matrix this lane addresses
+  for (int lw = warp; lw < D * BK / 32; lw += NWARP) {
     const int mt = lw >> lgk, kk = lw & ((1 << lgk) - 1);
-    const int r0 = 16 * mt + g, r1 = r0 + 8;
     uint32_t word = 0;
 #pragma unroll
-    for (int sl = 0; sl < (BK == 2 ? 4 : 2); ++sl) {
-      // slot sl: k-step and half, bit offsets of rows r0 and r1
-      const int ks = BK == 2 ? 2 * kk + (sl >> 1) : kk;
-      const int kh = BK == 2 ? (sl & 1) : sl;
-      const int b0 = BK == 2 ? (sl ? 8 + 2 * sl : 0) : 8 * sl;
-      const int b1 = BK == 2 ? 2 + 2 * sl : 8 * sl + 4;
-      const int col = 16 * ks + 8 * kh + 2 * t;
-      const float4 st = kst[col >> 1];
-      const float2 ss = kss[col >> 1];
-      const float2 a = __half22float2(*reinterpret_cast<const __half2*>(xk + r0 * XP + col));
-      const float2 b = __half22float2(*reinterpret_cast<const __half2*>(xk + r1 * XP + col));
-      word |= code_pair(a, st, ss, topk) << b0;
-      word |= code_pair(b, st, ss, topk) << b1;
+    for (int h = 0; h < (BK == 2 ? 2 : 1); ++h) {
+      const int ks = BK == 2 ? 2 * kk + h : kk;
+      uint32_t x[4];
+      ldsm_x4(x, xk + (16 * mt + lr + 8 * (lm & 1)) * XP + 16 * ks + 8 * (lm >> 1));
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh) {
+        // slot sl: bit offsets of rows r0 and r1
+        const int sl = BK == 2 ? 2 * h + kh : kh;
+        const int b0 = BK == 2 ? (sl ? 8 + 2 * sl : 0) : 8 * sl;
+        const int b1 = BK == 2 ? 2 + 2 * sl : 8 * sl + 4;
+        const int col = 16 * ks + 8 * kh + 2 * t;
+        uint32_t ca, cb;
+        code_quad(__half22float2(*reinterpret_cast<const __half2*>(&x[2 * kh])),
+                  __half22float2(*reinterpret_cast<const __half2*>(&x[2 * kh + 1])), kst[col >> 1],
+                  kss + (col >> 1), topk, ca, cb);
+        word |= (ca << b0) | (cb << b1);
+      }
     }
-    kc[wi] = word;
+    kc[((lw >> 2) << 7) | (lane << 2) | (lw & 3)] = word;
   }
-  for (int wi = tid; wi < D * BV; wi += kQuantThreads) {
-    const int l = (wi >> 2) & 31, lw = ((wi >> 7) << 2) | (wi & 3);
-    const int g = l >> 2, t = l & 3;
+  for (int lw = warp; lw < D * BV / 32; lw += NWARP) {
     const int mt = lw >> lgv, kk = lw & ((1 << lgv) - 1);
-    const int r0 = 16 * mt + g, r1 = r0 + 8;
-    const int gv = r0 >> 5;  // rows r0 and r1 share a channel group
+    const int gv = mt >> 1;  // rows r0 = 16 mt + g and r1 = r0 + 8 share a channel group
     uint32_t word = 0;
 #pragma unroll
-    for (int sl = 0; sl < (BV == 2 ? 4 : 2); ++sl) {
-      const int ks = BV == 2 ? 2 * kk + (sl >> 1) : kk;
-      const int kh = BV == 2 ? (sl & 1) : sl;
-      const int b0 = BV == 2 ? (sl ? 8 + 2 * sl : 0) : 8 * sl;
-      const int b1 = BV == 2 ? 2 + 2 * sl : 8 * sl + 4;
-      const int col = 16 * ks + 8 * kh + 2 * t;  // token
-      const float4 st = vst[gv * 16 + (col >> 1)];
-      const float2 ss = vss[gv * 16 + (col >> 1)];
-      const float2 a = make_float2(__half2float(xv[col * XP + r0]), __half2float(xv[(col + 1) * XP + r0]));
-      const float2 b = make_float2(__half2float(xv[col * XP + r1]), __half2float(xv[(col + 1) * XP + r1]));
-      word |= code_pair(a, st, ss, topv) << b0;
-      word |= code_pair(b, st, ss, topv) << b1;
+    for (int h = 0; h < (BV == 2 ? 2 : 1); ++h) {
+      const int ks = BV == 2 ? 2 * kk + h : kk;
+      uint32_t x[4];
+      ldsm_x4_trans(x, xv + (16 * ks + lr + 8 * (lm >> 1)) * XP + 16 * mt + 8 * (lm & 1));
+#pragma unroll
+      for (int kh = 0; kh < 2; ++kh) {
+        const int sl = BV == 2 ? 2 * h + kh : kh;
+        const int b0 = BV == 2 ? (sl ? 8 + 2 * sl : 0) : 8 * sl;
+        const int b1 = BV == 2 ? 2 + 2 * sl : 8 * sl + 4;
+        const int col = 16 * ks + 8 * kh + 2 * t;  // token
+        uint32_t ca, cb;
+        code_quad(__half22float2(*reinterpret_cast<const __half2*>(&x[2 * kh])),
+                  __half22float2(*reinterpret_cast<const __half2*>(&x[2 * kh + 1])),
+                  vst[gv * 16 + (col >> 1)], vss + gv * 16 + (col >> 1), topv, ca, cb);
+        word |= (ca << b0) | (cb << b1);
+      }
     }
-    vc[wi] = word;
+    vc[((lw >> 2) << 7) | (lane << 2) | (lw & 3)] = word;
   }
 }
 
