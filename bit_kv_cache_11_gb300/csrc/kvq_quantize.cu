@@ -490,44 +490,45 @@ __device__ __forceinline__ void quantize_block_frag(const QuantParams& q, const 
                            reinterpret_cast<__half2*>(blk + q.g.off_vm));
 }
 
+// The extra CTA (x == nflush) of pair p: the remainder tokens into the tail,
+// the first nsink new tokens into the sink window.
+__device__ __forceinline__ void copy_remainder(const QuantParams& q, const QuantRow& row, int p) {
+  const int D = q.g.D;
+  const int tid = threadIdx.x;
+  // remainder -> tail rows [dst_row0, ...) of buffer dst
+  const int rows = row.rem_end - row.rem_begin;
+  const int chunks = rows * (D / 8);
+  for (int c = tid; c < chunks; c += blockDim.x) {
+    const int r = c / (D / 8);
+    const int col = (c % (D / 8)) * 8;
+    const int jc = row.rem_begin + r;
+    const size_t dst = (static_cast<size_t>(p) * q.g.TC + row.dst_row0 + r) * D + col;
+    *reinterpret_cast<uint4*>(q.ktail[row.dst] + dst) =
+        *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, false) + col);
+    *reinterpret_cast<uint4*>(q.vtail[row.dst] + dst) =
+        *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, true) + col);
+  }
+  // the first nsink new tokens -> sink rows [sink0, sink0 + nsink)
+  const int schunks = row.nsink * (D / 8);
+  for (int c = tid; c < schunks; c += blockDim.x) {
+    const int r = c / (D / 8);
+    const int col = (c % (D / 8)) * 8;
+    const size_t src = (static_cast<size_t>(p) * q.new_stride + r) * D + col;
+    const size_t dst = (static_cast<size_t>(p) * q.g.NSK + row.sink0 + r) * D + col;
+    *reinterpret_cast<uint4*>(q.ksink + dst) = *reinterpret_cast<const uint4*>(q.knew + src);
+    *reinterpret_cast<uint4*>(q.vsink + dst) = *reinterpret_cast<const uint4*>(q.vnew + src);
+  }
+}
+
 template <int BK, int BV>
 __device__ __forceinline__ void quantize_block(const QuantParams& q, const QuantRow& row, int x,
                                                int p) {
   const int D = q.g.D, G = q.g.G;
   const int tid = threadIdx.x;
   if (x > row.nflush) return;
-  if constexpr (BK != 8 && BV != 8) {
-    if (x < row.nflush && q.g.frag_k && q.g.frag_v && q.g.nout == 0) {
-      if (D == 128) quantize_block_frag<BK, BV, 128>(q, row, x, p);
-      else quantize_block_frag<BK, BV, 64>(q, row, x, p);
-      return;
-    }
-  }
 
   if (x == row.nflush) {
-    // remainder -> tail rows [dst_row0, ...) of buffer dst
-    const int rows = row.rem_end - row.rem_begin;
-    const int chunks = rows * (D / 8);
-    for (int c = tid; c < chunks; c += blockDim.x) {
-      const int r = c / (D / 8);
-      const int col = (c % (D / 8)) * 8;
-      const int jc = row.rem_begin + r;
-      const size_t dst = (static_cast<size_t>(p) * q.g.TC + row.dst_row0 + r) * D + col;
-      *reinterpret_cast<uint4*>(q.ktail[row.dst] + dst) =
-          *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, false) + col);
-      *reinterpret_cast<uint4*>(q.vtail[row.dst] + dst) =
-          *reinterpret_cast<const uint4*>(combined_row(q, row, p, jc, true) + col);
-    }
-    // the first nsink new tokens -> sink rows [sink0, sink0 + nsink)
-    const int schunks = row.nsink * (D / 8);
-    for (int c = tid; c < schunks; c += blockDim.x) {
-      const int r = c / (D / 8);
-      const int col = (c % (D / 8)) * 8;
-      const size_t src = (static_cast<size_t>(p) * q.new_stride + r) * D + col;
-      const size_t dst = (static_cast<size_t>(p) * q.g.NSK + row.sink0 + r) * D + col;
-      *reinterpret_cast<uint4*>(q.ksink + dst) = *reinterpret_cast<const uint4*>(q.knew + src);
-      *reinterpret_cast<uint4*>(q.vsink + dst) = *reinterpret_cast<const uint4*>(q.vnew + src);
-    }
+    copy_remainder(q, row, p);
     return;
   }
 
@@ -766,6 +767,22 @@ __global__ void __launch_bounds__(kQuantThreads) quantize_kernel(const __grid_co
   quantize_block<BK, BV>(q, q.rows[RAGGED ? p / q.hkv : 0], x, p);
 }
 
+// The pages' geometry (fragment order on both sides, G = 32, 2- or 4-bit
+// codes, no outliers), head dimension D: a kernel of its own, so that its
+// registers are not those of the general path.
+template <int BK, int BV, int D, bool RAGGED>
+__global__ void __launch_bounds__(kQuantThreads) quantize_frag_kernel(const __grid_constant__ QuantParams q) {
+  const int x = blockIdx.x;
+  const int p = blockIdx.y;
+  const QuantRow& row = q.rows[RAGGED ? p / q.hkv : 0];
+  if (x > row.nflush) return;
+  if (x == row.nflush) {
+    copy_remainder(q, row, p);
+    return;
+  }
+  quantize_block_frag<BK, BV, D>(q, row, x, p);
+}
+
 __global__ void __launch_bounds__(kQuantThreads) dequantize_kernel(const DequantParams q) {
   const int i = blockIdx.x;
   const int p = blockIdx.y;
@@ -834,6 +851,15 @@ QuantFn quant_fn(int bk, int bv, bool ragged) {
 #undef KVQ_Q
   return nullptr;
 }
+QuantFn quant_frag_fn(int bk, int bv, int D, bool ragged) {
+#define KVQ_QF(BK_, BV_, D_) \
+  if (bk == BK_ && bv == BV_ && D == D_) \
+    return ragged ? quantize_frag_kernel<BK_, BV_, D_, true> : quantize_frag_kernel<BK_, BV_, D_, false>;
+  KVQ_QF(2, 2, 64) KVQ_QF(2, 4, 64) KVQ_QF(4, 2, 64) KVQ_QF(4, 4, 64)
+  KVQ_QF(2, 2, 128) KVQ_QF(2, 4, 128) KVQ_QF(4, 2, 128) KVQ_QF(4, 4, 128)
+#undef KVQ_QF
+  return nullptr;
+}
 }  // namespace
 
 // Opts every quantize instantiation into the shared memory of the largest
@@ -853,7 +879,9 @@ cudaError_t prepare_quantize() {
 
 cudaError_t launch_quantize(const QuantParams& q, cudaStream_t stream) {
   const size_t smem = quantize_smem_bytes(q.g.D, q.g.G, q.g.nout);
-  QuantFn fn = quant_fn(q.g.bk, q.g.bv, q.ragged != 0);
+  const bool frag = q.g.frag_k && q.g.frag_v && q.g.nout == 0 && q.g.bk != 8 && q.g.bv != 8;
+  QuantFn fn = frag ? quant_frag_fn(q.g.bk, q.g.bv, q.g.D, q.ragged != 0)
+                    : quant_fn(q.g.bk, q.g.bv, q.ragged != 0);
   if (fn == nullptr) return cudaErrorInvalidValue;
   int mx = 0;  // most blocks any row flushes
   const int nrows = q.ragged ? q.g.P / q.hkv : 1;
