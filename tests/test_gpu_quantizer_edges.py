@@ -22,6 +22,10 @@ groups (G channels of one token) of a cache, on both axis assignments:
   * FP8: quotients at and beyond 448, E4M3 ties, subnormal quotients, zero
     and subnormal scales.
 
+The pages' geometry (keys per channel, values per token, G = 32, 2 and 4
+bits) is quantized by a kernel of its own, with its own rounding; the cases
+cover it at D = 128 and D = 64.
+
 Bars: packed blocks and fp16 tails bit-exact and dequantized values
 bit-exact, through the C ABI, on every group.  Decode within 2e-3 max abs /
 1e-3 relative L2 of the oracle's fp64 attention on the groups whose values
@@ -225,6 +229,8 @@ CASES = [
     ("pages-2bit", 128, 1, 2, 32, 0, 1, False),
     ("pages-4bit-gqa4", 128, 4, 4, 32, 0, 1, False),
     ("pages-8bit-d64", 64, 2, 8, 32, 0, 1, False),
+    ("pages-2bit-d64", 64, 2, 2, 32, 0, 1, False),
+    ("pages-4bit-d64", 64, 1, 4, 32, 0, 1, False),
     ("flipped-2bit", 128, 1, 2, 32, 1, 0, False),
     ("flipped-8bit-g128", 128, 4, 8, 128, 1, 0, False),
     ("both-channel-4bit-g64", 64, 1, 4, 64, 0, 0, False),
