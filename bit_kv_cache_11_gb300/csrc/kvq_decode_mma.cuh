@@ -870,13 +870,28 @@ __global__ void __launch_bounds__(MmaCfg<D, BK, BV, R, ROPE, OUT>::NW * 32,
     const int mt = lane >> 4, g2 = lane & 7, hr = (lane >> 3) & 1;
     if constexpr (BK != 8) {
       constexpr int WPM = C::KWL / 2;  // words per m-tile
+      // word w of (row g2, slot tq) is component w & 3 of 16-byte chunk
+      // (w >> 2) * 32 + 4 g2 + tq: one 16-byte load brings four words
+      const uint4* kc4 = reinterpret_cast<const uint4*>(kc);
+      if constexpr (WPM >= 4) {
 #pragma unroll
-      for (int ww = 0; ww < WPM; ++ww)
+        for (int q4 = 0; q4 < WPM / 4; ++q4)
+#pragma unroll
+          for (int tq = 0; tq < 4; ++tq) {
+            const uint4 v = kc4[(mt * (WPM / 4) + q4) * 32 + 4 * g2 + tq];
+            kr[(4 * q4 + 0) * 4 + tq] = v.x;
+            kr[(4 * q4 + 1) * 4 + tq] = v.y;
+            kr[(4 * q4 + 2) * 4 + tq] = v.z;
+            kr[(4 * q4 + 3) * 4 + tq] = v.w;
+          }
+      } else {  // two words per m-tile: both m-tiles share a chunk (w = 2 mt + ww)
 #pragma unroll
         for (int tq = 0; tq < 4; ++tq) {
-          const int w = mt * WPM + ww;
-          kr[ww * 4 + tq] = kc[((w >> 2) * 32 + 4 * g2 + tq) * 4 + (w & 3)];
+          const uint4 v = kc4[4 * g2 + tq];
+          kr[tq] = mt ? v.z : v.x;
+          kr[4 + tq] = mt ? v.w : v.y;
         }
+      }
     }
     // right rotation that brings the code field of (e, row half hr,
     // pi = 2 (ks % 2) + kh) to the mantissa bits [23 - BK, 23)
